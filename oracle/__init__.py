@@ -1,0 +1,197 @@
+"""CPU fp64 oracle for paged-KV decode attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import this package.  The
+product path (``paged_kv_cache_23_gb300``) never imports it and shares no code
+with it: the arithmetic lives in ``pkv_oracle.c`` (plain C, fp64 loops), this
+module only compiles it with gcc and marshals numpy arrays through ctypes.
+
+Each wrapper names the passage of the source pages it follows; see the C file
+for the definitions written out.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pkv_oracle.c")
+_LIB = os.path.join(_HERE, "libpkv_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile pkv_oracle.c with gcc (OpenMP if the compiler has it)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    base = ["gcc", "-O2", "-shared", "-fPIC", "-o", tmp, _SRC, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I = ctypes.c_int
+            D = ctypes.c_double
+            sigs = {
+                "oracle_slot_mapping": [P, P, I, P, P, I, I, I],
+                "oracle_kv_append": [P, P, P, P, P, I, I, I, I, I],
+                "oracle_copy_blocks": [P, P, P, I, I, I, I, I],
+                "oracle_gather_kv": [P, P, P, P, P, I, P, I, I, I, I, I],
+                "oracle_attention": [P, P, P, P, P, I, P, P, I, I, I, I, I, I, D],
+                "oracle_attention_split": [P, P, P, P, I, P, P, P, P, I, P, P, I, I, I, I, I, I, D, I],
+                "oracle_spec_accept_greedy": [P, P, P, P, P, I, I, I],
+                "oracle_num_threads": [],
+            }
+            for name, argt in sigs.items():
+                f = getattr(lib, name)
+                f.argtypes = argt
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def slot_mapping(block_tables, seq_lens, append_lens, block_size, num_blocks):
+    """Slots of the last append_lens[b] positions of every sequence, packed in
+    sequence order ("Inference at Scale: KV Cache, Prefill, and Decode",
+    section 05, "The block table").  Returns (slots int64, status)."""
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    al = _c(append_lens, np.int32)
+    if bt.shape[0] != len(sl) or len(al) != len(sl):
+        raise ValueError("block_tables, seq_lens and append_lens disagree on the batch size")
+    n = int(np.clip(al, 0, None).sum())
+    slots = np.empty(max(n, 1), np.int64)
+    st = _load().oracle_slot_mapping(_p(slots), _p(bt), bt.shape[1], _p(sl), _p(al), len(sl),
+                                     block_size, num_blocks)
+    return slots[:n], st
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, slots):
+    """Write new K/V rows into their slots, in place (section 02 of "Inference
+    at Scale": decode appends one row per new token).  Returns status."""
+    assert k_cache.dtype == np.uint16 and k_cache.flags.c_contiguous
+    nb, nkv, bs, d = k_cache.shape
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    sl = _c(slots, np.int64)
+    if kn.shape != (len(sl), nkv, d) or vn.shape != kn.shape:
+        raise ValueError("k_new/v_new must be [num_tokens][n_kv][head_dim]")
+    return _load().oracle_kv_append(_p(k_cache), _p(v_cache), _p(kn), _p(vn), _p(sl), len(sl),
+                                    nb, bs, nkv, d)
+
+
+def copy_blocks(k_cache, v_cache, src_dst):
+    """Copy-on-write block copies, in place ("Chapter 31 Serving Efficiency",
+    31.3; "Inference at Scale", section 05).  Returns status."""
+    nb, nkv, bs, d = k_cache.shape
+    sd = _c(src_dst, np.int32).reshape(-1, 2)
+    return _load().oracle_copy_blocks(_p(k_cache), _p(v_cache), _p(sd), sd.shape[0], nb, bs, nkv, d)
+
+
+def gather_kv(k_cache, v_cache, block_tables, seq_lens):
+    """Contiguous [sum seq_len][n_kv][d] K and V read through the block table.
+    Returns (k, v, status)."""
+    nb, nkv, bs, d = k_cache.shape
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    tot = int(sl.sum())
+    ko = np.empty((max(tot, 1), nkv, d), np.uint16)
+    vo = np.empty((max(tot, 1), nkv, d), np.uint16)
+    st = _load().oracle_gather_kv(_p(ko), _p(vo), _p(k_cache), _p(v_cache), _p(bt), bt.shape[1],
+                                  _p(sl), len(sl), nb, bs, nkv, d)
+    return ko[:tot], vo[:tot], st
+
+
+def attention(q, k_cache, v_cache, block_tables, seq_lens, q_lens, scale):
+    """fp64 softmax attention through the block table, causal within the new
+    tokens (sections 07 and 08 of "Inference at Scale").  q is uint16 bf16
+    bits [sum q_len][n_q][d].  Returns (out float64, status)."""
+    nb, nkv, bs, d = k_cache.shape
+    q = _c(q, np.uint16)
+    nq = q.shape[1]
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ql = _c(q_lens, np.int32)
+    if q.shape[0] != int(np.clip(ql, 0, None).sum()) or q.shape[2] != d or nq % nkv:
+        raise ValueError("q must be [sum q_lens][n_q][head_dim] with n_q a multiple of n_kv")
+    out = np.zeros((max(q.shape[0], 1), nq, d), np.float64)
+    st = _load().oracle_attention(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(bt), bt.shape[1],
+                                  _p(sl), _p(ql), len(sl), nq, nkv, d, bs, nb, float(scale))
+    return out[: q.shape[0]], st
+
+
+def attention_split(q, k_cache, v_cache, block_tables, seq_lens, q_lens, scale, partition_tokens,
+                    want_partials=False):
+    """Flash-Decoding split-KV attention with log-sum-exp merge ("Inference at
+    Scale", section 07).  Returns (out, status) or, with want_partials,
+    (out, status, part_o, part_m, part_l) shaped [rows][n_q][nparts](, d)."""
+    nb, nkv, bs, d = k_cache.shape
+    q = _c(q, np.uint16)
+    nq = q.shape[1]
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ql = _c(q_lens, np.int32)
+    if q.shape[0] != int(np.clip(ql, 0, None).sum()) or q.shape[2] != d or nq % nkv:
+        raise ValueError("q must be [sum q_lens][n_q][head_dim] with n_q a multiple of n_kv")
+    P = int(partition_tokens)
+    if P <= 0:
+        raise ValueError("partition_tokens must be positive")
+    npm = max(1, -(-int(sl.max(initial=0)) // P))
+    rows = max(q.shape[0], 1)
+    out = np.zeros((rows, nq, d), np.float64)
+    po = pm = pl = None
+    if want_partials:
+        po = np.zeros((rows, nq, npm, d), np.float64)
+        pm = np.zeros((rows, nq, npm), np.float64)
+        pl = np.zeros((rows, nq, npm), np.float64)
+    st = _load().oracle_attention_split(_p(out), _p(po), _p(pm), _p(pl), npm, _p(q), _p(k_cache),
+                                        _p(v_cache), _p(bt), bt.shape[1], _p(sl), _p(ql), len(sl),
+                                        nq, nkv, d, bs, nb, float(scale), P)
+    n = q.shape[0]
+    if want_partials:
+        return out[:n], st, po[:n], pm[:n], pl[:n]
+    return out[:n], st
+
+
+def spec_accept_greedy(logits, draft):
+    """Greedy acceptance ("Spending the Idle" 12.4; "Inference at Scale" 08).
+    logits float32 [B][k+1][V], draft int32 [B][k].
+    Returns (accepted [B], next_token [B], argmax [B][k+1])."""
+    lg = _c(logits, np.float32)
+    B, k1, V = lg.shape
+    k = k1 - 1
+    dr = _c(draft, np.int32).reshape(B, k)
+    acc = np.empty(B, np.int32)
+    nxt = np.empty(B, np.int32)
+    am = np.empty((B, k1), np.int32)
+    _load().oracle_spec_accept_greedy(_p(acc), _p(nxt), _p(am), _p(lg), _p(dr), B, k, V)
+    return acc, nxt, am

@@ -1,0 +1,431 @@
+/*
+ * pkv_oracle.c -- plain, slow, fp64 CPU oracle for paged-KV decode attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py may load this library.  The product
+ * path (the CUDA library and its Python binding) never calls it, and this file
+ * shares no code, header, table or helper with the CUDA sources.
+ *
+ * Every function below is the plain definition of one step of the path, written
+ * out with loops and no blocking, fusion or reordering beyond what the
+ * definition states.  Floating point is fp64 throughout; bf16 inputs are
+ * widened exactly (a bf16 bit pattern is the top half of an IEEE fp32).
+ *
+ * Sources (web pages the method is taken from):
+ *   [KVC]  "Inference at Scale: KV Cache, Prefill, and Decode"
+ *          (blog.truongducdung.dev), sections 02, 03, 05, 07, 08.
+ *   [SE]   "Chapter 31 Serving Efficiency" (imbrooklyn.dev), 31.3, 31.4
+ *          (Example 31.2), 31.5.
+ *   [SI]   "Spending the Idle" (derivingsystems.com), 12.4.
+ *
+ * Cache layout (a choice; the pages only say K/V are read through the block
+ * table): k_cache, v_cache are [num_blocks][num_kv_heads][block_size][head_dim]
+ * bf16.  Logical token t of a sequence lives in physical block
+ * block_tables[b][t / block_size] at row t % block_size ([KVC] 05, "The block
+ * table").
+ *
+ * Status bits returned (same meaning as the CUDA library's, defined here
+ * independently):
+ *   1  a block id outside [0, num_blocks) was needed
+ *   2  a seq_len outside [0, max_blocks * block_size]
+ *   4  a q_len outside [0, seq_len]
+ *   8  a slot outside [-1.., num_blocks * block_size)  (negative = skip)
+ *   64 a copy pair outside [0, num_blocks)
+ * Output rows affected by bits 1, 2 or 4 are written as NaN.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ST_BAD_BLOCK 1
+#define ST_BAD_SEQLEN 2
+#define ST_BAD_QLEN 4
+#define ST_BAD_SLOT 8
+#define ST_BAD_PAIR 64
+
+static double widen_bf16(uint16_t bits) {
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* Offset (in elements) of row `row` of kv head `head` in physical block `blk`. */
+static int64_t cache_offset(int64_t blk, int head, int row, int n_kv, int bs, int d) {
+    return ((blk * n_kv + head) * (int64_t)bs + row) * (int64_t)d;
+}
+
+/*
+ * Slot mapping ([KVC] 05 "The block table"): the new tokens of sequence b are
+ * its last append_lens[b] positions; position pos goes to
+ * slot = block_tables[b][pos / bs] * bs + pos % bs.  Output is packed in
+ * sequence order.  Returns status bits.
+ */
+int oracle_slot_mapping(int64_t *slots, const int32_t *block_tables, int max_blocks,
+                        const int32_t *seq_lens, const int32_t *append_lens, int num_seqs,
+                        int block_size, int num_blocks) {
+    int status = 0;
+    int64_t o = 0;
+    for (int b = 0; b < num_seqs; b++) {
+        int L = seq_lens[b], A = append_lens[b];
+        int bad = 0;
+        if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size) { status |= ST_BAD_SEQLEN; bad = 1; }
+        if (A < 0 || A > L) { status |= ST_BAD_QLEN; bad = 1; }
+        if (A < 0) continue;
+        for (int i = 0; i < A; i++, o++) {
+            if (bad) { slots[o] = -1; continue; }
+            int pos = L - A + i;
+            int32_t blk = block_tables[(int64_t)b * max_blocks + pos / block_size];
+            if (blk < 0 || blk >= num_blocks) { status |= ST_BAD_BLOCK; slots[o] = -1; continue; }
+            slots[o] = (int64_t)blk * block_size + pos % block_size;
+        }
+    }
+    return status;
+}
+
+/*
+ * KV append ([KVC] 02 "The two phases of a request": a decode step appends one
+ * K/V row per new token).  k_new/v_new are [num_tokens][n_kv][d].  A negative
+ * slot means "skip"; a slot past the pool is an error and is skipped.
+ */
+int oracle_kv_append(uint16_t *k_cache, uint16_t *v_cache, const uint16_t *k_new,
+                     const uint16_t *v_new, const int64_t *slots, int num_tokens,
+                     int num_blocks, int block_size, int n_kv, int d) {
+    int status = 0;
+    for (int t = 0; t < num_tokens; t++) {
+        int64_t s = slots[t];
+        if (s < 0) continue;
+        if (s >= (int64_t)num_blocks * block_size) { status |= ST_BAD_SLOT; continue; }
+        int64_t blk = s / block_size;
+        int row = (int)(s % block_size);
+        for (int h = 0; h < n_kv; h++) {
+            for (int c = 0; c < d; c++) {
+                int64_t dst = cache_offset(blk, h, row, n_kv, block_size, d) + c;
+                int64_t src = ((int64_t)t * n_kv + h) * d + c;
+                k_cache[dst] = k_new[src];
+                v_cache[dst] = v_new[src];
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * Copy-on-write block copy ([SE] 31.3: share blocks, copy a block when a
+ * branch appends; [KVC] 05 "Block sharing and copy-on-write").  src_dst is
+ * [n][2]; every byte of K and V of block src is copied to block dst, pairs in
+ * order.
+ */
+int oracle_copy_blocks(uint16_t *k_cache, uint16_t *v_cache, const int32_t *src_dst, int n,
+                       int num_blocks, int block_size, int n_kv, int d) {
+    int status = 0;
+    int64_t per_block = (int64_t)n_kv * block_size * d;
+    for (int i = 0; i < n; i++) {
+        int32_t s = src_dst[2 * i], t = src_dst[2 * i + 1];
+        if (s < 0 || s >= num_blocks || t < 0 || t >= num_blocks) { status |= ST_BAD_PAIR; continue; }
+        for (int64_t e = 0; e < per_block; e++) {
+            k_cache[(int64_t)t * per_block + e] = k_cache[(int64_t)s * per_block + e];
+            v_cache[(int64_t)t * per_block + e] = v_cache[(int64_t)s * per_block + e];
+        }
+    }
+    return status;
+}
+
+/*
+ * Block-table gather ([KVC] 05 "The block table"): the K/V of each sequence,
+ * read through its block table, laid out contiguously as
+ * [sum seq_len][n_kv][d] in sequence order.
+ */
+int oracle_gather_kv(uint16_t *k_out, uint16_t *v_out, const uint16_t *k_cache,
+                     const uint16_t *v_cache, const int32_t *block_tables, int max_blocks,
+                     const int32_t *seq_lens, int num_seqs, int num_blocks, int block_size,
+                     int n_kv, int d) {
+    int status = 0;
+    int64_t o = 0;
+    for (int b = 0; b < num_seqs; b++) {
+        int L = seq_lens[b];
+        if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size) { status |= ST_BAD_SEQLEN; continue; }
+        for (int t = 0; t < L; t++, o++) {
+            int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+            for (int h = 0; h < n_kv; h++) {
+                for (int c = 0; c < d; c++) {
+                    int64_t dst = (o * n_kv + h) * d + c;
+                    if (blk < 0 || blk >= num_blocks) {
+                        k_out[dst] = 0x7fc0;  /* bf16 quiet NaN */
+                        v_out[dst] = 0x7fc0;
+                        status |= ST_BAD_BLOCK;
+                        continue;
+                    }
+                    int64_t src = cache_offset(blk, h, t % block_size, n_kv, block_size, d) + c;
+                    k_out[dst] = k_cache[src];
+                    v_out[dst] = v_cache[src];
+                }
+            }
+        }
+    }
+    return status;
+}
+
+/* Shared validation of one sequence for the attention functions. */
+static int check_seq(int L, int ql, int max_blocks, int block_size) {
+    int st = 0;
+    if (L < 0 || (int64_t)L > (int64_t)max_blocks * block_size) st |= ST_BAD_SEQLEN;
+    if (ql < 0 || ql > L) st |= ST_BAD_QLEN;
+    return st;
+}
+
+/*
+ * Softmax attention over K/V gathered through the block table -- the plain
+ * definition that paged, online and split attention all reach exactly
+ * ([KVC] 07 "Online softmax": the same computation with a different order of
+ * additions; [SE] 31.4).
+ *
+ * For sequence b with seq_len L and q_len ql, query i (0 <= i < ql) sits at
+ * position p = L - ql + i and sees positions 0..p (causal within the new
+ * tokens, [KVC] 08: the verify pass is like a short prefill).  Query head h
+ * uses kv head h / g, g = n_q / n_kv ([KVC] 04 "GQA").
+ *   s_t = scale * <q, K_t>,  M = max_t s_t,  w_t = exp(s_t - M),
+ *   o   = sum_t w_t V_t / sum_t w_t.
+ * q is [sum ql][n_q][d]; out is [sum ql][n_q][d] fp64.
+ */
+int oracle_attention(double *out, const uint16_t *q, const uint16_t *k_cache,
+                     const uint16_t *v_cache, const int32_t *block_tables, int max_blocks,
+                     const int32_t *seq_lens, const int32_t *q_lens, int num_seqs, int n_q,
+                     int n_kv, int d, int block_size, int num_blocks, double scale) {
+    int status = 0;
+    int g = n_q / n_kv;
+    int64_t *row0 = (int64_t *)malloc(sizeof(int64_t) * (num_seqs + 1));
+    row0[0] = 0;
+    for (int b = 0; b < num_seqs; b++) row0[b + 1] = row0[b] + (q_lens[b] > 0 ? q_lens[b] : 0);
+    for (int b = 0; b < num_seqs; b++) status |= check_seq(seq_lens[b], q_lens[b], max_blocks, block_size);
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
+    for (int b = 0; b < num_seqs; b++) {
+        int L = seq_lens[b], ql = q_lens[b];
+        if (ql <= 0) continue;
+        int seq_bad = check_seq(L, ql, max_blocks, block_size);
+        double *s = (double *)malloc(sizeof(double) * (L > 0 ? L : 1));
+        for (int i = 0; i < ql; i++) {
+            int64_t r = row0[b] + i;
+            int p = L - ql + i;
+            for (int h = 0; h < n_q; h++) {
+                double *o = out + (r * n_q + h) * d;
+                const uint16_t *qv = q + (r * n_q + h) * d;
+                int j = h / g;
+                int bad = seq_bad;
+                for (int t = 0; t <= p && !bad; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    if (blk < 0 || blk >= num_blocks) { bad = 1; status |= ST_BAD_BLOCK; }
+                }
+                if (bad) {
+                    for (int c = 0; c < d; c++) o[c] = NAN;
+                    continue;
+                }
+                /* scores */
+                for (int t = 0; t <= p; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    const uint16_t *kt = k_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                    double acc = 0.0;
+                    for (int c = 0; c < d; c++) acc += widen_bf16(qv[c]) * widen_bf16(kt[c]);
+                    s[t] = scale * acc;
+                }
+                double M = -INFINITY;
+                for (int t = 0; t <= p; t++) if (s[t] > M) M = s[t];
+                double den = 0.0;
+                for (int t = 0; t <= p; t++) { s[t] = exp(s[t] - M); den += s[t]; }
+                for (int c = 0; c < d; c++) o[c] = 0.0;
+                for (int t = 0; t <= p; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    const uint16_t *vt = v_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                    for (int c = 0; c < d; c++) o[c] += s[t] * widen_bf16(vt[c]);
+                }
+                for (int c = 0; c < d; c++) o[c] /= den;
+            }
+        }
+        free(s);
+    }
+    free(row0);
+    return status;
+}
+
+/*
+ * Split-KV attention with a log-sum-exp merge, in the order Flash-Decoding
+ * describes it ([KVC] 07 "FlashAttention-2, FlashAttention-3, and
+ * Flash-Decoding"): the visible positions of each query are cut into
+ * partitions [k*P, (k+1)*P); each partition yields a partial result
+ * (running max m_k, sum l_k = sum exp(s - m_k), normalised output o_k); the
+ * partials are merged with the online-softmax rescaling:
+ *   M = max_k m_k,  l = sum_k l_k exp(m_k - M),
+ *   o = sum_k o_k l_k exp(m_k - M) / l.
+ * A partition with no visible position has m = -inf, l = 0 and weight 0
+ * ([SE] Example 31.2: combine tile statistics, not tile averages).
+ *
+ * part_o / part_m / part_l (may be NULL) receive the partials for every
+ * (row, head, partition) as [sum ql][n_q][nparts_max](*d), where
+ * nparts_max = ceil(max over sequences of seq_len / P); unused entries are
+ * set to o = 0, m = -inf, l = 0.
+ */
+int oracle_attention_split(double *out, double *part_o, double *part_m, double *part_l,
+                           int nparts_max, const uint16_t *q, const uint16_t *k_cache,
+                           const uint16_t *v_cache, const int32_t *block_tables, int max_blocks,
+                           const int32_t *seq_lens, const int32_t *q_lens, int num_seqs, int n_q,
+                           int n_kv, int d, int block_size, int num_blocks, double scale,
+                           int partition_tokens) {
+    int status = 0;
+    int g = n_q / n_kv;
+    int P = partition_tokens;
+    int64_t *row0 = (int64_t *)malloc(sizeof(int64_t) * (num_seqs + 1));
+    row0[0] = 0;
+    for (int b = 0; b < num_seqs; b++) row0[b + 1] = row0[b] + (q_lens[b] > 0 ? q_lens[b] : 0);
+    for (int b = 0; b < num_seqs; b++) status |= check_seq(seq_lens[b], q_lens[b], max_blocks, block_size);
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
+    for (int b = 0; b < num_seqs; b++) {
+        int L = seq_lens[b], ql = q_lens[b];
+        if (ql <= 0) continue;
+        int seq_bad = check_seq(L, ql, max_blocks, block_size);
+        double *po = (double *)malloc(sizeof(double) * (size_t)nparts_max * d);
+        double *pm = (double *)malloc(sizeof(double) * (size_t)nparts_max);
+        double *pl = (double *)malloc(sizeof(double) * (size_t)nparts_max);
+        for (int i = 0; i < ql; i++) {
+            int64_t r = row0[b] + i;
+            int p = L - ql + i; /* last visible position */
+            for (int h = 0; h < n_q; h++) {
+                double *o = out + (r * n_q + h) * d;
+                const uint16_t *qv = q + (r * n_q + h) * d;
+                int j = h / g;
+                int bad = seq_bad;
+                for (int t = 0; t <= p && !bad; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    if (blk < 0 || blk >= num_blocks) { bad = 1; status |= ST_BAD_BLOCK; }
+                }
+                for (int k = 0; k < nparts_max; k++) {
+                    pm[k] = -INFINITY;
+                    pl[k] = 0.0;
+                    for (int c = 0; c < d; c++) po[(size_t)k * d + c] = 0.0;
+                }
+                if (!bad) {
+                    /* one partial per partition */
+                    for (int k = 0; k < nparts_max; k++) {
+                        int lo = k * P, hi = (k + 1) * P - 1;
+                        if (hi > p) hi = p;
+                        if (lo > hi) continue; /* nothing visible: m=-inf, l=0 */
+                        double m = -INFINITY;
+                        for (int t = lo; t <= hi; t++) {
+                            int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                            const uint16_t *kt = k_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                            double acc = 0.0;
+                            for (int c = 0; c < d; c++) acc += widen_bf16(qv[c]) * widen_bf16(kt[c]);
+                            double st = scale * acc;
+                            if (st > m) m = st;
+                        }
+                        double l = 0.0;
+                        double *ok = po + (size_t)k * d;
+                        for (int t = lo; t <= hi; t++) {
+                            int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                            const uint16_t *kt = k_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                            const uint16_t *vt = v_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                            double acc = 0.0;
+                            for (int c = 0; c < d; c++) acc += widen_bf16(qv[c]) * widen_bf16(kt[c]);
+                            double w = exp(scale * acc - m);
+                            l += w;
+                            for (int c = 0; c < d; c++) ok[c] += w * widen_bf16(vt[c]);
+                        }
+                        for (int c = 0; c < d; c++) ok[c] /= l;
+                        pm[k] = m;
+                        pl[k] = l;
+                    }
+                    /* merge */
+                    double M = -INFINITY;
+                    for (int k = 0; k < nparts_max; k++) if (pm[k] > M) M = pm[k];
+                    double lsum = 0.0;
+                    for (int c = 0; c < d; c++) o[c] = 0.0;
+                    for (int k = 0; k < nparts_max; k++) {
+                        if (pm[k] == -INFINITY) continue; /* empty partition, weight 0 */
+                        double wk = pl[k] * exp(pm[k] - M);
+                        lsum += wk;
+                        for (int c = 0; c < d; c++) o[c] += po[(size_t)k * d + c] * wk;
+                    }
+                    for (int c = 0; c < d; c++) o[c] /= lsum;
+                } else {
+                    for (int c = 0; c < d; c++) o[c] = NAN;
+                }
+                if (part_o) {
+                    for (int k = 0; k < nparts_max; k++) {
+                        size_t idx = ((size_t)r * n_q + h) * nparts_max + k;
+                        part_m[idx] = pm[k];
+                        part_l[idx] = pl[k];
+                        for (int c = 0; c < d; c++) part_o[idx * d + c] = po[(size_t)k * d + c];
+                    }
+                }
+            }
+        }
+        free(po);
+        free(pm);
+        free(pl);
+    }
+    free(row0);
+    return status;
+}
+
+/*
+ * "a beats b" for the argmax: NaN is greater than every number and the first
+ * index wins among equal values (numpy/torch argmax convention).
+ */
+static int beats(float a, int64_t ia, float b, int64_t ib) {
+    int an = isnan(a), bn = isnan(b);
+    if (an != bn) return an;
+    if (!an && a != b) return a > b;
+    return ia < ib;
+}
+
+/*
+ * Greedy speculative acceptance ([SI] 12.4: accept the drafts that match what
+ * the model would pick and stop at the first that does not; [KVC] 08: with
+ * greedy decoding accept a draft token if it matches the target's argmax, and
+ * always add one target token).
+ *   logits [B][k+1][V] fp32, draft [B][k] int32.
+ *   argmax[b][j]  = first index of the maximum of row (b, j)   (j = 0..k)
+ *   accepted[b]   = number of leading j < k with draft[b][j] == argmax[b][j]
+ *   next_token[b] = argmax[b][accepted[b]]   (the correction or bonus token)
+ * argmax may be NULL.
+ */
+int oracle_spec_accept_greedy(int32_t *accepted, int32_t *next_token, int32_t *argmax,
+                              const float *logits, const int32_t *draft, int B, int k, int V) {
+    for (int b = 0; b < B; b++) {
+        int32_t *rowmax = (int32_t *)malloc(sizeof(int32_t) * (k + 1));
+        for (int j = 0; j <= k; j++) {
+            const float *row = logits + ((int64_t)b * (k + 1) + j) * V;
+            int64_t best = 0;
+            for (int64_t v = 1; v < V; v++)
+                if (beats(row[v], v, row[best], best)) best = v;
+            rowmax[j] = (int32_t)best;
+            if (argmax) argmax[b * (k + 1) + j] = (int32_t)best;
+        }
+        int a = 0;
+        while (a < k && draft[b * k + a] == rowmax[a]) a++;
+        accepted[b] = a;
+        next_token[b] = rowmax[a];
+        free(rowmax);
+    }
+    return 0;
+}
+
+/* Number of threads the oracle's parallel loops use (1 without OpenMP). */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    int n = 1;
+#pragma omp parallel
+    {
+#pragma omp single
+        n = omp_get_num_threads();
+    }
+    return n;
+#else
+    return 1;
+#endif
+}
