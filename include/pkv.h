@@ -1,0 +1,219 @@
+/*
+ * pkv.h -- C ABI of libpkv, paged-KV decode attention for GB300 (sm_103a).
+ *
+ * The operations follow these web pages:
+ *   [KVC] "Inference at Scale: KV Cache, Prefill, and Decode"
+ *         (blog.truongducdung.dev): section 02 (decode appends one K/V row and
+ *         rereads the cache; GQA intensity), 03 (bytes per token), 05 (block
+ *         table, block sharing and copy-on-write), 07 (online softmax,
+ *         FlashAttention loop, Flash-Decoding split-KV + log-sum-exp merge),
+ *         08 (speculative verification, greedy rule).
+ *   [SE]  "Chapter 31 Serving Efficiency" (imbrooklyn.dev): 31.3 (shared
+ *         prefix, copy a block when a branch appends), 31.4 (Example 31.2,
+ *         combine tile statistics), 31.5 (greedy acceptance).
+ *   [SI]  "Spending the Idle" (derivingsystems.com): 12.4 (accept the
+ *         longest matching prefix, stop at the first miss).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument is DEVICE memory on the current CUDA device,
+ *   allocated and owned by the caller.  The library allocates no device
+ *   memory; kernels that need scratch take a caller-provided workspace.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream).  Nothing synchronises the host.
+ * - bf16 tensors hold raw bfloat16 values (2 bytes each), 16-byte aligned.
+ * - Cache layout: k_cache and v_cache are separate pools
+ *   [num_blocks][num_kv_heads][block_size][head_dim] bf16, so one
+ *   (block, kv head) tile is block_size * head_dim * 2 contiguous bytes.
+ *   Logical token t of sequence b is row t % block_size of physical block
+ *   block_tables[b * max_blocks + t / block_size] ([KVC] 05).
+ * - block_tables: int32 [num_seqs][max_blocks]; entries past a sequence's
+ *   last block are never read.
+ * - Query head h reads kv head h / g, g = num_q_heads / num_kv_heads
+ *   ([KVC] 04, GQA: contiguous groups).
+ * - Return value: PKV_OK (0) when the work was enqueued; a negative PKV_ERR_*
+ *   when the host detected a bad argument (nothing was enqueued) or the launch
+ *   failed.
+ * - Device-detected input errors (block id out of range, bad lengths, bad
+ *   slots) are OR-ed into *status (device int32, may be NULL) as
+ *   PKV_STATUS_* bits; the affected outputs are written as NaN or skipped as
+ *   documented per call.  No kernel traps, asserts or spins without a bound:
+ *   a wait that runs out sets PKV_STATUS_TIMEOUT.
+ * - Results are deterministic: no floating-point atomics, and the attention
+ *   result does not depend on where the physical blocks sit in the pool.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_OK 0
+#define PKV_ERR_NULL (-1)        /* a required pointer is NULL */
+#define PKV_ERR_SIZE (-2)        /* a size or count argument is out of range */
+#define PKV_ERR_UNSUPPORTED (-3) /* head_dim, block_size or head grouping not supported */
+#define PKV_ERR_WORKSPACE (-4)   /* workspace missing or smaller than required */
+#define PKV_ERR_ALIGN (-5)       /* a pointer is not 16-byte aligned */
+#define PKV_ERR_CUDA (-6)        /* a CUDA runtime call or launch failed */
+#define PKV_ERR_DEVICE (-7)      /* the current device is not an sm_103 GPU */
+
+#define PKV_STATUS_BAD_BLOCK 1   /* a needed block id is outside [0, num_blocks) */
+#define PKV_STATUS_BAD_SEQLEN 2  /* a seq_len is < 0, > max_blocks*block_size or > max_seq_len */
+#define PKV_STATUS_BAD_QLEN 4    /* a q_len/append_len is < 0 or > seq_len, or rows overflow */
+#define PKV_STATUS_BAD_SLOT 8    /* a slot is >= num_blocks*block_size */
+#define PKV_STATUS_TIMEOUT 32    /* a bounded device wait ran out (library bug) */
+#define PKV_STATUS_BAD_PAIR 64   /* a copy pair names a block outside the pool */
+
+/* Attention flags. */
+#define PKV_ATTN_DECODE_TENSOR_CORES 1 /* run q_len = 1 rows on the mma path too */
+
+/* Library version, 100 * major + minor. */
+int pkv_version(void);
+
+/* Text for a PKV_ERR_* return code or a single PKV_STATUS_* bit. */
+const char* pkv_error_string(int rc);
+const char* pkv_status_string(int bit);
+
+/*
+ * a1. Slot mapping ([KVC] 05, "The block table").
+ * The new tokens of sequence b are its last append_lens[b] positions
+ * pos in [seq_lens[b] - append_lens[b], seq_lens[b]); each gets
+ *   slots[o] = block_tables[b][pos / block_size] * block_size + pos % block_size
+ * packed in sequence order (o runs over sequences, then positions).
+ *   slots        int64 [num_slots] out; num_slots must equal sum(append_lens)
+ *   seq_lens     int32 [num_seqs], append_lens int32 [num_seqs]
+ * Invalid lengths (PKV_STATUS_BAD_SEQLEN / BAD_QLEN) or block ids
+ * (BAD_BLOCK) give slot -1 ("skip" for pkv_kv_append).
+ * num_seqs <= 16384.
+ */
+int pkv_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
+                     const int32_t* seq_lens, const int32_t* append_lens, int num_seqs,
+                     int num_slots, int block_size, int num_blocks, int32_t* status,
+                     void* stream);
+
+/*
+ * a2. KV append ([KVC] 02: each decode step appends one K/V row per new
+ * token before attention rereads the cache).
+ *   k_new, v_new  bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slots         int64 [num_tokens]; slot < 0 skips the token,
+ *                 slot >= num_blocks*block_size sets PKV_STATUS_BAD_SLOT and
+ *                 skips it.
+ * Row slots[t] % block_size of block slots[t] / block_size receives token t,
+ * all kv heads.  Bit-exact copy.  Two tokens with the same slot race.
+ * head_dim must be a multiple of 8.
+ */
+int pkv_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                  const int64_t* slots, int num_tokens, int num_blocks, int block_size,
+                  int num_kv_heads, int head_dim, int32_t* status, void* stream);
+
+/*
+ * a3. Copy-on-write block copy ([SE] 31.3: share physical blocks and copy a
+ * block when a branch appends; [KVC] 05 "Block sharing and copy-on-write").
+ *   src_dst  int32 [num_pairs][2]: every byte of K and V of block src is
+ *            copied to block dst.
+ * Destinations must be distinct and must not also be sources in the same
+ * call (pairs run in parallel).  A pair outside [0, num_blocks) sets
+ * PKV_STATUS_BAD_PAIR and is skipped.  Bit-exact.
+ */
+int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst, int num_pairs,
+                    int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                    int32_t* status, void* stream);
+
+/*
+ * a4 as a standalone utility: block-table gather ([KVC] 05: the kernel
+ * reads K and V through the block table).  Writes each sequence's K/V
+ * contiguously:
+ *   k_out, v_out  bf16 [sum seq_lens][num_kv_heads][head_dim]
+ *   out_offsets   int64 [num_seqs]: first output row of sequence b
+ * A bad block id writes NaN rows and sets PKV_STATUS_BAD_BLOCK; a bad
+ * seq_len skips the sequence and sets PKV_STATUS_BAD_SEQLEN.  Bit-exact.
+ */
+int pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                  const int64_t* out_offsets, int num_seqs, int num_blocks, int block_size,
+                  int num_kv_heads, int head_dim, int32_t* status, void* stream);
+
+/*
+ * Partition length pkv_paged_attention_decode uses when partition_tokens is
+ * 0, for a batch of num_seqs sequences no longer than max_seq_len.
+ */
+int pkv_attention_auto_partition(int num_seqs, int total_q, int num_kv_heads, int max_seq_len);
+
+/*
+ * Workspace bytes pkv_paged_attention_decode needs for these bounds
+ * (total_q = sum of q_lens, max_seq_len >= every seq_len).  The same
+ * workspace may be reused by calls on the same stream.
+ */
+size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int max_seq_len, int partition_tokens);
+
+/*
+ * a4-a8. Paged attention for decode, speculative verification and chunked
+ * prefill in one launch.
+ *
+ * Computes, for every sequence b, query i < q_lens[b] and query head h,
+ * the softmax attention of q over the K/V of kv head h / g read through the
+ * block table ([KVC] 05), causal within the new tokens: query i sits at
+ * position p = seq_lens[b] - q_lens[b] + i and sees positions 0..p ([KVC] 08:
+ * the verify pass is like a short prefill):
+ *   s_t = scale * <q, K_t>,  o = sum_t softmax(s)_t V_t.
+ * It is evaluated with the online-softmax recurrence ([KVC] 07: running max
+ * m, running sum l, rescale O by exp(m_old - m_new)), split into partitions
+ * of partition_tokens positions whose partial (O, m, l) are merged with the
+ * log-sum-exp rescaling of Flash-Decoding ([KVC] 07; [SE] Example 31.2:
+ * combine tile statistics, not tile averages).  Arithmetic is fp32 on bf16
+ * inputs; out is bf16 (round to nearest even).
+ *
+ *   out, q        bf16 [total_q][num_q_heads][head_dim], sequences in batch
+ *                 order (the first q_lens[0] rows belong to sequence 0, ...)
+ *   seq_lens      int32 [num_seqs], INCLUDING the new tokens, whose K/V must
+ *                 already be in the cache (pkv_kv_append)
+ *   q_lens        int32 [num_seqs]: 1 = decode, k > 1 = speculative verify
+ *                 or a prefill chunk, 0 = no rows
+ *   max_seq_len   host bound on every seq_len (sizes the workspace)
+ *   head_dim      64 or 128; block_size a power of two in [1, 256];
+ *                 g = num_q_heads / num_kv_heads an integer in [1, 64]
+ *   partition_tokens  multiple of 16, or 0 for pkv_attention_auto_partition;
+ *                 at most 1024 partitions per sequence
+ *   flags         0, or PKV_ATTN_DECODE_TENSOR_CORES
+ *   workspace     >= pkv_attention_workspace_bytes(...) bytes, 256-byte
+ *                 aligned; scratch, contents need not be initialised
+ * Rows of a sequence with a bad length, or that read a bad block id, are
+ * NaN and set the matching PKV_STATUS_* bit.  Output rows are written once;
+ * the result is bit-identical under any permutation of the physical blocks.
+ */
+int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                               const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
+                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, float scale, int partition_tokens, int flags,
+                               void* workspace, size_t workspace_bytes, int32_t* status,
+                               void* stream);
+
+/*
+ * a9. Greedy speculative acceptance ([SI] 12.4; [KVC] 08: with greedy
+ * decoding a draft token is accepted when it equals the target's argmax;
+ * stop at the first mismatch; the round always adds one target token).
+ *   logits      fp32 [num_seqs][k+1][vocab]: target scores at the k drafted
+ *               positions and the one after them
+ *   draft       int32 [num_seqs][k]
+ *   argmax_out  int32 [num_seqs][k+1] out: first index of the row maximum
+ *               (NaN counts as the maximum, the first NaN wins)
+ *   accepted    int32 [num_seqs] out: leading j < k with draft == argmax
+ *   next_token  int32 [num_seqs] out: argmax_out[b][accepted[b]] (the
+ *               correction, or the bonus token when all k are accepted)
+ * Exact integers.  vocab >= 1, 1 <= k <= 64.
+ */
+int pkv_spec_accept_greedy(const float* logits, const int32_t* draft, int num_seqs, int k,
+                           int vocab, int32_t* argmax_out, int32_t* accepted, int32_t* next_token,
+                           void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

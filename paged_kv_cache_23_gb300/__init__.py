@@ -1,0 +1,196 @@
+"""paged_kv_cache_23_gb300 -- paged-KV decode attention for GB300 (sm_103a).
+
+A thin ctypes binding over ``libpkv.so`` (C ABI in ``include/pkv.h``).  The
+functions here only marshal torch tensors (device pointers, sizes, the current
+CUDA stream) into the C calls; every step of the path runs in the library's
+CUDA kernels.  There is no CPU fallback: if the library is missing or the
+device is not a GB300, calls raise.
+
+Entry points (same names as the C ABI without the ``pkv_`` prefix):
+    slot_mapping, kv_append, copy_blocks, gather_kv,
+    attention_auto_partition, attention_workspace_bytes,
+    paged_attention_decode, spec_accept_greedy
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpkv.so")
+_lock = threading.Lock()
+_lib = None
+
+PKV_STATUS_BAD_BLOCK = 1
+PKV_STATUS_BAD_SEQLEN = 2
+PKV_STATUS_BAD_QLEN = 4
+PKV_STATUS_BAD_SLOT = 8
+PKV_STATUS_TIMEOUT = 32
+PKV_STATUS_BAD_PAIR = 64
+PKV_ATTN_DECODE_TENSOR_CORES = 1
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "pkv_version": ([], _I),
+    "pkv_error_string": ([_I], ctypes.c_char_p),
+    "pkv_status_string": ([_I], ctypes.c_char_p),
+    "pkv_slot_mapping": ([_P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_kv_append": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_copy_blocks": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_gather_kv": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_attention_auto_partition": ([_I, _I, _I, _I], _I),
+    "pkv_attention_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], ctypes.c_size_t),
+    "pkv_paged_attention_decode": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                    ctypes.c_float, _I, _I, _P, ctypes.c_size_t, _P, _P], _I),
+    "pkv_spec_accept_greedy": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+}
+
+
+def build(force: bool = False) -> str:
+    from . import _build
+    return _build.build(force=force)
+
+
+def lib():
+    """The loaded libpkv.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libpkv.so is not built ({LIB_PATH}); run __graft_entry__.build() "
+                                   "or python -m paged_kv_cache_23_gb300._build")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (argt, rest) in _SIGS.items():
+                f = getattr(L, name)
+                f.argtypes = argt
+                f.restype = rest
+            _lib = L
+    return _lib
+
+
+class PkvError(RuntimeError):
+    pass
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        msg = lib().pkv_error_string(rc).decode()
+        raise PkvError(f"{what}: {msg} (code {rc})")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev(t, name, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise PkvError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise PkvError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise PkvError(f"{name} must be {dtype}, got {t.dtype}")
+    return t
+
+
+def status_bits(code: int):
+    return [lib().pkv_status_string(1 << i).decode() for i in range(8) if code & (1 << i)]
+
+
+def slot_mapping(slots, block_tables, seq_lens, append_lens, block_size, num_blocks, status=None, stream=None):
+    """a1: slots[int64, sum(append_lens)] of each sequence's last append_lens[b] positions."""
+    _dev(slots, "slots", torch.int64)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(append_lens, "append_lens", torch.int32)
+    rc = lib().pkv_slot_mapping(_ptr(slots), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                _ptr(append_lens), seq_lens.numel(), slots.numel(), block_size, num_blocks,
+                                _ptr(status), _stream(stream))
+    _check(rc, "pkv_slot_mapping")
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, slots, status=None, stream=None):
+    """a2: write k_new/v_new [T][n_kv][d] (bf16) into the cache rows given by slots."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new)):
+        _dev(t, n, torch.bfloat16)
+    _dev(slots, "slots", torch.int64)
+    nb, nkv, bs, d = k_cache.shape
+    rc = lib().pkv_kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(slots), slots.numel(), nb,
+                             bs, nkv, d, _ptr(status), _stream(stream))
+    _check(rc, "pkv_kv_append")
+
+
+def copy_blocks(k_cache, v_cache, src_dst, status=None, stream=None):
+    """a3: copy-on-write block copies, src_dst int32 [n][2]."""
+    _dev(k_cache, "k_cache", torch.bfloat16)
+    _dev(v_cache, "v_cache", torch.bfloat16)
+    _dev(src_dst, "src_dst", torch.int32)
+    nb, nkv, bs, d = k_cache.shape
+    rc = lib().pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst), src_dst.numel() // 2, nb, bs, nkv, d,
+                               _ptr(status), _stream(stream))
+    _check(rc, "pkv_copy_blocks")
+
+
+def gather_kv(k_out, v_out, k_cache, v_cache, block_tables, seq_lens, out_offsets, status=None, stream=None):
+    """a4 as a utility: contiguous [sum seq_len][n_kv][d] K/V through the block table."""
+    for n, t in (("k_out", k_out), ("v_out", v_out), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, n, torch.bfloat16)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(out_offsets, "out_offsets", torch.int64)
+    nb, nkv, bs, d = k_cache.shape
+    rc = lib().pkv_gather_kv(_ptr(k_out), _ptr(v_out), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                             block_tables.shape[1], _ptr(seq_lens), _ptr(out_offsets), seq_lens.numel(), nb, bs, nkv,
+                             d, _ptr(status), _stream(stream))
+    _check(rc, "pkv_gather_kv")
+
+
+def attention_auto_partition(num_seqs, total_q, num_kv_heads, max_seq_len) -> int:
+    return int(lib().pkv_attention_auto_partition(num_seqs, total_q, num_kv_heads, max_seq_len))
+
+
+def attention_workspace_bytes(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, max_seq_len,
+                              partition_tokens=0) -> int:
+    return int(lib().pkv_attention_workspace_bytes(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
+                                                   max_seq_len, partition_tokens))
+
+
+def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, q_lens, max_seq_len, scale,
+                           workspace, partition_tokens=0, flags=0, status=None, stream=None):
+    """a4-a8: paged attention (decode, speculative verify, prefill chunks) into out [total_q][n_q][d]."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, n, torch.bfloat16)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(q_lens, "q_lens", torch.int32)
+    _dev(workspace, "workspace")
+    nb, nkv, bs, d = k_cache.shape
+    total_q, nq, _ = q.shape
+    rc = lib().pkv_paged_attention_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                          block_tables.shape[1], _ptr(seq_lens), _ptr(q_lens), seq_lens.numel(),
+                                          total_q, int(max_seq_len), nq, nkv, d, bs, nb, float(scale),
+                                          int(partition_tokens), int(flags), _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _ptr(status),
+                                          _stream(stream))
+    _check(rc, "pkv_paged_attention_decode")
+
+
+def spec_accept_greedy(logits, draft, argmax_out, accepted, next_token, stream=None):
+    """a9: greedy acceptance; logits fp32 [B][k+1][V], draft int32 [B][k]."""
+    _dev(logits, "logits", torch.float32)
+    _dev(draft, "draft", torch.int32)
+    _dev(argmax_out, "argmax_out", torch.int32)
+    _dev(accepted, "accepted", torch.int32)
+    _dev(next_token, "next_token", torch.int32)
+    B, k1, V = logits.shape
+    rc = lib().pkv_spec_accept_greedy(_ptr(logits), _ptr(draft), B, k1 - 1, V, _ptr(argmax_out), _ptr(accepted),
+                                      _ptr(next_token), _stream(stream))
+    _check(rc, "pkv_spec_accept_greedy")

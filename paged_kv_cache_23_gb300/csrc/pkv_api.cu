@@ -1,0 +1,104 @@
+// pkv_api.cu -- version, error strings and host helpers of libpkv.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "pkv.h"
+#include "pkv_host.h"
+
+namespace pkv {
+namespace host {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm[kMaxDevices];
+int g_ok[kMaxDevices];  // 0 unknown, 1 sm_103, 2 other
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
+void probe(int dev) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    g_sm[dev] = sms > 0 ? sms : 1;
+    g_ok[dev] = (major == 10 && minor == 3) ? 1 : 2;
+}
+}  // namespace
+
+int check_device() {
+    const int dev = current_device();
+    if (dev < 0) return PKV_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ok[dev] == 0) probe(dev);
+    return g_ok[dev] == 1 ? PKV_OK : PKV_ERR_DEVICE;
+}
+
+int sm_count() {
+    const int dev = current_device();
+    if (dev < 0) return 1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ok[dev] == 0) probe(dev);
+    return g_sm[dev];
+}
+
+int encode_tiled_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
+                    uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_encode == nullptr) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return -1;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+    }
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -1;
+}
+
+}  // namespace host
+}  // namespace pkv
+
+extern "C" int pkv_version(void) { return 100; }
+
+extern "C" const char* pkv_error_string(int rc) {
+    switch (rc) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_NULL: return "a required pointer is NULL";
+        case PKV_ERR_SIZE: return "a size or count argument is out of range";
+        case PKV_ERR_UNSUPPORTED: return "head_dim, block_size or head grouping not supported";
+        case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+        case PKV_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+        case PKV_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+        case PKV_ERR_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
+        default: return "unknown error code";
+    }
+}
+
+extern "C" const char* pkv_status_string(int bit) {
+    switch (bit) {
+        case PKV_STATUS_BAD_BLOCK: return "block id outside the pool";
+        case PKV_STATUS_BAD_SEQLEN: return "seq_len out of range";
+        case PKV_STATUS_BAD_QLEN: return "q_len or append_len out of range";
+        case PKV_STATUS_BAD_SLOT: return "slot outside the pool";
+        case PKV_STATUS_TIMEOUT: return "a bounded device wait ran out";
+        case PKV_STATUS_BAD_PAIR: return "copy pair outside the pool";
+        default: return "unknown status bit";
+    }
+}

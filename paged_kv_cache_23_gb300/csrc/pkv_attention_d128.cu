@@ -1,0 +1,9 @@
+// pkv_attention_d128.cu -- paged attention kernels for head_dim 128.
+#include "pkv_attention.cuh"
+
+namespace pkv {
+int dispatch_attention_d128(int GD, const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p, long long mi,
+                            cudaStream_t st) {
+    return dispatch_g<128>(GD, tmk, tmv, p, mi, st);
+}
+}  // namespace pkv

@@ -1,0 +1,9 @@
+// pkv_attention_d64.cu -- paged attention kernels for head_dim 64.
+#include "pkv_attention.cuh"
+
+namespace pkv {
+int dispatch_attention_d64(int GD, const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p, long long mi,
+                            cudaStream_t st) {
+    return dispatch_g<64>(GD, tmk, tmv, p, mi, st);
+}
+}  // namespace pkv

@@ -1,0 +1,279 @@
+// pkv_cache_ops.cu -- cache maintenance kernels of libpkv:
+//   slot mapping, KV append, copy-on-write block copy, block-table gather.
+//
+// "Inference at Scale: KV Cache, Prefill, and Decode", section 05 ("The
+// block table", "Block sharing and copy-on-write") and section 02 (decode
+// appends one K/V row per new token); "Chapter 31 Serving Efficiency", 31.3.
+//
+// All four are byte movers: 16-byte vector loads and stores, grid-stride loops
+// sized to the SM count.  Their cost is small next to the attention reread.
+#include "pkv_common.cuh"
+#include "pkv_host.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// Slot mapping: one CTA of 1024 threads; append_lens are scanned in shared
+// memory, then every output slot finds its sequence by binary search.
+// ---------------------------------------------------------------------------
+constexpr int kSlotMaxSeqs = 16384;
+
+__global__ void __launch_bounds__(1024) slot_mapping_kernel(int64_t* __restrict__ slots,
+                                                            const int32_t* __restrict__ block_tables,
+                                                            int max_blocks, const int32_t* __restrict__ seq_lens,
+                                                            const int32_t* __restrict__ append_lens, int num_seqs,
+                                                            int num_slots, int block_size, int num_blocks,
+                                                            int32_t* status) {
+    extern __shared__ int sh[];
+    int* start = sh;                   // [num_seqs + 1] first output slot of each sequence
+    int* bad = sh + num_seqs + 1;      // [num_seqs] invalid-length flag
+    __shared__ int tmp[32];
+    int bits = 0;
+    int carry = 0;
+    for (int base = 0; base < num_seqs; base += 1024) {
+        const int b = base + threadIdx.x;
+        int A = 0;
+        if (b < num_seqs) {
+            const int L = seq_lens[b];
+            const int a = append_lens[b];
+            int flag = 0;
+            if (L < 0 || (long long)L > (long long)max_blocks * block_size) flag |= PKV_STATUS_BAD_SEQLEN;
+            if (a < 0 || a > L) flag |= PKV_STATUS_BAD_QLEN;
+            bad[b] = flag;
+            bits |= flag;
+            A = a > 0 ? a : 0;
+        }
+        int tot;
+        const int ex = block_exclusive_scan_1024(A, tmp, &tot);
+        if (b < num_seqs) start[b] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) start[num_seqs] = carry;
+    if (carry != num_slots) bits |= PKV_STATUS_BAD_QLEN;
+    __syncthreads();
+    const int n = carry < num_slots ? carry : num_slots;
+    for (int o = threadIdx.x; o < num_slots; o += 1024) {
+        if (o >= n) {
+            slots[o] = -1;
+            continue;
+        }
+        int lo = 0, hi = num_seqs - 1;  // last b with start[b] <= o
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (start[mid] <= o) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo;
+        if (bad[b]) {
+            slots[o] = -1;
+            continue;
+        }
+        const int L = seq_lens[b];
+        const int A = start[b + 1] - start[b];
+        const int pos = L - A + (o - start[b]);
+        const int32_t blk = block_tables[(long long)b * max_blocks + pos / block_size];
+        if (blk < 0 || blk >= num_blocks) {
+            bits |= PKV_STATUS_BAD_BLOCK;
+            slots[o] = -1;
+            continue;
+        }
+        slots[o] = (int64_t)blk * block_size + pos % block_size;
+    }
+    report(status, bits);
+}
+
+// ---------------------------------------------------------------------------
+// KV append: one 16-byte chunk per thread-iteration, K and V together.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                                        const uint4* __restrict__ k_new,
+                                                        const uint4* __restrict__ v_new,
+                                                        const int64_t* __restrict__ slots, int num_tokens,
+                                                        int num_blocks, int block_size, int num_kv_heads,
+                                                        int chunks_per_row, int32_t* status) {
+    const long long per_tok = (long long)num_kv_heads * chunks_per_row;
+    const long long total = (long long)num_tokens * per_tok;
+    const long long cap = (long long)num_blocks * block_size;
+    int bits = 0;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long t = i / per_tok;
+        const long long rem = i - t * per_tok;
+        const int h = (int)(rem / chunks_per_row);
+        const int c = (int)(rem - (long long)h * chunks_per_row);
+        const int64_t s = slots[t];
+        if (s < 0) continue;
+        if (s >= cap) {
+            bits |= PKV_STATUS_BAD_SLOT;
+            continue;
+        }
+        const long long blk = s / block_size;
+        const int row = (int)(s - blk * block_size);
+        const long long dst = ((blk * num_kv_heads + h) * block_size + row) * chunks_per_row + c;
+        k_cache[dst] = ld_nc_v4(k_new + i);
+        v_cache[dst] = ld_nc_v4(v_new + i);
+    }
+    report(status, bits);
+}
+
+// ---------------------------------------------------------------------------
+// Copy blocks: blockIdx.y = pair, grid-stride over the block's 16-byte chunks.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                                          const int32_t* __restrict__ src_dst, int num_blocks,
+                                                          long long chunks_per_block, int32_t* status) {
+    const int pair = blockIdx.y;
+    const int32_t s = src_dst[2 * pair], d = src_dst[2 * pair + 1];
+    if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report(status, PKV_STATUS_BAD_PAIR);
+        return;
+    }
+    const uint4* ks = k_cache + (long long)s * chunks_per_block;
+    const uint4* vs = v_cache + (long long)s * chunks_per_block;
+    uint4* kd = k_cache + (long long)d * chunks_per_block;
+    uint4* vd = v_cache + (long long)d * chunks_per_block;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < chunks_per_block;
+         i += (long long)gridDim.x * blockDim.x) {
+        const uint4 a = ks[i];
+        const uint4 b = vs[i];
+        kd[i] = a;
+        vd[i] = b;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Gather: blockIdx.x = logical block, blockIdx.y = sequence.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) gather_kv_kernel(uint4* __restrict__ k_out, uint4* __restrict__ v_out,
+                                                        const uint4* __restrict__ k_cache,
+                                                        const uint4* __restrict__ v_cache,
+                                                        const int32_t* __restrict__ block_tables, int max_blocks,
+                                                        const int32_t* __restrict__ seq_lens,
+                                                        const int64_t* __restrict__ out_offsets, int num_blocks,
+                                                        int block_size, int num_kv_heads, int chunks_per_row,
+                                                        int32_t* status) {
+    const int b = blockIdx.y;
+    const int L = seq_lens[b];
+    if (L < 0 || (long long)L > (long long)max_blocks * block_size) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) report(status, PKV_STATUS_BAD_SEQLEN);
+        return;
+    }
+    for (int lb = blockIdx.x; (long long)lb * block_size < L; lb += gridDim.x) {
+        const int rows = min(block_size, L - lb * block_size);
+        const int32_t blk = block_tables[(long long)b * max_blocks + lb];
+        const bool ok = blk >= 0 && blk < num_blocks;
+        if (!ok && threadIdx.x == 0) report(status, PKV_STATUS_BAD_BLOCK);
+        const long long row0 = out_offsets[b] + (long long)lb * block_size;
+        const int per_row = num_kv_heads * chunks_per_row;
+        const int n = rows * per_row;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const int r = i / per_row;
+            const int rem = i - r * per_row;
+            const int h = rem / chunks_per_row;
+            const int c = rem - h * chunks_per_row;
+            const long long dst = (row0 + r) * per_row + rem;
+            if (!ok) {
+                const uint4 nan = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+                k_out[dst] = nan;
+                v_out[dst] = nan;
+                continue;
+            }
+            const long long src = (((long long)blk * num_kv_heads + h) * block_size + r) * chunks_per_row + c;
+            k_out[dst] = k_cache[src];
+            v_out[dst] = v_cache[src];
+        }
+    }
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int pkv_slot_mapping(int64_t* slots, const int32_t* block_tables, int max_blocks,
+                                const int32_t* seq_lens, const int32_t* append_lens, int num_seqs,
+                                int num_slots, int block_size, int num_blocks, int32_t* status,
+                                void* stream) {
+    if (num_seqs < 0 || num_slots < 0 || num_seqs > kSlotMaxSeqs || max_blocks < 1 || block_size < 1 ||
+        num_blocks < 1)
+        return PKV_ERR_SIZE;
+    if (num_seqs == 0 || num_slots == 0) return PKV_OK;
+    if (!slots || !block_tables || !seq_lens || !append_lens) return PKV_ERR_NULL;
+    const int rc = host::check_device();
+    if (rc) return rc;
+    const size_t smem = sizeof(int) * (2 * (size_t)num_seqs + 1);
+    if (smem > 48 * 1024) {
+        if (cudaFuncSetAttribute(slot_mapping_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    slot_mapping_kernel<<<1, 1024, smem, (cudaStream_t)stream>>>(slots, block_tables, max_blocks, seq_lens,
+                                                                 append_lens, num_seqs, num_slots, block_size,
+                                                                 num_blocks, status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                             const int64_t* slots, int num_tokens, int num_blocks, int block_size,
+                             int num_kv_heads, int head_dim, int32_t* status, void* stream) {
+    if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || num_kv_heads < 1 || head_dim < 8) return PKV_ERR_SIZE;
+    if (head_dim % 8) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !slots) return PKV_ERR_NULL;
+    if (!host::aligned16(k_cache) || !host::aligned16(v_cache) || !host::aligned16(k_new) || !host::aligned16(v_new))
+        return PKV_ERR_ALIGN;
+    const int rc = host::check_device();
+    if (rc) return rc;
+    const int cpr = head_dim / 8;
+    const long long total = (long long)num_tokens * num_kv_heads * cpr;
+    const long long want = (total + 255) / 256;
+    const int grid = (int)(want < host::sm_count() * 8LL ? want : host::sm_count() * 8LL);
+    kv_append_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new,
+                                                             (const uint4*)v_new, slots, num_tokens, num_blocks,
+                                                             block_size, num_kv_heads, cpr, status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst, int num_pairs,
+                               int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                               int32_t* status, void* stream) {
+    if (num_pairs < 0 || num_pairs > 65535 || num_blocks < 1 || block_size < 1 || num_kv_heads < 1 ||
+        head_dim < 8)
+        return PKV_ERR_SIZE;
+    if (head_dim % 8) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !src_dst) return PKV_ERR_NULL;
+    if (!host::aligned16(k_cache) || !host::aligned16(v_cache)) return PKV_ERR_ALIGN;
+    const int rc = host::check_device();
+    if (rc) return rc;
+    const long long cpb = (long long)num_kv_heads * block_size * head_dim / 8;
+    long long gx = (cpb + 255) / 256;
+    const long long cap = (host::sm_count() * 8LL + num_pairs - 1) / num_pairs;
+    if (gx > cap) gx = cap;
+    if (gx < 1) gx = 1;
+    dim3 grid((unsigned)gx, (unsigned)num_pairs);
+    copy_blocks_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((uint4*)k_cache, (uint4*)v_cache, src_dst, num_blocks,
+                                                               cpb, status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                             const int64_t* out_offsets, int num_seqs, int num_blocks, int block_size,
+                             int num_kv_heads, int head_dim, int32_t* status, void* stream) {
+    if (num_seqs < 0 || num_seqs > 65535 || max_blocks < 1 || num_blocks < 1 || block_size < 1 ||
+        num_kv_heads < 1 || head_dim < 8)
+        return PKV_ERR_SIZE;
+    if (head_dim % 8) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PKV_OK;
+    if (!k_out || !v_out || !k_cache || !v_cache || !block_tables || !seq_lens || !out_offsets) return PKV_ERR_NULL;
+    if (!host::aligned16(k_out) || !host::aligned16(v_out) || !host::aligned16(k_cache) || !host::aligned16(v_cache))
+        return PKV_ERR_ALIGN;
+    const int rc = host::check_device();
+    if (rc) return rc;
+    const int gx = max_blocks < 1024 ? max_blocks : 1024;
+    dim3 grid(gx, num_seqs);
+    gather_kv_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((uint4*)k_out, (uint4*)v_out, (const uint4*)k_cache,
+                                                             (const uint4*)v_cache, block_tables, max_blocks, seq_lens,
+                                                             out_offsets, num_blocks, block_size, num_kv_heads,
+                                                             head_dim / 8, status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}

@@ -1,0 +1,92 @@
+"""One step of the paged-KV path on the GPU, through the C ABI.
+
+A step over a workload (see ``workloads``) is: copy-on-write block copies,
+slot mapping of the appended tokens, KV append, paged attention over the
+whole batch, and -- when the workload carries target logits and drafts --
+greedy speculative acceptance.  Everything runs in libpkv's kernels on one
+CUDA stream; this module only owns the device buffers.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (attention_workspace_bytes, copy_blocks, kv_append, paged_attention_decode, slot_mapping,
+               spec_accept_greedy)
+
+
+def to_device_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+    return t.to(device).view(torch.bfloat16)
+
+
+def bf16_to_bits(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+class DeviceStep:
+    """Device-resident inputs of one step, plus outputs and scratch."""
+
+    def __init__(self, w, device="cuda", max_seq_len=None, partition_tokens=None, flags=0):
+        self.w = w
+        self.device = torch.device(device)
+        dev = self.device
+        self.k_cache = to_device_bf16(w.k_cache, dev)
+        self.v_cache = to_device_bf16(w.v_cache, dev)
+        self.k_init = None
+        self.block_tables = torch.from_numpy(w.block_tables).to(dev)
+        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
+        self.q_lens = torch.from_numpy(w.q_lens).to(dev)
+        self.append_lens = torch.from_numpy(w.append_lens).to(dev)
+        self.k_new = to_device_bf16(w.k_new, dev)
+        self.v_new = to_device_bf16(w.v_new, dev)
+        self.cow = torch.from_numpy(np.ascontiguousarray(w.cow, np.int32)).to(dev)
+        self.q = to_device_bf16(w.q, dev)
+        self.n_slots = int(w.append_lens.sum())
+        self.slots = torch.empty(max(self.n_slots, 1), dtype=torch.int64, device=dev)[: self.n_slots]
+        self.out = torch.empty((w.total_q, w.n_q, w.head_dim), dtype=torch.bfloat16, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.max_seq_len = int(max_seq_len if max_seq_len is not None else max(1, int(w.seq_lens.max())))
+        self.partition_tokens = int(partition_tokens if partition_tokens is not None else w.partition_tokens)
+        self.flags = int(flags)
+        nbytes = attention_workspace_bytes(w.num_seqs, w.total_q, w.n_q, w.n_kv, w.head_dim, self.max_seq_len,
+                                           self.partition_tokens)
+        self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+        self.spec = w.logits is not None
+        if self.spec:
+            B, k1, V = w.logits.shape
+            self.logits = torch.from_numpy(w.logits).to(dev)
+            self.draft = torch.from_numpy(w.draft).to(dev)
+            self.argmax = torch.empty((B, k1), dtype=torch.int32, device=dev)
+            self.accepted = torch.empty(B, dtype=torch.int32, device=dev)
+            self.next_token = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def reset_cache(self):
+        """Restore the cache to the state before the step (for repeated steps)."""
+        self.k_cache.copy_(to_device_bf16(self.w.k_cache, self.device))
+        self.v_cache.copy_(to_device_bf16(self.w.v_cache, self.device))
+
+    def cache_ops(self, stream=None):
+        w = self.w
+        if self.cow.numel():
+            copy_blocks(self.k_cache, self.v_cache, self.cow, status=self.status, stream=stream)
+        if self.n_slots:
+            slot_mapping(self.slots, self.block_tables, self.seq_lens, self.append_lens, w.block_size, w.num_blocks,
+                         status=self.status, stream=stream)
+            kv_append(self.k_cache, self.v_cache, self.k_new, self.v_new, self.slots, status=self.status,
+                      stream=stream)
+
+    def attention(self, stream=None):
+        paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
+                               self.q_lens, self.max_seq_len, self.w.scale, self.workspace,
+                               partition_tokens=self.partition_tokens, flags=self.flags, status=self.status,
+                               stream=stream)
+
+    def accept(self, stream=None):
+        if self.spec:
+            spec_accept_greedy(self.logits, self.draft, self.argmax, self.accepted, self.next_token, stream=stream)
+
+    def step(self, stream=None):
+        self.cache_ops(stream)
+        self.attention(stream)
+        self.accept(stream)
