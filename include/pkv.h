@@ -60,6 +60,7 @@ extern "C" {
 #define PKV_ERR_ALIGN (-5)       /* a pointer is not 16-byte aligned */
 #define PKV_ERR_CUDA (-6)        /* a CUDA runtime call or launch failed */
 #define PKV_ERR_DEVICE (-7)      /* the current device is not an sm_103 GPU */
+#define PKV_ERR_SCRATCH_LIMIT (-8) /* the problem needs more scratch than the fixed no-alloc buffer */
 
 #define PKV_STATUS_BAD_BLOCK 1   /* a needed block id is outside [0, num_blocks) */
 #define PKV_STATUS_BAD_SEQLEN 2  /* a seq_len is < 0, > max_blocks*block_size or > max_seq_len */
@@ -193,6 +194,36 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, co
                                int num_blocks, float scale, int partition_tokens, int flags,
                                void* workspace, size_t workspace_bytes, int32_t* status,
                                void* stream);
+
+/*
+ * No-allocation variant of pkv_paged_attention_decode.  The source pages have
+ * no counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory on the call path -- code running inside another
+ * runtime's allocator or memory-pool hooks (a nested cudaMalloc would re-enter
+ * it), latency-critical loops that must not block on the driver allocator,
+ * and plugins that are handed only their inputs and outputs.
+ *
+ * Same arguments, semantics and results as pkv_paged_attention_decode, minus
+ * the workspace: the scratch lives in a fixed device array inside the library
+ * (pkv_noalloc_scratch_bytes() bytes, 32 MiB), which every GPU that loads the
+ * library holds until the process exits.  The call allocates nothing.
+ * - Returns PKV_ERR_SCRATCH_LIMIT, launching nothing, when
+ *   pkv_attention_workspace_bytes(...) for these sizes exceeds that array.
+ * - The first call on a device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ * - All calls share the array.  Calls that overlap on the GPU (other streams,
+ *   unordered host threads) race on it and give wrong results; calls ordered
+ *   on one stream are safe (each call re-initialises what it uses).
+ */
+size_t pkv_noalloc_scratch_bytes(void);
+int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                       const void* v_cache, const int32_t* block_tables,
+                                       int max_blocks, const int32_t* seq_lens,
+                                       const int32_t* q_lens, int num_seqs, int total_q,
+                                       int max_seq_len, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int num_blocks, float scale,
+                                       int partition_tokens, int flags, int32_t* status,
+                                       void* stream);
 
 /*
  * a9. Greedy speculative acceptance ([SI] 12.4; [KVC] 08: with greedy

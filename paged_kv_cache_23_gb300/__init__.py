@@ -31,6 +31,7 @@ PKV_STATUS_BAD_SLOT = 8
 PKV_STATUS_TIMEOUT = 32
 PKV_STATUS_BAD_PAIR = 64
 PKV_ATTN_DECODE_TENSOR_CORES = 1
+PKV_ERR_SCRATCH_LIMIT = -8
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -47,6 +48,9 @@ _SIGS = {
     "pkv_paged_attention_decode": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                     ctypes.c_float, _I, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_spec_accept_greedy": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+    "pkv_noalloc_scratch_bytes": ([], ctypes.c_size_t),
+    "pkv_paged_attention_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                            ctypes.c_float, _I, _I, _P, _P], _I),
 }
 
 
@@ -194,3 +198,27 @@ def spec_accept_greedy(logits, draft, argmax_out, accepted, next_token, stream=N
     rc = lib().pkv_spec_accept_greedy(_ptr(logits), _ptr(draft), B, k1 - 1, V, _ptr(argmax_out), _ptr(accepted),
                                       _ptr(next_token), _stream(stream))
     _check(rc, "pkv_spec_accept_greedy")
+
+
+def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, q_lens, max_seq_len, scale,
+                                   partition_tokens=0, flags=0, status=None, stream=None):
+    """paged_attention_decode without a workspace: for callers that cannot
+    allocate device memory; the scratch is the library's fixed device array
+    (noalloc_scratch_bytes()).  Calls overlapping on the GPU race on it."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, n, torch.bfloat16)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(q_lens, "q_lens", torch.int32)
+    nb, nkv, bs, d = k_cache.shape
+    total_q, nq, _ = q.shape
+    rc = lib().pkv_paged_attention_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                                  _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
+                                                  _ptr(q_lens), seq_lens.numel(), total_q, int(max_seq_len), nq, nkv,
+                                                  d, bs, nb, float(scale), int(partition_tokens), int(flags),
+                                                  _ptr(status), _stream(stream))
+    _check(rc, "pkv_paged_attention_decode_noalloc")
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(lib().pkv_noalloc_scratch_bytes())

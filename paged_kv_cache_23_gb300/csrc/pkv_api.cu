@@ -87,6 +87,7 @@ extern "C" const char* pkv_error_string(int rc) {
         case PKV_ERR_ALIGN: return "a pointer is not 16-byte aligned";
         case PKV_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
         case PKV_ERR_DEVICE: return "the current device is not an sm_103 (GB300) GPU";
+        case PKV_ERR_SCRATCH_LIMIT: return "needs more scratch than the no-alloc entry point's fixed buffer";
         default: return "unknown error code";
     }
 }
