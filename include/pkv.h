@@ -70,7 +70,7 @@ extern "C" {
 #define PKV_STATUS_BAD_PAIR 64   /* a copy pair names a block outside the pool */
 
 /* Attention flags. */
-#define PKV_ATTN_DECODE_TENSOR_CORES 1 /* run q_len = 1 rows on the mma path too */
+#define PKV_ATTN_DECODE_CUDA_CORES 1 /* run q_len = 1 rows on the CUDA-core FMA path */
 
 /* Library version, 100 * major + minor. */
 int pkv_version(void);
@@ -180,7 +180,9 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *                 g = num_q_heads / num_kv_heads an integer in [1, 64]
  *   partition_tokens  multiple of 16, or 0 for pkv_attention_auto_partition;
  *                 at most 1024 partitions per sequence
- *   flags         0, or PKV_ATTN_DECODE_TENSOR_CORES
+ *   flags         0, or PKV_ATTN_DECODE_CUDA_CORES (q_len = 1 rows on the
+ *                 CUDA-core FMA path; by default every row uses the tensor
+ *                 cores, measured faster on GB300)
  *   workspace     >= pkv_attention_workspace_bytes(...) bytes, 256-byte
  *                 aligned; scratch, contents need not be initialised
  * Rows of a sequence with a bad length, or that read a bad block id, are

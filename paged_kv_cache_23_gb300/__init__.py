@@ -30,7 +30,7 @@ PKV_STATUS_BAD_QLEN = 4
 PKV_STATUS_BAD_SLOT = 8
 PKV_STATUS_TIMEOUT = 32
 PKV_STATUS_BAD_PAIR = 64
-PKV_ATTN_DECODE_TENSOR_CORES = 1
+PKV_ATTN_DECODE_CUDA_CORES = 1
 PKV_ERR_SCRATCH_LIMIT = -8
 
 _P = ctypes.c_void_p

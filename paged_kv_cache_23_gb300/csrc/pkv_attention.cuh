@@ -12,24 +12,28 @@
 //   section 08  verification of k drafted tokens is a short causal prefill.
 //
 // How it runs on GB300 (sm_103a):
-//   * A small planning kernel turns (seq_lens, q_lens) into a list of work
-//     items (sequence, kv head, partition[, query tile]) -- multi-query items
-//     first -- and zeroes the merge tickets.
-//   * The attention kernel is persistent (grid = SMs x resident CTAs).  Each CTA
-//     has one producer warp and four consumer warps.  The producer takes items
-//     from a global atomic queue, reads block-table entries 32 at a time, and
-//     streams every 16-token (block, kv head) tile of K and V into an 8-stage
-//     shared-memory ring with 2-D TMA loads (128-byte swizzle) completing on
-//     mbarriers.  It never waits for compute except through the ring.
-//   * Single-query rows (decode, q_len = 1) run on CUDA cores: the g query
-//     heads of a GQA group share each K/V tile; 8 lanes own one token's dot
-//     product, packed fp32x2 FMAs, a split-butterfly reduction leaves one head
-//     per lane pair, warp-shuffle max/sum for the online softmax.  The four
-//     consumer warps take alternate tiles and are combined at the end.
+//   * A planning kernel turns (seq_lens, q_lens) into per-sequence records and
+//     a list of 16-byte work items (sequence, partition, query tile, head
+//     group): multi-query items first, then full decode partitions, then
+//     partition tails; it also zeroes the merge tickets.
+//   * The attention kernel is persistent, one CTA per SM: one producer warp and
+//     eight consumer warps.  A pipeline stage is 16 tokens of K and V for a
+//     group of kv heads of one block -- for the 8B shape all 8 heads, 32 KB of
+//     K plus 32 KB of V -- fetched with one 5-D TMA box per tensor (128-byte
+//     swizzle) into a 3-slot, 192 KB shared-memory ring.  A TMA-issuing thread
+//     sustains only a couple of copies per microsecond whatever their size, so
+//     copies have to be tens of KB for one producer warp to keep HBM busy.
+//   * Single-query rows (decode, q_len = 1) run on CUDA cores, one warp per kv
+//     head: the g query heads of the GQA group share each K/V tile; 8 lanes own
+//     one token's dot product (packed fp32x2 FMAs), a split-butterfly reduction
+//     leaves one head per lane pair, warp-shuffle max/sum for the online
+//     softmax.  A warp copies its head's slice into registers and releases the
+//     stage at once.
 //   * Multi-query rows (speculative k > 1, prefill chunks) run on tensor cores
-//     (mma.sync m16n8k16 bf16 -> fp32): rows = (query, head) pairs, 16 per
-//     warp; S = Q K^T and O += P V with ldmatrix from the swizzled tiles; the
-//     causal limit of each row is applied to the scores.
+//     (mma.sync m16n8k16 bf16 -> fp32): rows are (query, head) pairs, 16 per
+//     warp; the warps of one kv head split its rows; S = Q K^T and O += P V
+//     from ldmatrix fragments of the swizzled stage; each row's causal limit
+//     is applied to the scores.
 //   * A partition's partial (O, m, l) goes to the workspace; the CTA that
 //     finishes the last partition of a group (an atomic ticket, no waiting)
 //     merges them in partition order, so results are deterministic.
@@ -41,162 +45,217 @@
 namespace pkv {
 
 constexpr int kTileT = 16;                  // tokens per pipeline stage
-constexpr int kCWarps = 4;                  // consumer warps
-constexpr int kThreads = (kCWarps + 1) * 32;
-constexpr int kStages = 8;
+constexpr int kCWarps = 8;                  // consumer warps
+constexpr int kCThreads = kCWarps * 32;
+constexpr int kThreads = kCThreads + 32;    // + producer warp
+constexpr int kMaxHPS = 8;                  // kv heads per stage
+constexpr int kRingSlots = 3;
 constexpr int kSlots = 4;                   // item descriptors in flight
-constexpr int kMqRows = 64;                 // (query, head) rows per multi-query item
 constexpr int kMaxParts = 1024;             // partitions per sequence
 constexpr int kPlanThreads = 1024;
+constexpr int kMergeW = 2048;               // float2 merge weights in shared memory
 
 enum { KIND_END = -1, KIND_DEC = 0, KIND_MQ = 1 };
 
 struct Desc {
-    int b, kvh, part, nparts;
+    int b, part, nparts, hg;        // sequence, partition, partitions of the group, head group
     int t_begin, t_end, t_vis, q_row0;
-    int nq, kind, pad0, pad1;
+    int nq, kind, hps, wph;         // queries in the tile, kind, kv heads per stage, warps per kv head
 };
-static_assert(sizeof(Desc) == 48, "descriptor is three int4");
+
+// Tensor maps over a cache pool viewed as [num_blocks][n_kv][bs][D/64][64]
+// (innermost last), one per box height in kv heads (1, 2, 4, 8).
+struct TMaps {
+    CUtensorMap k[4];
+    CUtensorMap v[4];
+};
 
 struct AttnParams {
     __nv_bfloat16* out;
     const __nv_bfloat16* q;
     const int32_t* block_tables;
-    const int4* items;
-    int* hdr;        // [0] item count, [1] queue head
-    int* tickets;    // [total_q * n_kv]
-    float* part_o;   // [(row * n_q + h) * np_max + part][D]
-    float2* part_ml; // [(row * n_q + h) * np_max + part] = (m in log2 units, l)
+    const int4* items;   // {b, part, qt, hg}
+    const int4* seqs;    // {seq_len, q_len, first query row, kind | hps << 4 | wph << 8 | qt_len << 12}
+    int* hdr;            // [0] item count, [1] queue head
+    int* tickets;        // [total_q * n_kv]
+    float* part_o;       // [(row * n_q + h) * np_max + part][D]
+    float2* part_ml;     // [(row * n_q + h) * np_max + part] = (m in log2 units, l)
     int32_t* status;
-    int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, flags;
-    float scale_log2;  // scale * log2(e): scores live in base-2 units
-};
-
-struct PlanParams {
-    const int32_t* seq_lens;
-    const int32_t* q_lens;
-    int4* items;
-    int* hdr;
-    int* seq_q0;
-    int* seq_flag;
-    int* seq_mq_off;
-    int* seq_dec_off;
-    int* tickets;
-    __nv_bfloat16* out;
-    int32_t* status;
-    int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, decode_ok;
+    int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, P, row_bytes;
+    float scale_log2;    // scale * log2(e): scores live in base-2 units
 };
 
 template <int D>
 struct Smem {
-    uint8_t kv[kStages][2][D / 64][kTileT * 128];  // [stage][K,V][128-byte box][16 rows x 128 B], swizzled
-    float comb_o[kCWarps][16 * D];                 // per-warp partial O; reused as the [64][D] result
-    float comb_m[kCWarps][16];
-    float comb_l[kCWarps][16];
-    float fin_m[kMqRows];
-    float fin_l[kMqRows];
-    float pbuf[kCWarps][kTileT * 8];               // decode: p[token][head]
-    float corr[kCWarps][8];
+    static constexpr int kHalf = kTileT * kMaxHPS * D * 2;   // K (or V) bytes of one stage
+    uint8_t kv[kRingSlots][2][kHalf];                        // [slot][K,V][rows of 128 B], swizzled
+    float2 W[kMergeW];                                       // merge weights
+    float pbuf[kCWarps][kTileT * 8];                         // decode: p[token][head]
     Desc desc[kSlots];
     int poison[kSlots];
     int okw[kCWarps];
     int bcast;
     int abort;
-    uint64_t full[kStages], empty[kStages], ifull[kSlots], iempty[kSlots];
+    uint64_t full[kRingSlots], empty[kRingSlots], ifull[kSlots], iempty[kSlots];
 };
 
-__device__ __forceinline__ void consumer_bar() { named_bar(1, kCWarps * 32); }
+__device__ __forceinline__ void consumer_bar() { named_bar(1, kCThreads); }
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ int log2i(int x) { return 31 - __clz(x); }
+
+// Index of the 128-byte shared-memory row that holds (head h of the stage,
+// token r of the tile, 64-column box x): the TMA boxes of one stage are
+// [op][head][rows of the op][box], one op per block when block_size < 16.
+// Rows per op are a power of two, 1 << lb; hps_lb = hps << lb, h_lb = h << lb.
+__device__ __forceinline__ int srow(int h_lb, int r, int x, int hps_lb, int lb, int nb) {
+    return (((r >> lb) * hps_lb + h_lb + (r & ((1 << lb) - 1))) * nb) + x;
+}
+
+__device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            int c4, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Work-item record -> descriptor (the same arithmetic the planning kernel used
+// to count items).
+__device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, const AttnParams& p) {
+    Desc d;
+    d.b = it.x;
+    d.part = it.y;
+    const int qt = it.z;
+    d.hg = it.w;
+    const int L = sq.x, ql = sq.y, q0 = sq.z;
+    d.kind = sq.w & 15;
+    d.hps = (sq.w >> 4) & 15;
+    d.wph = (sq.w >> 8) & 15;
+    const int QT = (sq.w >> 12) & 4095;
+    if (d.kind == KIND_DEC) {
+        d.nq = 1;
+        d.t_vis = L;
+        d.q_row0 = q0;
+    } else {
+        d.nq = min(QT, ql - qt * QT);
+        d.t_vis = L - ql + qt * QT + d.nq;
+        d.q_row0 = q0 + qt * QT;
+    }
+    d.nparts = ceil_div(d.t_vis, p.P);
+    d.t_begin = d.part * p.P;
+    d.t_end = min(d.t_begin + p.P, d.t_vis);
+    return d;
+}
 
 // ---------------------------------------------------------------------------
-// Producer warp: item queue, block-table reads, TMA tile stream.
+// Producer warp: item queue, block-table reads, TMA stage stream.
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void producer(Smem<D>& sm, const CUtensorMap* tmk, const CUtensorMap* tmv,
-                                         const AttnParams& p, int lane) {
+__device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const AttnParams& p, int lane) {
+    constexpr int NB = D / 64;
     volatile int* abort = &sm.abort;
-    if (lane == 0) {
-        prefetch_tmap(tmk);
-        prefetch_tmap(tmv);
+    if (lane < 4) {
+        prefetch_tmap(&tm->k[lane]);
+        prefetch_tmap(&tm->v[lane]);
     }
     const int num_items = p.hdr[0];
+    const int bsr = p.bs < kTileT ? p.bs : kTileT;
     int next = 0;
     if (lane == 0) next = atomicAdd(&p.hdr[1], 1);
     next = __shfl_sync(kFull, next, 0);
-    const int box_rows = p.bs < kTileT ? p.bs : kTileT;
     uint32_t g = 0;
     for (int islot = 0;; ++islot) {
         const int si = islot % kSlots;
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&sm.iempty[si], ((islot / kSlots) & 1) ^ 1, abort);
-        ok = __shfl_sync(kFull, ok, 0);
-        if (!ok) break;  // abort: publish nothing more
         const int cur = next;
         const bool end = cur >= num_items || *abort;
         Desc d;
         if (!end) {
-            const int4 a = p.items[3LL * cur], b = p.items[3LL * cur + 1], c = p.items[3LL * cur + 2];
-            d = Desc{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
-            if (lane == 0) next = atomicAdd(&p.hdr[1], 1);
-            next = __shfl_sync(kFull, next, 0);
+            const int4 it = __ldg(p.items + cur);
+            const int4 sq = __ldg(p.seqs + it.x);
+            d = make_desc(it, sq, p);
         } else {
-            d = Desc{0, 0, 0, 1, 0, 0, 0, 0, 0, KIND_END, 0, 0};
+            d = Desc{0, 0, 1, 0, 0, 0, 0, 0, 0, KIND_END, 1, 1};
         }
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&sm.iempty[si], ((islot / kSlots) & 1) ^ 1, abort);
+        ok = __shfl_sync(kFull, ok, 0);
+        if (!ok) break;  // abort: publish nothing more
         if (lane == 0) {
             sm.desc[si] = d;
             sm.poison[si] = 0;
             mbar_arrive(&sm.ifull[si]);
         }
         if (end) break;
+        if (lane == 0) next = atomicAdd(&p.hdr[1], 1);  // next item, used after this one's stages
+        next = __shfl_sync(kFull, next, 0);
+        const CUtensorMap* mk = &tm->k[log2i(d.hps)];
+        const CUtensorMap* mv = &tm->v[log2i(d.hps)];
+        const uint32_t op_bytes = (uint32_t)d.hps * bsr * D * 2;
         const int tb = d.t_begin / kTileT, te = (d.t_end + kTileT - 1) / kTileT;
         const int32_t* bt = p.block_tables + (long long)d.b * p.max_blocks;
+        bool stopped = false;
         const int e_lim = (d.t_end + p.bs - 1) / p.bs;
-        int tab_base = -(1 << 30), tab = 0;
+        int tab_base = tb * kTileT / p.bs;
+        int tab = tab_base + lane < e_lim ? __ldg(bt + tab_base + lane) : 0;
+        int tab_next = tab_base + 32 + lane < e_lim ? __ldg(bt + tab_base + 32 + lane) : 0;
         for (int i = tb; i < te; ++i, ++g) {
             const int t0 = i * kTileT;
             const int tvalid = min(kTileT, d.t_end - t0);
             const int e0 = t0 / p.bs;
             const int ne = p.bs >= kTileT ? 1 : (tvalid + p.bs - 1) / p.bs;
-            if (e0 < tab_base || e0 + ne > tab_base + 32) {
-                tab_base = e0;
-                const int e = e0 + lane;
-                tab = e < e_lim ? __ldg(bt + e) : 0;
+            if (e0 >= tab_base + 32) {
+                // entries advance by at most 16 per stage: shift in the prefetched batch
+                tab = tab_next;
+                tab_base += 32;
+                const int en = tab_base + 32 + lane;
+                tab_next = en < e_lim ? __ldg(bt + en) : 0;
             }
-            int my = __shfl_sync(kFull, tab, (e0 - tab_base + lane) & 31);
+            const int off = e0 - tab_base + lane;  // in [0, 48)
+            const int lo = __shfl_sync(kFull, tab, off & 31);
+            const int hi = __shfl_sync(kFull, tab_next, off & 31);
+            int my = off < 32 ? lo : hi;
             const bool in = lane < ne;
             const bool okb = !in || (my >= 0 && my < p.num_blocks);
             if (!okb) my = 0;
             const unsigned badmask = __ballot_sync(kFull, !okb);
-            const int s = (int)(g % kStages);
+            const int s = (int)(g % kRingSlots);
+            bool got = true;
             if (lane == 0) {
                 if (badmask) {
                     sm.poison[si] = 1;
                     report(p.status, PKV_STATUS_BAD_BLOCK);
                 }
-                mbar_wait(&sm.empty[s], ((g / kStages) & 1) ^ 1, abort);
-                mbar_arrive_expect_tx(&sm.full[s], 2u * (D / 64) * ne * box_rows * 128u);
+                got = mbar_wait(&sm.empty[s], ((g / kRingSlots) & 1) ^ 1, abort);
+                if (got) mbar_arrive_expect_tx(&sm.full[s], 2u * ne * op_bytes);
             }
-            for (int k = 0; k < ne; ++k) {
-                const int blk = __shfl_sync(kFull, my, k);
-                if (lane == 0) {
-                    const int y = (blk * p.n_kv + d.kvh) * p.bs + (p.bs > kTileT ? (t0 % p.bs) : 0);
-#pragma unroll
-                    for (int x = 0; x < D / 64; ++x) {
-                        tma_load_2d(&sm.kv[s][0][x][k * box_rows * 128], tmk, x * 64, y, &sm.full[s]);
-                        tma_load_2d(&sm.kv[s][1][x][k * box_rows * 128], tmv, x * 64, y, &sm.full[s]);
-                    }
-                }
+            if (!__shfl_sync(kFull, got, 0)) {
+                stopped = true;  // never arm a barrier whose previous phase is still open
+                break;
+            }
+            // one box per tensor and block: every head of the group, 16 (or block_size) rows
+            if (lane < ne) {
+                const int row0 = p.bs > kTileT ? (t0 % p.bs) : 0;
+                uint8_t* dk = &sm.kv[s][0][lane * op_bytes];
+                uint8_t* dv = &sm.kv[s][1][lane * op_bytes];
+                tma_load_5d(dk, mk, 0, 0, row0, d.hg * d.hps, my, &sm.full[s]);
+                tma_load_5d(dv, mv, 0, 0, row0, d.hg * d.hps, my, &sm.full[s]);
             }
             __syncwarp();
         }
+        if (stopped) break;
     }
-    // drain: wait (bounded) until every issued tile has landed
+    // drain: wait (bounded) until every issued stage has landed
     if (lane == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kRingSlots; ++s) {
             if (g <= (uint32_t)s) continue;
-            const uint32_t last = g - 1 - ((g - 1 - s) % kStages);
-            mbar_wait(&sm.full[s], (last / kStages) & 1, abort);
+            const uint32_t last = g - 1 - ((g - 1 - s) % kRingSlots);
+            mbar_wait(&sm.full[s], (last / kRingSlots) & 1, abort);
         }
     }
+    (void)NB;
 }
 
 // ---------------------------------------------------------------------------
@@ -226,66 +285,45 @@ __device__ __forceinline__ float reduce8(float* v, int li) {
     return v[0];
 }
 
+// Output row of item row r: rows are [kv head of the group][query][q head].
+struct RowMap {
+    int G, nq, hps, n_q;
+    __device__ __forceinline__ long long orow(const Desc& d, int r) const {
+        const int per = nq * G;
+        const int hw = r / per, lr = r - hw * per;
+        const int qi = lr / G, hh = lr - qi * G;
+        const int kvh = d.hg * hps + hw;
+        return (long long)(d.q_row0 + qi) * n_q + (long long)kvh * G + hh;
+    }
+};
+
 // ---------------------------------------------------------------------------
-// Item epilogue: direct bf16 write, or partial + ticket + merge.
-// F_o = comb_o viewed as [64][D] (unnormalised), fin_m / fin_l per row.
+// Ticket and merge of the partial results of a group of partitions.  Called
+// by all consumer threads after the item's partials are written.
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void finish_item(Smem<D>& sm, const AttnParams& p, const Desc& d, int R, bool poisoned,
-                                            int tid) {
+__device__ __forceinline__ void ticket_and_merge(Smem<D>& sm, const AttnParams& p, const Desc& d, int R, int tid) {
     constexpr int C8 = D / 8;
-    const float* Fo = &sm.comb_o[0][0];
-    const int G = p.G;
-    const float qnan = __int_as_float(0x7fc00000);
-    if (d.nparts == 1) {
-        for (int e = tid; e < R * C8; e += kCWarps * 32) {
-            const int r = e / C8, c = (e - r * C8) * 8;
-            const int qi = r / G, hh = r - qi * G;
-            const long long orow = (long long)(d.q_row0 + qi) * p.n_q + (long long)d.kvh * G + hh;
-            const float inv = 1.0f / sm.fin_l[r];
-            const float* src = Fo + r * D + c;
-            uint4 v;
-            v.x = float2_to_bf16x2(src[0] * inv, src[1] * inv);
-            v.y = float2_to_bf16x2(src[2] * inv, src[3] * inv);
-            v.z = float2_to_bf16x2(src[4] * inv, src[5] * inv);
-            v.w = float2_to_bf16x2(src[6] * inv, src[7] * inv);
-            if (poisoned) v = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-            *reinterpret_cast<uint4*>(p.out + orow * D + c) = v;
-        }
-        return;
-    }
-    // partial of this partition
-    for (int e = tid; e < R * C8; e += kCWarps * 32) {
-        const int r = e / C8, c = (e - r * C8) * 8;
-        const int qi = r / G, hh = r - qi * G;
-        const long long orow = (long long)(d.q_row0 + qi) * p.n_q + (long long)d.kvh * G + hh;
-        const float* src = Fo + r * D + c;
-        float4 a = make_float4(src[0], src[1], src[2], src[3]);
-        float4 b = make_float4(src[4], src[5], src[6], src[7]);
-        if (poisoned) a = b = make_float4(qnan, qnan, qnan, qnan);
-        float4* dst = reinterpret_cast<float4*>(p.part_o + ((orow * p.np_max + d.part) * D + c));
-        __stcg(dst, a);
-        __stcg(dst + 1, b);
-        if (c == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(sm.fin_m[r], sm.fin_l[r]));
-    }
-    __threadfence();
+    // every thread's partial stores happen before the barrier; the release
+    // fence of the signalling thread orders them before its ticket at GPU scope
     consumer_bar();
-    if (tid == 0) sm.bcast = atomicAdd(&p.tickets[(long long)d.q_row0 * p.n_kv + d.kvh], 1);
+    if (tid == 0) {
+        __threadfence();
+        sm.bcast = atomicAdd(&p.tickets[(long long)d.q_row0 * p.n_kv + d.hg * d.hps], 1);
+    }
     consumer_bar();
     if (sm.bcast != d.nparts - 1) return;
     __threadfence();
-    // last partition of this group: merge every partition in order
+    const RowMap rm{p.G, d.nq, d.hps, p.n_q};
     const int np = d.nparts;
-    float2* W = reinterpret_cast<float2*>(&sm.comb_o[0][0]);
-    if (R * np <= 32 * D) {
-        for (int e = tid; e < R * np; e += kCWarps * 32) {
+    float2* W = sm.W;
+    if (R * np <= kMergeW) {
+        for (int e = tid; e < R * np; e += kCThreads) {
             const int r = e / np, pp = e - r * np;
-            const int qi = r / G, hh = r - qi * G;
-            const long long orow = (long long)(d.q_row0 + qi) * p.n_q + (long long)d.kvh * G + hh;
-            W[e] = __ldcg(p.part_ml + orow * p.np_max + pp);
+            W[e] = __ldcg(p.part_ml + rm.orow(d, r) * p.np_max + pp);
         }
         consumer_bar();
-        for (int r = tid; r < R; r += kCWarps * 32) {
+        for (int r = tid; r < R; r += kCThreads) {
             float M = -INFINITY;
             for (int pp = 0; pp < np; ++pp) M = fmaxf(M, W[r * np + pp].x);
             const float mu = M == -INFINITY ? 0.f : M;
@@ -295,10 +333,9 @@ __device__ __forceinline__ void finish_item(Smem<D>& sm, const AttnParams& p, co
             for (int pp = 0; pp < np; ++pp) W[r * np + pp].x = exp2f(W[r * np + pp].x - mu) * invL;
         }
         consumer_bar();
-        for (int e = tid; e < R * C8; e += kCWarps * 32) {
+        for (int e = tid; e < R * C8; e += kCThreads) {
             const int r = e / C8, c = (e - r * C8) * 8;
-            const int qi = r / G, hh = r - qi * G;
-            const long long orow = (long long)(d.q_row0 + qi) * p.n_q + (long long)d.kvh * G + hh;
+            const long long orow = rm.orow(d, r);
             float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
             const float4* src = reinterpret_cast<const float4*>(p.part_o + (orow * p.np_max) * D + c);
 #pragma unroll 4
@@ -318,10 +355,9 @@ __device__ __forceinline__ void finish_item(Smem<D>& sm, const AttnParams& p, co
         }
     } else {
         // many partitions: statistics straight from global memory
-        for (int e = tid; e < R * C8; e += kCWarps * 32) {
+        for (int e = tid; e < R * C8; e += kCThreads) {
             const int r = e / C8, c = (e - r * C8) * 8;
-            const int qi = r / G, hh = r - qi * G;
-            const long long orow = (long long)(d.q_row0 + qi) * p.n_q + (long long)d.kvh * G + hh;
+            const long long orow = rm.orow(d, r);
             const float2* ml = p.part_ml + orow * p.np_max;
             float M = -INFINITY;
             for (int pp = 0; pp < np; ++pp) M = fmaxf(M, __ldcg(ml + pp).x);
@@ -349,19 +385,27 @@ __device__ __forceinline__ void finish_item(Smem<D>& sm, const AttnParams& p, co
 }
 
 // ---------------------------------------------------------------------------
-// Decode item on CUDA cores (q_len = 1, G query heads share the K/V tiles).
+// Decode item on CUDA cores (q_len = 1): warp w < hps owns kv head
+// hg * hps + w and its G query heads over every stage of the item.
+// Lane layout: grp = lane / 8 owns tokens grp, grp+4, grp+8, grp+12 of a stage
+// for the QK dot products (li = lane % 8 covers 8 dims per 128-byte box); for
+// PV every lane owns D/32 output dims of all G heads.
 // ---------------------------------------------------------------------------
 template <int D, int G>
 __device__ __forceinline__ void decode_item(Smem<D>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
-                                            uint32_t gbase, int ntiles, volatile int* abort) {
+                                            uint32_t gbase, int ntiles, int si, volatile int* abort) {
     constexpr int NB = D / 64;   // 128-byte boxes per row
     constexpr int HL = 8 / G;    // lanes per head in an 8-lane group
     constexpr int DV = D / 32;   // PV dims per lane
+    const bool active = warp < d.hps;
+    const int lb = log2i(p.bs < kTileT ? p.bs : kTileT);
+    const int hps_lb = d.hps << lb, h_lb = warp << lb;
     const int grp = lane >> 3, li = lane & 7;
     const int myh = li / HL;
+    const int kvh = d.hg * d.hps + warp;
     float2 q2[G][4 * NB];
-    {
-        const __nv_bfloat16* qb = p.q + ((long long)d.q_row0 * p.n_q + (long long)d.kvh * G) * D;
+    if (active) {
+        const __nv_bfloat16* qb = p.q + ((long long)d.q_row0 * p.n_q + (long long)kvh * G) * D;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -386,12 +430,17 @@ __device__ __forceinline__ void decode_item(Smem<D>& sm, const AttnParams& p, co
     const int vch = DV == 4 ? ((lane & 15) >> 1) : (lane >> 2);
     const int voff = DV == 4 ? ((lane & 1) << 3) : ((lane & 3) << 2);
     const int tb = d.t_begin / kTileT;
-    for (int i = warp; i < ntiles; i += kCWarps) {
+    for (int i = 0; i < ntiles; ++i) {
         const uint32_t gi = gbase + i;
-        const int s = (int)(gi % kStages);
-        mbar_wait(&sm.full[s], (gi / kStages) & 1, abort);
-        const uint8_t* kb = &sm.kv[s][0][0][0];
-        const uint8_t* vb = &sm.kv[s][1][0][0];
+        const int s = (int)(gi % kRingSlots);
+        mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort);
+        if (!active) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            continue;
+        }
+        const uint8_t* kb = &sm.kv[s][0][0];
+        const uint8_t* vb = &sm.kv[s][1][0];
         const int t0 = (tb + i) * kTileT;
         const int nvalid = min(kTileT, d.t_end - t0);
         float sc[4];
@@ -403,8 +452,8 @@ __device__ __forceinline__ void decode_item(Smem<D>& sm, const AttnParams& p, co
             for (int h = 0; h < G; ++h) a[h] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int x = 0; x < NB; ++x) {
-                const uint4 kv = *reinterpret_cast<const uint4*>(kb + x * (kTileT * 128) + row * 128 +
-                                                                 ((li ^ (row & 7)) << 4));
+                const int R = srow(h_lb, row, x, hps_lb, lb, NB);
+                const uint4 kv = *reinterpret_cast<const uint4*>(kb + R * 128 + ((li ^ (R & 7)) << 4));
                 const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
@@ -438,89 +487,104 @@ __device__ __forceinline__ void decode_item(Smem<D>& sm, const AttnParams& p, co
         if ((li % HL) == 0) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) sm.pbuf[warp][(grp + 4 * r) * G + myh] = ps[r];
-            if (grp == 0) sm.corr[warp][myh] = cr;
         }
         __syncwarp();
+        // the correction factor is uniform over a head's lanes: fetch each head's
 #pragma unroll
         for (int h = 0; h < G; ++h) {
-            const float c = sm.corr[warp][h];
+            const float c = __shfl_sync(kFull, cr, h * HL);
 #pragma unroll
             for (int j = 0; j < DV / 2; ++j) acc[h][j] = __fmul2_rn(acc[h][j], make_float2(c, c));
         }
-        const uint8_t* vrow = vb + vbox * (kTileT * 128) + voff;
-        for (int t = 0; t < nvalid; ++t) {
-            float pv[G];
 #pragma unroll
-            for (int h = 0; h < G; ++h) pv[h] = sm.pbuf[warp][t * G + h];
-            const uint8_t* src = vrow + t * 128 + ((vch ^ (t & 7)) << 4);
-            if constexpr (DV == 4) {
-                const uint2 w = *reinterpret_cast<const uint2*>(src);
-                const float2 f0 = bf16x2_to_float2(w.x), f1 = bf16x2_to_float2(w.y);
+        for (int t = 0; t < kTileT; ++t) {
+            if (t < nvalid) {  // rows past the valid tokens may hold anything, even NaN
+                float pv[G];
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float2 pp = make_float2(pv[h], pv[h]);
-                    acc[h][0] = __ffma2_rn(pp, f0, acc[h][0]);
-                    acc[h][1] = __ffma2_rn(pp, f1, acc[h][1]);
+                for (int h = 0; h < G; ++h) pv[h] = sm.pbuf[warp][t * G + h];
+                const int R = srow(h_lb, t, vbox, hps_lb, lb, NB);
+                const uint8_t* src = vb + R * 128 + ((vch ^ (R & 7)) << 4) + voff;
+                uint32_t vw[2];
+                if constexpr (DV == 4) {
+                    const uint2 w = *reinterpret_cast<const uint2*>(src);
+                    vw[0] = w.x;
+                    vw[1] = w.y;
+                } else {
+                    vw[0] = *reinterpret_cast<const uint32_t*>(src);
                 }
-            } else {
-                const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
-                const float2 f0 = bf16x2_to_float2(w);
 #pragma unroll
-                for (int h = 0; h < G; ++h) acc[h][0] = __ffma2_rn(make_float2(pv[h], pv[h]), f0, acc[h][0]);
+                for (int j = 0; j < DV / 2; ++j) {
+                    const float2 f = bf16x2_to_float2(vw[j]);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) acc[h][j] = __ffma2_rn(make_float2(pv[h], pv[h]), f, acc[h][j]);
+                }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s], kCWarps);
+        __syncwarp();  // pbuf is rewritten by this warp's next stage; the stage is read
+        if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
     }
-    // per-warp state -> shared memory, then combine the four warps
-    if (grp == 0 && (li % HL) == 0) {
-        sm.comb_m[warp][myh] = m_run;
-        sm.comb_l[warp][myh] = l_run;
+    // finish: per head, m and l are uniform over its lanes; lane h*HL holds them.
+    // The producer raises poison before it arms the stage with the bad block,
+    // so after the last stage's wait the flag is final.
+    const bool pois = sm.poison[si] != 0;
+    if (active) {
+        float mh[G], lh[G];
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            mh[h] = __shfl_sync(kFull, m_run, h * HL);
+            lh[h] = __shfl_sync(kFull, l_run, h * HL);
+        }
+        if (d.nparts == 1) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const long long orow = (long long)d.q_row0 * p.n_q + (long long)kvh * G + h;
+                const float inv = 1.0f / lh[h];
+                uint32_t w[DV / 2];
+#pragma unroll
+                for (int j = 0; j < DV / 2; ++j)
+                    w[j] = pois ? 0x7fc07fc0u : float2_to_bf16x2(acc[h][j].x * inv, acc[h][j].y * inv);
+                __nv_bfloat16* dst = p.out + orow * D + DV * lane;
+                if constexpr (DV == 4)
+                    *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+                else
+                    *reinterpret_cast<uint32_t*>(dst) = w[0];
+            }
+        } else {
+            const float qnan = __int_as_float(0x7fc00000);
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const long long orow = (long long)d.q_row0 * p.n_q + (long long)kvh * G + h;
+                float* dst = p.part_o + (orow * p.np_max + d.part) * D + DV * lane;
+#pragma unroll
+                for (int j = 0; j < DV / 2; ++j) {
+                    const float2 v = pois ? make_float2(qnan, qnan) : acc[h][j];
+                    __stcg(reinterpret_cast<float2*>(dst + 2 * j), v);
+                }
+                if (lane == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(mh[h], lh[h]));
+            }
+        }
     }
-#pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int j = 0; j < DV / 2; ++j) {
-            sm.comb_o[warp][h * D + DV * lane + 2 * j] = acc[h][j].x;
-            sm.comb_o[warp][h * D + DV * lane + 2 * j + 1] = acc[h][j].y;
-        }
-    consumer_bar();
-    const int tid = warp * 32 + lane;
-    for (int e = tid; e < G * D; e += kCWarps * 32) {
-        const int h = e / D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kCWarps; ++w) M = fmaxf(M, sm.comb_m[w][h]);
-        const float mu = M == -INFINITY ? 0.f : M;
-        float o = 0.f, L = 0.f;
-#pragma unroll
-        for (int w = 0; w < kCWarps; ++w) {
-            const float f = exp2f(sm.comb_m[w][h] - mu);
-            o += sm.comb_o[w][e] * f;
-            L += sm.comb_l[w][h] * f;
-        }
-        sm.comb_o[0][e] = o;  // each element is read and written by this thread only
-        if (e - h * D == 0) {
-            sm.fin_m[h] = M;
-            sm.fin_l[h] = L;
-        }
-    }
-    consumer_bar();
 }
 
 // ---------------------------------------------------------------------------
 // Multi-query item on tensor cores (mma.sync m16n8k16, bf16 in, fp32 acc).
+// Warp w serves kv head hw = w / wph of the group and its rows
+// [16 rw, 16 rw + 16), rw = w % wph, of the query tile (rows are (query,
+// q head) pairs of that kv head).
 // ---------------------------------------------------------------------------
 template <int D>
 __device__ __forceinline__ void mq_item(Smem<D>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
-                                        uint32_t gbase, int ntiles, volatile int* abort) {
+                                        uint32_t gbase, int ntiles, int si, volatile int* abort) {
+    constexpr int NB = D / 64;
     const int G = p.G;
-    const int R = d.nq * G;
-    const int RG = R <= 16 ? 1 : (R <= 32 ? 2 : 4);
-    const int TG = kCWarps / RG;
-    const int rg = warp % RG, tg = warp / RG;
+    const int per = d.nq * G;                      // rows per kv head in this tile
+    const int hw = warp / d.wph, rw = warp - hw * d.wph;
+    const bool active = hw < d.hps && rw * 16 < per;
+    const int lb = log2i(p.bs < kTileT ? p.bs : kTileT);
+    const int hps_lb = d.hps << lb, h_lb = hw << lb;
+    const int kvh = d.hg * d.hps + hw;
     const int qd = lane & 3, qr = lane >> 2;
-    const int rA = rg * 16 + qr, rB = rA + 8;
+    const int rA = rw * 16 + qr, rB = rA + 8;
     auto row_lim = [&](int r) {
         int qi = r / G;
         if (qi >= d.nq) qi = d.nq - 1;
@@ -532,9 +596,9 @@ __device__ __forceinline__ void mq_item(Smem<D>& sm, const AttnParams& p, const 
     {
         auto qptr = [&](int r) -> const uint32_t* {
             const int qi = r / G, hh = r - qi * G;
-            if (qi >= d.nq) return nullptr;
+            if (!active || qi >= d.nq) return nullptr;
             return reinterpret_cast<const uint32_t*>(
-                p.q + ((long long)(d.q_row0 + qi) * p.n_q + (long long)d.kvh * G + hh) * D);
+                p.q + ((long long)(d.q_row0 + qi) * p.n_q + (long long)kvh * G + hh) * D);
         };
         const uint32_t* pa = qptr(rA);
         const uint32_t* pb = qptr(rB);
@@ -552,27 +616,32 @@ __device__ __forceinline__ void mq_item(Smem<D>& sm, const AttnParams& p, const 
     for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
     const int tb = d.t_begin / kTileT;
-    // ldmatrix row addresses (per lane) inside a tile
+    // ldmatrix row addresses (per lane) inside a stage
     const int mi = lane >> 3, mrow = lane & 7;
-    const int k_tok = ((mi >> 1) << 3) + mrow;  // K: matrices (tok 0-7, d lo), (tok 0-7, d hi), (tok 8-15, ...)
+    const int k_tok = ((mi >> 1) << 3) + mrow;  // K: (tok 0-7, d lo), (tok 0-7, d hi), (tok 8-15, d lo), ...
     const int k_hi = mi & 1;
     const int v_tok = ((mi & 1) << 3) + mrow;   // V: (tok 0-7, d lo), (tok 8-15, d lo), (tok 0-7, d hi), ...
     const int v_hi = mi >> 1;
-    for (int i = tg; i < ntiles; i += TG) {
+    for (int i = 0; i < ntiles; ++i) {
         const uint32_t gi = gbase + i;
-        const int s = (int)(gi % kStages);
-        mbar_wait(&sm.full[s], (gi / kStages) & 1, abort);
-        const uint32_t kb = smem_u32(&sm.kv[s][0][0][0]);
-        const uint32_t vb = smem_u32(&sm.kv[s][1][0][0]);
+        const int s = (int)(gi % kRingSlots);
+        mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort);
+        if (!active) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            continue;
+        }
+        const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
+        const uint32_t vb = smem_u32(&sm.kv[s][1][0]);
         const int t0 = (tb + i) * kTileT;
         const int nvalid = min(kTileT, d.t_end - t0);
         float sf[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
             const int chunk = 2 * ks + k_hi;
-            const uint32_t addr = kb + (chunk >> 3) * (kTileT * 128) + k_tok * 128 + (((chunk & 7) ^ (k_tok & 7)) << 4);
+            const int R = srow(h_lb, k_tok, chunk >> 3, hps_lb, lb, NB);
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(addr, b0, b1, b2, b3);
+            ldsm_x4(kb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
             mma_bf16_16816(sf[0], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
             mma_bf16_16816(sf[1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
         }
@@ -632,63 +701,44 @@ __device__ __forceinline__ void mq_item(Smem<D>& sm, const AttnParams& p, const 
 #pragma unroll
         for (int dp = 0; dp < D / 16; ++dp) {
             const int chunk = 2 * dp + v_hi;
-            const uint32_t addr = vb + (chunk >> 3) * (kTileT * 128) + v_tok * 128 + (((chunk & 7) ^ (v_tok & 7)) << 4);
+            const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(addr, b0, b1, b2, b3);
-            b0 &= keep0;
-            b1 &= keep1;
-            b2 &= keep0;
-            b3 &= keep1;
-            mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
-            mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0 & keep0, b1 & keep1);
+            mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & keep0, b3 & keep1);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s], (uint32_t)TG);
+        if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
     }
-    // per-warp state -> shared memory
-    float* ow = &sm.comb_o[warp][0];
+    if (!active) return;
+    const bool poisoned = sm.poison[si] != 0;  // final after the last stage's wait
+    // finish from registers: rows rA, rB of kv head kvh
+    const float qnan = __int_as_float(0x7fc00000);
+    const float mfin[2] = {mA, mB}, lfin[2] = {lA, lB};
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-        const int c = 8 * nt + 2 * qd;
-        ow[qr * D + c] = o[nt][0];
-        ow[qr * D + c + 1] = o[nt][1];
-        ow[(qr + 8) * D + c] = o[nt][2];
-        ow[(qr + 8) * D + c + 1] = o[nt][3];
-    }
-    if (qd == 0) {
-        sm.comb_m[warp][qr] = mA;
-        sm.comb_l[warp][qr] = lA;
-        sm.comb_m[warp][qr + 8] = mB;
-        sm.comb_l[warp][qr + 8] = lB;
-    }
-    consumer_bar();
-    const int tid = warp * 32 + lane;
-    if (TG > 1) {
-        // rows of group rg live in warp rg (tg = 0); fold in warps rg + RG * tg
-        for (int e = tid; e < RG * 16 * D; e += kCWarps * 32) {
-            const int g = e / (16 * D), loc = e - g * 16 * D, r = loc / D;
-            float M = -INFINITY;
-            for (int t = 0; t < TG; ++t) M = fmaxf(M, sm.comb_m[g + RG * t][r]);
-            const float mu = M == -INFINITY ? 0.f : M;
-            float acc = 0.f, L = 0.f;
-            for (int t = 0; t < TG; ++t) {
-                const float f = exp2f(sm.comb_m[g + RG * t][r] - mu);
-                acc += sm.comb_o[g + RG * t][loc] * f;
-                L += sm.comb_l[g + RG * t][r] * f;
+    for (int half = 0; half < 2; ++half) {
+        const int r = half ? rB : rA;
+        const int qi = r / G, hh = r - qi * G;
+        if (qi >= d.nq) continue;
+        const long long orow = (long long)(d.q_row0 + qi) * p.n_q + (long long)kvh * G + hh;
+        if (d.nparts == 1) {
+            const float inv = 1.0f / lfin[half];
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                const uint32_t w = poisoned ? 0x7fc07fc0u
+                                            : float2_to_bf16x2(o[nt][2 * half] * inv, o[nt][2 * half + 1] * inv);
+                *reinterpret_cast<uint32_t*>(p.out + orow * D + 8 * nt + 2 * qd) = w;
             }
-            sm.comb_o[g][loc] = acc;
-            if (loc - r * D == 0) {
-                sm.fin_m[g * 16 + r] = M;
-                sm.fin_l[g * 16 + r] = L;
+        } else {
+            float* dst = p.part_o + (orow * p.np_max + d.part) * D;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                const float2 v = poisoned ? make_float2(qnan, qnan) : make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+                __stcg(reinterpret_cast<float2*>(dst + 8 * nt + 2 * qd), v);
             }
-        }
-    } else {
-        for (int r = tid; r < kMqRows; r += kCWarps * 32) {
-            sm.fin_m[r] = sm.comb_m[r >> 4][r & 15];
-            sm.fin_l[r] = sm.comb_l[r >> 4][r & 15];
+            if (qd == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(mfin[half], lfin[half]));
         }
     }
-    consumer_bar();
 }
 
 // ---------------------------------------------------------------------------
@@ -714,33 +764,31 @@ __device__ __forceinline__ void consumer(Smem<D>& sm, const AttnParams& p, int w
         int R;
         if constexpr (GD > 0) {
             if (d.kind == KIND_DEC) {
-                decode_item<D, GD>(sm, p, d, warp, lane, g, ntiles, abort);
-                R = GD;
+                decode_item<D, GD>(sm, p, d, warp, lane, g, ntiles, si, abort);
+                R = d.hps * GD;
             } else {
-                mq_item<D>(sm, p, d, warp, lane, g, ntiles, abort);
-                R = d.nq * p.G;
+                mq_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
+                R = d.hps * d.nq * p.G;
             }
         } else {
-            mq_item<D>(sm, p, d, warp, lane, g, ntiles, abort);
-            R = d.nq * p.G;
+            mq_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
+            R = d.hps * d.nq * p.G;
         }
-        const bool poisoned = sm.poison[si] != 0;
-        finish_item<D>(sm, p, d, R, poisoned, tid);
-        consumer_bar();  // comb buffers are free again
+        if (d.nparts > 1) ticket_and_merge<D>(sm, p, d, R, tid);
+        consumer_bar();  // every warp is done with this item
         if (lane == 0) mbar_arrive(&sm.iempty[si]);
         g += (uint32_t)ntiles;
     }
 }
 
 template <int D, int GD>
-__global__ void __launch_bounds__(kThreads, 2)
-    paged_attention_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                           const __grid_constant__ AttnParams p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_attention_kernel(const __grid_constant__ TMaps tm, const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kRingSlots; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kCWarps);
         }
@@ -753,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncthreads();
     if (warp == kCWarps) {
-        producer<D>(sm, &tmk, &tmv, p, lane);
+        producer<D>(sm, &tm, p, lane);
     } else {
         consumer<D, GD>(sm, p, warp, lane);
     }
@@ -761,10 +809,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 }
 
 template <int D, int GD>
-int launch_attention(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p, long long max_items,
-                            cudaStream_t st) {
+int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, cudaStream_t st) {
     static int configured[64] = {0};
-    static int occ[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     const size_t smem = sizeof(Smem<D>) + 1024;
@@ -773,35 +819,27 @@ int launch_attention(const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnP
         if (cudaFuncSetAttribute(paged_attention_kernel<D, GD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return PKV_ERR_CUDA;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_attention_kernel<D, GD>, kThreads, smem) !=
-                cudaSuccess ||
-            n < 1)
-            return PKV_ERR_CUDA;
-        occ[dev] = n;
         configured[dev] = 1;
     }
-    long long grid = (long long)host::sm_count() * occ[dev];
+    long long grid = host::sm_count();
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
-    paged_attention_kernel<D, GD><<<(unsigned)grid, kThreads, smem, st>>>(tmk, tmv, p);
+    paged_attention_kernel<D, GD><<<(unsigned)grid, kThreads, smem, st>>>(tm, p);
     return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 template <int D>
-int dispatch_g(int GD, const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p, long long mi,
-                      cudaStream_t st) {
+int dispatch_g(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st) {
     switch (GD) {
-        case 1: return launch_attention<D, 1>(tmk, tmv, p, mi, st);
-        case 2: return launch_attention<D, 2>(tmk, tmv, p, mi, st);
-        case 4: return launch_attention<D, 4>(tmk, tmv, p, mi, st);
-        case 8: return launch_attention<D, 8>(tmk, tmv, p, mi, st);
-        default: return launch_attention<D, 0>(tmk, tmv, p, mi, st);
+        case 1: return launch_attention<D, 1>(tm, p, mi, st);
+        case 2: return launch_attention<D, 2>(tm, p, mi, st);
+        case 4: return launch_attention<D, 4>(tm, p, mi, st);
+        case 8: return launch_attention<D, 8>(tm, p, mi, st);
+        default: return launch_attention<D, 0>(tm, p, mi, st);
     }
 }
 
-
-int dispatch_attention_d64(int GD, const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p, long long mi, cudaStream_t st);
-int dispatch_attention_d128(int GD, const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p, long long mi, cudaStream_t st);
+int dispatch_attention_d64(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
+int dispatch_attention_d128(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
 
 }  // namespace pkv

@@ -2,8 +2,7 @@
 #include "pkv_attention.cuh"
 
 namespace pkv {
-int dispatch_attention_d128(int GD, const CUtensorMap& tmk, const CUtensorMap& tmv, const AttnParams& p, long long mi,
-                            cudaStream_t st) {
-    return dispatch_g<128>(GD, tmk, tmv, p, mi, st);
+int dispatch_attention_d128(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st) {
+    return dispatch_g<128>(GD, tm, p, mi, st);
 }
 }  // namespace pkv

@@ -4,13 +4,55 @@
 
 namespace pkv {
 
-// ---------------------------------------------------------------------------
-// Planning kernel
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+struct PlanParams {
+    const int32_t* seq_lens;
+    const int32_t* q_lens;
+    int4* items;     // {b, part, qt, hg}
+    int4* seqs;      // {seq_len, q_len, first query row, kind | hps << 4 | wph << 8 | qt_len << 12}
+    int* hdr;
+    int* seq_q0;
+    int* seq_flag;
+    int* seq_off1;   // multi-query items: first item; decode: first full-partition item
+    int* seq_off2;   // decode: first tail item
+    int* tickets;
+    __nv_bfloat16* out;
+    int32_t* status;
+    int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, decode_ok;
+};
 
-__device__ __forceinline__ int mq_items_of(int L, int ql, int G, int P) {
-    const int QT = G >= kMqRows ? 1 : kMqRows / G;
+__host__ __device__ inline int gcd_pow2(int n, int m) {  // largest power of two <= m dividing n (m a power of 2)
+    int h = m;
+    while (h > 1 && n % h) h >>= 1;
+    return h;
+}
+
+// Shape of the work of one sequence: kind, kv heads per stage, warps per kv
+// head, queries per tile.
+struct SeqShape {
+    int kind, hps, wph, qt;
+};
+
+__device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_ok) {
+    SeqShape s;
+    if (ql == 1 && decode_ok) {
+        s.kind = KIND_DEC;
+        s.hps = gcd_pow2(n_kv, kMaxHPS);
+        s.wph = 1;
+        s.qt = 1;
+        return s;
+    }
+    s.kind = KIND_MQ;
+    const int rows = ql * G;
+    int w = 1;
+    while (w < kCWarps && 16 * w < rows) w <<= 1;
+    while (w < kCWarps && 16 * w < G) w <<= 1;
+    s.wph = w;
+    s.hps = gcd_pow2(n_kv, kCWarps / w);
+    s.qt = (16 * w) / G;
+    return s;
+}
+
+__device__ __forceinline__ int mq_parts_of(int L, int ql, int QT, int P) {
     int n = 0;
     for (int qt = 0; qt * QT < ql; ++qt) {
         const int last = min(ql, (qt + 1) * QT);
@@ -19,9 +61,12 @@ __device__ __forceinline__ int mq_items_of(int L, int ql, int G, int P) {
     return n;
 }
 
+// Work list for one call: multi-query items first (the compute-heavy tiles
+// start early), then every full decode partition, then decode partition tails
+// (the short items last, so the dynamic queue ends evenly).
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams pp) {
     __shared__ int tmp[32];
-    __shared__ int s_total_mq;
+    __shared__ int s_tot[2];
     const int tid = threadIdx.x;
     int bits = 0;
     // pass A: query row offsets and validity
@@ -49,38 +94,50 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         carry += tot;
     }
     __syncthreads();
-    // pass B: item counts
-    int carry_mq = 0, carry_dec = 0;
+    // pass B: item counts per class, per-sequence records
+    int c_mq = 0, c_full = 0, c_tail = 0;
     for (int base = 0; base < pp.num_seqs; base += kPlanThreads) {
         const int b = base + tid;
-        int nmq = 0, ndec = 0;
-        if (b < pp.num_seqs && pp.seq_flag[b] == 0) {
-            const int L = pp.seq_lens[b], ql = pp.q_lens[b];
-            if (ql == 1 && pp.decode_ok)
-                ndec = ceil_div(L, pp.P) * pp.n_kv;
-            else if (ql > 0)
-                nmq = mq_items_of(L, ql, pp.G, pp.P) * pp.n_kv;
-        }
-        int tm, td;
-        const int exm = block_exclusive_scan_1024(nmq, tmp, &tm);
-        const int exd = block_exclusive_scan_1024(ndec, tmp, &td);
+        int nmq = 0, nfull = 0, ntail = 0;
+        bool dec = false;
         if (b < pp.num_seqs) {
-            pp.seq_mq_off[b] = carry_mq + exm;
-            pp.seq_dec_off[b] = carry_dec + exd;
+            const int L = pp.seq_lens[b], ql = pp.q_lens[b];
+            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
+            dec = sh.kind == KIND_DEC;
+            const int ngroups = pp.n_kv / sh.hps;
+            if (pp.seq_flag[b] == 0) {
+                if (dec) {
+                    const int np = ceil_div(L, pp.P);
+                    nfull = (np - 1) * ngroups;
+                    ntail = ngroups;
+                } else if (ql > 0) {
+                    nmq = mq_parts_of(L, ql, sh.qt, pp.P) * ngroups;
+                }
+            }
+            pp.seqs[b] = make_int4(L, ql, pp.seq_q0[b], sh.kind | (sh.hps << 4) | (sh.wph << 8) | (sh.qt << 12));
         }
-        carry_mq += tm;
-        carry_dec += td;
+        int tm, tf, tt;
+        const int exm = block_exclusive_scan_1024(nmq, tmp, &tm);
+        const int exf = block_exclusive_scan_1024(nfull, tmp, &tf);
+        const int ext = block_exclusive_scan_1024(ntail, tmp, &tt);
+        if (b < pp.num_seqs) {
+            pp.seq_off1[b] = dec ? c_full + exf : c_mq + exm;
+            pp.seq_off2[b] = c_tail + ext;
+        }
+        c_mq += tm;
+        c_full += tf;
+        c_tail += tt;
     }
     if (tid == 0) {
-        s_total_mq = carry_mq;
-        pp.hdr[0] = carry_mq + carry_dec;
+        s_tot[0] = c_mq;
+        s_tot[1] = c_mq + c_full;
+        pp.hdr[0] = c_mq + c_full + c_tail;
         pp.hdr[1] = 0;
     }
     for (long long i = tid; i < (long long)pp.total_q * pp.n_kv; i += kPlanThreads) pp.tickets[i] = 0;
     __syncthreads();
-    const int total_mq = s_total_mq;
+    const int base_full = s_tot[0], base_tail = s_tot[1];
     const int warp = tid >> 5, lane = tid & 31;
-    const int QT = pp.G >= kMqRows ? 1 : kMqRows / pp.G;
     for (int b = warp; b < pp.num_seqs; b += kPlanThreads / 32) {
         const int flag = pp.seq_flag[b];
         const int L = pp.seq_lens[b], ql = pp.q_lens[b];
@@ -95,30 +152,27 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             continue;
         }
         if (ql <= 0) continue;
-        if (ql == 1 && pp.decode_ok) {
-            const int nparts = ceil_div(L, pp.P);
-            const int base = total_mq + pp.seq_dec_off[b];
-            for (int it = lane; it < nparts * pp.n_kv; it += 32) {
-                const int part = it / pp.n_kv, kvh = it - part * pp.n_kv;
-                int4* d = pp.items + 3LL * (base + it);
-                d[0] = make_int4(b, kvh, part, nparts);
-                d[1] = make_int4(part * pp.P, min((part + 1) * pp.P, L), L, q0);
-                d[2] = make_int4(1, KIND_DEC, 0, 0);
+        const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
+        const int ngroups = pp.n_kv / sh.hps;
+        if (sh.kind == KIND_DEC) {
+            const int np = ceil_div(L, pp.P);
+            const int f0 = base_full + pp.seq_off1[b];
+            for (int it = lane; it < (np - 1) * ngroups; it += 32) {
+                const int part = it / ngroups, hg = it - part * ngroups;
+                pp.items[f0 + it] = make_int4(b, part, 0, hg);
             }
+            const int t0 = base_tail + pp.seq_off2[b];
+            for (int hg = lane; hg < ngroups; hg += 32) pp.items[t0 + hg] = make_int4(b, np - 1, 0, hg);
         } else {
-            int base = pp.seq_mq_off[b];
-            for (int qt = 0; qt * QT < ql; ++qt) {
-                const int nq = min(QT, ql - qt * QT);
-                const int t_vis = L - ql + qt * QT + nq;
-                const int nparts = ceil_div(t_vis, pp.P);
-                for (int it = lane; it < nparts * pp.n_kv; it += 32) {
-                    const int part = it / pp.n_kv, kvh = it - part * pp.n_kv;
-                    int4* d = pp.items + 3LL * (base + it);
-                    d[0] = make_int4(b, kvh, part, nparts);
-                    d[1] = make_int4(part * pp.P, min((part + 1) * pp.P, t_vis), t_vis, q0 + qt * QT);
-                    d[2] = make_int4(nq, KIND_MQ, 0, 0);
+            int base = pp.seq_off1[b];
+            for (int qt = 0; qt * sh.qt < ql; ++qt) {
+                const int nq = min(sh.qt, ql - qt * sh.qt);
+                const int np = ceil_div(L - ql + qt * sh.qt + nq, pp.P);
+                for (int it = lane; it < np * ngroups; it += 32) {
+                    const int part = it / ngroups, hg = it - part * ngroups;
+                    pp.items[base + it] = make_int4(b, part, qt, hg);
                 }
-                base += nparts * pp.n_kv;
+                base += np * ngroups;
             }
         }
     }
@@ -126,7 +180,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 }
 
 struct WsLayout {
-    size_t hdr, items, seq, tickets, ml, o, total;
+    size_t hdr, items, seqs, seqaux, tickets, ml, o, total;
     long long max_items;
     int np_max;
 };
@@ -142,8 +196,10 @@ static WsLayout ws_layout(int num_seqs, int total_q, int n_q, int n_kv, int D, i
     w.hdr = off;
     off = align256(off + 64);
     w.items = off;
-    off = align256(off + (size_t)w.max_items * 48);
-    w.seq = off;
+    off = align256(off + (size_t)w.max_items * sizeof(int4));
+    w.seqs = off;
+    off = align256(off + (size_t)num_seqs * sizeof(int4));
+    w.seqaux = off;
     off = align256(off + (size_t)num_seqs * 4 * sizeof(int));
     w.tickets = off;
     off = align256(off + (size_t)total_q * n_kv * sizeof(int));
@@ -189,10 +245,10 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (num_q_heads % num_kv_heads) return PKV_ERR_UNSUPPORTED;
     const int G = num_q_heads / num_kv_heads;
-    if (G > kMqRows) return PKV_ERR_UNSUPPORTED;
+    if (G > 64) return PKV_ERR_UNSUPPORTED;
     if ((block_size & (block_size - 1)) || block_size > 256) return PKV_ERR_UNSUPPORTED;
     if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31)) return PKV_ERR_SIZE;
-    if (flags & ~PKV_ATTN_DECODE_TENSOR_CORES) return PKV_ERR_SIZE;
+    if (flags & ~PKV_ATTN_DECODE_CUDA_CORES) return PKV_ERR_SIZE;
     if (num_seqs == 0 || total_q == 0) return PKV_OK;
     if (num_seqs > (1 << 24) || total_q > (1 << 20)) return PKV_ERR_SIZE;
     int P = partition_tokens;
@@ -209,29 +265,39 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     const int rc = host::check_device();
     if (rc) return rc;
 
-    CUtensorMap tmk, tmv;
-    const uint64_t rows = (uint64_t)num_blocks * num_kv_heads * block_size;
-    const uint32_t box_rows = block_size < kTileT ? (uint32_t)block_size : (uint32_t)kTileT;
-    if (host::encode_tiled_2d(&tmk, k_cache, head_dim, rows, (uint64_t)head_dim * 2, 64, box_rows,
-                              CU_TENSOR_MAP_SWIZZLE_128B) ||
-        host::encode_tiled_2d(&tmv, v_cache, head_dim, rows, (uint64_t)head_dim * 2, 64, box_rows,
-                              CU_TENSOR_MAP_SWIZZLE_128B))
-        return PKV_ERR_CUDA;
+    // 5-D views [num_blocks][n_kv][bs][D/64][64] of each pool, one per box height in kv heads
+    TMaps tm;
+    {
+        const uint32_t box_rows = block_size < kTileT ? (uint32_t)block_size : (uint32_t)kTileT;
+        const uint64_t dims[5] = {64, (uint64_t)head_dim / 64, (uint64_t)block_size, (uint64_t)num_kv_heads,
+                                  (uint64_t)num_blocks};
+        const uint64_t strides[4] = {128, (uint64_t)head_dim * 2, (uint64_t)block_size * head_dim * 2,
+                                     (uint64_t)num_kv_heads * block_size * head_dim * 2};
+        for (int i = 0; i < 4; ++i) {
+            uint32_t hb = 1u << i;
+            if (hb > (uint32_t)num_kv_heads) hb = (uint32_t)num_kv_heads;
+            const uint32_t box[5] = {64, (uint32_t)head_dim / 64, box_rows, hb, 1};
+            if (host::encode_tiled(&tm.k[i], k_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                host::encode_tiled(&tm.v[i], v_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return PKV_ERR_CUDA;
+        }
+    }
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    int* seq = reinterpret_cast<int*>(ws + w.seq);
+    int* aux = reinterpret_cast<int*>(ws + w.seqaux);
     const int GD = (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
-    const bool decode_ok = GD > 0 && !(flags & PKV_ATTN_DECODE_TENSOR_CORES);
+    const bool decode_ok = GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
 
     PlanParams pp{};
     pp.seq_lens = seq_lens;
     pp.q_lens = q_lens;
     pp.items = reinterpret_cast<int4*>(ws + w.items);
+    pp.seqs = reinterpret_cast<int4*>(ws + w.seqs);
     pp.hdr = reinterpret_cast<int*>(ws + w.hdr);
-    pp.seq_q0 = seq;
-    pp.seq_flag = seq + num_seqs;
-    pp.seq_mq_off = seq + 2 * num_seqs;
-    pp.seq_dec_off = seq + 3 * num_seqs;
+    pp.seq_q0 = aux;
+    pp.seq_flag = aux + num_seqs;
+    pp.seq_off1 = aux + 2 * num_seqs;
+    pp.seq_off2 = aux + 3 * num_seqs;
     pp.tickets = reinterpret_cast<int*>(ws + w.tickets);
     pp.out = static_cast<__nv_bfloat16*>(out);
     pp.status = status;
@@ -255,6 +321,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     ap.q = static_cast<const __nv_bfloat16*>(q);
     ap.block_tables = block_tables;
     ap.items = pp.items;
+    ap.seqs = pp.seqs;
     ap.hdr = pp.hdr;
     ap.tickets = pp.tickets;
     ap.part_o = reinterpret_cast<float*>(ws + w.o);
@@ -267,8 +334,9 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     ap.bs = block_size;
     ap.num_blocks = num_blocks;
     ap.np_max = w.np_max;
-    ap.flags = flags;
+    ap.P = P;
+    ap.row_bytes = head_dim * 2;
     ap.scale_log2 = scale * 1.4426950408889634f;
-    if (head_dim == 128) return dispatch_attention_d128(decode_ok ? GD : 0, tmk, tmv, ap, w.max_items, st);
-    return dispatch_attention_d64(decode_ok ? GD : 0, tmk, tmv, ap, w.max_items, st);
+    if (head_dim == 128) return dispatch_attention_d128(decode_ok ? GD : 0, tm, ap, w.max_items, st);
+    return dispatch_attention_d64(decode_ok ? GD : 0, tm, ap, w.max_items, st);
 }

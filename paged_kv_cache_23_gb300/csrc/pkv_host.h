@@ -17,10 +17,12 @@ int sm_count();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// cuTensorMapEncodeTiled through cudaGetDriverEntryPointByVersion, so the
-// library needs no link-time dependency on libcuda.  Returns 0 on success.
-int encode_tiled_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t outer, uint64_t row_bytes,
-                    uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
+// cuTensorMapEncodeTiled (bf16 elements) through
+// cudaGetDriverEntryPointByVersion, so the library needs no link-time
+// dependency on libcuda.  dims/box have `rank` entries, innermost first;
+// strides (bytes) has rank - 1.  Returns 0 on success.
+int encode_tiled(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                 const uint32_t* box, CUtensorMapSwizzle swizzle);
 
 }  // namespace host
 }  // namespace pkv

@@ -72,9 +72,9 @@ def test_small_workloads_match_oracle(name):
         assert np.array_equal(ds.next_token.cpu().numpy(), nxt)
 
 
-@pytest.mark.parametrize("name", ["decode", "mix", "spec", "long"])
-def test_decode_rows_on_tensor_cores_match_oracle(name):
-    run_and_check(wl.SMALL[name](), flags=pkv.PKV_ATTN_DECODE_TENSOR_CORES)
+@pytest.mark.parametrize("name", ["tiny", "decode", "mix", "spec", "long"])
+def test_decode_rows_on_cuda_cores_match_oracle(name):
+    run_and_check(wl.SMALL[name](), flags=pkv.PKV_ATTN_DECODE_CUDA_CORES)
 
 
 @pytest.mark.parametrize("P", [16, 32, 48, 160, 4096])
