@@ -55,7 +55,8 @@ constexpr int kMaxParts = 1024;             // partitions per sequence
 constexpr int kPlanThreads = 1024;
 constexpr int kMergeW = 2048;               // float2 merge weights in shared memory
 
-enum { KIND_END = -1, KIND_DEC = 0, KIND_MQ = 1 };
+// KIND_DEC: q_len = 1 rows on tensor cores; KIND_DECF: on CUDA cores; KIND_MQ: q_len > 1.
+enum { KIND_END = -1, KIND_DEC = 0, KIND_MQ = 1, KIND_DECF = 2 };
 
 struct Desc {
     int b, part, nparts, hg;        // sequence, partition, partitions of the group, head group
@@ -105,6 +106,13 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 
 __device__ __forceinline__ int log2i(int x) { return 31 - __clz(x); }
 
+// Transpose of an 8x8 b16 matrix held one 32-bit pair per lane.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // Index of the 128-byte shared-memory row that holds (head h of the stage,
 // token r of the tile, 64-column box x): the TMA boxes of one stage are
 // [op][head][rows of the op][box], one op per block when block_size < 16.
@@ -135,7 +143,7 @@ __device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, const At
     d.hps = (sq.w >> 4) & 15;
     d.wph = (sq.w >> 8) & 15;
     const int QT = (sq.w >> 12) & 4095;
-    if (d.kind == KIND_DEC) {
+    if (d.kind != KIND_MQ) {
         d.nq = 1;
         d.t_vis = L;
         d.q_row0 = q0;
@@ -567,6 +575,148 @@ __device__ __forceinline__ void decode_item(Smem<D>& sm, const AttnParams& p, co
 }
 
 // ---------------------------------------------------------------------------
+// Decode item on tensor cores (q_len = 1): warp w < hps owns kv head
+// hg * hps + w.  The product is taken transposed, tokens on the M axis and the
+// G <= 8 query heads of the group on N:
+//   S^T[16 x 8]  = K_tile[16 x D] . Q^T[D x 8]          (D/16 mma m16n8k16)
+//   O^T[D x 8]  += V_tile^T[D x 16] . P^T[16 x 8]       (D/16 mma)
+// so half of N is padding at G = 4 instead of three quarters of M.  P^T's
+// B fragments are the S^T accumulators transposed in registers (movmatrix).
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ __forceinline__ void decode_tc_item(Smem<D>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
+                                               uint32_t gbase, int ntiles, int si, volatile int* abort) {
+    constexpr int NB = D / 64;
+    constexpr int NT = D / 16;
+    const int G = p.G;
+    const bool active = warp < d.hps;
+    const int lb = log2i(p.bs < kTileT ? p.bs : kTileT);
+    const int hps_lb = d.hps << lb, h_lb = warp << lb;
+    const int kvh = d.hg * d.hps + warp;
+    const int qd = lane & 3, qr = lane >> 2;
+    // Q^T as B fragments: n = query head qr of the group, k = dims
+    uint32_t qb[NT][2];
+    {
+        const uint32_t* qrow =
+            (active && qr < G)
+                ? reinterpret_cast<const uint32_t*>(p.q + ((long long)d.q_row0 * p.n_q + (long long)kvh * G + qr) * D)
+                : nullptr;
+#pragma unroll
+        for (int ks = 0; ks < NT; ++ks) {
+            qb[ks][0] = qrow ? qrow[8 * ks + qd] : 0u;
+            qb[ks][1] = qrow ? qrow[8 * ks + 4 + qd] : 0u;
+        }
+    }
+    float o[NT][4];  // O^T tile mt: (dim 16mt + qr [+8], head 2qd [+1])
+#pragma unroll
+    for (int mt = 0; mt < NT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2qd, 2qd + 1
+    const int mi = lane >> 3, mr = lane & 7;
+    const int a_tok = ((mi & 1) << 3) + mr, a_hi = mi >> 1;   // K: (t0-7,lo) (t8-15,lo) (t0-7,hi) (t8-15,hi)
+    const int v_tok = ((mi >> 1) << 3) + mr, v_hi = mi & 1;   // V: (t0-7,lo) (t0-7,hi) (t8-15,lo) (t8-15,hi)
+    const int tb = d.t_begin / kTileT;
+    for (int i = 0; i < ntiles; ++i) {
+        const uint32_t gi = gbase + i;
+        const int s = (int)(gi % kRingSlots);
+        mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort);
+        if (!active) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            continue;
+        }
+        const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
+        const uint32_t vb = smem_u32(&sm.kv[s][1][0]);
+        const int t0 = (tb + i) * kTileT;
+        const int nvalid = min(kTileT, d.t_end - t0);
+        // S^T, two accumulators to halve the dependent mma chain
+        float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < NT; ++ks) {
+            const int chunk = 2 * ks + a_hi;
+            const int R = srow(h_lb, a_tok, chunk >> 3, hps_lb, lb, NB);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(kb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
+            mma_bf16_16816((ks & 1) ? cb : ca, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        }
+        // (token qr, head 2qd), (qr, 2qd+1), (qr+8, 2qd), (qr+8, 2qd+1)
+        const bool va = qr < nvalid, vb8 = qr + 8 < nvalid;
+        const float s0 = va ? (ca[0] + cb[0]) * p.scale_log2 : -INFINITY;
+        const float s1 = va ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;
+        const float s2 = vb8 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;
+        const float s3 = vb8 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;
+        float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+#pragma unroll
+        for (int o8 = 4; o8 < 32; o8 <<= 1) {
+            x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, o8));
+            x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, o8));
+        }
+        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+        const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
+        const float c0 = exp2f(m0 - u0), c1 = exp2f(m1 - u1);
+        const float p0 = exp2f(s0 - u0), p1 = exp2f(s1 - u1), p2 = exp2f(s2 - u0), p3 = exp2f(s3 - u1);
+        float y0 = p0 + p2, y1 = p1 + p3;
+#pragma unroll
+        for (int o8 = 4; o8 < 32; o8 <<= 1) {
+            y0 += __shfl_xor_sync(kFull, y0, o8);
+            y1 += __shfl_xor_sync(kFull, y1, o8);
+        }
+        l0 = l0 * c0 + y0;
+        l1 = l1 * c1 + y1;
+        m0 = n0;
+        m1 = n1;
+#pragma unroll
+        for (int mt = 0; mt < NT; ++mt) {
+            o[mt][0] *= c0;
+            o[mt][1] *= c1;
+            o[mt][2] *= c0;
+            o[mt][3] *= c1;
+        }
+        const uint32_t pb0 = movmatrix_trans(float2_to_bf16x2(p0, p1));  // (tokens 2qd, 2qd+1; head qr)
+        const uint32_t pb1 = movmatrix_trans(float2_to_bf16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; head qr)
+        // V rows past the valid tokens may hold anything (even NaN): zero them
+        const uint32_t klo = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t khi = (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (9 + 2 * qd < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int mt = 0; mt < NT; ++mt) {
+            const int chunk = 2 * mt + v_hi;
+            const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
+            mma_bf16_16816(o[mt], a0 & klo, a1 & klo, a2 & khi, a3 & khi, pb0, pb1);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
+    }
+    if (!active) return;
+    const bool poisoned = sm.poison[si] != 0;  // final after the last stage's wait
+    const float qnan = __int_as_float(0x7fc00000);
+    const float mh[2] = {m0, m1}, lh[2] = {l0, l1};
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const int h = 2 * qd + j;
+        if (h >= G) continue;
+        const long long orow = (long long)d.q_row0 * p.n_q + (long long)kvh * G + h;
+        if (d.nparts == 1) {
+            const float inv = 1.0f / lh[j];
+            __nv_bfloat16* dst = p.out + orow * D + qr;
+#pragma unroll
+            for (int mt = 0; mt < NT; ++mt) {
+                dst[16 * mt] = poisoned ? __float2bfloat16_rn(qnan) : __float2bfloat16_rn(o[mt][j] * inv);
+                dst[16 * mt + 8] = poisoned ? __float2bfloat16_rn(qnan) : __float2bfloat16_rn(o[mt][2 + j] * inv);
+            }
+        } else {
+            float* dst = p.part_o + (orow * p.np_max + d.part) * D + qr;
+#pragma unroll
+            for (int mt = 0; mt < NT; ++mt) {
+                __stcg(dst + 16 * mt, poisoned ? qnan : o[mt][j]);
+                __stcg(dst + 16 * mt + 8, poisoned ? qnan : o[mt][2 + j]);
+            }
+            if (qr == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(mh[j], lh[j]));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Multi-query item on tensor cores (mma.sync m16n8k16, bf16 in, fp32 acc).
 // Warp w serves kv head hw = w / wph of the group and its rows
 // [16 rw, 16 rw + 16), rw = w % wph, of the query tile (rows are (query,
@@ -761,18 +911,13 @@ __device__ __forceinline__ void consumer(Smem<D>& sm, const AttnParams& p, int w
         consumer_bar();  // okw is rewritten next item
         if (!go) break;
         const int ntiles = (d.t_end + kTileT - 1) / kTileT - d.t_begin / kTileT;
-        int R;
-        if constexpr (GD > 0) {
-            if (d.kind == KIND_DEC) {
-                decode_item<D, GD>(sm, p, d, warp, lane, g, ntiles, si, abort);
-                R = d.hps * GD;
-            } else {
-                mq_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
-                R = d.hps * d.nq * p.G;
-            }
-        } else {
+        const int R = d.hps * d.nq * p.G;
+        if (d.kind == KIND_DEC) {
+            decode_tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
+        } else if (d.kind == KIND_MQ) {
             mq_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
-            R = d.hps * d.nq * p.G;
+        } else {
+            if constexpr (GD > 0) decode_item<D, GD>(sm, p, d, warp, lane, g, ntiles, si, abort);
         }
         if (d.nparts > 1) ticket_and_merge<D>(sm, p, d, R, tid);
         consumer_bar();  // every warp is done with this item

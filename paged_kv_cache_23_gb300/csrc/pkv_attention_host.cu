@@ -32,10 +32,11 @@ struct SeqShape {
     int kind, hps, wph, qt;
 };
 
-__device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_ok) {
+// decode_fma: run q_len = 1 rows on the CUDA-core path (else tensor cores).
+__device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_fma) {
     SeqShape s;
-    if (ql == 1 && decode_ok) {
-        s.kind = KIND_DEC;
+    if (ql == 1 && G <= 8) {
+        s.kind = decode_fma ? KIND_DECF : KIND_DEC;
         s.hps = gcd_pow2(n_kv, kMaxHPS);
         s.wph = 1;
         s.qt = 1;
@@ -103,7 +104,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         if (b < pp.num_seqs) {
             const int L = pp.seq_lens[b], ql = pp.q_lens[b];
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
-            dec = sh.kind == KIND_DEC;
+            dec = sh.kind != KIND_MQ;
             const int ngroups = pp.n_kv / sh.hps;
             if (pp.seq_flag[b] == 0) {
                 if (dec) {
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         if (ql <= 0) continue;
         const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
         const int ngroups = pp.n_kv / sh.hps;
-        if (sh.kind == KIND_DEC) {
+        if (sh.kind != KIND_MQ) {
             const int np = ceil_div(L, pp.P);
             const int f0 = base_full + pp.seq_off1[b];
             for (int it = lane; it < (np - 1) * ngroups; it += 32) {
@@ -286,7 +287,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* aux = reinterpret_cast<int*>(ws + w.seqaux);
     const int GD = (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
-    const bool decode_ok = GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
+    const bool decode_fma = GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
 
     PlanParams pp{};
     pp.seq_lens = seq_lens;
@@ -311,7 +312,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     pp.max_blocks = max_blocks;
     pp.bs = block_size;
     pp.max_seq_len = max_seq_len;
-    pp.decode_ok = decode_ok ? 1 : 0;
+    pp.decode_ok = decode_fma ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     plan_kernel<<<1, kPlanThreads, 0, st>>>(pp);
     if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
@@ -337,6 +338,6 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     ap.P = P;
     ap.row_bytes = head_dim * 2;
     ap.scale_log2 = scale * 1.4426950408889634f;
-    if (head_dim == 128) return dispatch_attention_d128(decode_ok ? GD : 0, tm, ap, w.max_items, st);
-    return dispatch_attention_d64(decode_ok ? GD : 0, tm, ap, w.max_items, st);
+    if (head_dim == 128) return dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st);
+    return dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
 }
