@@ -14,8 +14,9 @@
 // How it runs on GB300 (sm_103a):
 //   * A planning kernel turns (seq_lens, q_lens) into per-sequence records and
 //     a list of 16-byte work items (sequence, partition, query tile, head
-//     group): multi-query items first, then full decode partitions, then
-//     partition tails; it also zeroes the merge tickets.
+//     group): multi-query items first, then every full decode partition, then
+//     the partition tails longest first, so the dynamic queue ends on short
+//     items.  It also records how many partitions each query row has.
 //   * The attention kernel is persistent, one CTA per SM: one producer warp and
 //     eight consumer warps.  A pipeline stage is 16 tokens of K and V for a
 //     group of kv heads of one block -- for the 8B shape all 8 heads, 32 KB of
@@ -23,20 +24,19 @@
 //     swizzle) into a 3-slot, 192 KB shared-memory ring.  A TMA-issuing thread
 //     sustains only a couple of copies per microsecond whatever their size, so
 //     copies have to be tens of KB for one producer warp to keep HBM busy.
-//   * Single-query rows (decode, q_len = 1) run on CUDA cores, one warp per kv
-//     head: the g query heads of the GQA group share each K/V tile; 8 lanes own
-//     one token's dot product (packed fp32x2 FMAs), a split-butterfly reduction
-//     leaves one head per lane pair, warp-shuffle max/sum for the online
-//     softmax.  A warp copies its head's slice into registers and releases the
-//     stage at once.
-//   * Multi-query rows (speculative k > 1, prefill chunks) run on tensor cores
-//     (mma.sync m16n8k16 bf16 -> fp32): rows are (query, head) pairs, 16 per
-//     warp; the warps of one kv head split its rows; S = Q K^T and O += P V
-//     from ldmatrix fragments of the swizzled stage; each row's causal limit
-//     is applied to the scores.
-//   * A partition's partial (O, m, l) goes to the workspace; the CTA that
-//     finishes the last partition of a group (an atomic ticket, no waiting)
-//     merges them in partition order, so results are deterministic.
+//   * Single-query rows (decode, q_len = 1) run on tensor cores (mma.sync
+//     m16n8k16 bf16 -> fp32), one warp per kv head, in the transposed form
+//     S^T = K Q^T: the 16 tokens of a stage on M, the g query heads of the GQA
+//     group on N, so g = 4 pads N = 8 rather than M = 16.  A CUDA-core variant
+//     (8 lanes per token, packed fp32x2 FMAs) is kept behind a flag.
+//   * Multi-query rows (speculative k > 1, prefill chunks) also run on tensor
+//     cores, rows = (query, head) pairs, 16 per warp; the warps of one kv head
+//     split its rows; each row's causal limit is applied to the scores.
+//   * Consumer warps run independently: each waits for its own stages and
+//     releases them as it finishes, with no CTA-wide barrier per item.
+//   * A partition's partial (O, m, l) goes to the workspace; a separate combine
+//     kernel, launched as a programmatic dependent of the attention kernel,
+//     merges the partials of each row in partition order (deterministic).
 #pragma once
 
 #include "pkv_common.cuh"
@@ -53,7 +53,7 @@ constexpr int kRingSlots = 3;
 constexpr int kSlots = 4;                   // item descriptors in flight
 constexpr int kMaxParts = 1024;             // partitions per sequence
 constexpr int kPlanThreads = 1024;
-constexpr int kMergeW = 2048;               // float2 merge weights in shared memory
+constexpr int kTailBuckets = 256;           // tail-length classes of the longest-first ordering
 
 // KIND_DEC: q_len = 1 rows on tensor cores; KIND_DECF: on CUDA cores; KIND_MQ: q_len > 1.
 enum { KIND_END = -1, KIND_DEC = 0, KIND_MQ = 1, KIND_DECF = 2 };
@@ -78,7 +78,6 @@ struct AttnParams {
     const int4* items;   // {b, part, qt, hg}
     const int4* seqs;    // {seq_len, q_len, first query row, kind | hps << 4 | wph << 8 | qt_len << 12}
     int* hdr;            // [0] item count, [1] queue head
-    int* tickets;        // [total_q * n_kv]
     float* part_o;       // [(row * n_q + h) * np_max + part][D]
     float2* part_ml;     // [(row * n_q + h) * np_max + part] = (m in log2 units, l)
     int32_t* status;
@@ -90,17 +89,12 @@ template <int D>
 struct Smem {
     static constexpr int kHalf = kTileT * kMaxHPS * D * 2;   // K (or V) bytes of one stage
     uint8_t kv[kRingSlots][2][kHalf];                        // [slot][K,V][rows of 128 B], swizzled
-    float2 W[kMergeW];                                       // merge weights
     float pbuf[kCWarps][kTileT * 8];                         // decode: p[token][head]
     Desc desc[kSlots];
     int poison[kSlots];
-    int okw[kCWarps];
-    int bcast;
     int abort;
     uint64_t full[kRingSlots], empty[kRingSlots], ifull[kSlots], iempty[kSlots];
 };
-
-__device__ __forceinline__ void consumer_bar() { named_bar(1, kCThreads); }
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -291,105 +285,6 @@ __device__ __forceinline__ float reduce8(float* v, int li) {
     split_step<(G > 1 ? G / 2 : 1)>(v, li, 2);
     split_step<(G > 2 ? G / 4 : 1)>(v, li, 1);
     return v[0];
-}
-
-// Output row of item row r: rows are [kv head of the group][query][q head].
-struct RowMap {
-    int G, nq, hps, n_q;
-    __device__ __forceinline__ long long orow(const Desc& d, int r) const {
-        const int per = nq * G;
-        const int hw = r / per, lr = r - hw * per;
-        const int qi = lr / G, hh = lr - qi * G;
-        const int kvh = d.hg * hps + hw;
-        return (long long)(d.q_row0 + qi) * n_q + (long long)kvh * G + hh;
-    }
-};
-
-// ---------------------------------------------------------------------------
-// Ticket and merge of the partial results of a group of partitions.  Called
-// by all consumer threads after the item's partials are written.
-// ---------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void ticket_and_merge(Smem<D>& sm, const AttnParams& p, const Desc& d, int R, int tid) {
-    constexpr int C8 = D / 8;
-    // every thread's partial stores happen before the barrier; the release
-    // fence of the signalling thread orders them before its ticket at GPU scope
-    consumer_bar();
-    if (tid == 0) {
-        __threadfence();
-        sm.bcast = atomicAdd(&p.tickets[(long long)d.q_row0 * p.n_kv + d.hg * d.hps], 1);
-    }
-    consumer_bar();
-    if (sm.bcast != d.nparts - 1) return;
-    __threadfence();
-    const RowMap rm{p.G, d.nq, d.hps, p.n_q};
-    const int np = d.nparts;
-    float2* W = sm.W;
-    if (R * np <= kMergeW) {
-        for (int e = tid; e < R * np; e += kCThreads) {
-            const int r = e / np, pp = e - r * np;
-            W[e] = __ldcg(p.part_ml + rm.orow(d, r) * p.np_max + pp);
-        }
-        consumer_bar();
-        for (int r = tid; r < R; r += kCThreads) {
-            float M = -INFINITY;
-            for (int pp = 0; pp < np; ++pp) M = fmaxf(M, W[r * np + pp].x);
-            const float mu = M == -INFINITY ? 0.f : M;
-            float L = 0.f;
-            for (int pp = 0; pp < np; ++pp) L += W[r * np + pp].y * exp2f(W[r * np + pp].x - mu);
-            const float invL = 1.0f / L;
-            for (int pp = 0; pp < np; ++pp) W[r * np + pp].x = exp2f(W[r * np + pp].x - mu) * invL;
-        }
-        consumer_bar();
-        for (int e = tid; e < R * C8; e += kCThreads) {
-            const int r = e / C8, c = (e - r * C8) * 8;
-            const long long orow = rm.orow(d, r);
-            float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            const float4* src = reinterpret_cast<const float4*>(p.part_o + (orow * p.np_max) * D + c);
-#pragma unroll 4
-            for (int pp = 0; pp < np; ++pp) {
-                const float w = W[r * np + pp].x;
-                const float4 a = __ldcg(src + (long long)pp * (D / 4));
-                const float4 b = __ldcg(src + (long long)pp * (D / 4) + 1);
-                acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-                acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
-            }
-            uint4 v;
-            v.x = float2_to_bf16x2(acc[0], acc[1]);
-            v.y = float2_to_bf16x2(acc[2], acc[3]);
-            v.z = float2_to_bf16x2(acc[4], acc[5]);
-            v.w = float2_to_bf16x2(acc[6], acc[7]);
-            *reinterpret_cast<uint4*>(p.out + orow * D + c) = v;
-        }
-    } else {
-        // many partitions: statistics straight from global memory
-        for (int e = tid; e < R * C8; e += kCThreads) {
-            const int r = e / C8, c = (e - r * C8) * 8;
-            const long long orow = rm.orow(d, r);
-            const float2* ml = p.part_ml + orow * p.np_max;
-            float M = -INFINITY;
-            for (int pp = 0; pp < np; ++pp) M = fmaxf(M, __ldcg(ml + pp).x);
-            const float mu = M == -INFINITY ? 0.f : M;
-            float L = 0.f, acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-            const float4* src = reinterpret_cast<const float4*>(p.part_o + (orow * p.np_max) * D + c);
-            for (int pp = 0; pp < np; ++pp) {
-                const float2 s = __ldcg(ml + pp);
-                const float w = exp2f(s.x - mu);
-                L += s.y * w;
-                const float4 a = __ldcg(src + (long long)pp * (D / 4));
-                const float4 b = __ldcg(src + (long long)pp * (D / 4) + 1);
-                acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-                acc[4] += w * b.x; acc[5] += w * b.y; acc[6] += w * b.z; acc[7] += w * b.w;
-            }
-            const float invL = 1.0f / L;
-            uint4 v;
-            v.x = float2_to_bf16x2(acc[0] * invL, acc[1] * invL);
-            v.y = float2_to_bf16x2(acc[2] * invL, acc[3] * invL);
-            v.z = float2_to_bf16x2(acc[4] * invL, acc[5] * invL);
-            v.w = float2_to_bf16x2(acc[6] * invL, acc[7] * invL);
-            *reinterpret_cast<uint4*>(p.out + orow * D + c) = v;
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -892,26 +787,112 @@ __device__ __forceinline__ void mq_item(Smem<D>& sm, const AttnParams& p, const 
 }
 
 // ---------------------------------------------------------------------------
+// Combine kernel: one warp per (query row, q head) whose row was split into
+// np > 1 partitions.  With M = max_p m_p and w_p = 2^(m_p - M),
+//   O = (sum_p w_p O_p) / (sum_p w_p l_p)
+// summed in partition order ("Chapter 31 Serving Efficiency", Example 31.2;
+// "Inference at Scale", section 07, Flash-Decoding's log-sum-exp merge).
+// ---------------------------------------------------------------------------
+struct CombineParams {
+    __nv_bfloat16* out;
+    const float* part_o;
+    const float2* part_ml;
+    const int* row_np;   // [total_q] partitions of each query row (0 or 1: nothing to merge)
+    int total_q, n_q, np_max;
+};
+
+constexpr int kCombineThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams c) {
+    constexpr int V = D / 32;  // output dims per lane (4 or 2)
+    pdl_wait();                // the attention grid has finished and its partials are visible
+    pdl_launch();
+    const int lane = threadIdx.x & 31;
+    const long long nwarps = (long long)gridDim.x * (kCombineThreads / 32);
+    const long long rows = (long long)c.total_q * c.n_q;
+    for (long long orow = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); orow < rows;
+         orow += nwarps) {
+        const int np = __ldg(c.row_np + orow / c.n_q);
+        if (np <= 1) continue;
+        const float2* ml = c.part_ml + orow * c.np_max;
+        float M = -INFINITY;
+        for (int pp = lane; pp < np; pp += 32) M = fmaxf(M, __ldcg(&ml[pp].x));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
+        const float mu = M == -INFINITY ? 0.f : M;
+        float acc[V];
+#pragma unroll
+        for (int j = 0; j < V; ++j) acc[j] = 0.f;
+        float L = 0.f;
+        const float* src = c.part_o + orow * c.np_max * D + lane * V;
+        for (int p0 = 0; p0 < np; p0 += 32) {
+            // lane j holds the weight of partition p0 + j
+            float w = 0.f, lw = 0.f;
+            if (p0 + lane < np) {
+                const float2 s = __ldcg(ml + p0 + lane);
+                w = exp2f(s.x - mu);
+                lw = s.y * w;
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) lw += __shfl_xor_sync(kFull, lw, o);
+            L += lw;
+            const int n = min(32, np - p0);
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) {
+                const float wj = __shfl_sync(kFull, w, j);
+                const float* sp = src + (long long)(p0 + j) * D;
+                if constexpr (V == 4) {
+                    const float4 a = __ldcg(reinterpret_cast<const float4*>(sp));
+                    acc[0] += wj * a.x;
+                    acc[1] += wj * a.y;
+                    acc[2] += wj * a.z;
+                    acc[3] += wj * a.w;
+                } else {
+                    const float2 a = __ldcg(reinterpret_cast<const float2*>(sp));
+                    acc[0] += wj * a.x;
+                    acc[1] += wj * a.y;
+                }
+            }
+        }
+        const float inv = 1.0f / L;
+        __nv_bfloat16* dst = c.out + orow * D + lane * V;
+        if constexpr (V == 4) {
+            uint2 v;
+            v.x = float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
+            v.y = float2_to_bf16x2(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2*>(dst) = v;
+        } else {
+            *reinterpret_cast<uint32_t*>(dst) = float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
+        }
+    }
+}
+
+template <int D>
+int launch_combine(const CombineParams& c, cudaStream_t st) {
+    const long long warps = (long long)c.total_q * c.n_q;
+    long long grid = (warps + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
+    const long long cap = (long long)host::sm_count() * 8;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    const cudaError_t e =
+        host::launch_pdl(combine_kernel<D>, dim3((unsigned)grid), dim3(kCombineThreads), 0, st, c);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
 // Consumer warps
 // ---------------------------------------------------------------------------
 template <int D, int GD>
 __device__ __forceinline__ void consumer(Smem<D>& sm, const AttnParams& p, int warp, int lane) {
     volatile int* abort = &sm.abort;
-    const int tid = warp * 32 + lane;
     uint32_t g = 0;
     for (int islot = 0;; ++islot) {
         const int si = islot % kSlots;
-        const bool ok = mbar_wait(&sm.ifull[si], (islot / kSlots) & 1, abort);
-        if (lane == 0) sm.okw[warp] = ok ? 1 : 0;
-        consumer_bar();
+        if (!mbar_wait(&sm.ifull[si], (islot / kSlots) & 1, abort)) break;  // timed out: abort is set
         const Desc d = sm.desc[si];
-        bool go = d.kind != KIND_END;
-#pragma unroll
-        for (int w = 0; w < kCWarps; ++w) go = go && sm.okw[w] != 0;
-        consumer_bar();  // okw is rewritten next item
-        if (!go) break;
+        if (d.kind == KIND_END) break;
         const int ntiles = (d.t_end + kTileT - 1) / kTileT - d.t_begin / kTileT;
-        const int R = d.hps * d.nq * p.G;
         if (d.kind == KIND_DEC) {
             decode_tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
         } else if (d.kind == KIND_MQ) {
@@ -919,9 +900,8 @@ __device__ __forceinline__ void consumer(Smem<D>& sm, const AttnParams& p, int w
         } else {
             if constexpr (GD > 0) decode_item<D, GD>(sm, p, d, warp, lane, g, ntiles, si, abort);
         }
-        if (d.nparts > 1) ticket_and_merge<D>(sm, p, d, R, tid);
-        consumer_bar();  // every warp is done with this item
-        if (lane == 0) mbar_arrive(&sm.iempty[si]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.iempty[si]);  // this warp is done with the descriptor
         g += (uint32_t)ntiles;
     }
 }
@@ -945,6 +925,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();    // the planning kernel's records are complete and visible
+    pdl_launch();  // the combine kernel may be scheduled; it waits for this grid to finish
     if (warp == kCWarps) {
         producer<D>(sm, &tm, p, lane);
     } else {
@@ -969,8 +951,9 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     long long grid = host::sm_count();
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
-    paged_attention_kernel<D, GD><<<(unsigned)grid, kThreads, smem, st>>>(tm, p);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const cudaError_t e =
+        host::launch_pdl(paged_attention_kernel<D, GD>, dim3((unsigned)grid), dim3(kThreads), smem, st, tm, p);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 template <int D>
@@ -986,5 +969,7 @@ int dispatch_g(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaS
 
 int dispatch_attention_d64(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
 int dispatch_attention_d128(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
+int combine_d64(const CombineParams& c, cudaStream_t st);
+int combine_d128(const CombineParams& c, cudaStream_t st);
 
 }  // namespace pkv

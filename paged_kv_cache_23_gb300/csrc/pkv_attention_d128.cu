@@ -1,8 +1,9 @@
-// pkv_attention_d128.cu -- paged attention kernels for head_dim 128.
+// pkv_attention_d128.cu -- paged attention and combine kernels for head_dim 128.
 #include "pkv_attention.cuh"
 
 namespace pkv {
 int dispatch_attention_d128(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st) {
     return dispatch_g<128>(GD, tm, p, mi, st);
 }
+int combine_d128(const CombineParams& c, cudaStream_t st) { return launch_combine<128>(c, st); }
 }  // namespace pkv

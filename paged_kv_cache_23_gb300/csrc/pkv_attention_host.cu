@@ -13,8 +13,7 @@ struct PlanParams {
     int* seq_q0;
     int* seq_flag;
     int* seq_off1;   // multi-query items: first item; decode: first full-partition item
-    int* seq_off2;   // decode: first tail item
-    int* tickets;
+    int* row_np;     // [total_q] partitions of each query row
     __nv_bfloat16* out;
     int32_t* status;
     int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, decode_ok;
@@ -62,21 +61,38 @@ __device__ __forceinline__ int mq_parts_of(int L, int ql, int QT, int P) {
     return n;
 }
 
+// Per-sequence values the planning passes share.
+struct SeqRec {
+    int L, ql, q0, flag, off1;
+};
+
 // Work list for one call: multi-query items first (the compute-heavy tiles
-// start early), then every full decode partition, then decode partition tails
-// (the short items last, so the dynamic queue ends evenly).
+// start early), then every full decode partition, then the decode partition
+// tails ordered longest first (counting sort over kTailBuckets length
+// classes), so the dynamic queue ends on the shortest items.  One thread owns
+// one sequence in every pass.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams pp) {
     __shared__ int tmp[32];
-    __shared__ int s_tot[2];
+    __shared__ int hist[kTailBuckets];
+    __shared__ int s_base[2];
     const int tid = threadIdx.x;
+    if (tid < kTailBuckets) hist[tid] = 0;
+    // the previous kernel in the stream (e.g. the KV append, or the last
+    // step's combine that still reads this workspace) must be complete
+    pdl_wait();
+    pdl_launch();
+    __syncthreads();
     int bits = 0;
-    // pass A: query row offsets and validity
+    SeqRec keep{0, 0, 0, 0, 0};  // this thread's sequence of the first chunk
+    // pass A: query rows, validity, item counts, per-sequence records
     long long carry = 0;
+    int c_mq = 0, c_full = 0;
     for (int base = 0; base < pp.num_seqs; base += kPlanThreads) {
         const int b = base + tid;
-        int qlc = 0, flag = 0;
+        int qlc = 0, flag = 0, L = 0, ql = 0;
         if (b < pp.num_seqs) {
-            const int L = pp.seq_lens[b], ql = pp.q_lens[b];
+            L = pp.seq_lens[b];
+            ql = pp.q_lens[b];
             if (L < 0 || (long long)L > (long long)pp.max_blocks * pp.bs || L > pp.max_seq_len)
                 flag |= PKV_STATUS_BAD_SEQLEN;
             if (ql < 0 || ql > L) flag |= PKV_STATUS_BAD_QLEN;
@@ -85,71 +101,77 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         }
         int tot;
         const int ex = block_exclusive_scan_1024(qlc, tmp, &tot);
-        if (b < pp.num_seqs) {
-            const long long q0 = carry + ex;
-            if (q0 + qlc > pp.total_q) flag |= PKV_STATUS_BAD_QLEN;  // rows would overflow q/out
-            pp.seq_q0[b] = (int)(q0 < pp.total_q ? q0 : pp.total_q);
-            pp.seq_flag[b] = flag;
-            bits |= flag;
-        }
-        carry += tot;
-    }
-    __syncthreads();
-    // pass B: item counts per class, per-sequence records
-    int c_mq = 0, c_full = 0, c_tail = 0;
-    for (int base = 0; base < pp.num_seqs; base += kPlanThreads) {
-        const int b = base + tid;
-        int nmq = 0, nfull = 0, ntail = 0;
+        int nmq = 0, nfull = 0, q0 = 0;
         bool dec = false;
         if (b < pp.num_seqs) {
-            const int L = pp.seq_lens[b], ql = pp.q_lens[b];
+            const long long q0l = carry + ex;
+            if (q0l + qlc > pp.total_q) flag |= PKV_STATUS_BAD_QLEN;  // rows would overflow q/out
+            q0 = (int)(q0l < pp.total_q ? q0l : pp.total_q);
+            bits |= flag;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
             dec = sh.kind != KIND_MQ;
             const int ngroups = pp.n_kv / sh.hps;
-            if (pp.seq_flag[b] == 0) {
+            if (flag == 0) {
                 if (dec) {
                     const int np = ceil_div(L, pp.P);
                     nfull = (np - 1) * ngroups;
-                    ntail = ngroups;
+                    const int tl = L - (np - 1) * pp.P;  // in [1, P]
+                    atomicAdd(&hist[(int)(((long long)(pp.P - tl) * kTailBuckets) / pp.P)], ngroups);
                 } else if (ql > 0) {
                     nmq = mq_parts_of(L, ql, sh.qt, pp.P) * ngroups;
                 }
             }
-            pp.seqs[b] = make_int4(L, ql, pp.seq_q0[b], sh.kind | (sh.hps << 4) | (sh.wph << 8) | (sh.qt << 12));
+            pp.seqs[b] = make_int4(L, ql, q0, sh.kind | (sh.hps << 4) | (sh.wph << 8) | (sh.qt << 12));
         }
-        int tm, tf, tt;
+        carry += tot;
+        int tm, tf;
         const int exm = block_exclusive_scan_1024(nmq, tmp, &tm);
         const int exf = block_exclusive_scan_1024(nfull, tmp, &tf);
-        const int ext = block_exclusive_scan_1024(ntail, tmp, &tt);
         if (b < pp.num_seqs) {
-            pp.seq_off1[b] = dec ? c_full + exf : c_mq + exm;
-            pp.seq_off2[b] = c_tail + ext;
+            const int off1 = dec ? c_full + exf : c_mq + exm;
+            if (base == 0) {
+                keep = SeqRec{L, ql, q0, flag, off1};
+            } else {
+                pp.seq_q0[b] = q0;
+                pp.seq_flag[b] = flag;
+                pp.seq_off1[b] = off1;
+            }
         }
         c_mq += tm;
         c_full += tf;
-        c_tail += tt;
+    }
+    // tail buckets -> first slot of each bucket (exclusive scan)
+    __syncthreads();
+    int c_tail;
+    {
+        const int v = tid < kTailBuckets ? hist[tid] : 0;
+        const int ex = block_exclusive_scan_1024(v, tmp, &c_tail);
+        if (tid < kTailBuckets) hist[tid] = c_mq + c_full + ex;
     }
     if (tid == 0) {
-        s_tot[0] = c_mq;
-        s_tot[1] = c_mq + c_full;
+        s_base[0] = c_mq;
         pp.hdr[0] = c_mq + c_full + c_tail;
         pp.hdr[1] = 0;
     }
-    for (long long i = tid; i < (long long)pp.total_q * pp.n_kv; i += kPlanThreads) pp.tickets[i] = 0;
+    // rows past the last sequence's queries belong to nobody: nothing to merge
+    for (long long r = carry + tid; r < pp.total_q; r += kPlanThreads) pp.row_np[r] = 0;
     __syncthreads();
-    const int base_full = s_tot[0], base_tail = s_tot[1];
-    const int warp = tid >> 5, lane = tid & 31;
-    for (int b = warp; b < pp.num_seqs; b += kPlanThreads / 32) {
-        const int flag = pp.seq_flag[b];
-        const int L = pp.seq_lens[b], ql = pp.q_lens[b];
-        const int q0 = pp.seq_q0[b];
-        if (flag) {
+    const int base_full = s_base[0];
+    // pass B: items and per-row partition counts, one thread per sequence
+    for (int base = 0; base < pp.num_seqs; base += kPlanThreads) {
+        const int b = base + tid;
+        if (b >= pp.num_seqs) break;
+        SeqRec r = keep;
+        if (base > 0) r = SeqRec{pp.seq_lens[b], pp.q_lens[b], pp.seq_q0[b], pp.seq_flag[b], pp.seq_off1[b]};
+        const int L = r.L, ql = r.ql, q0 = r.q0;
+        if (r.flag) {
             // rows of an invalid sequence are NaN (inside the q/out extent)
             const int qlc = ql > 0 ? min(ql, pp.total_q) : 0;
             const int rows = min(qlc, pp.total_q - q0);
             const long long n16 = (long long)rows * pp.n_q * pp.D / 8;
             uint4* o = reinterpret_cast<uint4*>(pp.out + (long long)q0 * pp.n_q * pp.D);
-            for (long long e = lane; e < n16; e += 32) o[e] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+            for (long long e = 0; e < n16; ++e) o[e] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+            for (int i = 0; i < rows; ++i) pp.row_np[q0 + i] = 0;
             continue;
         }
         if (ql <= 0) continue;
@@ -157,23 +179,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         const int ngroups = pp.n_kv / sh.hps;
         if (sh.kind != KIND_MQ) {
             const int np = ceil_div(L, pp.P);
-            const int f0 = base_full + pp.seq_off1[b];
-            for (int it = lane; it < (np - 1) * ngroups; it += 32) {
-                const int part = it / ngroups, hg = it - part * ngroups;
-                pp.items[f0 + it] = make_int4(b, part, 0, hg);
-            }
-            const int t0 = base_tail + pp.seq_off2[b];
-            for (int hg = lane; hg < ngroups; hg += 32) pp.items[t0 + hg] = make_int4(b, np - 1, 0, hg);
+            int4* f = pp.items + base_full + r.off1;
+            for (int part = 0; part < np - 1; ++part)
+                for (int hg = 0; hg < ngroups; ++hg) *f++ = make_int4(b, part, 0, hg);
+            const int tl = L - (np - 1) * pp.P;
+            const int t0 = atomicAdd(&hist[(int)(((long long)(pp.P - tl) * kTailBuckets) / pp.P)], ngroups);
+            for (int hg = 0; hg < ngroups; ++hg) pp.items[t0 + hg] = make_int4(b, np - 1, 0, hg);
+            pp.row_np[q0] = np;
         } else {
-            int base = pp.seq_off1[b];
+            int4* f = pp.items + r.off1;
             for (int qt = 0; qt * sh.qt < ql; ++qt) {
                 const int nq = min(sh.qt, ql - qt * sh.qt);
                 const int np = ceil_div(L - ql + qt * sh.qt + nq, pp.P);
-                for (int it = lane; it < np * ngroups; it += 32) {
-                    const int part = it / ngroups, hg = it - part * ngroups;
-                    pp.items[base + it] = make_int4(b, part, qt, hg);
-                }
-                base += np * ngroups;
+                for (int part = 0; part < np; ++part)
+                    for (int hg = 0; hg < ngroups; ++hg) *f++ = make_int4(b, part, qt, hg);
+                for (int i = 0; i < nq; ++i) pp.row_np[q0 + qt * sh.qt + i] = np;
             }
         }
     }
@@ -181,7 +201,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
 }
 
 struct WsLayout {
-    size_t hdr, items, seqs, seqaux, tickets, ml, o, total;
+    size_t hdr, items, seqs, seqaux, rownp, ml, o, total;
     long long max_items;
     int np_max;
 };
@@ -202,8 +222,8 @@ static WsLayout ws_layout(int num_seqs, int total_q, int n_q, int n_kv, int D, i
     off = align256(off + (size_t)num_seqs * sizeof(int4));
     w.seqaux = off;
     off = align256(off + (size_t)num_seqs * 4 * sizeof(int));
-    w.tickets = off;
-    off = align256(off + (size_t)total_q * n_kv * sizeof(int));
+    w.rownp = off;
+    off = align256(off + (size_t)total_q * sizeof(int));
     w.ml = off;
     off = align256(off + (size_t)total_q * n_q * w.np_max * sizeof(float2));
     w.o = off;
@@ -298,8 +318,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     pp.seq_q0 = aux;
     pp.seq_flag = aux + num_seqs;
     pp.seq_off1 = aux + 2 * num_seqs;
-    pp.seq_off2 = aux + 3 * num_seqs;
-    pp.tickets = reinterpret_cast<int*>(ws + w.tickets);
+    pp.row_np = reinterpret_cast<int*>(ws + w.rownp);
     pp.out = static_cast<__nv_bfloat16*>(out);
     pp.status = status;
     pp.num_seqs = num_seqs;
@@ -314,8 +333,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     pp.max_seq_len = max_seq_len;
     pp.decode_ok = decode_fma ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    plan_kernel<<<1, kPlanThreads, 0, st>>>(pp);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+    if (host::launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess) return PKV_ERR_CUDA;
 
     AttnParams ap{};
     ap.out = static_cast<__nv_bfloat16*>(out);
@@ -324,7 +342,6 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     ap.items = pp.items;
     ap.seqs = pp.seqs;
     ap.hdr = pp.hdr;
-    ap.tickets = pp.tickets;
     ap.part_o = reinterpret_cast<float*>(ws + w.o);
     ap.part_ml = reinterpret_cast<float2*>(ws + w.ml);
     ap.status = status;
@@ -338,6 +355,16 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     ap.P = P;
     ap.row_bytes = head_dim * 2;
     ap.scale_log2 = scale * 1.4426950408889634f;
-    if (head_dim == 128) return dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st);
-    return dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
+    const int rc2 = head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st)
+                                    : dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
+    if (rc2 != PKV_OK || w.np_max <= 1) return rc2;  // one partition per row: outputs are final
+    CombineParams cp{};
+    cp.out = ap.out;
+    cp.part_o = ap.part_o;
+    cp.part_ml = ap.part_ml;
+    cp.row_np = pp.row_np;
+    cp.total_q = total_q;
+    cp.n_q = num_q_heads;
+    cp.np_max = w.np_max;
+    return head_dim == 128 ? combine_d128(cp, st) : combine_d64(cp, st);
 }

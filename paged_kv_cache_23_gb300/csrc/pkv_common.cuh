@@ -94,6 +94,13 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
 }
 
 // ---- named barrier among the consumer warps --------------------------------
+// Programmatic dependent launch.  pdl_wait blocks until the previous kernel
+// in the stream has completed and its writes are visible (a no-op when the
+// kernel was launched without the attribute); pdl_launch lets the next
+// kernel's CTAs be scheduled before this one ends.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -14,7 +14,7 @@
 // once per device, by the first call made with that device current; make that
 // first call before any stream capture starts.  All calls share the array, and
 // it keeps whatever the last call left in it: the planning kernel re-initialises
-// everything it needs (item queue, merge tickets) on every call, but two calls
+// everything it needs (item queue, per-row partition counts) on every call, but two calls
 // that overlap on the GPU (different streams, or different host threads on the
 // same device without ordering) race on it and give wrong results.
 #include <mutex>

@@ -90,3 +90,36 @@ class DeviceStep:
         self.cache_ops(stream)
         self.attention(stream)
         self.accept(stream)
+
+
+def main(argv=None):
+    """Run a few steps of one workload (a small case for profilers):
+    ``python -m paged_kv_cache_23_gb300.runner --workload mix --batch 64 --steps 3``."""
+    import argparse
+
+    from . import workloads
+
+    ap = argparse.ArgumentParser(description=main.__doc__)
+    ap.add_argument("--workload", default="mix", choices=sorted(workloads.FULL))
+    ap.add_argument("--batch", type=int, default=0, help="batch size of the mix workload (0 = 256)")
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--partition", type=int, default=0)
+    ap.add_argument("--flags", type=int, default=0)
+    a = ap.parse_args(argv)
+    if a.workload == "mix" and a.batch:
+        w = workloads.mix(B=a.batch)
+    else:
+        w = workloads.FULL[a.workload]()
+    ds = DeviceStep(w, partition_tokens=a.partition or None, flags=a.flags)
+    for _ in range(a.steps):
+        ds.cache_ops()
+        ds.attention()
+        ds.accept()
+    torch.cuda.synchronize()
+    st = int(ds.status.item())
+    print(f"{a.workload}: {a.steps} steps, status {st}")
+    return 0 if st == 0 else 1
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())
