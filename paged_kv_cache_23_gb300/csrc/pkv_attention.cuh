@@ -51,6 +51,8 @@ constexpr int kThreads = kCThreads + 32;    // + producer warp
 constexpr int kMaxHPS = 8;                  // kv heads per stage
 constexpr int kRingSlots = 3;
 constexpr int kSlots = 4;                   // item descriptors in flight
+constexpr int kClaimAhead = 6;              // stages before an item's end at which the next is claimed
+constexpr float kRescaleSlack = 8.0f;       // lazy-rescale threshold of the running max, base-2 units
 constexpr int kMaxParts = 1024;             // partitions per sequence
 constexpr int kPlanThreads = 1024;
 constexpr int kTailBuckets = 256;           // tail-length classes of the longest-first ordering
@@ -191,8 +193,6 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
             mbar_arrive(&sm.ifull[si]);
         }
         if (end) break;
-        if (lane == 0) next = atomicAdd(&p.hdr[1], 1);  // next item, used after this one's stages
-        next = __shfl_sync(kFull, next, 0);
         const CUtensorMap* mk = &tm->k[log2i(d.hps)];
         const CUtensorMap* mv = &tm->v[log2i(d.hps)];
         const uint32_t op_bytes = (uint32_t)d.hps * bsr * D * 2;
@@ -203,7 +203,11 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
         int tab_base = tb * kTileT / p.bs;
         int tab = tab_base + lane < e_lim ? __ldg(bt + tab_base + lane) : 0;
         int tab_next = tab_base + 32 + lane < e_lim ? __ldg(bt + tab_base + 32 + lane) : 0;
+        // the next item is claimed a few stages before this one's last, so a
+        // CTA never holds a second item for long and the queue balances finely
+        const int i_claim = max(tb, te - kClaimAhead);
         for (int i = tb; i < te; ++i, ++g) {
+            if (i == i_claim && lane == 0) next = atomicAdd(&p.hdr[1], 1);
             const int t0 = i * kTileT;
             const int tvalid = min(kTileT, d.t_end - t0);
             const int e0 = t0 / p.bs;
@@ -248,6 +252,7 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
             __syncwarp();
         }
         if (stopped) break;
+        next = __shfl_sync(kFull, next, 0);
     }
     // drain: wait (bounded) until every issued stage has landed
     if (lane == 0) {
@@ -539,50 +544,70 @@ __device__ __forceinline__ void decode_tc_item(Smem<D>& sm, const AttnParams& p,
         const float s1 = va ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;
         const float s2 = vb8 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;
         const float s3 = vb8 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;
-        float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+        // The reference maxima m0, m1 move only when a new score exceeds them
+        // by more than kRescaleSlack (base-2 units), so most stages need no
+        // max reduction and no rescale of O; probabilities stay <= 2^slack.
+        // The softmax is unchanged: O and l are relative to the same m.
+        const bool fits = __all_sync(kFull, fmaxf(s0, s2) <= m0 + kRescaleSlack && fmaxf(s1, s3) <= m1 + kRescaleSlack);
+        if (!fits) {
+            float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
 #pragma unroll
-        for (int o8 = 4; o8 < 32; o8 <<= 1) {
-            x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, o8));
-            x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, o8));
+            for (int o8 = 4; o8 < 32; o8 <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, o8));
+                x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, o8));
+            }
+            const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+            const float c0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0), c1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+            l0 *= c0;
+            l1 *= c1;
+#pragma unroll
+            for (int mt = 0; mt < NT; ++mt) {
+                o[mt][0] *= c0;
+                o[mt][1] *= c1;
+                o[mt][2] *= c0;
+                o[mt][3] *= c1;
+            }
+            m0 = n0;
+            m1 = n1;
         }
-        const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-        const float u0 = n0 == -INFINITY ? 0.f : n0, u1 = n1 == -INFINITY ? 0.f : n1;
-        const float c0 = exp2f(m0 - u0), c1 = exp2f(m1 - u1);
+        const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
         const float p0 = exp2f(s0 - u0), p1 = exp2f(s1 - u1), p2 = exp2f(s2 - u0), p3 = exp2f(s3 - u1);
-        float y0 = p0 + p2, y1 = p1 + p3;
-#pragma unroll
-        for (int o8 = 4; o8 < 32; o8 <<= 1) {
-            y0 += __shfl_xor_sync(kFull, y0, o8);
-            y1 += __shfl_xor_sync(kFull, y1, o8);
-        }
-        l0 = l0 * c0 + y0;
-        l1 = l1 * c1 + y1;
-        m0 = n0;
-        m1 = n1;
-#pragma unroll
-        for (int mt = 0; mt < NT; ++mt) {
-            o[mt][0] *= c0;
-            o[mt][1] *= c1;
-            o[mt][2] *= c0;
-            o[mt][3] *= c1;
-        }
+        // l stays a per-lane partial sum (this lane's tokens); reduced once at the end
+        l0 += p0 + p2;
+        l1 += p1 + p3;
         const uint32_t pb0 = movmatrix_trans(float2_to_bf16x2(p0, p1));  // (tokens 2qd, 2qd+1; head qr)
         const uint32_t pb1 = movmatrix_trans(float2_to_bf16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; head qr)
-        // V rows past the valid tokens may hold anything (even NaN): zero them
-        const uint32_t klo = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t khi = (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (9 + 2 * qd < nvalid ? 0xffff0000u : 0u);
+        if (nvalid == kTileT) {
 #pragma unroll
-        for (int mt = 0; mt < NT; ++mt) {
-            const int chunk = 2 * mt + v_hi;
-            const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
-            mma_bf16_16816(o[mt], a0 & klo, a1 & klo, a2 & khi, a3 & khi, pb0, pb1);
+            for (int mt = 0; mt < NT; ++mt) {
+                const int chunk = 2 * mt + v_hi;
+                const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
+                mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
+            }
+        } else {
+            // V rows past the valid tokens may hold anything (even NaN): zero them
+            const uint32_t klo = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+            const uint32_t khi = (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (9 + 2 * qd < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int mt = 0; mt < NT; ++mt) {
+                const int chunk = 2 * mt + v_hi;
+                const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
+                mma_bf16_16816(o[mt], a0 & klo, a1 & klo, a2 & khi, a3 & khi, pb0, pb1);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
     }
     if (!active) return;
+#pragma unroll
+    for (int o8 = 4; o8 < 32; o8 <<= 1) {
+        l0 += __shfl_xor_sync(kFull, l0, o8);
+        l1 += __shfl_xor_sync(kFull, l1, o8);
+    }
     const bool poisoned = sm.poison[si] != 0;  // final after the last stage's wait
     const float qnan = __int_as_float(0x7fc00000);
     const float mh[2] = {m0, m1}, lh[2] = {l0, l1};
@@ -801,11 +826,12 @@ struct CombineParams {
     int total_q, n_q, np_max;
 };
 
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = 128;
 
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_constant__ CombineParams c) {
     constexpr int V = D / 32;  // output dims per lane (4 or 2)
+    constexpr int U = 8;       // partitions whose loads are in flight together
     pdl_wait();                // the attention grid has finished and its partials are visible
     pdl_launch();
     const int lane = threadIdx.x & 31;
@@ -816,6 +842,8 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
         const int np = __ldg(c.row_np + orow / c.n_q);
         if (np <= 1) continue;
         const float2* ml = c.part_ml + orow * c.np_max;
+        const float* src = c.part_o + orow * c.np_max * D + lane * V;
+        // statistics: lane j holds partitions j, j + 32, ...
         float M = -INFINITY;
         for (int pp = lane; pp < np; pp += 32) M = fmaxf(M, __ldcg(&ml[pp].x));
 #pragma unroll
@@ -825,36 +853,46 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
 #pragma unroll
         for (int j = 0; j < V; ++j) acc[j] = 0.f;
         float L = 0.f;
-        const float* src = c.part_o + orow * c.np_max * D + lane * V;
         for (int p0 = 0; p0 < np; p0 += 32) {
-            // lane j holds the weight of partition p0 + j
-            float w = 0.f, lw = 0.f;
+            float w = 0.f;
             if (p0 + lane < np) {
                 const float2 s = __ldcg(ml + p0 + lane);
                 w = exp2f(s.x - mu);
-                lw = s.y * w;
+                L += s.y * w;
             }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) lw += __shfl_xor_sync(kFull, lw, o);
-            L += lw;
             const int n = min(32, np - p0);
-#pragma unroll 4
-            for (int j = 0; j < n; ++j) {
-                const float wj = __shfl_sync(kFull, w, j);
-                const float* sp = src + (long long)(p0 + j) * D;
-                if constexpr (V == 4) {
-                    const float4 a = __ldcg(reinterpret_cast<const float4*>(sp));
-                    acc[0] += wj * a.x;
-                    acc[1] += wj * a.y;
-                    acc[2] += wj * a.z;
-                    acc[3] += wj * a.w;
-                } else {
-                    const float2 a = __ldcg(reinterpret_cast<const float2*>(sp));
-                    acc[0] += wj * a.x;
-                    acc[1] += wj * a.y;
+            for (int u0 = 0; u0 < n; u0 += U) {
+                // U partitions' loads in flight before any of them is used
+                float a[U][V];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    if (u0 + u < n) {
+                        const float* sp = src + (long long)(p0 + u0 + u) * D;
+                        if constexpr (V == 4) {
+                            const float4 t = __ldcg(reinterpret_cast<const float4*>(sp));
+                            a[u][0] = t.x;
+                            a[u][1] = t.y;
+                            a[u][2] = t.z;
+                            a[u][3] = t.w;
+                        } else {
+                            const float2 t = __ldcg(reinterpret_cast<const float2*>(sp));
+                            a[u][0] = t.x;
+                            a[u][1] = t.y;
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const float wu = __shfl_sync(kFull, w, (u0 + u) & 31);
+                    if (u0 + u < n) {
+#pragma unroll
+                        for (int j = 0; j < V; ++j) acc[j] += wu * a[u][j];
+                    }
                 }
             }
         }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(kFull, L, o);
         const float inv = 1.0f / L;
         __nv_bfloat16* dst = c.out + orow * D + lane * V;
         if constexpr (V == 4) {
@@ -872,7 +910,7 @@ template <int D>
 int launch_combine(const CombineParams& c, cudaStream_t st) {
     const long long warps = (long long)c.total_q * c.n_q;
     long long grid = (warps + kCombineThreads / 32 - 1) / (kCombineThreads / 32);
-    const long long cap = (long long)host::sm_count() * 8;
+    const long long cap = (long long)host::sm_count() * 16;
     if (grid > cap) grid = cap;
     if (grid < 1) grid = 1;
     const cudaError_t e =

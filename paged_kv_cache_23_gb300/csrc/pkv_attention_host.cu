@@ -10,9 +10,10 @@ struct PlanParams {
     int4* items;     // {b, part, qt, hg}
     int4* seqs;      // {seq_len, q_len, first query row, kind | hps << 4 | wph << 8 | qt_len << 12}
     int* hdr;
-    int* seq_q0;
-    int* seq_flag;
-    int* seq_off1;   // multi-query items: first item; decode: first full-partition item
+    int* seq_q0;     // first query row
+    int* seq_flag;   // PKV_STATUS_* bits of the sequence (0 = valid)
+    int* seq_mq;     // exclusive prefix of multi-query item counts
+    int* seq_full;   // exclusive prefix of full decode-partition item counts
     int* row_np;     // [total_q] partitions of each query row
     __nv_bfloat16* out;
     int32_t* status;
@@ -61,21 +62,38 @@ __device__ __forceinline__ int mq_parts_of(int L, int ql, int QT, int P) {
     return n;
 }
 
-// Per-sequence values the planning passes share.
-struct SeqRec {
-    int L, ql, q0, flag, off1;
-};
+// Largest i in [0, n) with a[i] <= x, for a non-decreasing a with a[0] <= x.
+__device__ __forceinline__ int last_le(const int* a, int n, int x) {
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a[mid] <= x) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+constexpr int kPlanSmemSeqs = 2048;  // batches up to this size search shared-memory copies
 
 // Work list for one call: multi-query items first (the compute-heavy tiles
 // start early), then every full decode partition, then the decode partition
 // tails ordered longest first (counting sort over kTailBuckets length
-// classes), so the dynamic queue ends on the shortest items.  One thread owns
-// one sequence in every pass.
+// classes), so the dynamic queue ends on the shortest items.
+//   pass A  one thread per sequence: validity, query rows, item counts and
+//           their prefix sums, tail-length histogram;
+//   pass B  items and per-row partition counts written over the item (row)
+//           index space, one thread per item (row), which finds its sequence
+//           by binary search in the prefix sums -- consecutive threads write
+//           consecutive 16-byte items, so the stores coalesce.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams pp) {
     __shared__ int tmp[32];
     __shared__ int hist[kTailBuckets];
-    __shared__ int s_base[2];
+    __shared__ int s_q0[kPlanSmemSeqs], s_mq[kPlanSmemSeqs], s_full[kPlanSmemSeqs];
     const int tid = threadIdx.x;
+    const int n = pp.num_seqs;
+    const bool small = n <= kPlanSmemSeqs;
+    int* a_q0 = small ? s_q0 : pp.seq_q0;
+    int* a_mq = small ? s_mq : pp.seq_mq;
+    int* a_full = small ? s_full : pp.seq_full;
     if (tid < kTailBuckets) hist[tid] = 0;
     // the previous kernel in the stream (e.g. the KV append, or the last
     // step's combine that still reads this workspace) must be complete
@@ -83,14 +101,13 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     pdl_launch();
     __syncthreads();
     int bits = 0;
-    SeqRec keep{0, 0, 0, 0, 0};  // this thread's sequence of the first chunk
-    // pass A: query rows, validity, item counts, per-sequence records
+    // pass A
     long long carry = 0;
     int c_mq = 0, c_full = 0;
-    for (int base = 0; base < pp.num_seqs; base += kPlanThreads) {
+    for (int base = 0; base < n; base += kPlanThreads) {
         const int b = base + tid;
         int qlc = 0, flag = 0, L = 0, ql = 0;
-        if (b < pp.num_seqs) {
+        if (b < n) {
             L = pp.seq_lens[b];
             ql = pp.q_lens[b];
             if (L < 0 || (long long)L > (long long)pp.max_blocks * pp.bs || L > pp.max_seq_len)
@@ -102,17 +119,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         int tot;
         const int ex = block_exclusive_scan_1024(qlc, tmp, &tot);
         int nmq = 0, nfull = 0, q0 = 0;
-        bool dec = false;
-        if (b < pp.num_seqs) {
+        if (b < n) {
             const long long q0l = carry + ex;
             if (q0l + qlc > pp.total_q) flag |= PKV_STATUS_BAD_QLEN;  // rows would overflow q/out
             q0 = (int)(q0l < pp.total_q ? q0l : pp.total_q);
             bits |= flag;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
-            dec = sh.kind != KIND_MQ;
             const int ngroups = pp.n_kv / sh.hps;
             if (flag == 0) {
-                if (dec) {
+                if (sh.kind != KIND_MQ) {
                     const int np = ceil_div(L, pp.P);
                     nfull = (np - 1) * ngroups;
                     const int tl = L - (np - 1) * pp.P;  // in [1, P]
@@ -122,20 +137,16 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
                 }
             }
             pp.seqs[b] = make_int4(L, ql, q0, sh.kind | (sh.hps << 4) | (sh.wph << 8) | (sh.qt << 12));
+            pp.seq_flag[b] = flag;
         }
         carry += tot;
         int tm, tf;
         const int exm = block_exclusive_scan_1024(nmq, tmp, &tm);
         const int exf = block_exclusive_scan_1024(nfull, tmp, &tf);
-        if (b < pp.num_seqs) {
-            const int off1 = dec ? c_full + exf : c_mq + exm;
-            if (base == 0) {
-                keep = SeqRec{L, ql, q0, flag, off1};
-            } else {
-                pp.seq_q0[b] = q0;
-                pp.seq_flag[b] = flag;
-                pp.seq_off1[b] = off1;
-            }
+        if (b < n) {
+            a_q0[b] = q0;
+            a_mq[b] = c_mq + exm;
+            a_full[b] = c_full + exf;
         }
         c_mq += tm;
         c_full += tf;
@@ -149,53 +160,78 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         if (tid < kTailBuckets) hist[tid] = c_mq + c_full + ex;
     }
     if (tid == 0) {
-        s_base[0] = c_mq;
         pp.hdr[0] = c_mq + c_full + c_tail;
         pp.hdr[1] = 0;
     }
-    // rows past the last sequence's queries belong to nobody: nothing to merge
-    for (long long r = carry + tid; r < pp.total_q; r += kPlanThreads) pp.row_np[r] = 0;
     __syncthreads();
-    const int base_full = s_base[0];
-    // pass B: items and per-row partition counts, one thread per sequence
-    for (int base = 0; base < pp.num_seqs; base += kPlanThreads) {
-        const int b = base + tid;
-        if (b >= pp.num_seqs) break;
-        SeqRec r = keep;
-        if (base > 0) r = SeqRec{pp.seq_lens[b], pp.q_lens[b], pp.seq_q0[b], pp.seq_flag[b], pp.seq_off1[b]};
-        const int L = r.L, ql = r.ql, q0 = r.q0;
-        if (r.flag) {
+    // pass B1: one thread per sequence -- decode tails and invalid sequences
+    for (int b = tid; b < n; b += kPlanThreads) {
+        const int4 sq = pp.seqs[b];
+        const int L = sq.x, ql = sq.y, q0 = sq.z;
+        if (pp.seq_flag[b]) {
             // rows of an invalid sequence are NaN (inside the q/out extent)
             const int qlc = ql > 0 ? min(ql, pp.total_q) : 0;
             const int rows = min(qlc, pp.total_q - q0);
             const long long n16 = (long long)rows * pp.n_q * pp.D / 8;
             uint4* o = reinterpret_cast<uint4*>(pp.out + (long long)q0 * pp.n_q * pp.D);
             for (long long e = 0; e < n16; ++e) o[e] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-            for (int i = 0; i < rows; ++i) pp.row_np[q0 + i] = 0;
             continue;
         }
-        if (ql <= 0) continue;
-        const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
-        const int ngroups = pp.n_kv / sh.hps;
-        if (sh.kind != KIND_MQ) {
-            const int np = ceil_div(L, pp.P);
-            int4* f = pp.items + base_full + r.off1;
-            for (int part = 0; part < np - 1; ++part)
-                for (int hg = 0; hg < ngroups; ++hg) *f++ = make_int4(b, part, 0, hg);
-            const int tl = L - (np - 1) * pp.P;
-            const int t0 = atomicAdd(&hist[(int)(((long long)(pp.P - tl) * kTailBuckets) / pp.P)], ngroups);
-            for (int hg = 0; hg < ngroups; ++hg) pp.items[t0 + hg] = make_int4(b, np - 1, 0, hg);
-            pp.row_np[q0] = np;
-        } else {
-            int4* f = pp.items + r.off1;
-            for (int qt = 0; qt * sh.qt < ql; ++qt) {
-                const int nq = min(sh.qt, ql - qt * sh.qt);
-                const int np = ceil_div(L - ql + qt * sh.qt + nq, pp.P);
-                for (int part = 0; part < np; ++part)
-                    for (int hg = 0; hg < ngroups; ++hg) *f++ = make_int4(b, part, qt, hg);
-                for (int i = 0; i < nq; ++i) pp.row_np[q0 + qt * sh.qt + i] = np;
+        if (ql <= 0 || (sq.w & 15) == KIND_MQ) continue;
+        const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
+        const int np = ceil_div(L, pp.P);
+        const int tl = L - (np - 1) * pp.P;
+        const int t0 = atomicAdd(&hist[(int)(((long long)(pp.P - tl) * kTailBuckets) / pp.P)], ngroups);
+        for (int hg = 0; hg < ngroups; ++hg) pp.items[t0 + hg] = make_int4(b, np - 1, 0, hg);
+    }
+    // pass B2: multi-query items
+    for (int it = tid; it < c_mq; it += kPlanThreads) {
+        const int b = last_le(a_mq, n, it);
+        int li = it - a_mq[b];
+        const int4 sq = pp.seqs[b];
+        const int L = sq.x, ql = sq.y, QT = (sq.w >> 12) & 4095;
+        const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
+        for (int qt = 0; qt * QT < ql; ++qt) {
+            const int nq = min(QT, ql - qt * QT);
+            const int cnt = ceil_div(L - ql + qt * QT + nq, pp.P) * ngroups;
+            if (li < cnt) {
+                const int part = li / ngroups;
+                pp.items[it] = make_int4(b, part, qt, li - part * ngroups);
+                break;
+            }
+            li -= cnt;
+        }
+    }
+    // pass B3: full decode partitions
+    {
+        const int ngroups = pp.n_kv / gcd_pow2(pp.n_kv, kMaxHPS);
+        for (int it = tid; it < c_full; it += kPlanThreads) {
+            const int b = last_le(a_full, n, it);
+            const int li = it - a_full[b];
+            const int part = li / ngroups;
+            pp.items[c_mq + it] = make_int4(b, part, 0, li - part * ngroups);
+        }
+    }
+    // pass B4: partitions per query row (0 for rows of invalid sequences and
+    // rows past the last sequence's queries: nothing to merge)
+    for (int r = tid; r < pp.total_q; r += kPlanThreads) {
+        int np = 0;
+        if (r < carry) {
+            const int b = last_le(a_q0, n, r);
+            const int4 sq = pp.seqs[b];
+            const int L = sq.x, ql = sq.y, q0 = sq.z;
+            if (pp.seq_flag[b] == 0 && r - q0 < ql) {
+                if ((sq.w & 15) != KIND_MQ) {
+                    np = ceil_div(L, pp.P);
+                } else {
+                    const int QT = (sq.w >> 12) & 4095;
+                    const int qt = (r - q0) / QT;
+                    const int nq = min(QT, ql - qt * QT);
+                    np = ceil_div(L - ql + qt * QT + nq, pp.P);
+                }
             }
         }
+        pp.row_np[r] = np;
     }
     if (bits) report(pp.status, bits);
 }
@@ -317,7 +353,8 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     pp.hdr = reinterpret_cast<int*>(ws + w.hdr);
     pp.seq_q0 = aux;
     pp.seq_flag = aux + num_seqs;
-    pp.seq_off1 = aux + 2 * num_seqs;
+    pp.seq_mq = aux + 2 * num_seqs;
+    pp.seq_full = aux + 3 * num_seqs;
     pp.row_np = reinterpret_cast<int*>(ws + w.rownp);
     pp.out = static_cast<__nv_bfloat16*>(out);
     pp.status = status;
