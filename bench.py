@@ -263,6 +263,7 @@ def run_gpu(args):
     attn_ms = [a.elapsed_time(z) for a, z in ev]
     ms_step = aggregate_max(total_ms, ws, device) / args.steps
     st = int(ds.status.item())
+    chosen_P = int(ds.workspace[8:12].view(torch.int32).item())  # partition length the planning kernel used
 
     # end to end through the public API: pinned host inputs -> device, step, result -> host
     e2e = end_to_end(ds, w, args, stream, device, ws)
@@ -281,7 +282,7 @@ def run_gpu(args):
             "config": {"workload": WORKLOAD, "global_batch": 256 * ws, "seq_len": "log-normal median 1024",
                        "parallelism": f"replicas x{ws} (independent batches)" if ws > 1 else "single GPU",
                        "l2": "inputs larger than L2 (~1.2 GB unique K/V per step vs 126 MB L2); no flush",
-                       "partition_tokens": ds.partition_tokens, "flags": ds.flags},
+                       "partition_tokens": ds.partition_tokens or f"auto ({chosen_P})", "flags": ds.flags},
             "seq_steps_per_s": seqs_all / (ms_step / 1e3),
             "kv_bytes_per_step": {"unique": b["kv_unique"], "logical": b["kv_logical"],
                                   "step_unique": b["step_unique"]},
@@ -290,7 +291,7 @@ def run_gpu(args):
                          "kernel": "pkv_paged_attention_decode (plan + attention kernels)",
                          "peak_kind": peak_kind, "attention_ms": attn_avg,
                          "frac_of_nominal_8tbs": achieved / 8000.0},
-            "clocks": clocks, "e2e": e2e, "gpu_launches": 5 * args.steps, "status": st, "parity": parity}
+            "clocks": clocks, "e2e": e2e, "gpu_launches": ds.launches_per_step() * args.steps, "status": st, "parity": parity}
     if rank == 0:
         line["cpu_baseline"] = cpu_baseline(w, b)
     print(json.dumps(line), flush=True)
@@ -322,22 +323,23 @@ def spot_check(w, ds, device):
 
 
 def end_to_end(ds, w, args, stream, device, ws):
+    """The step through the public API from pinned host memory: one upload
+    of every per-step input, the step, and the output read back."""
     import torch
-    host = {}
-    for name in ("q", "k_new", "v_new", "block_tables", "seq_lens", "q_lens", "append_lens", "cow"):
-        t = getattr(ds, name)
-        host[name] = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        host[name].copy_(t.cpu())
+    host = ds.pinned_inputs()
     out_host = torch.empty(ds.out.shape, dtype=ds.out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = host.numel()
     d2h = out_host.numel() * out_host.element_size()
     steps = max(1, args.steps // 2)
-    for _ in range(2):
-        for n, t in host.items():
-            getattr(ds, n).copy_(t, non_blocking=True)
+
+    def one():
+        ds.upload(host, stream)
         ds.cache_ops(stream)
         ds.attention(stream)
         out_host.copy_(ds.out, non_blocking=True)
+
+    for _ in range(2):
+        one()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     z = torch.cuda.Event(enable_timing=True)
@@ -346,11 +348,7 @@ def end_to_end(ds, w, args, stream, device, ws):
     torch.cuda.synchronize()
     a.record(stream)
     for _ in range(steps):
-        for n, t in host.items():
-            getattr(ds, n).copy_(t, non_blocking=True)
-        ds.cache_ops(stream)
-        ds.attention(stream)
-        out_host.copy_(ds.out, non_blocking=True)
+        one()
     z.record(stream)
     torch.cuda.synchronize()
     ms = aggregate_max(a.elapsed_time(z), ws, device) / steps

@@ -139,8 +139,11 @@ int pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_c
                   int num_kv_heads, int head_dim, int32_t* status, void* stream);
 
 /*
- * Partition length pkv_paged_attention_decode uses when partition_tokens is
- * 0, for a batch of num_seqs sequences no longer than max_seq_len.
+ * Smallest partition length pkv_paged_attention_decode uses when
+ * partition_tokens is 0, for a batch of num_seqs sequences no longer than
+ * max_seq_len (512, doubled while a sequence would have more than 1024
+ * partitions).  It sizes the workspace; the call itself may take a longer
+ * partition (see partition_tokens below).
  */
 int pkv_attention_auto_partition(int num_seqs, int total_q, int num_kv_heads, int max_seq_len);
 
@@ -178,8 +181,13 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *   max_seq_len   host bound on every seq_len (sizes the workspace)
  *   head_dim      64 or 128; block_size a power of two in [1, 256];
  *                 g = num_q_heads / num_kv_heads an integer in [1, 64]
- *   partition_tokens  multiple of 16, or 0 for pkv_attention_auto_partition;
- *                 at most 1024 partitions per sequence
+ *   partition_tokens  multiple of 16, at most 1024 partitions per sequence;
+ *                 or 0: automatic -- the planning kernel starts from
+ *                 pkv_attention_auto_partition(...) and doubles it (up to
+ *                 8192) while the batch would give more than 3 partitions
+ *                 per SM (fewer, longer partitions cost fewer partial
+ *                 results); the length used is the int at byte offset 8 of
+ *                 the workspace after the call
  *   flags         0, or PKV_ATTN_DECODE_CUDA_CORES (q_len = 1 rows on the
  *                 CUDA-core FMA path; by default every row uses the tensor
  *                 cores, measured faster on GB300)

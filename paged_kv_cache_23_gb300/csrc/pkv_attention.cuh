@@ -79,11 +79,11 @@ struct AttnParams {
     const int32_t* block_tables;
     const int4* items;   // {b, part, qt, hg}
     const int4* seqs;    // {seq_len, q_len, first query row, kind | hps << 4 | wph << 8 | qt_len << 12}
-    int* hdr;            // [0] item count, [1] queue head
+    int* hdr;            // [0] item count, [1] queue head, [2] partition length
     float* part_o;       // [(row * n_q + h) * np_max + part][D]
     float2* part_ml;     // [(row * n_q + h) * np_max + part] = (m in log2 units, l)
     int32_t* status;
-    int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, P, row_bytes;
+    int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, row_bytes;
     float scale_log2;    // scale * log2(e): scores live in base-2 units
 };
 
@@ -128,7 +128,7 @@ __device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* m
 
 // Work-item record -> descriptor (the same arithmetic the planning kernel used
 // to count items).
-__device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, const AttnParams& p) {
+__device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, int P) {
     Desc d;
     d.b = it.x;
     d.part = it.y;
@@ -148,9 +148,9 @@ __device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, const At
         d.t_vis = L - ql + qt * QT + d.nq;
         d.q_row0 = q0 + qt * QT;
     }
-    d.nparts = ceil_div(d.t_vis, p.P);
-    d.t_begin = d.part * p.P;
-    d.t_end = min(d.t_begin + p.P, d.t_vis);
+    d.nparts = ceil_div(d.t_vis, P);
+    d.t_begin = d.part * P;
+    d.t_end = min(d.t_begin + P, d.t_vis);
     return d;
 }
 
@@ -166,6 +166,7 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
         prefetch_tmap(&tm->v[lane]);
     }
     const int num_items = p.hdr[0];
+    const int P = p.hdr[2];  // partition length the planning kernel chose
     const int bsr = p.bs < kTileT ? p.bs : kTileT;
     int next = 0;
     if (lane == 0) next = atomicAdd(&p.hdr[1], 1);
@@ -179,7 +180,7 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
         if (!end) {
             const int4 it = __ldg(p.items + cur);
             const int4 sq = __ldg(p.seqs + it.x);
-            d = make_desc(it, sq, p);
+            d = make_desc(it, sq, P);
         } else {
             d = Desc{0, 0, 1, 0, 0, 0, 0, 0, 0, KIND_END, 1, 1};
         }

@@ -18,6 +18,8 @@ struct PlanParams {
     __nv_bfloat16* out;
     int32_t* status;
     int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, decode_ok;
+    int adapt_P;     // 1: P is a floor; the planning kernel may double it
+    int sms;         // SM count (persistent CTAs of the attention kernel)
 };
 
 __host__ __device__ inline int gcd_pow2(int n, int m) {  // largest power of two <= m dividing n (m a power of 2)
@@ -73,6 +75,8 @@ __device__ __forceinline__ int last_le(const int* a, int n, int x) {
 }
 
 constexpr int kPlanSmemSeqs = 2048;  // batches up to this size search shared-memory copies
+constexpr int kAutoPMax = 8192;       // automatic partition length: upper bound
+constexpr int kAutoItemsPerSM = 3;    // automatic partition length: target partitions per SM
 
 // Work list for one call: multi-query items first (the compute-heavy tiles
 // start early), then every full decode partition, then the decode partition
@@ -99,6 +103,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     // step's combine that still reads this workspace) must be complete
     pdl_wait();
     pdl_launch();
+    int P = pp.P;
+    if (pp.adapt_P) {
+        // automatic partition length: the floor P, doubled (up to kAutoPMax)
+        // while the batch would give more than kAutoItemsPerSM partitions per
+        // SM -- fewer, longer items cost fewer partial results and item
+        // switches, and the longest-first order keeps the queue balanced
+        long long tok = 0;
+        for (int b = tid; b < n; b += kPlanThreads) {
+            const int L = pp.seq_lens[b], ql = pp.q_lens[b];
+            if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len) continue;
+            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
+            tok += (long long)L * (pp.n_kv / sh.hps) * (sh.kind == KIND_MQ ? ceil_div(ql, sh.qt) : 1);
+        }
+        // block sum in units of 16 tokens (fits an int for any accepted batch)
+        int tot16;
+        block_exclusive_scan_1024((int)min(tok >> 4, (long long)(1 << 30) / kPlanThreads), tmp, &tot16);
+        const long long T = (long long)tot16 << 4;
+        while (P < kAutoPMax && T > (long long)P * kAutoItemsPerSM * pp.sms) P <<= 1;
+    }
+    if (tid == 0) pp.hdr[2] = P;
     __syncthreads();
     int bits = 0;
     // pass A
@@ -128,12 +152,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             const int ngroups = pp.n_kv / sh.hps;
             if (flag == 0) {
                 if (sh.kind != KIND_MQ) {
-                    const int np = ceil_div(L, pp.P);
+                    const int np = ceil_div(L, P);
                     nfull = (np - 1) * ngroups;
-                    const int tl = L - (np - 1) * pp.P;  // in [1, P]
-                    atomicAdd(&hist[(int)(((long long)(pp.P - tl) * kTailBuckets) / pp.P)], ngroups);
+                    const int tl = L - (np - 1) * P;  // in [1, P]
+                    atomicAdd(&hist[(int)(((long long)(P - tl) * kTailBuckets) / P)], ngroups);
                 } else if (ql > 0) {
-                    nmq = mq_parts_of(L, ql, sh.qt, pp.P) * ngroups;
+                    nmq = mq_parts_of(L, ql, sh.qt, P) * ngroups;
                 }
             }
             pp.seqs[b] = make_int4(L, ql, q0, sh.kind | (sh.hps << 4) | (sh.wph << 8) | (sh.qt << 12));
@@ -179,9 +203,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         }
         if (ql <= 0 || (sq.w & 15) == KIND_MQ) continue;
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
-        const int np = ceil_div(L, pp.P);
-        const int tl = L - (np - 1) * pp.P;
-        const int t0 = atomicAdd(&hist[(int)(((long long)(pp.P - tl) * kTailBuckets) / pp.P)], ngroups);
+        const int np = ceil_div(L, P);
+        const int tl = L - (np - 1) * P;
+        const int t0 = atomicAdd(&hist[(int)(((long long)(P - tl) * kTailBuckets) / P)], ngroups);
         for (int hg = 0; hg < ngroups; ++hg) pp.items[t0 + hg] = make_int4(b, np - 1, 0, hg);
     }
     // pass B2: multi-query items
@@ -193,7 +217,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
         for (int qt = 0; qt * QT < ql; ++qt) {
             const int nq = min(QT, ql - qt * QT);
-            const int cnt = ceil_div(L - ql + qt * QT + nq, pp.P) * ngroups;
+            const int cnt = ceil_div(L - ql + qt * QT + nq, P) * ngroups;
             if (li < cnt) {
                 const int part = li / ngroups;
                 pp.items[it] = make_int4(b, part, qt, li - part * ngroups);
@@ -222,12 +246,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             const int L = sq.x, ql = sq.y, q0 = sq.z;
             if (pp.seq_flag[b] == 0 && r - q0 < ql) {
                 if ((sq.w & 15) != KIND_MQ) {
-                    np = ceil_div(L, pp.P);
+                    np = ceil_div(L, P);
                 } else {
                     const int QT = (sq.w >> 12) & 4095;
                     const int qt = (r - q0) / QT;
                     const int nq = min(QT, ql - qt * QT);
-                    np = ceil_div(L - ql + qt * QT + nq, pp.P);
+                    np = ceil_div(L - ql + qt * QT + nq, P);
                 }
             }
         }
@@ -369,6 +393,8 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     pp.bs = block_size;
     pp.max_seq_len = max_seq_len;
     pp.decode_ok = decode_fma ? 1 : 0;
+    pp.adapt_P = partition_tokens == 0 ? 1 : 0;
+    pp.sms = host::sm_count();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (host::launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess) return PKV_ERR_CUDA;
 
@@ -389,7 +415,6 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     ap.bs = block_size;
     ap.num_blocks = num_blocks;
     ap.np_max = w.np_max;
-    ap.P = P;
     ap.row_bytes = head_dim * 2;
     ap.scale_log2 = scale * 1.4426950408889634f;
     const int rc2 = head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st)

@@ -11,7 +11,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (attention_workspace_bytes, copy_blocks, kv_append, paged_attention_decode, slot_mapping,
+from . import (attention_auto_partition, attention_workspace_bytes, copy_blocks, kv_append, paged_attention_decode, slot_mapping,
                spec_accept_greedy)
 
 
@@ -33,15 +33,28 @@ class DeviceStep:
         dev = self.device
         self.k_cache = to_device_bf16(w.k_cache, dev)
         self.v_cache = to_device_bf16(w.v_cache, dev)
-        self.k_init = None
-        self.block_tables = torch.from_numpy(w.block_tables).to(dev)
-        self.seq_lens = torch.from_numpy(w.seq_lens).to(dev)
-        self.q_lens = torch.from_numpy(w.q_lens).to(dev)
-        self.append_lens = torch.from_numpy(w.append_lens).to(dev)
-        self.k_new = to_device_bf16(w.k_new, dev)
-        self.v_new = to_device_bf16(w.v_new, dev)
-        self.cow = torch.from_numpy(np.ascontiguousarray(w.cow, np.int32)).to(dev)
-        self.q = to_device_bf16(w.q, dev)
+        # the per-step inputs live in one device arena (256-byte aligned
+        # slices), so a step's host -> device upload is a single copy
+        parts = [("q", w.q, torch.bfloat16), ("k_new", w.k_new, torch.bfloat16),
+                 ("v_new", w.v_new, torch.bfloat16), ("block_tables", w.block_tables, torch.int32),
+                 ("seq_lens", w.seq_lens, torch.int32), ("q_lens", w.q_lens, torch.int32),
+                 ("append_lens", w.append_lens, torch.int32),
+                 ("cow", np.ascontiguousarray(w.cow, np.int32).reshape(-1, 2), torch.int32)]
+        layout, off = [], 0
+        for name, arr, dt in parts:
+            nbytes = int(arr.nbytes)
+            layout.append((name, off, nbytes, tuple(arr.shape), dt))
+            off += (nbytes + 255) // 256 * 256
+        self.arena_bytes = max(off, 256)
+        host = torch.empty(self.arena_bytes, dtype=torch.uint8)
+        hv = host.numpy()
+        for (name, o, nbytes, shape, dt), (_, arr, _) in zip(layout, parts):
+            hv[o:o + nbytes] = np.ascontiguousarray(arr).view(np.uint8).reshape(-1)
+        self.arena = host.to(dev)
+        self._layout = layout
+        self._host_arena = host
+        for name, o, nbytes, shape, dt in layout:
+            setattr(self, name, self.arena[o:o + nbytes].view(dt).view(shape))
         self.n_slots = int(w.append_lens.sum())
         self.slots = torch.empty(max(self.n_slots, 1), dtype=torch.int64, device=dev)[: self.n_slots]
         self.out = torch.empty((w.total_q, w.n_q, w.head_dim), dtype=torch.bfloat16, device=dev)
@@ -60,6 +73,27 @@ class DeviceStep:
             self.argmax = torch.empty((B, k1), dtype=torch.int32, device=dev)
             self.accepted = torch.empty(B, dtype=torch.int32, device=dev)
             self.next_token = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def launches_per_step(self) -> int:
+        """Kernels one step() launches: copy_blocks, slot_mapping + kv_append,
+        plan + attention (+ combine when a row can span partitions), and the
+        two acceptance kernels."""
+        n = (1 if self.cow.numel() else 0) + (2 if self.n_slots else 0) + 2
+        np_max = -(-self.max_seq_len // max(self.partition_tokens or attention_auto_partition(
+            self.w.num_seqs, self.w.total_q, self.w.n_kv, self.max_seq_len), 1))
+        n += 1 if np_max > 1 else 0
+        return n + (2 if self.spec else 0)
+
+    def pinned_inputs(self) -> torch.Tensor:
+        """The step's inputs as one pinned host buffer in the arena layout."""
+        return self._host_arena.pin_memory()
+
+    def upload(self, host: torch.Tensor, stream=None):
+        """One host -> device copy of every per-step input (q, new K/V rows,
+        block tables, lengths, copy-on-write pairs)."""
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        with torch.cuda.stream(s):
+            self.arena.copy_(host, non_blocking=True)
 
     def reset_cache(self):
         """Restore the cache to the state before the step (for repeated steps)."""
