@@ -7,6 +7,9 @@
 //
 // All four are byte movers: 16-byte vector loads and stores, grid-stride loops
 // sized to the SM count.  Their cost is small next to the attention reread.
+// They are launched as programmatic dependents (each waits for the previous
+// kernel of the stream before touching memory), so back-to-back launches
+// overlap their launch latency.
 #include "pkv_common.cuh"
 #include "pkv_host.h"
 
@@ -28,6 +31,8 @@ __global__ void __launch_bounds__(1024) slot_mapping_kernel(int64_t* __restrict_
     int* start = sh;                   // [num_seqs + 1] first output slot of each sequence
     int* bad = sh + num_seqs + 1;      // [num_seqs] invalid-length flag
     __shared__ int tmp[32];
+    pdl_wait();  // programmatic dependent launch: the previous kernel's writes are visible
+    pdl_launch();
     int bits = 0;
     int carry = 0;
     for (int base = 0; base < num_seqs; base += 1024) {
@@ -90,6 +95,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
                                                         const int64_t* __restrict__ slots, int num_tokens,
                                                         int num_blocks, int block_size, int num_kv_heads,
                                                         int chunks_per_row, int32_t* status) {
+    pdl_wait();
+    pdl_launch();
     const long long per_tok = (long long)num_kv_heads * chunks_per_row;
     const long long total = (long long)num_tokens * per_tok;
     const long long cap = (long long)num_blocks * block_size;
@@ -121,6 +128,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                                           const int32_t* __restrict__ src_dst, int num_blocks,
                                                           long long chunks_per_block, int32_t* status) {
+    pdl_wait();
+    pdl_launch();
     const int pair = blockIdx.y;
     const int32_t s = src_dst[2 * pair], d = src_dst[2 * pair + 1];
     if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
@@ -151,6 +160,8 @@ __global__ void __launch_bounds__(256) gather_kv_kernel(uint4* __restrict__ k_ou
                                                         const int64_t* __restrict__ out_offsets, int num_blocks,
                                                         int block_size, int num_kv_heads, int chunks_per_row,
                                                         int32_t* status) {
+    pdl_wait();
+    pdl_launch();
     const int b = blockIdx.y;
     const int L = seq_lens[b];
     if (L < 0 || (long long)L > (long long)max_blocks * block_size) {
@@ -205,10 +216,10 @@ extern "C" int pkv_slot_mapping(int64_t* slots, const int32_t* block_tables, int
             cudaSuccess)
             return PKV_ERR_CUDA;
     }
-    slot_mapping_kernel<<<1, 1024, smem, (cudaStream_t)stream>>>(slots, block_tables, max_blocks, seq_lens,
-                                                                 append_lens, num_seqs, num_slots, block_size,
-                                                                 num_blocks, status);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const cudaError_t e = host::launch_pdl(slot_mapping_kernel, dim3(1), dim3(1024), smem, (cudaStream_t)stream,
+                                           slots, block_tables, max_blocks, seq_lens, append_lens, num_seqs,
+                                           num_slots, block_size, num_blocks, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 extern "C" int pkv_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
@@ -226,10 +237,11 @@ extern "C" int pkv_kv_append(void* k_cache, void* v_cache, const void* k_new, co
     const long long total = (long long)num_tokens * num_kv_heads * cpr;
     const long long want = (total + 255) / 256;
     const int grid = (int)(want < host::sm_count() * 8LL ? want : host::sm_count() * 8LL);
-    kv_append_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new,
-                                                             (const uint4*)v_new, slots, num_tokens, num_blocks,
-                                                             block_size, num_kv_heads, cpr, status);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const cudaError_t e = host::launch_pdl(kv_append_kernel, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
+                                           (uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new,
+                                           (const uint4*)v_new, slots, num_tokens, num_blocks, block_size,
+                                           num_kv_heads, cpr, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 extern "C" int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst, int num_pairs,
@@ -250,9 +262,9 @@ extern "C" int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_
     if (gx > cap) gx = cap;
     if (gx < 1) gx = 1;
     dim3 grid((unsigned)gx, (unsigned)num_pairs);
-    copy_blocks_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((uint4*)k_cache, (uint4*)v_cache, src_dst, num_blocks,
-                                                               cpb, status);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const cudaError_t e = host::launch_pdl(copy_blocks_kernel, grid, dim3(256), 0, (cudaStream_t)stream,
+                                           (uint4*)k_cache, (uint4*)v_cache, src_dst, num_blocks, cpb, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 extern "C" int pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_cache,
@@ -271,9 +283,9 @@ extern "C" int pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, cons
     if (rc) return rc;
     const int gx = max_blocks < 1024 ? max_blocks : 1024;
     dim3 grid(gx, num_seqs);
-    gather_kv_kernel<<<grid, 256, 0, (cudaStream_t)stream>>>((uint4*)k_out, (uint4*)v_out, (const uint4*)k_cache,
-                                                             (const uint4*)v_cache, block_tables, max_blocks, seq_lens,
-                                                             out_offsets, num_blocks, block_size, num_kv_heads,
-                                                             head_dim / 8, status);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const cudaError_t e = host::launch_pdl(gather_kv_kernel, grid, dim3(256), 0, (cudaStream_t)stream,
+                                           (uint4*)k_out, (uint4*)v_out, (const uint4*)k_cache,
+                                           (const uint4*)v_cache, block_tables, max_blocks, seq_lens, out_offsets,
+                                           num_blocks, block_size, num_kv_heads, head_dim / 8, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
