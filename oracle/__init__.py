@@ -56,6 +56,7 @@ def _load():
                 "oracle_attention": [P, P, P, P, P, I, P, P, I, I, I, I, I, I, D],
                 "oracle_attention_split": [P, P, P, P, I, P, P, P, P, I, P, P, I, I, I, I, I, I, D, I],
                 "oracle_spec_accept_greedy": [P, P, P, P, P, I, I, I],
+                "oracle_spec_accept_sample": [P, P, P, P, P, P, P, I, I, I],
                 "oracle_num_threads": [],
             }
             for name, argt in sigs.items():
@@ -180,6 +181,27 @@ def attention_split(q, k_cache, v_cache, block_tables, seq_lens, q_lens, scale, 
     if want_partials:
         return out[:n], st, po[:n], pm[:n], pl[:n]
     return out[:n], st
+
+
+def spec_accept_sample(p, q, draft, r, s):
+    """Modified rejection sampling ("Chapter 31 Serving Efficiency" 31.5,
+    Example 31.3; "Spending the Idle" 12.4): accept draft x_j iff
+    r_j * q_j(x_j) < p_j(x_j) (fp32), else draw the next token from
+    max(0, p_j - q_j) by integer inverse CDF with s_b; all accepted -> draw from
+    p_k.  p float32 [B][k+1][V], q float32 [B][k][V], draft int32 [B][k],
+    r float32 [B][k], s float32 [B].  Returns (accepted [B], next_token [B],
+    status bits)."""
+    pp = _c(p, np.float32)
+    B, k1, V = pp.shape
+    k = k1 - 1
+    qq = _c(q, np.float32).reshape(B, k, V)
+    dr = _c(draft, np.int32).reshape(B, k)
+    rr = _c(r, np.float32).reshape(B, k)
+    ss = _c(s, np.float32).reshape(B)
+    acc = np.empty(B, np.int32)
+    nxt = np.empty(B, np.int32)
+    st = _load().oracle_spec_accept_sample(_p(acc), _p(nxt), _p(pp), _p(qq), _p(dr), _p(rr), _p(ss), B, k, V)
+    return acc, nxt, int(st)
 
 
 def spec_accept_greedy(logits, draft):

@@ -17,6 +17,7 @@
  *   [SE]   "Chapter 31 Serving Efficiency" (imbrooklyn.dev), 31.3, 31.4
  *          (Example 31.2), 31.5.
  *   [SI]   "Spending the Idle" (derivingsystems.com), 12.4.
+ *   ([SE] 31.5 with Example 31.3 for the rejection-sampling acceptance.)
  *
  * Cache layout (a choice; the pages only say K/V are read through the block
  * table): k_cache, v_cache are [num_blocks][num_kv_heads][block_size][head_dim]
@@ -31,6 +32,8 @@
  *   4  a q_len outside [0, seq_len]
  *   8  a slot outside [-1.., num_blocks * block_size)  (negative = skip)
  *   64 a copy pair outside [0, num_blocks)
+ *   128 a draft token outside [0, vocab)
+ *   256 a sampling distribution with no positive weight
  * Output rows affected by bits 1, 2 or 4 are written as NaN.
  */
 #include <math.h>
@@ -413,6 +416,102 @@ int oracle_spec_accept_greedy(int32_t *accepted, int32_t *next_token, int32_t *a
         free(rowmax);
     }
     return 0;
+}
+
+/*
+ * Stochastic speculative acceptance -- modified rejection sampling
+ * ([SE] 31.5 and Example 31.3; [SI] 12.4; [KVC] 08 "Why the output keeps the
+ * exact distribution").
+ *
+ * For each sequence b, the drafts x_j ~ q_j, j = 0..k-1, are checked in order:
+ * x_j is accepted with probability min(1, p_j(x_j) / q_j(x_j)), decided with
+ * the caller's uniform r_j as  r_j * q_j(x_j) < p_j(x_j)  (fp32 multiply and
+ * compare: the decision is an integer, so it is taken in the precision the
+ * GPU kernel uses).  At the first rejection j* the round ends and the next
+ * token is drawn from the normalised positive part max(0, p_j* - q_j*); when
+ * all k drafts are accepted it is drawn from p_k (the extra target position).
+ *
+ * The draw is inverse-CDF sampling with the caller's uniform s_b over the
+ * distribution quantised to units of 2^-32: w_t = quant(value_t), where the
+ * residual value is the fp32 difference p - q, quant(x) = 0 for x <= 0 or NaN,
+ * 2^32 for x >= 1, else floor(x * 2^32); T = floor(s * sum w) exactly; the
+ * token is the smallest t whose inclusive prefix sum of w exceeds T.  Integer
+ * sums make the draw independent of summation order.  If every weight of the
+ * chosen distribution is zero, the residual falls back to p_j*; if that is
+ * zero too, next = -1 and status bit 256 is set.  A draft outside [0, V) is
+ * rejected and sets status bit 128.
+ *
+ * p  [B][k+1][V] fp32, q [B][k][V] fp32, draft [B][k], r [B][k], s [B].
+ * Outputs accepted [B] (0..k) and next_token [B].  Returns the status bits.
+ */
+static uint64_t quant32(float x) {
+    if (!(x > 0.0f)) return 0;            /* <= 0 or NaN */
+    if (x >= 1.0f) return (uint64_t)1 << 32;
+    return (uint64_t)(x * 4294967296.0f); /* exact scaling by 2^32, truncation */
+}
+
+/* floor(s * total) for s in [0, 1): s = m * 2^(e - 24) with integer m < 2^24 */
+static uint64_t scaled_floor(float s, uint64_t total) {
+    if (!(s > 0.0f)) return 0;
+    if (s >= 1.0f) return total ? total - 1 : 0;
+    int e;
+    const double f = frexp((double)s, &e);          /* s = f * 2^e, f in [0.5, 1) */
+    const uint64_t m = (uint64_t)ldexp(f, 24);       /* exact: s has 24 significant bits */
+    const unsigned __int128 prod = (unsigned __int128)m * total;
+    const int sh = 24 - e;                           /* s = m * 2^-sh, sh >= 25 */
+    return sh >= 128 ? 0 : (uint64_t)(prod >> sh);
+}
+
+static int64_t inverse_cdf(const uint64_t *w, int64_t V, float s) {
+    uint64_t total = 0;
+    for (int64_t t = 0; t < V; t++) total += w[t];
+    if (total == 0) return -1;
+    const uint64_t T = scaled_floor(s, total);
+    uint64_t c = 0;
+    for (int64_t t = 0; t < V; t++) {
+        c += w[t];
+        if (c > T) return t;
+    }
+    return V - 1; /* not reached: T < total */
+}
+
+int oracle_spec_accept_sample(int32_t *accepted, int32_t *next_token, const float *p, const float *q,
+                              const int32_t *draft, const float *r, const float *s, int B, int k, int V) {
+    int status = 0;
+    uint64_t *w = (uint64_t *)malloc(sizeof(uint64_t) * (size_t)(V > 0 ? V : 1));
+    for (int b = 0; b < B; b++) {
+        int j = 0;
+        for (; j < k; j++) {
+            const int32_t x = draft[(int64_t)b * k + j];
+            if (x < 0 || x >= V) {
+                status |= 128;
+                break;
+            }
+            const float px = p[((int64_t)b * (k + 1) + j) * V + x];
+            const float qx = q[((int64_t)b * k + j) * V + x];
+            const float rq = r[(int64_t)b * k + j] * qx; /* one fp32 rounding */
+            if (!(rq < px)) break;
+        }
+        accepted[b] = j;
+        const float *pj = p + ((int64_t)b * (k + 1) + j) * V;
+        int64_t t;
+        if (j < k) {
+            const float *qj = q + ((int64_t)b * k + j) * V;
+            for (int64_t u = 0; u < V; u++) w[u] = quant32(pj[u] - qj[u]);
+            t = inverse_cdf(w, V, s[b]);
+            if (t < 0) {
+                for (int64_t u = 0; u < V; u++) w[u] = quant32(pj[u]);
+                t = inverse_cdf(w, V, s[b]);
+            }
+        } else {
+            for (int64_t u = 0; u < V; u++) w[u] = quant32(pj[u]);
+            t = inverse_cdf(w, V, s[b]);
+        }
+        if (t < 0) status |= 256;
+        next_token[b] = (int32_t)t;
+    }
+    free(w);
+    return status;
 }
 
 /* Number of threads the oracle's parallel loops use (1 without OpenMP). */

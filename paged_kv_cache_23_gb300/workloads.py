@@ -302,6 +302,52 @@ def spec(B: int = 32, lo: int = 2048, hi: int = 8192, k: int = 5, vocab: int = 1
     return w
 
 
+@dataclass
+class SampleInputs:
+    """Inputs of stochastic speculative acceptance: target distributions
+    p [B][k+1][V], draft distributions q [B][k][V] (fp32, each row sums to 1),
+    drafts [B][k] drawn from q, acceptance uniforms r [B][k] and one sampling
+    uniform s [B] (fp32 in [0, 1))."""
+    p: np.ndarray
+    q: np.ndarray
+    draft: np.ndarray
+    r: np.ndarray
+    s: np.ndarray
+    meta: dict = field(default_factory=dict)
+
+
+def _softmax_rows(z: np.ndarray) -> np.ndarray:
+    z = z.astype(np.float64)
+    z = z - z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return (e / e.sum(axis=-1, keepdims=True)).astype(np.float32)
+
+
+def spec_sample(B: int = 32, k: int = 5, vocab: int = 128256, temp: float = 2.0, noise: float = 1.0,
+                seed: int = 0) -> SampleInputs:
+    """Distributions for stochastic verification: target logits
+    temp * N(0, 1) per row, p = softmax; the draft model's logits are the
+    target's plus noise * N(0, 1), q = softmax (so p and q overlap the way a
+    good small proposer does); each draft is drawn from its q row by inverse
+    CDF; r and s uniform in [0, 1)."""
+    ss = np.random.SeedSequence([seed, 23])
+    g = np.random.Generator(np.random.PCG64(ss))
+    z = (temp * g.standard_normal((B, k + 1, vocab), dtype=np.float32)).astype(np.float32)
+    p = _softmax_rows(z)
+    zq = z[:, :k, :] + (noise * g.standard_normal((B, k, vocab), dtype=np.float32)).astype(np.float32)
+    q = _softmax_rows(zq)
+    u = g.random((B, k))
+    c = np.cumsum(q.astype(np.float64), axis=-1)
+    draft = np.empty((B, k), np.int32)
+    for b in range(B):
+        for j in range(k):
+            draft[b, j] = min(int(np.searchsorted(c[b, j], u[b, j] * c[b, j, -1], side="right")), vocab - 1)
+    r = g.random((B, k), dtype=np.float32)
+    s_ = g.random(B, dtype=np.float32)
+    return SampleInputs(p=p, q=q, draft=draft, r=r, s=s_,
+                        meta=dict(B=B, k=k, vocab=vocab, temp=temp, noise=noise, seed=seed))
+
+
 def long_context(B: int = 8, ctx: int = 131072, chunk: int = 512, chunk_prefix: int = 8192,
                  partition_tokens: int = 4096, seed: int = 0, n_q=32, n_kv=8, d=128, bs=16) -> Workload:
     """B decodes of ctx tokens each (q_len 1, one appended token) plus one
