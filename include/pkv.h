@@ -68,6 +68,8 @@ extern "C" {
 #define PKV_STATUS_BAD_SLOT 8    /* a slot is >= num_blocks*block_size */
 #define PKV_STATUS_TIMEOUT 32    /* a bounded device wait ran out (library bug) */
 #define PKV_STATUS_BAD_PAIR 64   /* a copy pair names a block outside the pool */
+#define PKV_STATUS_BAD_TOKEN 128 /* a draft token is outside [0, vocab) */
+#define PKV_STATUS_BAD_DIST 256  /* a sampling distribution has no positive weight */
 
 /* Attention flags. */
 #define PKV_ATTN_DECODE_CUDA_CORES 1 /* run q_len = 1 rows on the CUDA-core FMA path */
@@ -252,6 +254,39 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
 int pkv_spec_accept_greedy(const float* logits, const int32_t* draft, int num_seqs, int k,
                            int vocab, int32_t* argmax_out, int32_t* accepted, int32_t* next_token,
                            void* stream);
+
+/*
+ * Stochastic speculative acceptance: modified rejection sampling ([SE] 31.5
+ * and Example 31.3; [SI] 12.4; [KVC] 08 "Why the output keeps the exact
+ * distribution").  For each sequence the drafts are checked in order: draft
+ * x_j (drawn by the caller from q_j) is accepted with probability
+ * min(1, p_j(x_j) / q_j(x_j)); at the first rejection j the round ends and the
+ * next token is drawn from the normalised positive part max(0, p_j - q_j);
+ * when all k drafts pass it is drawn from p_k, the target's distribution after
+ * them.  The emitted tokens are distributed exactly as the target's.
+ *   p           fp32 [num_seqs][k+1][vocab]  target distributions (rows sum to 1)
+ *   q           fp32 [num_seqs][k][vocab]    draft distributions
+ *   draft       int32 [num_seqs][k]
+ *   r           fp32 [num_seqs][k] uniforms in [0, 1): x_j is accepted iff
+ *               r_j * q_j(x_j) < p_j(x_j), fp32 multiply (round to nearest)
+ *   s           fp32 [num_seqs] uniform in [0, 1) for the one draw of the round
+ *   accepted    int32 [num_seqs] out: number of leading drafts accepted (0..k)
+ *   next_token  int32 [num_seqs] out: the drawn token
+ *   status      PKV_STATUS_* bits, may be null
+ * The draw: weights w_t = quant(value_t), value = the fp32 difference p - q
+ * (or p), quant(x) = 0 for x <= 0 or NaN, 2^32 for x >= 1, else
+ * floor(x * 2^32); T = floor(s * sum_t w_t) exactly; next_token = the smallest
+ * t whose inclusive prefix sum of w exceeds T.  Integer sums make the token
+ * independent of summation order, so it is reproducible and bit-exact against
+ * a reference.  A residual with no positive weight falls back to p_j; if that
+ * has none either, next_token = -1 and PKV_STATUS_BAD_DIST is set.  A draft
+ * outside [0, vocab) is rejected at its position and sets
+ * PKV_STATUS_BAD_TOKEN.  1 <= k <= 1024, vocab >= 1.  Reads the two rows of
+ * the rejected position (one when all pass) plus 2k scalars per sequence.
+ */
+int pkv_spec_accept_sample(const float* p, const float* q, const int32_t* draft, const float* r,
+                           const float* s, int num_seqs, int k, int vocab, int32_t* accepted,
+                           int32_t* next_token, int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

@@ -30,6 +30,8 @@ PKV_STATUS_BAD_QLEN = 4
 PKV_STATUS_BAD_SLOT = 8
 PKV_STATUS_TIMEOUT = 32
 PKV_STATUS_BAD_PAIR = 64
+PKV_STATUS_BAD_TOKEN = 128
+PKV_STATUS_BAD_DIST = 256
 PKV_ATTN_DECODE_CUDA_CORES = 1
 PKV_ERR_SCRATCH_LIMIT = -8
 
@@ -48,6 +50,7 @@ _SIGS = {
     "pkv_paged_attention_decode": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                     ctypes.c_float, _I, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_spec_accept_greedy": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+    "pkv_spec_accept_sample": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
     "pkv_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "pkv_paged_attention_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                             ctypes.c_float, _I, _I, _P, _P], _I),
@@ -106,7 +109,7 @@ def _dev(t, name, dtype=None):
 
 
 def status_bits(code: int):
-    return [lib().pkv_status_string(1 << i).decode() for i in range(8) if code & (1 << i)]
+    return [lib().pkv_status_string(1 << i).decode() for i in range(10) if code & (1 << i)]
 
 
 def slot_mapping(slots, block_tables, seq_lens, append_lens, block_size, num_blocks, status=None, stream=None):
@@ -198,6 +201,24 @@ def spec_accept_greedy(logits, draft, argmax_out, accepted, next_token, stream=N
     rc = lib().pkv_spec_accept_greedy(_ptr(logits), _ptr(draft), B, k1 - 1, V, _ptr(argmax_out), _ptr(accepted),
                                       _ptr(next_token), _stream(stream))
     _check(rc, "pkv_spec_accept_greedy")
+
+
+def spec_accept_sample(p, q, draft, r, s, accepted, next_token, status=None, stream=None):
+    """Stochastic acceptance (modified rejection sampling): p fp32 [B][k+1][V],
+    q fp32 [B][k][V], draft int32 [B][k], uniforms r fp32 [B][k] and s fp32 [B]."""
+    _dev(p, "p", torch.float32)
+    _dev(q, "q", torch.float32)
+    _dev(draft, "draft", torch.int32)
+    _dev(r, "r", torch.float32)
+    _dev(s, "s", torch.float32)
+    _dev(accepted, "accepted", torch.int32)
+    _dev(next_token, "next_token", torch.int32)
+    B, k1, V = p.shape
+    if tuple(q.shape) != (B, k1 - 1, V) or tuple(draft.shape) != (B, k1 - 1) or tuple(r.shape) != (B, k1 - 1):
+        raise ValueError("spec_accept_sample: q [B][k][V], draft and r [B][k] must match p [B][k+1][V]")
+    rc = lib().pkv_spec_accept_sample(_ptr(p), _ptr(q), _ptr(draft), _ptr(r), _ptr(s), B, k1 - 1, V, _ptr(accepted),
+                                      _ptr(next_token), _ptr(status), _stream(stream))
+    _check(rc, "pkv_spec_accept_sample")
 
 
 def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, q_lens, max_seq_len, scale,

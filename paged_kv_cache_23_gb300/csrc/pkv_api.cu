@@ -105,6 +105,8 @@ extern "C" const char* pkv_status_string(int bit) {
         case PKV_STATUS_BAD_SLOT: return "slot outside the pool";
         case PKV_STATUS_TIMEOUT: return "a bounded device wait ran out";
         case PKV_STATUS_BAD_PAIR: return "copy pair outside the pool";
+        case PKV_STATUS_BAD_TOKEN: return "draft token outside the vocabulary";
+        case PKV_STATUS_BAD_DIST: return "sampling distribution without positive weight";
         default: return "unknown status bit";
     }
 }

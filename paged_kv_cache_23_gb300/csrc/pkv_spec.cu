@@ -1,4 +1,5 @@
-// pkv_spec.cu -- greedy speculative acceptance.
+// pkv_spec.cu -- speculative acceptance: greedy, and stochastic (modified
+// rejection sampling, further down).
 //
 // "Spending the Idle" 12.4 and "Inference at Scale: KV Cache, Prefill, and
 // Decode" section 08: under greedy decoding a drafted token is accepted when it
@@ -128,9 +129,241 @@ __global__ void accept_kernel(const int32_t* __restrict__ argmax, const int32_t*
     next_token[b] = am[a];
 }
 
+// ---------------------------------------------------------------------------
+// Stochastic acceptance: modified rejection sampling ("Chapter 31 Serving
+// Efficiency" 31.5, Example 31.3; "Spending the Idle" 12.4; "Inference at
+// Scale" section 08).  Draft x_j is accepted iff r_j * q_j(x_j) < p_j(x_j)
+// (fp32); at the first rejection j* the next token is drawn from
+// max(0, p_j* - q_j*), or from p_k when all k drafts pass.  The draw is an
+// inverse CDF over weights quantised to 2^-32 (integer sums: the same token
+// whatever the summation order): T = floor(s * total), token = the first t
+// whose inclusive prefix sum exceeds T.
+//
+// One 8-CTA cluster per sequence: every CTA finds j* (k loads), sums the
+// weights of its eighth of the row, the slice totals are exchanged through
+// distributed shared memory, and the CTA whose slice holds T rescans it in
+// index order with a block-wide scan.  HBM traffic: the p and q rows of j*
+// (2 x 4V bytes; 4V when all drafts pass), read once, plus an L2 rescan of
+// one eighth of them.
+// ---------------------------------------------------------------------------
+constexpr int kSampleCluster = 8;
+constexpr int kSampleThreads = 256;
+
+__device__ __forceinline__ uint64_t quant32(float x) {
+    if (!(x > 0.0f)) return 0;  // <= 0 or NaN
+    if (x >= 1.0f) return 1ull << 32;
+    return __float2ull_rz(x * 4294967296.0f);  // exact scaling by 2^32, then truncation
+}
+
+// floor(s * total) for s in [0, 1), exactly (128-bit product of s's integer
+// significand and total).
+__device__ __forceinline__ uint64_t scaled_floor(float s, uint64_t total) {
+    if (!(s > 0.0f)) return 0;
+    if (s >= 1.0f) return total ? total - 1 : 0;
+    const uint32_t bits = __float_as_uint(s);
+    const int e = (int)((bits >> 23) & 255);
+    const uint64_t m = e ? ((bits & 0x7fffffu) | 0x800000u) : (bits & 0x7fffffu);
+    const int sh = e ? 150 - e : 149;  // s = m * 2^-sh
+    const uint64_t lo = m * total, hi = __umul64hi(m, total);
+    if (sh >= 128) return 0;
+    if (sh >= 64) return hi >> (sh - 64);
+    return (hi << (64 - sh)) | (lo >> sh);
+}
+
+__device__ __forceinline__ uint64_t sample_weight(const float* pr, const float* qr, long long t, int residual) {
+    const float pv = __ldg(pr + t);
+    return residual ? quant32(__fsub_rn(pv, __ldg(qr + t))) : quant32(pv);
+}
+
+__device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* wsum) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    if (lane == 0) wsum[warp] = v;
+    __syncthreads();
+    uint64_t t = 0;
+#pragma unroll
+    for (int w = 0; w < kSampleThreads / 32; ++w) t += wsum[w];
+    __syncthreads();
+    return t;
+}
+
+// Inclusive block scan (uint64), returns this thread's inclusive prefix and the block total.
+__device__ __forceinline__ uint64_t block_scan_u64(uint64_t v, uint64_t* wsum, uint64_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint64_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    uint64_t before = 0, t = 0;
+#pragma unroll
+    for (int w = 0; w < kSampleThreads / 32; ++w) {
+        if (w < warp) before += wsum[w];
+        t += wsum[w];
+    }
+    __syncthreads();
+    *total = t;
+    return before + x;
+}
+
+__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSampleThreads)
+    spec_sample_kernel(const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ draft,
+                       const float* __restrict__ r, const float* __restrict__ s, int num_seqs, int k, int vocab,
+                       int vec4, int32_t* __restrict__ accepted, int32_t* __restrict__ next_token,
+                       int32_t* status) {
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = (int)cluster.block_rank();
+    __shared__ uint64_t wsum[kSampleThreads / 32];
+    __shared__ uint64_t slice_total;
+    __shared__ int s_rej, s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long V = vocab;
+    long long per = (V + kSampleCluster - 1) / kSampleCluster;
+    per = (per + 3) & ~3LL;
+    const long long lo = rank * per < V ? rank * per : V;
+    const long long hi = lo + per < V ? lo + per : V;
+    pdl_wait();
+    pdl_launch();
+    for (int b = blockIdx.y; b < num_seqs; b += gridDim.y) {
+        // accepted length: the first draft that fails r * q(x) < p(x)
+        if (warp == 0) {
+            int rej = k, bad = 0;
+            for (int c0 = 0; c0 < k; c0 += 32) {
+                const int j = c0 + lane;
+                bool ok = true, isbad = false;
+                if (j < k) {
+                    const int32_t x = draft[(long long)b * k + j];
+                    if (x < 0 || x >= vocab) {
+                        ok = false;
+                        isbad = true;
+                    } else {
+                        const float px = __ldg(p + ((long long)b * (k + 1) + j) * V + x);
+                        const float qx = __ldg(q + ((long long)b * k + j) * V + x);
+                        ok = __fmul_rn(__ldg(r + (long long)b * k + j), qx) < px;
+                    }
+                }
+                const unsigned m = __ballot_sync(kFull, !ok);
+                if (m) {
+                    const int first = __ffs(m) - 1;
+                    rej = c0 + first;
+                    bad = __shfl_sync(kFull, (int)isbad, first);
+                    break;
+                }
+            }
+            if (lane == 0) {
+                s_rej = rej;
+                s_bad = bad;
+            }
+        }
+        __syncthreads();
+        const int j = s_rej;
+        const float* pr = p + ((long long)b * (k + 1) + j) * V;
+        const float* qr = j < k ? q + ((long long)b * k + j) * V : p;
+        int residual = j < k ? 1 : 0;
+        uint64_t total = 0, before = 0, mine = 0;
+        for (;;) {
+            // this CTA's slice total
+            uint64_t acc = 0;
+            if (vec4) {
+                const float4* p4 = reinterpret_cast<const float4*>(pr + lo);
+                const float4* q4 = reinterpret_cast<const float4*>(qr + lo);
+                const long long n4 = (hi - lo) >> 2;
+                for (long long i = tid; i < n4; i += kSampleThreads) {
+                    const float4 a = __ldg(p4 + i);
+                    if (residual) {
+                        const float4 c = __ldg(q4 + i);
+                        acc += quant32(__fsub_rn(a.x, c.x)) + quant32(__fsub_rn(a.y, c.y)) +
+                               quant32(__fsub_rn(a.z, c.z)) + quant32(__fsub_rn(a.w, c.w));
+                    } else {
+                        acc += quant32(a.x) + quant32(a.y) + quant32(a.z) + quant32(a.w);
+                    }
+                }
+                for (long long t = lo + 4 * n4 + tid; t < hi; t += kSampleThreads) acc += sample_weight(pr, qr, t, residual);
+            } else {
+                for (long long t = lo + tid; t < hi; t += kSampleThreads) acc += sample_weight(pr, qr, t, residual);
+            }
+            mine = block_sum_u64(acc, wsum);
+            if (tid == 0) slice_total = mine;
+            cluster.sync();
+            total = 0;
+            before = 0;
+            for (int c = 0; c < kSampleCluster; ++c) {
+                const uint64_t t = *cluster.map_shared_rank(&slice_total, c);
+                if (c < rank) before += t;
+                total += t;
+            }
+            cluster.sync();  // slice_total is rewritten by a second pass
+            if (total == 0 && residual) {
+                residual = 0;  // no positive residual: draw from p itself
+                continue;
+            }
+            break;
+        }
+        if (rank == 0 && tid == 0) {
+            accepted[b] = j;
+            int bits = s_bad && j < k ? PKV_STATUS_BAD_TOKEN : 0;
+            if (total == 0) {
+                next_token[b] = -1;
+                bits |= PKV_STATUS_BAD_DIST;
+            }
+            if (bits) report(status, bits);
+        }
+        const uint64_t T = scaled_floor(__ldg(s + b), total);
+        if (total > 0 && mine > 0 && T >= before && T - before < mine) {
+            // rescan this slice in index order: 4 consecutive tokens per thread
+            uint64_t run = before;
+            for (long long c = lo; c < hi; c += 4 * kSampleThreads) {
+                const long long e0 = c + 4 * tid;
+                uint64_t w4[4] = {0, 0, 0, 0};
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (e0 + u < hi) w4[u] = sample_weight(pr, qr, e0 + u, residual);
+                uint64_t chunk;
+                const uint64_t incl = block_scan_u64(w4[0] + w4[1] + w4[2] + w4[3], wsum, &chunk);
+                if (run + chunk > T) {
+                    // the thread whose inclusive prefix first exceeds T - run owns the token
+                    const uint64_t excl = incl - (w4[0] + w4[1] + w4[2] + w4[3]);
+                    if (run + excl <= T && run + incl > T) {
+                        uint64_t cum = run + excl;
+                        int u = 0;
+                        for (; u < 3; ++u) {
+                            cum += w4[u];
+                            if (cum > T) break;
+                        }
+                        next_token[b] = (int32_t)(e0 + u);
+                    }
+                    break;
+                }
+                run += chunk;
+            }
+        }
+        cluster.sync();  // shared state is reused for the next sequence
+    }
+}
+
 }  // namespace pkv
 
 using namespace pkv;
+
+extern "C" int pkv_spec_accept_sample(const float* p, const float* q, const int32_t* draft, const float* r,
+                                      const float* s, int num_seqs, int k, int vocab, int32_t* accepted,
+                                      int32_t* next_token, int32_t* status, void* stream) {
+    if (num_seqs < 0 || k < 1 || k > 1024 || vocab < 1) return PKV_ERR_SIZE;
+    if (num_seqs == 0) return PKV_OK;
+    if (!p || !q || !draft || !r || !s || !accepted || !next_token) return PKV_ERR_NULL;
+    const int rc = host::check_device();
+    if (rc) return rc;
+    if ((long long)num_seqs * (k + 1) * vocab > (1LL << 40)) return PKV_ERR_SIZE;
+    const int vec4 = (vocab % 4 == 0) && host::aligned16(p) && host::aligned16(q);
+    dim3 grid(kSampleCluster, (unsigned)(num_seqs < 65535 ? num_seqs : 65535));
+    const cudaError_t e = host::launch_pdl(spec_sample_kernel, grid, dim3(kSampleThreads), 0, (cudaStream_t)stream,
+                                           p, q, draft, r, s, num_seqs, k, vocab, vec4, accepted, next_token, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
 
 extern "C" int pkv_spec_accept_greedy(const float* logits, const int32_t* draft, int num_seqs, int k, int vocab,
                                       int32_t* argmax_out, int32_t* accepted, int32_t* next_token, void* stream) {
