@@ -156,9 +156,48 @@ def aggregate_sum(value: float, world_size: int, device=None) -> float:
     return float(t.item())
 
 
-def make_workload(seed: int):
+# --workload: the headline mix (default) and the other attention workloads of
+# the path; "sample" is the stochastic acceptance kernel alone.
+SHAPE = "Llama-3-8B attention shape: 32 q / 8 kv heads, head_dim 128, bf16 KV, block_size 16"
+WORKLOADS = {
+    "mix": dict(desc=WORKLOAD, batch=256, seq="log-normal median 1024", max_seq_len=32768),
+    "decode": dict(desc="8B decode, " + SHAPE + ": batch 64, seq_len ~ U[512, 4096], q_len 1, 1 appended "
+                   "token/seq", batch=64, seq="U[512, 4096]", max_seq_len=None),
+    "spec": dict(desc="speculative verify, " + SHAPE + ": batch 32, seq_len ~ U[2048, 8192], q_len 5 causal, "
+                 "greedy acceptance over logits [32, 6, 128256] fp32", batch=32, seq="U[2048, 8192]",
+                 max_seq_len=None),
+    "long": dict(desc="long context + chunk, " + SHAPE + ": 8 decodes of 131072 tokens + one 512-query chunk "
+                 "over 8192 + 512, in one call", batch=9, seq="131072 (x8) and 8704", max_seq_len=None),
+    "sample": dict(desc="stochastic speculative acceptance (modified rejection sampling): batch 32, k 5, "
+                   "vocab 128256, p/q fp32 softmax rows, drafts drawn from q", batch=32, seq="n/a",
+                   max_seq_len=None),
+}
+
+
+def make_workload(seed: int, name: str = "mix"):
     from paged_kv_cache_23_gb300 import workloads as wl
-    return wl.mix(B=256, median=1024, sigma=1.0, clip=(16, 32768), share=0.5, prefix=2048, seed=seed)
+    if name == "mix":
+        return wl.mix(B=256, median=1024, sigma=1.0, clip=(16, 32768), share=0.5, prefix=2048, seed=seed)
+    if name == "decode":
+        return wl.decode(64, 512, 4096, seed)
+    if name == "spec":
+        return wl.spec(32, 2048, 8192, 5, 128256, 0.7, seed)
+    if name == "long":
+        return wl.long_context(8, 131072, 512, 8192, 4096, seed)
+    if name == "sample":
+        return wl.spec_sample(B=32, k=5, vocab=128256, seed=seed)
+    raise ValueError(name)
+
+
+def step_bytes_of(w):
+    """Unique bytes of one step: the attention step, plus the logits scan of
+    greedy acceptance when the workload carries logits."""
+    from paged_kv_cache_23_gb300 import accounting
+    b = accounting.step_bytes(w)
+    if w.logits is not None:
+        b["accept"] = accounting.accept_greedy_bytes(w)
+        b["step_unique"] += b["accept"]
+    return b
 
 
 def oracle_step_time(w, reps: int = 1):
@@ -173,6 +212,18 @@ def oracle_step_time(w, reps: int = 1):
         slots, _ = oracle.slot_mapping(w.block_tables, w.seq_lens, w.append_lens, w.block_size, w.num_blocks)
         oracle.kv_append(k, v, w.k_new, w.v_new, slots)
         oracle.attention(w.q, k, v, w.block_tables, w.seq_lens, w.q_lens, w.scale)
+        if w.logits is not None:
+            oracle.spec_accept_greedy(w.logits, w.draft)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def oracle_sample_time(x, reps: int = 1):
+    import oracle
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.spec_accept_sample(x.p, x.q, x.draft, x.r, x.s)
         times.append(time.perf_counter() - t0)
     return times
 
@@ -181,28 +232,44 @@ def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
         return 0
-    from paged_kv_cache_23_gb300 import accounting
     import oracle
-    w = make_workload(0)
-    b = accounting.step_bytes(w)
+    from paged_kv_cache_23_gb300 import accounting
+    spec = WORKLOADS[args.workload]
+    w = make_workload(0, args.workload)
     oracle.build()
-    # each step: the whole batch (256 sequences); warm-up steps untimed
-    oracle_step_time(w, max(0, args.warmup))
-    t = oracle_step_time(w, args.steps)
+    if args.workload == "sample":
+        acc, _, _ = oracle.spec_accept_sample(w.p, w.q, w.draft, w.r, w.s)
+        nbytes = accounting.accept_sample_bytes(w, acc)
+        oracle_sample_time(w, max(0, args.warmup))
+        t = oracle_sample_time(w, args.steps)
+        sample = "the whole batch of 32 sequences per step (C oracle)"
+    else:
+        nbytes = step_bytes_of(w)["step_unique"]
+        # each step: the whole batch; warm-up steps untimed
+        oracle_step_time(w, max(0, args.warmup))
+        t = oracle_step_time(w, args.steps)
+        sample = f"the whole batch-{spec['batch']} step per step (fp64 C oracle, OpenMP)"
     mean = sum(t) / len(t)
-    value = b["step_unique"] / mean / 1e9
+    value = nbytes / mean / 1e9
     cores = oracle.num_threads()
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": 256, "seq_len": "log-normal median 1024",
+    line = {"impl": "reference", "metric": metric_of(args.workload), "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": spec["desc"], "global_batch": spec["batch"], "seq_len": spec["seq"],
                        "parallelism": "cpu oracle, rank 0 only", "l2": "n/a (host)"},
-            "seq_steps_per_s": 256 / mean,
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                             "sample": "the whole batch-256 step per step (fp64 C oracle, OpenMP)"},
+            "seq_steps_per_s": spec["batch"] / mean,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def metric_of(name: str) -> str:
+    if name == "mix":
+        return METRIC
+    if name == "sample":
+        return "stochastic speculative acceptance GB/s (% of GB300 HBM peak); sequences/s"
+    return f"paged attention KV GB/s (% of GB300 HBM peak); seq-steps/s, {name} workload"
 
 
 def run_gpu(args):
@@ -219,9 +286,11 @@ def run_gpu(args):
     from paged_kv_cache_23_gb300 import accounting
     from paged_kv_cache_23_gb300.runner import DeviceStep
 
-    w = make_workload(rank)        # weak scaling: each rank owns its own batch of 256 sequences
-    b = accounting.step_bytes(w)
-    ds = DeviceStep(w, device=device, max_seq_len=32768, partition_tokens=args.partition, flags=args.flags)
+    spec = WORKLOADS[args.workload]
+    w = make_workload(rank, args.workload)   # weak scaling: each rank owns its own batch
+    b = step_bytes_of(w)
+    ds = DeviceStep(w, device=device, max_seq_len=spec["max_seq_len"], partition_tokens=args.partition,
+                    flags=args.flags)
     stream = torch.cuda.current_stream(device)
 
     # parity spot check on this very run: a few sequences against the oracle
@@ -233,6 +302,7 @@ def run_gpu(args):
     def step():
         ds.cache_ops(stream)
         ds.attention(stream)
+        ds.accept(stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -254,6 +324,7 @@ def run_gpu(args):
         ev[i][0].record(stream)
         ds.attention(stream)
         ev[i][1].record(stream)
+        ds.accept(stream)
     stop.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
@@ -276,18 +347,20 @@ def run_gpu(args):
     achieved = b["attention_unique"] / (attn_avg / 1e3) / 1e9
     if rank != 0:
         return 0
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+    line = {"metric": metric_of(args.workload), "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "global_batch": 256 * ws, "seq_len": "log-normal median 1024",
+            "config": {"workload": spec["desc"], "global_batch": spec["batch"] * ws, "seq_len": spec["seq"],
                        "parallelism": f"replicas x{ws} (independent batches)" if ws > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (~1.2 GB unique K/V per step vs 126 MB L2); no flush",
+                       "l2": f"inputs larger than L2 ({b['kv_unique'] / 1e9:.2f} GB unique K/V per step vs "
+                             "126 MB L2); no flush",
                        "partition_tokens": ds.partition_tokens or f"auto ({chosen_P})", "flags": ds.flags},
             "seq_steps_per_s": seqs_all / (ms_step / 1e3),
+            "seq_steps_per_s_attention": seqs_all / (attn_avg / 1e3),
             "kv_bytes_per_step": {"unique": b["kv_unique"], "logical": b["kv_logical"],
                                   "step_unique": b["step_unique"]},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": load_traffic(),
+                         "frac": achieved / peak, "traffic": load_traffic() if args.workload == "mix" else None,
                          "kernel": "pkv_paged_attention_decode (plan + attention kernels)",
                          "peak_kind": peak_kind, "attention_ms": attn_avg,
                          "frac_of_nominal_8tbs": achieved / 8000.0},
@@ -313,9 +386,11 @@ def spot_check(w, ds, device):
     oracle.copy_blocks(k, v, w.cow)
     slots, _ = oracle.slot_mapping(w.block_tables, w.seq_lens, w.append_lens, w.block_size, w.num_blocks)
     oracle.kv_append(k, v, w.k_new, w.v_new, slots)
-    pick = np.linspace(0, w.num_seqs - 1, 8).astype(int)
-    ref, _ = oracle.attention(w.q[pick], k, v, w.block_tables[pick], w.seq_lens[pick], w.q_lens[pick], w.scale)
-    got = wl.bf16_bits_to_f32(bf16_to_bits(ds.out)[pick]).astype(np.float64)
+    pick = np.unique(np.linspace(0, w.num_seqs - 1, 8).astype(int))
+    q0 = np.concatenate([[0], np.cumsum(w.q_lens.astype(np.int64))])
+    rows = np.concatenate([np.arange(q0[b], q0[b + 1]) for b in pick])
+    ref, _ = oracle.attention(w.q[rows], k, v, w.block_tables[pick], w.seq_lens[pick], w.q_lens[pick], w.scale)
+    got = wl.bf16_bits_to_f32(bf16_to_bits(ds.out)[rows]).astype(np.float64)
     err = np.abs(got - ref)
     ok = bool(np.all(err <= 1e-2 + 1e-2 * np.abs(ref)))
     return {"sequences": pick.tolist(), "max_abs_err": float(err.max()), "within_tol": ok,
@@ -336,6 +411,7 @@ def end_to_end(ds, w, args, stream, device, ws):
         ds.upload(host, stream)
         ds.cache_ops(stream)
         ds.attention(stream)
+        ds.accept(stream)
         out_host.copy_(ds.out, non_blocking=True)
 
     for _ in range(2):
@@ -359,13 +435,131 @@ def end_to_end(ds, w, args, stream, device, ws):
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
 
 
+def run_sample(args):
+    """Stochastic speculative acceptance alone: batch 32, k 5, vocab 128256."""
+    import torch
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the GPU arm needs a GB300)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import paged_kv_cache_23_gb300 as pkv
+    from paged_kv_cache_23_gb300 import accounting
+    spec = WORKLOADS["sample"]
+    x = make_workload(rank, "sample")
+    B, k1, V = x.p.shape
+    t = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(device, dt)
+    p, q, d, r, s = (t(x.p, torch.float32), t(x.q, torch.float32), t(x.draft, torch.int32), t(x.r, torch.float32),
+                     t(x.s, torch.float32))
+    acc = torch.empty(B, dtype=torch.int32, device=device)
+    nxt = torch.empty(B, dtype=torch.int32, device=device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    # the kernel reads only the rows the draws need (~30 MB of the 180 MB of p
+    # and q), the same rows every call, so a read of a 256 MB buffer evicts
+    # them from L2 before every call (a read leaves no dirty lines behind)
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=device)
+    flush_sink = torch.empty(1, dtype=torch.float32, device=device)
+
+    class _Flush:
+        @staticmethod
+        def zero_():
+            torch.sum(flush_buf, dim=0, keepdim=True, out=flush_sink)
+
+    flush = _Flush()
+
+    def call():
+        pkv.spec_accept_sample(p, q, d, r, s, acc, nxt, status=st, stream=stream)
+
+    parity = None
+    if rank == 0 and not args.no_check:
+        import oracle
+        call()
+        torch.cuda.synchronize()
+        ra, rn, rs = oracle.spec_accept_sample(x.p, x.q, x.draft, x.r, x.s)
+        parity = {"bit_exact": bool(np.array_equal(acc.cpu().numpy(), ra) and np.array_equal(nxt.cpu().numpy(), rn)),
+                  "status": int(st.item()), "oracle_status": int(rs)}
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = [a.elapsed_time(z) for a, z in ev]
+    ms_step = aggregate_max(sum(ms) / len(ms), ws, device)
+    nbytes = accounting.accept_sample_bytes(x, acc.cpu().numpy())
+    value = aggregate_sum(nbytes, ws, device) / (ms_step / 1e3) / 1e9
+    achieved = nbytes / (ms_step / 1e3) / 1e9
+    peak, peak_kind = load_peaks()
+    # end to end: the uniforms and drafts of a round come from the host each step
+    hr = torch.empty_like(r, device="cpu").pin_memory()
+    hs = torch.empty_like(s, device="cpu").pin_memory()
+    hd = torch.empty_like(d, device="cpu").pin_memory()
+    hr.copy_(r.cpu())
+    hs.copy_(s.cpu())
+    hd.copy_(d.cpu())
+    ho = torch.empty(2 * B, dtype=torch.int32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        r.copy_(hr, non_blocking=True)
+        s.copy_(hs, non_blocking=True)
+        d.copy_(hd, non_blocking=True)
+        call()
+        ho[:B].copy_(acc, non_blocking=True)
+        ho[B:].copy_(nxt, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = aggregate_max(e0.elapsed_time(e1) / args.steps, ws, device)
+    if rank != 0:
+        return 0
+    line = {"metric": metric_of("sample"), "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": spec["desc"], "global_batch": B * ws, "seq_len": spec["seq"],
+                       "parallelism": "single GPU" if ws == 1 else f"replicas x{ws}",
+                       "l2": "L2 flushed before every call by reading a 256 MB buffer"},
+            "sequences_per_s": B * ws / (ms_step / 1e3), "bytes_per_call": nbytes,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "kernel": "spec_sample_kernel", "peak_kind": peak_kind},
+            "clocks": clocks, "gpu_launches": args.steps, "status": int(st.item()), "parity": parity,
+            "e2e": {"value": nbytes / (ms_e2e / 1e3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": int(hr.numel() * 4 + hs.numel() * 4 + hd.numel() * 4),
+                    "d2h_bytes_per_step": int(ho.numel() * 4), "ms_per_step": ms_e2e}}
+    t_cpu = oracle_sample_time(x, 2)
+    line["cpu_baseline"] = {"value": nbytes / min(t_cpu) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": "the whole batch of 32 sequences (C oracle, one thread), best of 2"}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def cpu_baseline(w, b):
     import oracle
     oracle.build()
-    t = oracle_step_time(w, 2)
+    reps = 1 if int(w.seq_lens.max()) > 65536 else 2
+    t = oracle_step_time(w, reps)
     best = min(t)
     return {"value": b["step_unique"] / best / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "the full batch-256 step (copy, slots, append, fp64 attention), best of 2",
+            "sample": f"the full batch-{w.num_seqs} step (copy, slots, append, fp64 attention"
+                      f"{', greedy acceptance' if w.logits is not None else ''}), best of {reps}",
             "seq_steps_per_s": w.num_seqs / best}
 
 
@@ -377,10 +571,14 @@ def main(argv=None):
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--workload", default="mix", choices=sorted(WORKLOADS),
+                    help="mix (default, the headline), decode, spec, long, or sample (stochastic acceptance)")
     ap.add_argument("--no-check", action="store_true")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "sample":
+        return run_sample(args)
     return run_gpu(args)
 
 

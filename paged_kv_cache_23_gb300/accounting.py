@@ -64,6 +64,27 @@ def step_bytes(w, bytes_per_value: int = 2) -> dict:
                 step_unique=attn_unique + append + cow, step_logical=attn_logical + append + cow)
 
 
+def accept_greedy_bytes(w) -> int:
+    """Greedy acceptance ("Spending the Idle" 12.4): every logits row is
+    scanned for its argmax (4 B per score), plus drafts and the outputs."""
+    B, k1, V = w.logits.shape
+    return B * k1 * V * 4 + B * (k1 - 1) * 4 + B * k1 * 4 + 2 * B * 4
+
+
+def accept_sample_bytes(x, accepted) -> int:
+    """Stochastic acceptance ("Chapter 31 Serving Efficiency" 31.5): per
+    sequence the draft, r, p(x) and q(x) of each checked position, and the one
+    distribution the draw needs -- p and q rows of the rejected position
+    (8 B per token) or the p row after all drafts (4 B per token) -- plus s
+    and the two outputs."""
+    B, k1, V = x.p.shape
+    k = k1 - 1
+    acc = np.asarray(accepted, np.int64)
+    checked = np.minimum(acc + 1, k)
+    rows = np.where(acc < k, 8, 4) * V
+    return int((checked * 16).sum() + rows.sum() + B * 12)
+
+
 def attention_flops(w) -> int:
     """2 FLOP per multiply-add for QK^T and PV over the visible positions."""
     L = w.seq_lens.astype(np.int64)

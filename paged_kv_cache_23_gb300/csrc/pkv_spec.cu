@@ -140,14 +140,17 @@ __global__ void accept_kernel(const int32_t* __restrict__ argmax, const int32_t*
 // whose inclusive prefix sum exceeds T.
 //
 // One 8-CTA cluster per sequence: every CTA finds j* (k loads), sums the
-// weights of its eighth of the row, the slice totals are exchanged through
-// distributed shared memory, and the CTA whose slice holds T rescans it in
-// index order with a block-wide scan.  HBM traffic: the p and q rows of j*
-// (2 x 4V bytes; 4V when all drafts pass), read once, plus an L2 rescan of
-// one eighth of them.
+// weights of its eighth of the row in token order, keeping one partial sum
+// per 128-token segment; the slice totals are exchanged through distributed
+// shared memory; the CTA whose slice holds T finds the segment from its
+// partial sums and one warp rescans those 128 tokens.  HBM traffic: the p and
+// q rows of j* (2 x 4V bytes; 4V when all drafts pass), read once.
 // ---------------------------------------------------------------------------
 constexpr int kSampleCluster = 8;
-constexpr int kSampleThreads = 256;
+constexpr int kSampleThreads = 512;
+constexpr int kSampleWarps = kSampleThreads / 32;
+constexpr int kSampleChunk = 4 * kSampleThreads;  // tokens per chunk: 4 consecutive per thread
+constexpr int kSampleMaxSegs = 1024;               // (chunk, warp) partial sums kept per CTA
 
 __device__ __forceinline__ uint64_t quant32(float x) {
     if (!(x > 0.0f)) return 0;  // <= 0 or NaN
@@ -170,62 +173,62 @@ __device__ __forceinline__ uint64_t scaled_floor(float s, uint64_t total) {
     return (hi << (64 - sh)) | (lo >> sh);
 }
 
-__device__ __forceinline__ uint64_t sample_weight(const float* pr, const float* qr, long long t, int residual) {
-    const float pv = __ldg(pr + t);
-    return residual ? quant32(__fsub_rn(pv, __ldg(qr + t))) : quant32(pv);
+// Weights of tokens e0..e0+3 (0 past hi): quantised p - q (residual) or p.
+__device__ __forceinline__ void weights4(const float* pr, const float* qr, long long e0, long long hi, bool vec,
+                                         int residual, uint64_t w[4]) {
+    if (vec && e0 + 3 < hi) {
+        const float4 a = __ldg(reinterpret_cast<const float4*>(pr + e0));
+        if (residual) {
+            const float4 c = __ldg(reinterpret_cast<const float4*>(qr + e0));
+            w[0] = quant32(__fsub_rn(a.x, c.x));
+            w[1] = quant32(__fsub_rn(a.y, c.y));
+            w[2] = quant32(__fsub_rn(a.z, c.z));
+            w[3] = quant32(__fsub_rn(a.w, c.w));
+        } else {
+            w[0] = quant32(a.x);
+            w[1] = quant32(a.y);
+            w[2] = quant32(a.z);
+            w[3] = quant32(a.w);
+        }
+        return;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const long long t = e0 + u;
+        w[u] = 0;
+        if (t < hi) {
+            const float pv = __ldg(pr + t);
+            w[u] = residual ? quant32(__fsub_rn(pv, __ldg(qr + t))) : quant32(pv);
+        }
+    }
 }
 
-__device__ __forceinline__ uint64_t block_sum_u64(uint64_t v, uint64_t* wsum) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ __forceinline__ uint64_t warp_sum_u64(uint64_t v) {
 #pragma unroll
     for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-    if (lane == 0) wsum[warp] = v;
-    __syncthreads();
-    uint64_t t = 0;
-#pragma unroll
-    for (int w = 0; w < kSampleThreads / 32; ++w) t += wsum[w];
-    __syncthreads();
-    return t;
+    return v;
 }
 
-// Inclusive block scan (uint64), returns this thread's inclusive prefix and the block total.
-__device__ __forceinline__ uint64_t block_scan_u64(uint64_t v, uint64_t* wsum, uint64_t* total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint64_t x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint64_t y = __shfl_up_sync(kFull, x, o);
-        if (lane >= o) x += y;
-    }
-    if (lane == 31) wsum[warp] = x;
-    __syncthreads();
-    uint64_t before = 0, t = 0;
-#pragma unroll
-    for (int w = 0; w < kSampleThreads / 32; ++w) {
-        if (w < warp) before += wsum[w];
-        t += wsum[w];
-    }
-    __syncthreads();
-    *total = t;
-    return before + x;
-}
-
-__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSampleThreads)
+__global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSampleThreads, 2)
     spec_sample_kernel(const float* __restrict__ p, const float* __restrict__ q, const int32_t* __restrict__ draft,
                        const float* __restrict__ r, const float* __restrict__ s, int num_seqs, int k, int vocab,
                        int vec4, int32_t* __restrict__ accepted, int32_t* __restrict__ next_token,
                        int32_t* status) {
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
-    __shared__ uint64_t wsum[kSampleThreads / 32];
+    // partial sums per (chunk, warp) in token order: segment i covers tokens
+    // lo + (i / W) * chunk + (i % W) * 128 ... + 127
+    __shared__ uint64_t seg[kSampleMaxSegs];
     __shared__ uint64_t slice_total;
-    __shared__ int s_rej, s_bad;
+    __shared__ int s_rej, s_bad, s_seg;
+    __shared__ uint64_t s_run;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long V = vocab;
     long long per = (V + kSampleCluster - 1) / kSampleCluster;
     per = (per + 3) & ~3LL;
     const long long lo = rank * per < V ? rank * per : V;
     const long long hi = lo + per < V ? lo + per : V;
+    const int nchunks = (int)((hi - lo + kSampleChunk - 1) / kSampleChunk);  // <= kSampleMaxSegs / kSampleWarps
     pdl_wait();
     pdl_launch();
     for (int b = blockIdx.y; b < num_seqs; b += gridDim.y) {
@@ -263,40 +266,38 @@ __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSample
         const int j = s_rej;
         const float* pr = p + ((long long)b * (k + 1) + j) * V;
         const float* qr = j < k ? q + ((long long)b * k + j) * V : p;
+        const bool vec = vec4 != 0;
         int residual = j < k ? 1 : 0;
         uint64_t total = 0, before = 0, mine = 0;
         for (;;) {
-            // this CTA's slice total
+            // one pass over this CTA's slice in token order; each warp keeps the
+            // sum of its 128 tokens of every chunk
             uint64_t acc = 0;
-            if (vec4) {
-                const float4* p4 = reinterpret_cast<const float4*>(pr + lo);
-                const float4* q4 = reinterpret_cast<const float4*>(qr + lo);
-                const long long n4 = (hi - lo) >> 2;
-                for (long long i = tid; i < n4; i += kSampleThreads) {
-                    const float4 a = __ldg(p4 + i);
-                    if (residual) {
-                        const float4 c = __ldg(q4 + i);
-                        acc += quant32(__fsub_rn(a.x, c.x)) + quant32(__fsub_rn(a.y, c.y)) +
-                               quant32(__fsub_rn(a.z, c.z)) + quant32(__fsub_rn(a.w, c.w));
-                    } else {
-                        acc += quant32(a.x) + quant32(a.y) + quant32(a.z) + quant32(a.w);
-                    }
-                }
-                for (long long t = lo + 4 * n4 + tid; t < hi; t += kSampleThreads) acc += sample_weight(pr, qr, t, residual);
-            } else {
-                for (long long t = lo + tid; t < hi; t += kSampleThreads) acc += sample_weight(pr, qr, t, residual);
+#pragma unroll 8
+            for (int c = 0; c < nchunks; ++c) {
+                uint64_t w[4];
+                weights4(pr, qr, lo + (long long)c * kSampleChunk + 4 * tid, hi, vec, residual, w);
+                const uint64_t sw = warp_sum_u64(w[0] + w[1] + w[2] + w[3]);
+                if (lane == 0) seg[c * kSampleWarps + warp] = sw;
+                acc += sw;
             }
-            mine = block_sum_u64(acc, wsum);
-            if (tid == 0) slice_total = mine;
+            __syncthreads();
+            if (tid == 0) {
+                uint64_t t = 0;
+                for (int i = 0; i < nchunks * kSampleWarps; ++i) t += seg[i];
+                slice_total = t;
+            }
             cluster.sync();
             total = 0;
             before = 0;
             for (int c = 0; c < kSampleCluster; ++c) {
                 const uint64_t t = *cluster.map_shared_rank(&slice_total, c);
                 if (c < rank) before += t;
+                if (c == rank) mine = t;
                 total += t;
             }
             cluster.sync();  // slice_total is rewritten by a second pass
+            (void)acc;
             if (total == 0 && residual) {
                 residual = 0;  // no positive residual: draw from p itself
                 continue;
@@ -314,31 +315,55 @@ __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSample
         }
         const uint64_t T = scaled_floor(__ldg(s + b), total);
         if (total > 0 && mine > 0 && T >= before && T - before < mine) {
-            // rescan this slice in index order: 4 consecutive tokens per thread
-            uint64_t run = before;
-            for (long long c = lo; c < hi; c += 4 * kSampleThreads) {
-                const long long e0 = c + 4 * tid;
-                uint64_t w4[4] = {0, 0, 0, 0};
+            // the 128-token segment that holds T (warp 0 scans the segment sums,
+            // m consecutive segments per lane), then the token inside it
+            if (warp == 0) {
+                const int nseg = nchunks * kSampleWarps;
+                const int m = (nseg + 31) / 32;
+                const int i0 = lane * m, i1 = min(nseg, i0 + m);
+                uint64_t mine_s = 0;
+                for (int i = i0; i < i1; ++i) mine_s += seg[i];
+                uint64_t incl = mine_s;
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (e0 + u < hi) w4[u] = sample_weight(pr, qr, e0 + u, residual);
-                uint64_t chunk;
-                const uint64_t incl = block_scan_u64(w4[0] + w4[1] + w4[2] + w4[3], wsum, &chunk);
-                if (run + chunk > T) {
-                    // the thread whose inclusive prefix first exceeds T - run owns the token
-                    const uint64_t excl = incl - (w4[0] + w4[1] + w4[2] + w4[3]);
-                    if (run + excl <= T && run + incl > T) {
-                        uint64_t cum = run + excl;
-                        int u = 0;
-                        for (; u < 3; ++u) {
-                            cum += w4[u];
-                            if (cum > T) break;
-                        }
-                        next_token[b] = (int32_t)(e0 + u);
-                    }
-                    break;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint64_t y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
                 }
-                run += chunk;
+                uint64_t run = before + incl - mine_s;
+                if (run <= T && run + mine_s > T) {
+                    int i = i0;
+                    for (; i < i1 - 1; ++i) {
+                        if (run + seg[i] > T) break;
+                        run += seg[i];
+                    }
+                    s_seg = i;
+                    s_run = run;
+                }
+            }
+            __syncthreads();
+            if (warp == 0) {
+                const int i = s_seg;
+                const long long e0 = lo + (long long)(i / kSampleWarps) * kSampleChunk + (i % kSampleWarps) * 128 + 4 * lane;
+                uint64_t w[4];
+                weights4(pr, qr, e0, hi, vec, residual, w);
+                const uint64_t mine4 = w[0] + w[1] + w[2] + w[3];
+                uint64_t incl = mine4;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint64_t y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const uint64_t run = s_run;
+                const uint64_t excl = incl - mine4;
+                if (run + excl <= T && run + incl > T) {
+                    uint64_t cum = run + excl;
+                    int u = 0;
+                    for (; u < 3; ++u) {
+                        cum += w[u];
+                        if (cum > T) break;
+                    }
+                    next_token[b] = (int32_t)(e0 + u);
+                }
             }
         }
         cluster.sync();  // shared state is reused for the next sequence
@@ -358,6 +383,9 @@ extern "C" int pkv_spec_accept_sample(const float* p, const float* q, const int3
     const int rc = host::check_device();
     if (rc) return rc;
     if ((long long)num_seqs * (k + 1) * vocab > (1LL << 40)) return PKV_ERR_SIZE;
+    // each CTA of a cluster keeps one partial sum per (chunk, warp) of its slice
+    const long long slice = ((long long)vocab + kSampleCluster - 1) / kSampleCluster + 3;
+    if ((slice + kSampleChunk - 1) / kSampleChunk * kSampleWarps > kSampleMaxSegs) return PKV_ERR_SIZE;
     const int vec4 = (vocab % 4 == 0) && host::aligned16(p) && host::aligned16(q);
     dim3 grid(kSampleCluster, (unsigned)(num_seqs < 65535 ? num_seqs : 65535));
     const cudaError_t e = host::launch_pdl(spec_sample_kernel, grid, dim3(kSampleThreads), 0, (cudaStream_t)stream,
