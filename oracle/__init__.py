@@ -57,6 +57,10 @@ def _load():
                 "oracle_attention_split": [P, P, P, P, I, P, P, P, P, I, P, P, I, I, I, I, I, I, D, I],
                 "oracle_spec_accept_greedy": [P, P, P, P, P, I, I, I],
                 "oracle_spec_accept_sample": [P, P, P, P, P, P, P, I, I, I],
+                "oracle_e4m3_encode": [P, P, ctypes.c_int64],
+                "oracle_e4m3_decode": [P, P, ctypes.c_int64],
+                "oracle_kv_append_fp8": [P, P, P, P, P, I, I, I, I, I, P, P],
+                "oracle_attention_fp8": [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, D],
                 "oracle_num_threads": [],
             }
             for name, argt in sigs.items():
@@ -181,6 +185,51 @@ def attention_split(q, k_cache, v_cache, block_tables, seq_lens, q_lens, scale, 
     if want_partials:
         return out[:n], st, po[:n], pm[:n], pl[:n]
     return out[:n], st
+
+
+def e4m3_encode(x):
+    """fp32 -> e4m3 codes (round to nearest even, saturate to 448, NaN kept)."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load().oracle_e4m3_encode(_p(out), _p(x), x.size)
+    return out
+
+
+def e4m3_decode(codes):
+    """e4m3 codes -> exact fp64 values (NaN for S.1111.111)."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_e4m3_decode(_p(out), _p(c), c.size)
+    return out
+
+
+def kv_append_fp8(k_cache8, v_cache8, k_new, v_new, slots, k_scale, v_scale):
+    """Append bf16 rows into e4m3 pools in place ("Inference at Scale" 03, KV
+    cache quantization): code = e4m3(x * (1 / scale[head])).  Returns status."""
+    nb, nkv, bs, d = k_cache8.shape
+    assert k_cache8.dtype == np.uint8 and v_cache8.dtype == np.uint8
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    sl = _c(slots, np.int64)
+    return _load().oracle_kv_append_fp8(_p(k_cache8), _p(v_cache8), _p(kn), _p(vn), _p(sl), len(sl), nb, bs, nkv, d,
+                                        _p(_c(k_scale, np.float32)), _p(_c(v_scale, np.float32)))
+
+
+def attention_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_lens, q_lens, scale):
+    """attention() over e4m3 pools: K = e4m3(K) * k_scale[kv head], V likewise."""
+    qq = _c(q, np.uint16)
+    T, n_q, d = qq.shape
+    nb, nkv, bs, d2 = k_cache8.shape
+    if d2 != d or n_q % nkv or T < int(np.maximum(np.asarray(q_lens), 0).sum()):
+        raise ValueError("q must be [sum q_lens][n_q][head_dim] with n_q a multiple of n_kv")
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ql = _c(q_lens, np.int32)
+    out = np.zeros((T, n_q, d), np.float64)
+    st = _load().oracle_attention_fp8(_p(out), _p(qq), _p(_c(k_cache8, np.uint8)), _p(_c(v_cache8, np.uint8)),
+                                      _p(_c(k_scale, np.float32)), _p(_c(v_scale, np.float32)), _p(bt), bt.shape[1],
+                                      _p(sl), _p(ql), len(sl), n_q, nkv, d, bs, nb, float(scale))
+    return out, st
 
 
 def spec_accept_sample(p, q, draft, r, s):

@@ -419,6 +419,143 @@ int oracle_spec_accept_greedy(int32_t *accepted, int32_t *next_token, int32_t *a
 }
 
 /*
+ * FP8 KV cache ([KVC] 03 "KV cache quantization": store K and V in FP8,
+ * 1 byte per value, formats e4m3 and e5m2; this build takes e4m3).
+ *
+ * e4m3 (the "fn" variant: no infinities): sign bit, 4 exponent bits with bias
+ * 7, 3 mantissa bits; exponent field 0 holds subnormals m * 2^-9; code
+ * S.1111.111 is NaN; the largest finite magnitude is 1.75 * 2^8 = 448.
+ * Encoding rounds to the nearest representable value, ties to the even code,
+ * and saturates magnitudes above 448 to 448; NaN stays NaN (0x7f).
+ *
+ * Scales (a reading: the pages fix none): one fp32 dequantisation scale per kv
+ * head for K and one for V, supplied by the caller.  Appending a bf16 row
+ * stores e4m3(x * (1 / scale)), with 1 / scale and the product each rounded
+ * to fp32 (round to nearest even); reading decodes e4m3 and multiplies by the
+ * scale (exactly, in fp64 here).
+ */
+static double e4m3_value(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return s ? -v : v;
+}
+
+static uint8_t e4m3_encode(float x) {
+    if (isnan(x)) return 0x7f;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 448.0) return sign | 0x7e;
+    /* largest finite code whose magnitude is <= a (magnitudes grow with the code) */
+    int c = 0;
+    while (c < 0x7e && e4m3_value((uint8_t)(c + 1)) <= a) c++;
+    if (c < 0x7e) {
+        const double lo = e4m3_value((uint8_t)c), hi = e4m3_value((uint8_t)(c + 1));
+        if (a - lo > hi - a || (a - lo == hi - a && (c & 1))) c++;
+    }
+    return sign | (uint8_t)c;
+}
+
+int oracle_e4m3_encode(uint8_t *out, const float *in, int64_t n) {
+    for (int64_t i = 0; i < n; i++) out[i] = e4m3_encode(in[i]);
+    return 0;
+}
+
+int oracle_e4m3_decode(double *out, const uint8_t *in, int64_t n) {
+    for (int64_t i = 0; i < n; i++) out[i] = e4m3_value(in[i]);
+    return 0;
+}
+
+/* KV append into an e4m3 pool: as oracle_kv_append, each value quantised. */
+int oracle_kv_append_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_new, const uint16_t *v_new,
+                         const int64_t *slots, int num_tokens, int num_blocks, int block_size, int n_kv, int d,
+                         const float *k_scale, const float *v_scale) {
+    int status = 0;
+    for (int t = 0; t < num_tokens; t++) {
+        int64_t s = slots[t];
+        if (s < 0) continue;
+        if (s >= (int64_t)num_blocks * block_size) { status |= ST_BAD_SLOT; continue; }
+        int64_t blk = s / block_size;
+        int row = (int)(s % block_size);
+        for (int h = 0; h < n_kv; h++) {
+            const float ik = 1.0f / k_scale[h], iv = 1.0f / v_scale[h];
+            for (int c = 0; c < d; c++) {
+                int64_t dst = cache_offset(blk, h, row, n_kv, block_size, d) + c;
+                int64_t src = ((int64_t)t * n_kv + h) * d + c;
+                const float xk = (float)widen_bf16(k_new[src]) * ik;
+                const float xv = (float)widen_bf16(v_new[src]) * iv;
+                k_cache[dst] = e4m3_encode(xk);
+                v_cache[dst] = e4m3_encode(xv);
+            }
+        }
+    }
+    return status;
+}
+
+/*
+ * Attention over an e4m3 pool: oracle_attention with K_t = e4m3(K) * k_scale[j]
+ * and V_t = e4m3(V) * v_scale[j] for kv head j.
+ */
+int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                         const float *k_scale, const float *v_scale, const int32_t *block_tables, int max_blocks,
+                         const int32_t *seq_lens, const int32_t *q_lens, int num_seqs, int n_q, int n_kv, int d,
+                         int block_size, int num_blocks, double scale) {
+    int status = 0;
+    int g = n_q / n_kv;
+    int64_t *row0 = (int64_t *)malloc(sizeof(int64_t) * (num_seqs + 1));
+    row0[0] = 0;
+    for (int b = 0; b < num_seqs; b++) row0[b + 1] = row0[b] + (q_lens[b] > 0 ? q_lens[b] : 0);
+    for (int b = 0; b < num_seqs; b++) status |= check_seq(seq_lens[b], q_lens[b], max_blocks, block_size);
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
+    for (int b = 0; b < num_seqs; b++) {
+        int L = seq_lens[b], ql = q_lens[b];
+        if (ql <= 0) continue;
+        int seq_bad = check_seq(L, ql, max_blocks, block_size);
+        double *s = (double *)malloc(sizeof(double) * (L > 0 ? L : 1));
+        for (int i = 0; i < ql; i++) {
+            int64_t r = row0[b] + i;
+            int p = L - ql + i;
+            for (int h = 0; h < n_q; h++) {
+                double *o = out + (r * n_q + h) * d;
+                const uint16_t *qv = q + (r * n_q + h) * d;
+                int j = h / g;
+                int bad = seq_bad;
+                for (int t = 0; t <= p && !bad; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    if (blk < 0 || blk >= num_blocks) { bad = 1; status |= ST_BAD_BLOCK; }
+                }
+                if (bad) {
+                    for (int c = 0; c < d; c++) o[c] = NAN;
+                    continue;
+                }
+                for (int t = 0; t <= p; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    const uint8_t *kt = k_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                    double acc = 0.0;
+                    for (int c = 0; c < d; c++) acc += widen_bf16(qv[c]) * (e4m3_value(kt[c]) * (double)k_scale[j]);
+                    s[t] = scale * acc;
+                }
+                double M = -INFINITY;
+                for (int t = 0; t <= p; t++) if (s[t] > M) M = s[t];
+                double den = 0.0;
+                for (int t = 0; t <= p; t++) { s[t] = exp(s[t] - M); den += s[t]; }
+                for (int c = 0; c < d; c++) o[c] = 0.0;
+                for (int t = 0; t <= p; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    const uint8_t *vt = v_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                    for (int c = 0; c < d; c++) o[c] += s[t] * (e4m3_value(vt[c]) * (double)v_scale[j]);
+                }
+                for (int c = 0; c < d; c++) o[c] /= den;
+            }
+        }
+        free(s);
+    }
+    free(row0);
+    return status;
+}
+
+/*
  * Stochastic speculative acceptance -- modified rejection sampling
  * ([SE] 31.5 and Example 31.3; [SI] 12.4; [KVC] 08 "Why the output keeps the
  * exact distribution").

@@ -303,6 +303,36 @@ def spec(B: int = 32, lo: int = 2048, hi: int = 8192, k: int = 5, vocab: int = 1
 
 
 @dataclass
+class Fp8Pools:
+    """An e4m3 KV cache holding the same structure as a bf16 workload's pools:
+    uint8 codes [num_blocks][n_kv][bs][d] and one fp32 dequantisation scale per
+    kv head for K and for V."""
+    k_cache: np.ndarray
+    v_cache: np.ndarray
+    k_scale: np.ndarray
+    v_scale: np.ndarray
+
+
+def fp8_pools(w: Workload, seed: int = 0) -> Fp8Pools:
+    """Random e4m3 contents for the rows the bf16 workload holds (sign random,
+    exponent field 4..10 -- magnitudes 2^-3..15 --, mantissa random; no
+    encoding step), e4m3 NaN (0x7f) wherever the bf16 pool is NaN (unused
+    rows and spare blocks), and per-head scales 2^-3 * U[0.5, 1.5]."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 8])))
+    out = []
+    for pool in (w.k_cache, w.v_cache):
+        sign = g.integers(0, 2, size=pool.shape, dtype=np.uint8) << 7
+        expo = g.integers(4, 11, size=pool.shape, dtype=np.uint8) << 3
+        mant = g.integers(0, 8, size=pool.shape, dtype=np.uint8)
+        codes = sign | expo | mant
+        codes[(pool & 0x7FFF) > 0x7F80] = 0x7F
+        out.append(codes)
+    ks = (0.125 * g.uniform(0.5, 1.5, size=w.n_kv)).astype(np.float32)
+    vs = (0.125 * g.uniform(0.5, 1.5, size=w.n_kv)).astype(np.float32)
+    return Fp8Pools(out[0], out[1], ks, vs)
+
+
+@dataclass
 class SampleInputs:
     """Inputs of stochastic speculative acceptance: target distributions
     p [B][k+1][V], draft distributions q [B][k][V] (fp32, each row sums to 1),
