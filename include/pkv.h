@@ -238,6 +238,51 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
                                        void* stream);
 
 /*
+ * FP8 KV cache ([KVC] 03, "KV cache quantization": store K and V in FP8, one
+ * byte per value instead of two, halving the cache and the bytes decode
+ * attention rereads; the formats are e4m3 and e5m2 -- these entry points use
+ * e4m3, the variant without infinities: bias 7, 3 mantissa bits, largest
+ * finite 448, S.1111.111 = NaN).
+ *
+ * Pools are uint8 [num_blocks][num_kv_heads][block_size][head_dim] in the
+ * bf16 pools' layout.  Scales (the pages fix none): one fp32 dequantisation
+ * scale per kv head for K (k_scale[num_kv_heads]) and for V, device memory,
+ * chosen by the caller (for instance the head's largest magnitude / 448).
+ *
+ * pkv_kv_append_fp8: as pkv_kv_append, each bf16 value x of head h stored as
+ * e4m3(x * (1 / scale[h])) -- the reciprocal and the product rounded to fp32
+ * (nearest even), the conversion rounding to nearest even and saturating to
+ * +-448 (NaN stays NaN).  Bit-exact; pools need 8-byte alignment.
+ */
+int pkv_kv_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                      const int64_t* slot_mapping, const float* k_scale, const float* v_scale,
+                      int num_tokens, int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                      int32_t* status, void* stream);
+
+/* pkv_copy_blocks for e4m3 pools (head_dim a multiple of 16).  Bit-exact. */
+int pkv_copy_blocks_fp8(void* k_cache, void* v_cache, const int32_t* src_dst, int num_pairs,
+                        int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                        int32_t* status, void* stream);
+
+/*
+ * pkv_paged_attention_decode over e4m3 pools: the same softmax attention with
+ * K_t = e4m3(code) * k_scale[h / g] and V_t = e4m3(code) * v_scale[h / g]
+ * ([KVC] 03; the attention itself as in pkv_paged_attention_decode, [KVC]
+ * 05, 07, 08).  head_dim 128 and g <= 16; the other arguments, the workspace
+ * (pkv_attention_workspace_bytes), the outputs and the error behaviour are
+ * those of pkv_paged_attention_decode (no flags).  The products run on f16
+ * tensor cores: e4m3 -> f16 is exact, q is rounded from bf16 to f16 (exact
+ * for |q| in [6.1e-5, 65504]), accumulation is fp32, out is bf16.
+ */
+int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                   const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                                   int max_blocks, const int32_t* seq_lens, const int32_t* q_lens,
+                                   int num_seqs, int total_q, int max_seq_len, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   float scale, int partition_tokens, void* workspace,
+                                   size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * a9. Greedy speculative acceptance ([SI] 12.4; [KVC] 08: with greedy
  * decoding a draft token is accepted when it equals the target's argmax;
  * stop at the first mismatch; the round always adds one target token).

@@ -51,6 +51,10 @@ _SIGS = {
                                     ctypes.c_float, _I, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_spec_accept_greedy": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
     "pkv_spec_accept_sample": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+    "pkv_kv_append_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_copy_blocks_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_paged_attention_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                        ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "pkv_paged_attention_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                             ctypes.c_float, _I, _I, _P, _P], _I),
@@ -201,6 +205,56 @@ def spec_accept_greedy(logits, draft, argmax_out, accepted, next_token, stream=N
     rc = lib().pkv_spec_accept_greedy(_ptr(logits), _ptr(draft), B, k1 - 1, V, _ptr(argmax_out), _ptr(accepted),
                                       _ptr(next_token), _stream(stream))
     _check(rc, "pkv_spec_accept_greedy")
+
+
+def kv_append_fp8(k_cache, v_cache, k_new, v_new, slots, k_scale, v_scale, status=None, stream=None):
+    """Append bf16 rows into e4m3 pools (uint8 [nb][n_kv][bs][d]) with per-head scales."""
+    _dev(k_cache, "k_cache", torch.uint8)
+    _dev(v_cache, "v_cache", torch.uint8)
+    _dev(k_new, "k_new", torch.bfloat16)
+    _dev(v_new, "v_new", torch.bfloat16)
+    _dev(slots, "slots", torch.int64)
+    _dev(k_scale, "k_scale", torch.float32)
+    _dev(v_scale, "v_scale", torch.float32)
+    nb, nkv, bs, d = k_cache.shape
+    rc = lib().pkv_kv_append_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(slots), _ptr(k_scale),
+                                 _ptr(v_scale), slots.numel(), nb, bs, nkv, d, _ptr(status), _stream(stream))
+    _check(rc, "pkv_kv_append_fp8")
+
+
+def copy_blocks_fp8(k_cache, v_cache, src_dst, status=None, stream=None):
+    _dev(k_cache, "k_cache", torch.uint8)
+    _dev(v_cache, "v_cache", torch.uint8)
+    _dev(src_dst, "src_dst", torch.int32)
+    nb, nkv, bs, d = k_cache.shape
+    rc = lib().pkv_copy_blocks_fp8(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst), src_dst.shape[0], nb, bs, nkv, d,
+                                   _ptr(status), _stream(stream))
+    _check(rc, "pkv_copy_blocks_fp8")
+
+
+def paged_attention_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, q_lens,
+                               max_seq_len, scale, workspace, partition_tokens=0, status=None, stream=None):
+    """Paged attention over e4m3 pools (uint8 [nb][n_kv][bs][d]) with per-kv-head scales."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_cache, "k_cache", torch.uint8)
+    _dev(v_cache, "v_cache", torch.uint8)
+    _dev(k_scale, "k_scale", torch.float32)
+    _dev(v_scale, "v_scale", torch.float32)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(q_lens, "q_lens", torch.int32)
+    _dev(workspace, "workspace")
+    nb, nkv, bs, d = k_cache.shape
+    total_q, nq, _ = q.shape
+    rc = lib().pkv_paged_attention_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                              _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
+                                              _ptr(seq_lens), _ptr(q_lens), seq_lens.numel(), total_q,
+                                              int(max_seq_len), nq, nkv, d, bs, nb, float(scale),
+                                              int(partition_tokens), _ptr(workspace),
+                                              workspace.numel() * workspace.element_size(), _ptr(status),
+                                              _stream(stream))
+    _check(rc, "pkv_paged_attention_decode_fp8")
 
 
 def spec_accept_sample(p, q, draft, r, s, accepted, next_token, status=None, stream=None):

@@ -49,7 +49,7 @@ int sm_count() {
 }
 
 int encode_tiled(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                 const uint32_t* box, CUtensorMapSwizzle swizzle) {
+                 const uint32_t* box, CUtensorMapSwizzle swizzle, bool bytes) {
     {
         std::lock_guard<std::mutex> lk(g_mu);
         if (g_encode == nullptr) {
@@ -71,7 +71,8 @@ int encode_tiled(CUtensorMap* map, const void* base, int rank, const uint64_t* d
         es[i] = 1;
         if (i + 1 < rank) gs[i] = strides[i];
     }
-    const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), gd,
+    const CUresult r = g_encode(map, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                                (cuuint32_t)rank, const_cast<void*>(base), gd,
                                 gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : -1;

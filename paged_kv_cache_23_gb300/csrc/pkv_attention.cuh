@@ -83,19 +83,33 @@ struct AttnParams {
     float* part_o;       // [(row * n_q + h) * np_max + part][D]
     float2* part_ml;     // [(row * n_q + h) * np_max + part] = (m in log2 units, l)
     int32_t* status;
+    const float* k_scale;  // e4m3 pools: dequantisation scale per kv head (null for bf16)
+    const float* v_scale;
     int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, row_bytes;
     float scale_log2;    // scale * log2(e): scores live in base-2 units
 };
 
-template <int D>
+// Stage geometry of a pool: bf16 (2-byte values, 3 ring slots of 64 KB at the
+// 8B shape) or e4m3 (1-byte values, 6 ring slots of 32 KB -- the same 192 KB
+// of shared memory holds twice the stages, so twice the copies in flight).
+template <int D, bool F8>
+struct Geo {
+    static constexpr int kElem = F8 ? 1 : 2;
+    static constexpr int kRow = D * kElem;                  // bytes of one token of one head
+    static constexpr int kNB = kRow / 128;                  // 128-byte boxes per row
+    static constexpr int kSlots = F8 ? 6 : kRingSlots;      // ring slots
+    static constexpr int kHalf = kTileT * kMaxHPS * kRow;   // K (or V) bytes of one stage
+};
+
+template <int D, bool F8 = false>
 struct Smem {
-    static constexpr int kHalf = kTileT * kMaxHPS * D * 2;   // K (or V) bytes of one stage
-    uint8_t kv[kRingSlots][2][kHalf];                        // [slot][K,V][rows of 128 B], swizzled
+    using G = Geo<D, F8>;
+    uint8_t kv[G::kSlots][2][G::kHalf];                      // [slot][K,V][rows of 128 B], swizzled
     float pbuf[kCWarps][kTileT * 8];                         // decode: p[token][head]
     Desc desc[kSlots];
     int poison[kSlots];
     int abort;
-    uint64_t full[kRingSlots], empty[kRingSlots], ifull[kSlots], iempty[kSlots];
+    uint64_t full[G::kSlots], empty[G::kSlots], ifull[kSlots], iempty[kSlots];
 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -139,15 +153,11 @@ __device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, int P) {
     d.hps = (sq.w >> 4) & 15;
     d.wph = (sq.w >> 8) & 15;
     const int QT = (sq.w >> 12) & 4095;
-    if (d.kind != KIND_MQ) {
-        d.nq = 1;
-        d.t_vis = L;
-        d.q_row0 = q0;
-    } else {
-        d.nq = min(QT, ql - qt * QT);
-        d.t_vis = L - ql + qt * QT + d.nq;
-        d.q_row0 = q0 + qt * QT;
-    }
+    // query tile qt holds queries [qt*QT, qt*QT + nq); its last query sees t_vis
+    // positions (a decode row is a tile of one query: t_vis = L)
+    d.nq = min(QT, ql - qt * QT);
+    d.t_vis = L - ql + qt * QT + d.nq;
+    d.q_row0 = q0 + qt * QT;
     d.nparts = ceil_div(d.t_vis, P);
     d.t_begin = d.part * P;
     d.t_end = min(d.t_begin + P, d.t_vis);
@@ -157,9 +167,9 @@ __device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, int P) {
 // ---------------------------------------------------------------------------
 // Producer warp: item queue, block-table reads, TMA stage stream.
 // ---------------------------------------------------------------------------
-template <int D>
-__device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const AttnParams& p, int lane) {
-    constexpr int NB = D / 64;
+template <int D, bool F8>
+__device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const AttnParams& p, int lane) {
+    constexpr int RS = Geo<D, F8>::kSlots;
     volatile int* abort = &sm.abort;
     if (lane < 4) {
         prefetch_tmap(&tm->k[lane]);
@@ -196,7 +206,7 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
         if (end) break;
         const CUtensorMap* mk = &tm->k[log2i(d.hps)];
         const CUtensorMap* mv = &tm->v[log2i(d.hps)];
-        const uint32_t op_bytes = (uint32_t)d.hps * bsr * D * 2;
+        const uint32_t op_bytes = (uint32_t)d.hps * bsr * Geo<D, F8>::kRow;
         const int tb = d.t_begin / kTileT, te = (d.t_end + kTileT - 1) / kTileT;
         const int32_t* bt = p.block_tables + (long long)d.b * p.max_blocks;
         bool stopped = false;
@@ -220,22 +230,23 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
                 const int en = tab_base + 32 + lane;
                 tab_next = en < e_lim ? __ldg(bt + en) : 0;
             }
-            const int off = e0 - tab_base + lane;  // in [0, 48)
+            // lanes 2e and 2e+1 issue the K and the V copy of the stage's block e
+            const int off = e0 - tab_base + (lane >> 1);  // in [0, 48)
             const int lo = __shfl_sync(kFull, tab, off & 31);
             const int hi = __shfl_sync(kFull, tab_next, off & 31);
             int my = off < 32 ? lo : hi;
-            const bool in = lane < ne;
+            const bool in = (lane >> 1) < ne;
             const bool okb = !in || (my >= 0 && my < p.num_blocks);
             if (!okb) my = 0;
             const unsigned badmask = __ballot_sync(kFull, !okb);
-            const int s = (int)(g % kRingSlots);
+            const int s = (int)(g % RS);
             bool got = true;
             if (lane == 0) {
                 if (badmask) {
                     sm.poison[si] = 1;
                     report(p.status, PKV_STATUS_BAD_BLOCK);
                 }
-                got = mbar_wait(&sm.empty[s], ((g / kRingSlots) & 1) ^ 1, abort);
+                got = mbar_wait(&sm.empty[s], ((g / RS) & 1) ^ 1, abort);
                 if (got) mbar_arrive_expect_tx(&sm.full[s], 2u * ne * op_bytes);
             }
             if (!__shfl_sync(kFull, got, 0)) {
@@ -243,12 +254,11 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
                 break;
             }
             // one box per tensor and block: every head of the group, 16 (or block_size) rows
-            if (lane < ne) {
+            if (in) {
                 const int row0 = p.bs > kTileT ? (t0 % p.bs) : 0;
-                uint8_t* dk = &sm.kv[s][0][lane * op_bytes];
-                uint8_t* dv = &sm.kv[s][1][lane * op_bytes];
-                tma_load_5d(dk, mk, 0, 0, row0, d.hg * d.hps, my, &sm.full[s]);
-                tma_load_5d(dv, mv, 0, 0, row0, d.hg * d.hps, my, &sm.full[s]);
+                const int v = lane & 1;
+                tma_load_5d(&sm.kv[s][v][(lane >> 1) * op_bytes], v ? mv : mk, 0, 0, row0, d.hg * d.hps, my,
+                            &sm.full[s]);
             }
             __syncwarp();
         }
@@ -257,13 +267,12 @@ __device__ __forceinline__ void producer(Smem<D>& sm, const TMaps* tm, const Att
     }
     // drain: wait (bounded) until every issued stage has landed
     if (lane == 0) {
-        for (int s = 0; s < kRingSlots; ++s) {
+        for (int s = 0; s < RS; ++s) {
             if (g <= (uint32_t)s) continue;
-            const uint32_t last = g - 1 - ((g - 1 - s) % kRingSlots);
-            mbar_wait(&sm.full[s], (last / kRingSlots) & 1, abort);
+            const uint32_t last = g - 1 - ((g - 1 - s) % RS);
+            mbar_wait(&sm.full[s], (last / RS) & 1, abort);
         }
     }
-    (void)NB;
 }
 
 // ---------------------------------------------------------------------------
@@ -301,7 +310,7 @@ __device__ __forceinline__ float reduce8(float* v, int li) {
 // PV every lane owns D/32 output dims of all G heads.
 // ---------------------------------------------------------------------------
 template <int D, int G>
-__device__ __forceinline__ void decode_item(Smem<D>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
+__device__ __forceinline__ void decode_item(Smem<D, false>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
                                             uint32_t gbase, int ntiles, int si, volatile int* abort) {
     constexpr int NB = D / 64;   // 128-byte boxes per row
     constexpr int HL = 8 / G;    // lanes per head in an 8-lane group
@@ -485,7 +494,7 @@ __device__ __forceinline__ void decode_item(Smem<D>& sm, const AttnParams& p, co
 // B fragments are the S^T accumulators transposed in registers (movmatrix).
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void decode_tc_item(Smem<D>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
+__device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
                                                uint32_t gbase, int ntiles, int si, volatile int* abort) {
     constexpr int NB = D / 64;
     constexpr int NT = D / 16;
@@ -644,7 +653,7 @@ __device__ __forceinline__ void decode_tc_item(Smem<D>& sm, const AttnParams& p,
 // q head) pairs of that kv head).
 // ---------------------------------------------------------------------------
 template <int D>
-__device__ __forceinline__ void mq_item(Smem<D>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
+__device__ __forceinline__ void mq_item(Smem<D, false>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
                                         uint32_t gbase, int ntiles, int si, volatile int* abort) {
     constexpr int NB = D / 64;
     const int G = p.G;
@@ -813,6 +822,230 @@ __device__ __forceinline__ void mq_item(Smem<D>& sm, const AttnParams& p, const 
 }
 
 // ---------------------------------------------------------------------------
+// Item over an e4m3 pool ("Inference at Scale" section 03, KV cache
+// quantization), any query tile of nq <= 8 * NTN / g queries: warp w < hps owns
+// kv head hg * hps + w, in the transposed form of decode_tc_item with the
+// columns N = (query, q head) pairs of the tile, 8 per n-tile, each with its
+// own causal limit:
+//   S^T[16 x 8 NTN] = K_tile[16 x D] . Q^T,   O^T[D x 8 NTN] += V_tile^T . P^T
+// on f16 tensor cores (e4m3 -> f16 is exact; Q is rounded from bf16 to f16).
+//   K: an ldmatrix row of 16 codes gives a lane 4 consecutive dims (4 qd ..
+//      4 qd + 3) of its token; the two f16 pairs feed the k slots (2 qd, 2 qd + 1)
+//      and (2 qd + 8, 2 qd + 9), and Q^T's fragments use the same permutation
+//      of the dims, so the dot products are unchanged.
+//   V: ldmatrix.trans of the byte pairs gives a lane tokens (2 qd, 2 qd + 1) x
+//      dims (2 qr, 2 qr + 1); byte permutes split them into the m-rows qr
+//      (dim 2 qr) and qr + 8 (dim 2 qr + 1), so O^T row r of chunk c holds dim
+//      16 c + 2 (r mod 8) + r / 8.
+// The per-head scales fold into the score scale (K) and the output (V).
+// ---------------------------------------------------------------------------
+template <int D, int NTN>
+__device__ __forceinline__ void swap8_item(Smem<D, true>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
+                                           uint32_t gbase, int ntiles, int si, volatile int* abort) {
+    constexpr int RS = Geo<D, true>::kSlots;
+    constexpr int NC = D / 16;  // 16-code chunks per row: k-steps of S, m-tiles of O
+    static_assert(Geo<D, true>::kNB == 1, "e4m3 rows are one 128-byte box");
+    const int G = p.G;
+    const bool active = warp < d.hps;
+    const int lb = log2i(p.bs < kTileT ? p.bs : kTileT);
+    const int hps_lb = d.hps << lb, h_lb = warp << lb;
+    const int kvh = d.hg * d.hps + warp;
+    const int qd = lane & 3, qr = lane >> 2;
+    const int ncols = d.nq * G;
+    float ksc = 0.f, vsc = 0.f;
+    uint32_t qb[NTN][NC][2];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) {
+        const int c = 8 * nt + qr;
+        const __nv_bfloat16* qrow =
+            (active && c < ncols)
+                ? p.q + ((long long)(d.q_row0 + c / G) * p.n_q + (long long)kvh * G + c % G) * D
+                : nullptr;
+#pragma unroll
+        for (int kc = 0; kc < NC; ++kc) {
+            uint2 raw = make_uint2(0u, 0u);
+            if (qrow) raw = *reinterpret_cast<const uint2*>(qrow + 16 * kc + 4 * qd);
+            const float2 x01 = bf16x2_to_float2(raw.x), x23 = bf16x2_to_float2(raw.y);
+            qb[nt][kc][0] = float2_to_f16x2(x01.x, x01.y);
+            qb[nt][kc][1] = float2_to_f16x2(x23.x, x23.y);
+        }
+    }
+    if (active) {
+        ksc = __ldg(p.k_scale + kvh) * p.scale_log2;
+        vsc = __ldg(p.v_scale + kvh);
+    }
+    // last visible position of the two columns (2 qd, 2 qd + 1) of each n-tile
+    int lim[NTN][2];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c = 8 * nt + 2 * qd + j;
+            lim[nt][j] = c < ncols ? d.t_vis - d.nq + c / G : -1;
+        }
+    float o[NC][NTN][4];
+#pragma unroll
+    for (int mc = 0; mc < NC; ++mc)
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) o[mc][nt][0] = o[mc][nt][1] = o[mc][nt][2] = o[mc][nt][3] = 0.f;
+    float m[NTN][2], l[NTN][2];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.f;
+    const int mi = lane >> 3, mr = lane & 7;
+    const int a_tok = ((mi & 1) << 3) + mr, a_ch = mi >> 1;  // (t0-7, c) (t8-15, c) (t0-7, c+1) (t8-15, c+1)
+    const int tb = d.t_begin / kTileT;
+    for (int i = 0; i < ntiles; ++i) {
+        const uint32_t gi = gbase + i;
+        const int s = (int)(gi % RS);
+        mbar_wait(&sm.full[s], (gi / RS) & 1, abort);
+        if (!active) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[s]);
+            continue;
+        }
+        const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
+        const uint32_t vb = smem_u32(&sm.kv[s][1][0]);
+        const int t0 = (tb + i) * kTileT;
+        const int nvalid = min(kTileT, d.t_end - t0);
+        const int R = srow(h_lb, a_tok, 0, hps_lb, lb, 1);
+        // S^T
+        float sc[2][NTN][4];
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt) sc[u][nt][0] = sc[u][nt][1] = sc[u][nt][2] = sc[u][nt][3] = 0.f;
+#pragma unroll
+        for (int kc2 = 0; kc2 < NC / 2; ++kc2) {
+            const int chunk = 2 * kc2 + a_ch;
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(kb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), r0, r1, r2, r3);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
+                const uint32_t a0 = e4m3x2_to_f16x2(rA), a2 = e4m3x2_to_f16x2(rA >> 16);
+                const uint32_t a1 = e4m3x2_to_f16x2(rB), a3 = e4m3x2_to_f16x2(rB >> 16);
+                const int kc = 2 * kc2 + h;
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt)
+                    mma_f16_16816(sc[h][nt], a0, a1, a2, a3, qb[nt][kc][0], qb[nt][kc][1]);
+            }
+        }
+        // scores (token qr / qr + 8, column 2 qd / 2 qd + 1) with the partition
+        // end and each column's causal limit; lazy reference maxima as in
+        // decode_tc_item
+        const int ta = t0 + qr, tb8 = t0 + qr + 8;
+        const bool in_a = qr < nvalid, in_b = qr + 8 < nvalid;
+        float sv[NTN][4];
+        bool fits = true;
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            sv[nt][0] = in_a && ta <= lim[nt][0] ? (sc[0][nt][0] + sc[1][nt][0]) * ksc : -INFINITY;
+            sv[nt][1] = in_a && ta <= lim[nt][1] ? (sc[0][nt][1] + sc[1][nt][1]) * ksc : -INFINITY;
+            sv[nt][2] = in_b && tb8 <= lim[nt][0] ? (sc[0][nt][2] + sc[1][nt][2]) * ksc : -INFINITY;
+            sv[nt][3] = in_b && tb8 <= lim[nt][1] ? (sc[0][nt][3] + sc[1][nt][3]) * ksc : -INFINITY;
+            fits = fits && fmaxf(sv[nt][0], sv[nt][2]) <= m[nt][0] + kRescaleSlack &&
+                   fmaxf(sv[nt][1], sv[nt][3]) <= m[nt][1] + kRescaleSlack;
+        }
+        if (!__all_sync(kFull, fits)) {
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt) {
+                float x0 = fmaxf(sv[nt][0], sv[nt][2]), x1 = fmaxf(sv[nt][1], sv[nt][3]);
+#pragma unroll
+                for (int o8 = 4; o8 < 32; o8 <<= 1) {
+                    x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, o8));
+                    x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, o8));
+                }
+                const float n0 = fmaxf(m[nt][0], x0), n1 = fmaxf(m[nt][1], x1);
+                const float c0 = n0 == -INFINITY ? 1.f : exp2f(m[nt][0] - n0);
+                const float c1 = n1 == -INFINITY ? 1.f : exp2f(m[nt][1] - n1);
+                l[nt][0] *= c0;
+                l[nt][1] *= c1;
+#pragma unroll
+                for (int mc = 0; mc < NC; ++mc) {
+                    o[mc][nt][0] *= c0;
+                    o[mc][nt][1] *= c1;
+                    o[mc][nt][2] *= c0;
+                    o[mc][nt][3] *= c1;
+                }
+                m[nt][0] = n0;
+                m[nt][1] = n1;
+            }
+        }
+        uint32_t pb0[NTN], pb1[NTN];
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            const float u0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0], u1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
+            const float p0 = exp2f(sv[nt][0] - u0), p1 = exp2f(sv[nt][1] - u1);
+            const float p2 = exp2f(sv[nt][2] - u0), p3 = exp2f(sv[nt][3] - u1);
+            l[nt][0] += p0 + p2;
+            l[nt][1] += p1 + p3;
+            pb0[nt] = movmatrix_trans(float2_to_f16x2(p0, p1));  // (tokens 2qd, 2qd+1; column qr)
+            pb1[nt] = movmatrix_trans(float2_to_f16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; column qr)
+        }
+        // V rows past the valid tokens may hold anything (even NaN): zero them
+        const uint32_t klo = nvalid == kTileT ? 0xffffffffu
+                                              : (2 * qd < nvalid ? 0x0000ffffu : 0u) |
+                                                    (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t khi = nvalid == kTileT ? 0xffffffffu
+                                              : (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) |
+                                                    (9 + 2 * qd < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int kc2 = 0; kc2 < NC / 2; ++kc2) {
+            const int chunk = 2 * kc2 + a_ch;
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), r0, r1, r2, r3);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
+                // bytes (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0) and (t0 d1, t1 d1)
+                const uint32_t a0 = e4m3x2_to_f16x2(__byte_perm(rA, 0u, 0x4420)) & klo;
+                const uint32_t a1 = e4m3x2_to_f16x2(__byte_perm(rA, 0u, 0x4431)) & klo;
+                const uint32_t a2 = e4m3x2_to_f16x2(__byte_perm(rB, 0u, 0x4420)) & khi;
+                const uint32_t a3 = e4m3x2_to_f16x2(__byte_perm(rB, 0u, 0x4431)) & khi;
+                const int mc = 2 * kc2 + h;
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt) mma_f16_16816(o[mc][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
+    }
+    if (!active) return;
+    const bool poisoned = sm.poison[si] != 0;  // final after the last stage's wait
+    const float qnan = __int_as_float(0x7fc00000);
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            float lj = l[nt][j];
+#pragma unroll
+            for (int o8 = 4; o8 < 32; o8 <<= 1) lj += __shfl_xor_sync(kFull, lj, o8);
+            const int c = 8 * nt + 2 * qd + j;
+            if (c >= ncols) continue;
+            const long long orow = (long long)(d.q_row0 + c / G) * p.n_q + (long long)kvh * G + c % G;
+            if (d.nparts == 1) {
+                const float inv = vsc / lj;
+                __nv_bfloat16* dst = p.out + orow * D + 2 * qr;
+#pragma unroll
+                for (int mc = 0; mc < NC; ++mc) {
+                    const uint32_t v = poisoned ? 0x7fc07fc0u
+                                                : float2_to_bf16x2(o[mc][nt][j] * inv, o[mc][nt][2 + j] * inv);
+                    *reinterpret_cast<uint32_t*>(dst + 16 * mc) = v;
+                }
+            } else {
+                float* dst = p.part_o + (orow * p.np_max + d.part) * D + 2 * qr;
+#pragma unroll
+                for (int mc = 0; mc < NC; ++mc)
+                    __stcg(reinterpret_cast<float2*>(dst + 16 * mc),
+                           poisoned ? make_float2(qnan, qnan)
+                                    : make_float2(o[mc][nt][j] * vsc, o[mc][nt][2 + j] * vsc));
+                if (qr == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(m[nt][j], lj));
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Combine kernel: one warp per (query row, q head) whose row was split into
 // np > 1 partitions.  With M = max_p m_p and w_p = 2^(m_p - M),
 //   O = (sum_p w_p O_p) / (sum_p w_p l_p)
@@ -922,8 +1155,8 @@ int launch_combine(const CombineParams& c, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // Consumer warps
 // ---------------------------------------------------------------------------
-template <int D, int GD>
-__device__ __forceinline__ void consumer(Smem<D>& sm, const AttnParams& p, int warp, int lane) {
+template <int D, int GD, bool F8>
+__device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, int warp, int lane) {
     volatile int* abort = &sm.abort;
     uint32_t g = 0;
     for (int islot = 0;; ++islot) {
@@ -932,12 +1165,17 @@ __device__ __forceinline__ void consumer(Smem<D>& sm, const AttnParams& p, int w
         const Desc d = sm.desc[si];
         if (d.kind == KIND_END) break;
         const int ntiles = (d.t_end + kTileT - 1) / kTileT - d.t_begin / kTileT;
-        if (d.kind == KIND_DEC) {
-            decode_tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
-        } else if (d.kind == KIND_MQ) {
-            mq_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
+        if constexpr (F8) {
+            if (d.nq * p.G > 8) swap8_item<D, 2>(sm, p, d, warp, lane, g, ntiles, si, abort);
+            else swap8_item<D, 1>(sm, p, d, warp, lane, g, ntiles, si, abort);
         } else {
-            if constexpr (GD > 0) decode_item<D, GD>(sm, p, d, warp, lane, g, ntiles, si, abort);
+            if (d.kind == KIND_DEC) {
+                decode_tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
+            } else if (d.kind == KIND_MQ) {
+                mq_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
+            } else {
+                if constexpr (GD > 0) decode_item<D, GD>(sm, p, d, warp, lane, g, ntiles, si, abort);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.iempty[si]);  // this warp is done with the descriptor
@@ -945,14 +1183,16 @@ __device__ __forceinline__ void consumer(Smem<D>& sm, const AttnParams& p, int w
     }
 }
 
-template <int D, int GD>
+template <int D, int GD, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_attention_kernel(const __grid_constant__ TMaps tm, const __grid_constant__ AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
-    Smem<D>& sm = *reinterpret_cast<Smem<D>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    using SM = Smem<D, F8>;
+    constexpr int RS = Geo<D, F8>::kSlots;
+    SM& sm = *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRingSlots; ++s) {
+        for (int s = 0; s < RS; ++s) {
             mbar_init(&sm.full[s], 1);
             mbar_init(&sm.empty[s], kCWarps);
         }
@@ -967,22 +1207,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();    // the planning kernel's records are complete and visible
     pdl_launch();  // the combine kernel may be scheduled; it waits for this grid to finish
     if (warp == kCWarps) {
-        producer<D>(sm, &tm, p, lane);
+        producer<D, F8>(sm, &tm, p, lane);
     } else {
-        consumer<D, GD>(sm, p, warp, lane);
+        consumer<D, GD, F8>(sm, p, warp, lane);
     }
     if (threadIdx.x == 0 && sm.abort) report(p.status, PKV_STATUS_TIMEOUT);
 }
 
-template <int D, int GD>
+template <int D, int GD, bool F8 = false>
 int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, cudaStream_t st) {
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t smem = sizeof(Smem<D>) + 1024;
+    const size_t smem = sizeof(Smem<D, F8>) + 1024;
     if (dev < 0 || dev >= 64) return PKV_ERR_CUDA;
     if (!configured[dev]) {
-        if (cudaFuncSetAttribute(paged_attention_kernel<D, GD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(paged_attention_kernel<D, GD, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured[dev] = 1;
@@ -991,7 +1231,7 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
     const cudaError_t e =
-        host::launch_pdl(paged_attention_kernel<D, GD>, dim3((unsigned)grid), dim3(kThreads), smem, st, tm, p);
+        host::launch_pdl(paged_attention_kernel<D, GD, F8>, dim3((unsigned)grid), dim3(kThreads), smem, st, tm, p);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -1009,6 +1249,7 @@ int dispatch_g(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaS
 int dispatch_attention_d64(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
 int dispatch_attention_d128(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
 int combine_d64(const CombineParams& c, cudaStream_t st);
+int dispatch_attention_fp8_d128(const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
 int combine_d128(const CombineParams& c, cudaStream_t st);
 
 }  // namespace pkv

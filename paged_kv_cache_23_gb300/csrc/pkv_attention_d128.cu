@@ -1,4 +1,4 @@
-// pkv_attention_d128.cu -- paged attention and combine kernels for head_dim 128.
+// pkv_attention_d128.cu -- paged attention (bf16 and e4m3 pools) and combine kernels for head_dim 128.
 #include "pkv_attention.cuh"
 
 namespace pkv {
@@ -6,4 +6,7 @@ int dispatch_attention_d128(int GD, const TMaps& tm, const AttnParams& p, long l
     return dispatch_g<128>(GD, tm, p, mi, st);
 }
 int combine_d128(const CombineParams& c, cudaStream_t st) { return launch_combine<128>(c, st); }
+int dispatch_attention_fp8_d128(const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st) {
+    return launch_attention<128, 0, true>(tm, p, mi, st);
+}
 }  // namespace pkv

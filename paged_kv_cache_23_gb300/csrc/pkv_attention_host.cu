@@ -18,6 +18,7 @@ struct PlanParams {
     __nv_bfloat16* out;
     int32_t* status;
     int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, decode_ok;
+    int fp8;         // e4m3 pool: every row on the transposed tensor-core item
     int adapt_P;     // 1: P is a floor; the planning kernel may double it
     int sms;         // SM count (persistent CTAs of the attention kernel)
 };
@@ -35,8 +36,16 @@ struct SeqShape {
 };
 
 // decode_fma: run q_len = 1 rows on the CUDA-core path (else tensor cores).
-__device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_fma) {
+// fp8: e4m3 pool -- tiles of up to 16 (query, q head) columns per kv head.
+__device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_fma, int fp8 = 0) {
     SeqShape s;
+    if (fp8) {
+        s.kind = KIND_DEC;
+        s.hps = gcd_pow2(n_kv, kMaxHPS);
+        s.wph = 1;
+        s.qt = G <= 16 ? 16 / G : 1;
+        return s;
+    }
     if (ql == 1 && G <= 8) {
         s.kind = decode_fma ? KIND_DECF : KIND_DEC;
         s.hps = gcd_pow2(n_kv, kMaxHPS);
@@ -113,8 +122,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         for (int b = tid; b < n; b += kPlanThreads) {
             const int L = pp.seq_lens[b], ql = pp.q_lens[b];
             if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len) continue;
-            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
-            tok += (long long)L * (pp.n_kv / sh.hps) * (sh.kind == KIND_MQ ? ceil_div(ql, sh.qt) : 1);
+            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8);
+            const bool multi = sh.kind == KIND_MQ || ql > 1;
+            tok += (long long)L * (pp.n_kv / sh.hps) * (multi ? ceil_div(ql, sh.qt) : 1);
         }
         // block sum in units of 16 tokens (fits an int for any accepted batch)
         int tot16;
@@ -148,10 +158,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             if (q0l + qlc > pp.total_q) flag |= PKV_STATUS_BAD_QLEN;  // rows would overflow q/out
             q0 = (int)(q0l < pp.total_q ? q0l : pp.total_q);
             bits |= flag;
-            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok);
+            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8);
             const int ngroups = pp.n_kv / sh.hps;
             if (flag == 0) {
-                if (sh.kind != KIND_MQ) {
+                if (sh.kind != KIND_MQ && ql == 1) {
                     const int np = ceil_div(L, P);
                     nfull = (np - 1) * ngroups;
                     const int tl = L - (np - 1) * P;  // in [1, P]
@@ -201,7 +211,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             for (long long e = 0; e < n16; ++e) o[e] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
             continue;
         }
-        if (ql <= 0 || (sq.w & 15) == KIND_MQ) continue;
+        if (ql != 1 || (sq.w & 15) == KIND_MQ) continue;  // multi-query tiles are counted in pass B2
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
         const int np = ceil_div(L, P);
         const int tl = L - (np - 1) * P;
@@ -245,14 +255,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             const int4 sq = pp.seqs[b];
             const int L = sq.x, ql = sq.y, q0 = sq.z;
             if (pp.seq_flag[b] == 0 && r - q0 < ql) {
-                if ((sq.w & 15) != KIND_MQ) {
-                    np = ceil_div(L, P);
-                } else {
-                    const int QT = (sq.w >> 12) & 4095;
-                    const int qt = (r - q0) / QT;
-                    const int nq = min(QT, ql - qt * QT);
-                    np = ceil_div(L - ql + qt * QT + nq, P);
-                }
+                // query tile of row r; a decode row is a tile of one query
+                const int QT = (sq.w >> 12) & 4095;
+                const int qt = (r - q0) / QT;
+                const int nq = min(QT, ql - qt * QT);
+                np = ceil_div(L - ql + qt * QT + nq, P);
             }
         }
         pp.row_np[r] = np;
@@ -314,12 +321,16 @@ extern "C" size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int n
     return ws_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, max_seq_len, P).total;
 }
 
-extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-                                          const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
-                                          const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
-                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                                          int num_blocks, float scale, int partition_tokens, int flags,
-                                          void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+namespace {
+
+// Both entry points: bf16 pools (k_scale == nullptr) or e4m3 pools with
+// per-kv-head dequantisation scales.
+int run_attention(void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                  const float* v_scale, bool fp8, const int32_t* block_tables, int max_blocks,
+                  const int32_t* seq_lens, const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
+                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
+                  int partition_tokens, int flags, void* workspace, size_t workspace_bytes, int32_t* status,
+                  void* stream) {
     if (num_seqs < 0 || total_q < 0 || max_blocks < 1 || max_seq_len < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
         num_blocks < 1 || block_size < 1)
         return PKV_ERR_SIZE;
@@ -330,6 +341,8 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     if ((block_size & (block_size - 1)) || block_size > 256) return PKV_ERR_UNSUPPORTED;
     if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31)) return PKV_ERR_SIZE;
     if (flags & ~PKV_ATTN_DECODE_CUDA_CORES) return PKV_ERR_SIZE;
+    if (fp8 && (head_dim != 128 || G > 16)) return PKV_ERR_UNSUPPORTED;
+    if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
     if (num_seqs == 0 || total_q == 0) return PKV_OK;
     if (num_seqs > (1 << 24) || total_q > (1 << 20)) return PKV_ERR_SIZE;
     int P = partition_tokens;
@@ -346,20 +359,22 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     const int rc = host::check_device();
     if (rc) return rc;
 
-    // 5-D views [num_blocks][n_kv][bs][D/64][64] of each pool, one per box height in kv heads
+    // 5-D views [num_blocks][n_kv][bs][row / 128 B][128 B] of each pool, one per
+    // box height in kv heads (a row is D values of 2 bytes, or of 1 byte in e4m3)
     TMaps tm;
     {
+        const uint64_t row = (uint64_t)head_dim * (fp8 ? 1 : 2);
+        const uint64_t inner = fp8 ? 128 : 64;  // elements per 128-byte box
         const uint32_t box_rows = block_size < kTileT ? (uint32_t)block_size : (uint32_t)kTileT;
-        const uint64_t dims[5] = {64, (uint64_t)head_dim / 64, (uint64_t)block_size, (uint64_t)num_kv_heads,
+        const uint64_t dims[5] = {inner, row / 128, (uint64_t)block_size, (uint64_t)num_kv_heads,
                                   (uint64_t)num_blocks};
-        const uint64_t strides[4] = {128, (uint64_t)head_dim * 2, (uint64_t)block_size * head_dim * 2,
-                                     (uint64_t)num_kv_heads * block_size * head_dim * 2};
+        const uint64_t strides[4] = {128, row, (uint64_t)block_size * row, (uint64_t)num_kv_heads * block_size * row};
         for (int i = 0; i < 4; ++i) {
             uint32_t hb = 1u << i;
             if (hb > (uint32_t)num_kv_heads) hb = (uint32_t)num_kv_heads;
-            const uint32_t box[5] = {64, (uint32_t)head_dim / 64, box_rows, hb, 1};
-            if (host::encode_tiled(&tm.k[i], k_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-                host::encode_tiled(&tm.v[i], v_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            const uint32_t box[5] = {(uint32_t)inner, (uint32_t)(row / 128), box_rows, hb, 1};
+            if (host::encode_tiled(&tm.k[i], k_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, fp8) ||
+                host::encode_tiled(&tm.v[i], v_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, fp8))
                 return PKV_ERR_CUDA;
         }
     }
@@ -367,7 +382,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* aux = reinterpret_cast<int*>(ws + w.seqaux);
     const int GD = (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
-    const bool decode_fma = GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
+    const bool decode_fma = !fp8 && GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
 
     PlanParams pp{};
     pp.seq_lens = seq_lens;
@@ -394,6 +409,7 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     pp.max_seq_len = max_seq_len;
     pp.decode_ok = decode_fma ? 1 : 0;
     pp.adapt_P = partition_tokens == 0 ? 1 : 0;
+    pp.fp8 = fp8 ? 1 : 0;
     pp.sms = host::sm_count();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (host::launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess) return PKV_ERR_CUDA;
@@ -417,8 +433,11 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     ap.np_max = w.np_max;
     ap.row_bytes = head_dim * 2;
     ap.scale_log2 = scale * 1.4426950408889634f;
-    const int rc2 = head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st)
-                                    : dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
+    ap.k_scale = k_scale;
+    ap.v_scale = v_scale;
+    const int rc2 = fp8                ? dispatch_attention_fp8_d128(tm, ap, w.max_items, st)
+                    : head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st)
+                                      : dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
     if (rc2 != PKV_OK || w.np_max <= 1) return rc2;  // one partition per row: outputs are final
     CombineParams cp{};
     cp.out = ap.out;
@@ -429,4 +448,29 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
     cp.n_q = num_q_heads;
     cp.np_max = w.np_max;
     return head_dim == 128 ? combine_d128(cp, st) : combine_d64(cp, st);
+}
+
+}  // namespace
+
+extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                          const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                                          const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
+                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                          int num_blocks, float scale, int partition_tokens, int flags,
+                                          void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+    return run_attention(out, q, k_cache, v_cache, nullptr, nullptr, false, block_tables, max_blocks, seq_lens,
+                         q_lens, num_seqs, total_q, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                         num_blocks, scale, partition_tokens, flags, workspace, workspace_bytes, status, stream);
+}
+
+extern "C" int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                              const float* k_scale, const float* v_scale,
+                                              const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                                              const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
+                                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                              int num_blocks, float scale, int partition_tokens, void* workspace,
+                                              size_t workspace_bytes, int32_t* status, void* stream) {
+    return run_attention(out, q, k_cache, v_cache, k_scale, v_scale, true, block_tables, max_blocks, seq_lens,
+                         q_lens, num_seqs, total_q, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                         num_blocks, scale, partition_tokens, 0, workspace, workspace_bytes, status, stream);
 }

@@ -123,6 +123,57 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
 }
 
 // ---------------------------------------------------------------------------
+// KV append into e4m3 pools ("Inference at Scale" section 03, KV cache
+// quantization): code = e4m3(x * (1 / scale[head])), the reciprocal and the
+// product rounded to fp32 (nearest even), the conversion rounding to nearest
+// even and saturating to +-448.  8 values (16 bytes in, 8 out) per thread.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) kv_append_fp8_kernel(uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
+                                                            const uint4* __restrict__ k_new,
+                                                            const uint4* __restrict__ v_new,
+                                                            const int64_t* __restrict__ slots,
+                                                            const float* __restrict__ k_scale,
+                                                            const float* __restrict__ v_scale, int num_tokens,
+                                                            int num_blocks, int block_size, int num_kv_heads,
+                                                            int chunks_per_row, int32_t* status) {
+    pdl_wait();
+    pdl_launch();
+    const long long per_tok = (long long)num_kv_heads * chunks_per_row;
+    const long long total = (long long)num_tokens * per_tok;
+    const long long cap = (long long)num_blocks * block_size;
+    int bits = 0;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long t = i / per_tok;
+        const long long rem = i - t * per_tok;
+        const int h = (int)(rem / chunks_per_row);
+        const int c = (int)(rem - (long long)h * chunks_per_row);
+        const int64_t s = slots[t];
+        if (s < 0) continue;
+        if (s >= cap) {
+            bits |= PKV_STATUS_BAD_SLOT;
+            continue;
+        }
+        const long long blk = s / block_size;
+        const int row = (int)(s - blk * block_size);
+        const long long dst = ((blk * num_kv_heads + h) * block_size + row) * chunks_per_row + c;
+        const float ik = __fdiv_rn(1.0f, __ldg(k_scale + h)), iv = __fdiv_rn(1.0f, __ldg(v_scale + h));
+        const uint4 a = ld_nc_v4(k_new + i), b = ld_nc_v4(v_new + i);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+        uint32_t ck[4], cv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 xk = bf16x2_to_float2(wa[u]), xv = bf16x2_to_float2(wb[u]);
+            ck[u] = f32x2_to_e4m3x2(__fmul_rn(xk.x, ik), __fmul_rn(xk.y, ik));
+            cv[u] = f32x2_to_e4m3x2(__fmul_rn(xv.x, iv), __fmul_rn(xv.y, iv));
+        }
+        k_cache[dst] = make_uint2(ck[0] | (ck[1] << 16), ck[2] | (ck[3] << 16));
+        v_cache[dst] = make_uint2(cv[0] | (cv[1] << 16), cv[2] | (cv[3] << 16));
+    }
+    report(status, bits);
+}
+
+// ---------------------------------------------------------------------------
 // Copy blocks: blockIdx.y = pair, grid-stride over the block's 16-byte chunks.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
@@ -244,6 +295,30 @@ extern "C" int pkv_kv_append(void* k_cache, void* v_cache, const void* k_new, co
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+extern "C" int pkv_kv_append_fp8(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                                 const int64_t* slots, const float* k_scale, const float* v_scale, int num_tokens,
+                                 int num_blocks, int block_size, int num_kv_heads, int head_dim, int32_t* status,
+                                 void* stream) {
+    if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || num_kv_heads < 1 || head_dim < 8) return PKV_ERR_SIZE;
+    if (head_dim % 8) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !slots || !k_scale || !v_scale) return PKV_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(k_cache) & 7) || (reinterpret_cast<uintptr_t>(v_cache) & 7) ||
+        !host::aligned16(k_new) || !host::aligned16(v_new))
+        return PKV_ERR_ALIGN;
+    const int rc = host::check_device();
+    if (rc) return rc;
+    const int cpr = head_dim / 8;
+    const long long total = (long long)num_tokens * num_kv_heads * cpr;
+    const long long want = (total + 255) / 256;
+    const int grid = (int)(want < host::sm_count() * 8LL ? want : host::sm_count() * 8LL);
+    const cudaError_t e = host::launch_pdl(kv_append_fp8_kernel, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
+                                           (uint2*)k_cache, (uint2*)v_cache, (const uint4*)k_new,
+                                           (const uint4*)v_new, slots, k_scale, v_scale, num_tokens, num_blocks,
+                                           block_size, num_kv_heads, cpr, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 extern "C" int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst, int num_pairs,
                                int num_blocks, int block_size, int num_kv_heads, int head_dim,
                                int32_t* status, void* stream) {
@@ -288,4 +363,13 @@ extern "C" int pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, cons
                                            (const uint4*)v_cache, block_tables, max_blocks, seq_lens, out_offsets,
                                            num_blocks, block_size, num_kv_heads, head_dim / 8, status);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_copy_blocks_fp8(void* k_cache, void* v_cache, const int32_t* src_dst, int num_pairs,
+                                   int num_blocks, int block_size, int num_kv_heads, int head_dim, int32_t* status,
+                                   void* stream) {
+    // a block of 1-byte values is a block of 2-byte values of half the head_dim
+    if (head_dim % 16) return PKV_ERR_UNSUPPORTED;
+    return pkv_copy_blocks(k_cache, v_cache, src_dst, num_pairs, num_blocks, block_size, num_kv_heads, head_dim / 2,
+                           status, stream);
 }

@@ -17,12 +17,12 @@ int sm_count();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// cuTensorMapEncodeTiled (bf16 elements) through
+// cuTensorMapEncodeTiled (bf16 elements, or bytes when `bytes`) through
 // cudaGetDriverEntryPointByVersion, so the library needs no link-time
 // dependency on libcuda.  dims/box have `rank` entries, innermost first;
 // strides (bytes) has rank - 1.  Returns 0 on success.
 int encode_tiled(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                 const uint32_t* box, CUtensorMapSwizzle swizzle);
+                 const uint32_t* box, CUtensorMapSwizzle swizzle, bool bytes = false);
 
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel of the stream is finishing, and must call pdl_wait()

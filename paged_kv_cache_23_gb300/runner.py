@@ -11,7 +11,8 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (attention_auto_partition, attention_workspace_bytes, copy_blocks, kv_append, paged_attention_decode, slot_mapping,
+from . import (attention_auto_partition, attention_workspace_bytes, copy_blocks, copy_blocks_fp8, kv_append_fp8,
+               paged_attention_decode_fp8, kv_append, paged_attention_decode, slot_mapping,
                spec_accept_greedy)
 
 
@@ -27,12 +28,22 @@ def bf16_to_bits(t: torch.Tensor) -> np.ndarray:
 class DeviceStep:
     """Device-resident inputs of one step, plus outputs and scratch."""
 
-    def __init__(self, w, device="cuda", max_seq_len=None, partition_tokens=None, flags=0):
+    def __init__(self, w, device="cuda", max_seq_len=None, partition_tokens=None, flags=0, fp8=None):
+        """fp8: an e4m3 pool set (workloads.Fp8Pools) for the workload's
+        structure; the step then appends with quantisation and attends over
+        the e4m3 pools."""
         self.w = w
         self.device = torch.device(device)
         dev = self.device
-        self.k_cache = to_device_bf16(w.k_cache, dev)
-        self.v_cache = to_device_bf16(w.v_cache, dev)
+        self.fp8 = fp8
+        if fp8 is None:
+            self.k_cache = to_device_bf16(w.k_cache, dev)
+            self.v_cache = to_device_bf16(w.v_cache, dev)
+        else:
+            self.k_cache = torch.from_numpy(fp8.k_cache).to(dev)
+            self.v_cache = torch.from_numpy(fp8.v_cache).to(dev)
+            self.k_scale = torch.from_numpy(fp8.k_scale).to(dev)
+            self.v_scale = torch.from_numpy(fp8.v_scale).to(dev)
         # the per-step inputs live in one device arena (256-byte aligned
         # slices), so a step's host -> device upload is a single copy
         parts = [("q", w.q, torch.bfloat16), ("k_new", w.k_new, torch.bfloat16),
@@ -97,20 +108,35 @@ class DeviceStep:
 
     def reset_cache(self):
         """Restore the cache to the state before the step (for repeated steps)."""
-        self.k_cache.copy_(to_device_bf16(self.w.k_cache, self.device))
-        self.v_cache.copy_(to_device_bf16(self.w.v_cache, self.device))
+        if self.fp8 is None:
+            self.k_cache.copy_(to_device_bf16(self.w.k_cache, self.device))
+            self.v_cache.copy_(to_device_bf16(self.w.v_cache, self.device))
+        else:
+            self.k_cache.copy_(torch.from_numpy(self.fp8.k_cache))
+            self.v_cache.copy_(torch.from_numpy(self.fp8.v_cache))
 
     def cache_ops(self, stream=None):
         w = self.w
         if self.cow.numel():
-            copy_blocks(self.k_cache, self.v_cache, self.cow, status=self.status, stream=stream)
+            (copy_blocks if self.fp8 is None else copy_blocks_fp8)(self.k_cache, self.v_cache, self.cow,
+                                                                  status=self.status, stream=stream)
         if self.n_slots:
             slot_mapping(self.slots, self.block_tables, self.seq_lens, self.append_lens, w.block_size, w.num_blocks,
                          status=self.status, stream=stream)
-            kv_append(self.k_cache, self.v_cache, self.k_new, self.v_new, self.slots, status=self.status,
-                      stream=stream)
+            if self.fp8 is None:
+                kv_append(self.k_cache, self.v_cache, self.k_new, self.v_new, self.slots, status=self.status,
+                          stream=stream)
+            else:
+                kv_append_fp8(self.k_cache, self.v_cache, self.k_new, self.v_new, self.slots, self.k_scale,
+                              self.v_scale, status=self.status, stream=stream)
 
     def attention(self, stream=None):
+        if self.fp8 is not None:
+            paged_attention_decode_fp8(self.out, self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                                       self.block_tables, self.seq_lens, self.q_lens, self.max_seq_len, self.w.scale,
+                                       self.workspace, partition_tokens=self.partition_tokens, status=self.status,
+                                       stream=stream)
+            return
         paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
                                self.q_lens, self.max_seq_len, self.w.scale, self.workspace,
                                partition_tokens=self.partition_tokens, flags=self.flags, status=self.status,
