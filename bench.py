@@ -168,6 +168,12 @@ WORKLOADS = {
                  max_seq_len=None),
     "long": dict(desc="long context + chunk, " + SHAPE + ": 8 decodes of 131072 tokens + one 512-query chunk "
                  "over 8192 + 512, in one call", batch=9, seq="131072 (x8) and 8704", max_seq_len=None),
+    "mix_fp8": dict(desc="continuous-batching mix over an FP8 (e4m3) KV cache with per-kv-head scales, "
+                    + SHAPE + ": batch 256, log-normal ctx (median 1024, sigma 1, clip [16, 32768]), 50% share a "
+                    "2048-token prefix (CoW), q_len 1, 1 appended token/seq", batch=256,
+                    seq="log-normal median 1024", max_seq_len=32768, fp8=True),
+    "decode_fp8": dict(desc="8B decode over an FP8 (e4m3) KV cache, " + SHAPE + ": batch 64, seq_len ~ U[512, 4096], "
+                       "q_len 1", batch=64, seq="U[512, 4096]", max_seq_len=None, fp8=True),
     "sample": dict(desc="stochastic speculative acceptance (modified rejection sampling): batch 32, k 5, "
                    "vocab 128256, p/q fp32 softmax rows, drafts drawn from q", batch=32, seq="n/a",
                    max_seq_len=None),
@@ -176,8 +182,10 @@ WORKLOADS = {
 
 def make_workload(seed: int, name: str = "mix"):
     from paged_kv_cache_23_gb300 import workloads as wl
-    if name == "mix":
+    if name in ("mix", "mix_fp8"):
         return wl.mix(B=256, median=1024, sigma=1.0, clip=(16, 32768), share=0.5, prefix=2048, seed=seed)
+    if name == "decode_fp8":
+        return wl.decode(64, 512, 4096, seed)
     if name == "decode":
         return wl.decode(64, 512, 4096, seed)
     if name == "spec":
@@ -189,29 +197,56 @@ def make_workload(seed: int, name: str = "mix"):
     raise ValueError(name)
 
 
-def step_bytes_of(w):
+def step_bytes_of(w, fp8: bool = False):
     """Unique bytes of one step: the attention step, plus the logits scan of
     greedy acceptance when the workload carries logits."""
     from paged_kv_cache_23_gb300 import accounting
-    b = accounting.step_bytes(w)
+    b = accounting.step_bytes(w, kv_bytes=1 if fp8 else 2)
     if w.logits is not None:
         b["accept"] = accounting.accept_greedy_bytes(w)
         b["step_unique"] += b["accept"]
     return b
 
 
-def oracle_step_time(w, reps: int = 1):
+def _oracle_cache(w, pools=None):
+    """The oracle's cache after the step's copy-on-write and append."""
+    import oracle
+    if pools is None:
+        k = w.k_cache.copy()
+        v = w.v_cache.copy()
+        oracle.copy_blocks(k, v, w.cow)
+    else:
+        k = pools.k_cache.copy()
+        v = pools.v_cache.copy()
+        for src, dst in np.asarray(w.cow).reshape(-1, 2):
+            k[dst] = k[src]
+            v[dst] = v[src]
+    slots, _ = oracle.slot_mapping(w.block_tables, w.seq_lens, w.append_lens, w.block_size, w.num_blocks)
+    if pools is None:
+        oracle.kv_append(k, v, w.k_new, w.v_new, slots)
+    else:
+        oracle.kv_append_fp8(k, v, w.k_new, w.v_new, slots, pools.k_scale, pools.v_scale)
+    return k, v
+
+
+def _oracle_attention(w, k, v, pools, sel=None, rows=None):
+    import oracle
+    q = w.q if rows is None else w.q[rows]
+    bt, sl, ql = (w.block_tables, w.seq_lens, w.q_lens) if sel is None else \
+        (w.block_tables[sel], w.seq_lens[sel], w.q_lens[sel])
+    if pools is None:
+        return oracle.attention(q, k, v, bt, sl, ql, w.scale)
+    return oracle.attention_fp8(q, k, v, pools.k_scale, pools.v_scale, bt, sl, ql, w.scale)
+
+
+def oracle_step_time(w, reps: int = 1, pools=None):
     """Run the oracle's full step on the host: copy, slots, append, attention."""
     import oracle
     times = []
     for _ in range(reps):
         t0 = time.perf_counter()
-        k = w.k_cache.copy()
-        v = w.v_cache.copy()
-        oracle.copy_blocks(k, v, w.cow)
-        slots, _ = oracle.slot_mapping(w.block_tables, w.seq_lens, w.append_lens, w.block_size, w.num_blocks)
-        oracle.kv_append(k, v, w.k_new, w.v_new, slots)
-        oracle.attention(w.q, k, v, w.block_tables, w.seq_lens, w.q_lens, w.scale)
+        k, v = _oracle_cache(w, pools)
+        _oracle_attention(w, k, v, pools)
         if w.logits is not None:
             oracle.spec_accept_greedy(w.logits, w.draft)
         times.append(time.perf_counter() - t0)
@@ -244,10 +279,12 @@ def run_reference(args):
         t = oracle_sample_time(w, args.steps)
         sample = "the whole batch of 32 sequences per step (C oracle)"
     else:
-        nbytes = step_bytes_of(w)["step_unique"]
+        from paged_kv_cache_23_gb300 import workloads as wl
+        pools = wl.fp8_pools(w, 0) if spec.get("fp8") else None
+        nbytes = step_bytes_of(w, pools is not None)["step_unique"]
         # each step: the whole batch; warm-up steps untimed
-        oracle_step_time(w, max(0, args.warmup))
-        t = oracle_step_time(w, args.steps)
+        oracle_step_time(w, max(0, args.warmup), pools)
+        t = oracle_step_time(w, args.steps, pools)
         sample = f"the whole batch-{spec['batch']} step per step (fp64 C oracle, OpenMP)"
     mean = sum(t) / len(t)
     value = nbytes / mean / 1e9
@@ -288,15 +325,17 @@ def run_gpu(args):
 
     spec = WORKLOADS[args.workload]
     w = make_workload(rank, args.workload)   # weak scaling: each rank owns its own batch
-    b = step_bytes_of(w)
+    from paged_kv_cache_23_gb300 import workloads as wl
+    pools = wl.fp8_pools(w, rank) if spec.get("fp8") else None
+    b = step_bytes_of(w, pools is not None)
     ds = DeviceStep(w, device=device, max_seq_len=spec["max_seq_len"], partition_tokens=args.partition,
-                    flags=args.flags)
+                    flags=args.flags, fp8=pools)
     stream = torch.cuda.current_stream(device)
 
     # parity spot check on this very run: a few sequences against the oracle
     parity = None
     if rank == 0 and not args.no_check:
-        parity = spot_check(w, ds, device)
+        parity = spot_check(w, ds, device, pools)
         ds.reset_cache()
 
     def step():
@@ -349,7 +388,8 @@ def run_gpu(args):
         return 0
     line = {"metric": metric_of(args.workload), "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
             "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "e4m3 KV, bf16 q/out, f16 MMA" if pools is not None else "bf16",
+            "data": "synthetic",
             "config": {"workload": spec["desc"], "global_batch": spec["batch"] * ws, "seq_len": spec["seq"],
                        "parallelism": f"replicas x{ws} (independent batches)" if ws > 1 else "single GPU",
                        "l2": f"inputs larger than L2 ({b['kv_unique'] / 1e9:.2f} GB unique K/V per step vs "
@@ -366,14 +406,14 @@ def run_gpu(args):
                          "frac_of_nominal_8tbs": achieved / 8000.0},
             "clocks": clocks, "e2e": e2e, "gpu_launches": ds.launches_per_step() * args.steps, "status": st, "parity": parity}
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(w, b)
+        line["cpu_baseline"] = cpu_baseline(w, b, pools)
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
     return 0
 
 
-def spot_check(w, ds, device):
+def spot_check(w, ds, device, pools=None):
     """Sampled sequences of this run's output against the oracle."""
     import torch
     import oracle
@@ -381,15 +421,11 @@ def spot_check(w, ds, device):
     from paged_kv_cache_23_gb300.runner import bf16_to_bits
     ds.step()
     torch.cuda.synchronize()
-    k = w.k_cache.copy()
-    v = w.v_cache.copy()
-    oracle.copy_blocks(k, v, w.cow)
-    slots, _ = oracle.slot_mapping(w.block_tables, w.seq_lens, w.append_lens, w.block_size, w.num_blocks)
-    oracle.kv_append(k, v, w.k_new, w.v_new, slots)
+    k, v = _oracle_cache(w, pools)
     pick = np.unique(np.linspace(0, w.num_seqs - 1, 8).astype(int))
     q0 = np.concatenate([[0], np.cumsum(w.q_lens.astype(np.int64))])
     rows = np.concatenate([np.arange(q0[b], q0[b + 1]) for b in pick])
-    ref, _ = oracle.attention(w.q[rows], k, v, w.block_tables[pick], w.seq_lens[pick], w.q_lens[pick], w.scale)
+    ref, _ = _oracle_attention(w, k, v, pools, pick, rows)
     got = wl.bf16_bits_to_f32(bf16_to_bits(ds.out)[rows]).astype(np.float64)
     err = np.abs(got - ref)
     ok = bool(np.all(err <= 1e-2 + 1e-2 * np.abs(ref)))
@@ -551,11 +587,11 @@ def run_sample(args):
     return 0
 
 
-def cpu_baseline(w, b):
+def cpu_baseline(w, b, pools=None):
     import oracle
     oracle.build()
     reps = 1 if int(w.seq_lens.max()) > 65536 else 2
-    t = oracle_step_time(w, reps)
+    t = oracle_step_time(w, reps, pools)
     best = min(t)
     return {"value": b["step_unique"] / best / 1e9, "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"the full batch-{w.num_seqs} step (copy, slots, append, fp64 attention"

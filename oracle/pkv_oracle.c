@@ -502,6 +502,8 @@ int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
                          int block_size, int num_blocks, double scale) {
     int status = 0;
     int g = n_q / n_kv;
+    double val[256]; /* e4m3_value of every code, looked up below */
+    for (int c = 0; c < 256; c++) val[c] = e4m3_value((uint8_t)c);
     int64_t *row0 = (int64_t *)malloc(sizeof(int64_t) * (num_seqs + 1));
     row0[0] = 0;
     for (int b = 0; b < num_seqs; b++) row0[b + 1] = row0[b] + (q_lens[b] > 0 ? q_lens[b] : 0);
@@ -533,7 +535,7 @@ int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
                     int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
                     const uint8_t *kt = k_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
                     double acc = 0.0;
-                    for (int c = 0; c < d; c++) acc += widen_bf16(qv[c]) * (e4m3_value(kt[c]) * (double)k_scale[j]);
+                    for (int c = 0; c < d; c++) acc += widen_bf16(qv[c]) * (val[kt[c]] * (double)k_scale[j]);
                     s[t] = scale * acc;
                 }
                 double M = -INFINITY;
@@ -544,7 +546,7 @@ int oracle_attention_fp8(double *out, const uint16_t *q, const uint8_t *k_cache,
                 for (int t = 0; t <= p; t++) {
                     int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
                     const uint8_t *vt = v_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
-                    for (int c = 0; c < d; c++) o[c] += s[t] * (e4m3_value(vt[c]) * (double)v_scale[j]);
+                    for (int c = 0; c < d; c++) o[c] += s[t] * (val[vt[c]] * (double)v_scale[j]);
                 }
                 for (int c = 0; c < d; c++) o[c] /= den;
             }

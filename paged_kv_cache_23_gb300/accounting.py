@@ -19,8 +19,11 @@ def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, bytes_
     return 2 * num_layers * num_kv_heads * head_dim * bytes_per_value
 
 
-def step_bytes(w, bytes_per_value: int = 2) -> dict:
+def step_bytes(w, bytes_per_value: int = 2, kv_bytes: int | None = None) -> dict:
     """Algorithmic bytes of one step over workload ``w`` (one layer).
+
+    kv_bytes: bytes per cached K/V value (1 for an e4m3 pool, section 03 "KV
+    cache quantization"); queries, outputs and appended rows stay bf16.
 
     kv_logical  every sequence's visible K/V, counted once per sequence (the
                 query heads of a group share one read)
@@ -28,7 +31,8 @@ def step_bytes(w, bytes_per_value: int = 2) -> dict:
                 so blocks shared between sequences count once
     """
     bs = w.block_size
-    per_row = w.n_kv * w.head_dim * bytes_per_value * 2          # K and V of one token, all kv heads
+    kvb = bytes_per_value if kv_bytes is None else kv_bytes
+    per_row = w.n_kv * w.head_dim * kvb * 2                      # K and V of one token, all kv heads
     L = w.seq_lens.astype(np.int64)
     kv_logical = int(L.sum()) * per_row
     rows = []
@@ -55,8 +59,9 @@ def step_bytes(w, bytes_per_value: int = 2) -> dict:
     o_bytes = q_bytes
     tables = int(sum(-(-int(n) // bs) for n in L)) * 4 + 2 * 4 * w.num_seqs
     t_new = int(w.append_lens.sum())
-    append = 2 * t_new * per_row + t_new * 8          # read new rows, write them, read slots
-    cow = int(w.cow.shape[0]) * 2 * (w.n_kv * bs * w.head_dim * bytes_per_value * 2)
+    new_row = w.n_kv * w.head_dim * bytes_per_value * 2
+    append = t_new * (new_row + per_row) + t_new * 8  # read new rows, write them (cache format), read slots
+    cow = int(w.cow.shape[0]) * 2 * (w.n_kv * bs * w.head_dim * kvb * 2)
     attn_unique = kv_unique + q_bytes + o_bytes + tables
     attn_logical = kv_logical + q_bytes + o_bytes + tables
     return dict(kv_logical=kv_logical, kv_unique=kv_unique, q=q_bytes, o=o_bytes, tables=tables,
