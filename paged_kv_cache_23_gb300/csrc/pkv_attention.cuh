@@ -839,6 +839,154 @@ __device__ __forceinline__ void mq_item(Smem<D, false>& sm, const AttnParams& p,
 //      16 c + 2 (r mod 8) + r / 8.
 // The per-head scales fold into the score scale (K) and the output (V).
 // ---------------------------------------------------------------------------
+// NS consecutive stages (i0, i0 + 1, ...) of a swap8 item: their S products
+// are independent, so a warp running two at once hides more of the ldmatrix
+// and MMA latency.
+template <int D, int NTN, int NS>
+__device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, int i0, uint32_t gbase,
+                                             const uint32_t (&qb)[NTN][D / 16][2], const int (&lim)[NTN][2],
+                                             float (&o)[D / 16][NTN][4], float (&m)[NTN][2], float (&l)[NTN][2],
+                                             float ksc, int R, int a_ch, int lane, volatile int* abort) {
+    constexpr int RS = Geo<D, true>::kSlots;
+    constexpr int NC = D / 16;
+    const int qd = lane & 3, qr = lane >> 2;
+    const int tb = d.t_begin / kTileT;
+    int slot[NS], nvalid[NS], t0[NS];
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+        const uint32_t gi = gbase + i0 + u;
+        slot[u] = (int)(gi % RS);
+        mbar_wait(&sm.full[slot[u]], (gi / RS) & 1, abort);
+        t0[u] = (tb + i0 + u) * kTileT;
+        nvalid[u] = min(kTileT, d.t_end - t0[u]);
+    }
+    // S^T of every stage
+    float sc[NS][2][NTN][4];
+#pragma unroll
+    for (int u = 0; u < NS; ++u)
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt) sc[u][h][nt][0] = sc[u][h][nt][1] = sc[u][h][nt][2] = sc[u][h][nt][3] = 0.f;
+#pragma unroll
+    for (int kc2 = 0; kc2 < NC / 2; ++kc2) {
+        const int chunk = 2 * kc2 + a_ch;
+#pragma unroll
+        for (int u = 0; u < NS; ++u) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4(smem_u32(&sm.kv[slot[u]][0][0]) + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), r0, r1, r2, r3);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
+                const uint32_t a0 = e4m3x2_to_f16x2(rA), a2 = e4m3x2_to_f16x2(rA >> 16);
+                const uint32_t a1 = e4m3x2_to_f16x2(rB), a3 = e4m3x2_to_f16x2(rB >> 16);
+                const int kc = 2 * kc2 + h;
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt)
+                    mma_f16_16816(sc[u][h][nt], a0, a1, a2, a3, qb[nt][kc][0], qb[nt][kc][1]);
+            }
+        }
+    }
+    // scores (token qr / qr + 8, column 2 qd / 2 qd + 1) with the partition end
+    // and each column's causal limit; lazy reference maxima as in decode_tc_item
+    float sv[NS][NTN][4];
+    bool fits = true;
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+        const int ta = t0[u] + qr, tb8 = t0[u] + qr + 8;
+        const bool in_a = qr < nvalid[u], in_b = qr + 8 < nvalid[u];
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            sv[u][nt][0] = in_a && ta <= lim[nt][0] ? (sc[u][0][nt][0] + sc[u][1][nt][0]) * ksc : -INFINITY;
+            sv[u][nt][1] = in_a && ta <= lim[nt][1] ? (sc[u][0][nt][1] + sc[u][1][nt][1]) * ksc : -INFINITY;
+            sv[u][nt][2] = in_b && tb8 <= lim[nt][0] ? (sc[u][0][nt][2] + sc[u][1][nt][2]) * ksc : -INFINITY;
+            sv[u][nt][3] = in_b && tb8 <= lim[nt][1] ? (sc[u][0][nt][3] + sc[u][1][nt][3]) * ksc : -INFINITY;
+            fits = fits && fmaxf(sv[u][nt][0], sv[u][nt][2]) <= m[nt][0] + kRescaleSlack &&
+                   fmaxf(sv[u][nt][1], sv[u][nt][3]) <= m[nt][1] + kRescaleSlack;
+        }
+    }
+    if (!__all_sync(kFull, fits)) {
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            float x0 = -INFINITY, x1 = -INFINITY;
+#pragma unroll
+            for (int u = 0; u < NS; ++u) {
+                x0 = fmaxf(x0, fmaxf(sv[u][nt][0], sv[u][nt][2]));
+                x1 = fmaxf(x1, fmaxf(sv[u][nt][1], sv[u][nt][3]));
+            }
+#pragma unroll
+            for (int o8 = 4; o8 < 32; o8 <<= 1) {
+                x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, o8));
+                x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, o8));
+            }
+            const float n0 = fmaxf(m[nt][0], x0), n1 = fmaxf(m[nt][1], x1);
+            const float c0 = n0 == -INFINITY ? 1.f : exp2f(m[nt][0] - n0);
+            const float c1 = n1 == -INFINITY ? 1.f : exp2f(m[nt][1] - n1);
+            l[nt][0] *= c0;
+            l[nt][1] *= c1;
+#pragma unroll
+            for (int mc = 0; mc < NC; ++mc) {
+                o[mc][nt][0] *= c0;
+                o[mc][nt][1] *= c1;
+                o[mc][nt][2] *= c0;
+                o[mc][nt][3] *= c1;
+            }
+            m[nt][0] = n0;
+            m[nt][1] = n1;
+        }
+    }
+    uint32_t pb0[NS][NTN], pb1[NS][NTN];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) {
+        const float u0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0], u1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
+#pragma unroll
+        for (int u = 0; u < NS; ++u) {
+            const float p0 = exp2f(sv[u][nt][0] - u0), p1 = exp2f(sv[u][nt][1] - u1);
+            const float p2 = exp2f(sv[u][nt][2] - u0), p3 = exp2f(sv[u][nt][3] - u1);
+            l[nt][0] += p0 + p2;
+            l[nt][1] += p1 + p3;
+            pb0[u][nt] = movmatrix_trans(float2_to_f16x2(p0, p1));  // (tokens 2qd, 2qd+1; column qr)
+            pb1[u][nt] = movmatrix_trans(float2_to_f16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; column qr)
+        }
+    }
+    // V rows past the valid tokens may hold anything (even NaN): zero them
+    uint32_t klo[NS], khi[NS];
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+        const int nv = nvalid[u];
+        klo[u] = nv == kTileT ? 0xffffffffu
+                              : (2 * qd < nv ? 0x0000ffffu : 0u) | (2 * qd + 1 < nv ? 0xffff0000u : 0u);
+        khi[u] = nv == kTileT ? 0xffffffffu
+                              : (8 + 2 * qd < nv ? 0x0000ffffu : 0u) | (9 + 2 * qd < nv ? 0xffff0000u : 0u);
+    }
+#pragma unroll
+    for (int kc2 = 0; kc2 < NC / 2; ++kc2) {
+        const int chunk = 2 * kc2 + a_ch;
+#pragma unroll
+        for (int u = 0; u < NS; ++u) {
+            uint32_t r0, r1, r2, r3;
+            ldsm_x4_t(smem_u32(&sm.kv[slot[u]][1][0]) + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), r0, r1, r2, r3);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
+                // bytes (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0) and (t0 d1, t1 d1)
+                const uint32_t a0 = e4m3x2_to_f16x2(__byte_perm(rA, 0u, 0x4420)) & klo[u];
+                const uint32_t a1 = e4m3x2_to_f16x2(__byte_perm(rA, 0u, 0x4431)) & klo[u];
+                const uint32_t a2 = e4m3x2_to_f16x2(__byte_perm(rB, 0u, 0x4420)) & khi[u];
+                const uint32_t a3 = e4m3x2_to_f16x2(__byte_perm(rB, 0u, 0x4431)) & khi[u];
+                const int mc = 2 * kc2 + h;
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt) mma_f16_16816(o[mc][nt], a0, a1, a2, a3, pb0[u][nt], pb1[u][nt]);
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) {
+#pragma unroll
+        for (int u = 0; u < NS; ++u) mbar_arrive(&sm.empty[slot[u]]);  // one arrival per consumer warp and stage
+    }
+}
+
 template <int D, int NTN>
 __device__ __forceinline__ void swap8_item(Smem<D, true>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
                                            uint32_t gbase, int ntiles, int si, volatile int* abort) {
@@ -852,15 +1000,21 @@ __device__ __forceinline__ void swap8_item(Smem<D, true>& sm, const AttnParams& 
     const int kvh = d.hg * d.hps + warp;
     const int qd = lane & 3, qr = lane >> 2;
     const int ncols = d.nq * G;
-    float ksc = 0.f, vsc = 0.f;
+    if (!active) {
+        for (int i = 0; i < ntiles; ++i) {
+            const uint32_t gi = gbase + i;
+            mbar_wait(&sm.full[gi % RS], (gi / RS) & 1, abort);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[gi % RS]);
+        }
+        return;
+    }
     uint32_t qb[NTN][NC][2];
 #pragma unroll
     for (int nt = 0; nt < NTN; ++nt) {
         const int c = 8 * nt + qr;
         const __nv_bfloat16* qrow =
-            (active && c < ncols)
-                ? p.q + ((long long)(d.q_row0 + c / G) * p.n_q + (long long)kvh * G + c % G) * D
-                : nullptr;
+            c < ncols ? p.q + ((long long)(d.q_row0 + c / G) * p.n_q + (long long)kvh * G + c % G) * D : nullptr;
 #pragma unroll
         for (int kc = 0; kc < NC; ++kc) {
             uint2 raw = make_uint2(0u, 0u);
@@ -870,10 +1024,8 @@ __device__ __forceinline__ void swap8_item(Smem<D, true>& sm, const AttnParams& 
             qb[nt][kc][1] = float2_to_f16x2(x23.x, x23.y);
         }
     }
-    if (active) {
-        ksc = __ldg(p.k_scale + kvh) * p.scale_log2;
-        vsc = __ldg(p.v_scale + kvh);
-    }
+    const float ksc = __ldg(p.k_scale + kvh) * p.scale_log2;
+    const float vsc = __ldg(p.v_scale + kvh);
     // last visible position of the two columns (2 qd, 2 qd + 1) of each n-tile
     int lim[NTN][2];
 #pragma unroll
@@ -893,124 +1045,13 @@ __device__ __forceinline__ void swap8_item(Smem<D, true>& sm, const AttnParams& 
     for (int nt = 0; nt < NTN; ++nt) m[nt][0] = m[nt][1] = -INFINITY, l[nt][0] = l[nt][1] = 0.f;
     const int mi = lane >> 3, mr = lane & 7;
     const int a_tok = ((mi & 1) << 3) + mr, a_ch = mi >> 1;  // (t0-7, c) (t8-15, c) (t0-7, c+1) (t8-15, c+1)
-    const int tb = d.t_begin / kTileT;
-    for (int i = 0; i < ntiles; ++i) {
-        const uint32_t gi = gbase + i;
-        const int s = (int)(gi % RS);
-        mbar_wait(&sm.full[s], (gi / RS) & 1, abort);
-        if (!active) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[s]);
-            continue;
-        }
-        const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
-        const uint32_t vb = smem_u32(&sm.kv[s][1][0]);
-        const int t0 = (tb + i) * kTileT;
-        const int nvalid = min(kTileT, d.t_end - t0);
-        const int R = srow(h_lb, a_tok, 0, hps_lb, lb, 1);
-        // S^T
-        float sc[2][NTN][4];
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-            for (int nt = 0; nt < NTN; ++nt) sc[u][nt][0] = sc[u][nt][1] = sc[u][nt][2] = sc[u][nt][3] = 0.f;
-#pragma unroll
-        for (int kc2 = 0; kc2 < NC / 2; ++kc2) {
-            const int chunk = 2 * kc2 + a_ch;
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4(kb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), r0, r1, r2, r3);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
-                const uint32_t a0 = e4m3x2_to_f16x2(rA), a2 = e4m3x2_to_f16x2(rA >> 16);
-                const uint32_t a1 = e4m3x2_to_f16x2(rB), a3 = e4m3x2_to_f16x2(rB >> 16);
-                const int kc = 2 * kc2 + h;
-#pragma unroll
-                for (int nt = 0; nt < NTN; ++nt)
-                    mma_f16_16816(sc[h][nt], a0, a1, a2, a3, qb[nt][kc][0], qb[nt][kc][1]);
-            }
-        }
-        // scores (token qr / qr + 8, column 2 qd / 2 qd + 1) with the partition
-        // end and each column's causal limit; lazy reference maxima as in
-        // decode_tc_item
-        const int ta = t0 + qr, tb8 = t0 + qr + 8;
-        const bool in_a = qr < nvalid, in_b = qr + 8 < nvalid;
-        float sv[NTN][4];
-        bool fits = true;
-#pragma unroll
-        for (int nt = 0; nt < NTN; ++nt) {
-            sv[nt][0] = in_a && ta <= lim[nt][0] ? (sc[0][nt][0] + sc[1][nt][0]) * ksc : -INFINITY;
-            sv[nt][1] = in_a && ta <= lim[nt][1] ? (sc[0][nt][1] + sc[1][nt][1]) * ksc : -INFINITY;
-            sv[nt][2] = in_b && tb8 <= lim[nt][0] ? (sc[0][nt][2] + sc[1][nt][2]) * ksc : -INFINITY;
-            sv[nt][3] = in_b && tb8 <= lim[nt][1] ? (sc[0][nt][3] + sc[1][nt][3]) * ksc : -INFINITY;
-            fits = fits && fmaxf(sv[nt][0], sv[nt][2]) <= m[nt][0] + kRescaleSlack &&
-                   fmaxf(sv[nt][1], sv[nt][3]) <= m[nt][1] + kRescaleSlack;
-        }
-        if (!__all_sync(kFull, fits)) {
-#pragma unroll
-            for (int nt = 0; nt < NTN; ++nt) {
-                float x0 = fmaxf(sv[nt][0], sv[nt][2]), x1 = fmaxf(sv[nt][1], sv[nt][3]);
-#pragma unroll
-                for (int o8 = 4; o8 < 32; o8 <<= 1) {
-                    x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, o8));
-                    x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, o8));
-                }
-                const float n0 = fmaxf(m[nt][0], x0), n1 = fmaxf(m[nt][1], x1);
-                const float c0 = n0 == -INFINITY ? 1.f : exp2f(m[nt][0] - n0);
-                const float c1 = n1 == -INFINITY ? 1.f : exp2f(m[nt][1] - n1);
-                l[nt][0] *= c0;
-                l[nt][1] *= c1;
-#pragma unroll
-                for (int mc = 0; mc < NC; ++mc) {
-                    o[mc][nt][0] *= c0;
-                    o[mc][nt][1] *= c1;
-                    o[mc][nt][2] *= c0;
-                    o[mc][nt][3] *= c1;
-                }
-                m[nt][0] = n0;
-                m[nt][1] = n1;
-            }
-        }
-        uint32_t pb0[NTN], pb1[NTN];
-#pragma unroll
-        for (int nt = 0; nt < NTN; ++nt) {
-            const float u0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0], u1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
-            const float p0 = exp2f(sv[nt][0] - u0), p1 = exp2f(sv[nt][1] - u1);
-            const float p2 = exp2f(sv[nt][2] - u0), p3 = exp2f(sv[nt][3] - u1);
-            l[nt][0] += p0 + p2;
-            l[nt][1] += p1 + p3;
-            pb0[nt] = movmatrix_trans(float2_to_f16x2(p0, p1));  // (tokens 2qd, 2qd+1; column qr)
-            pb1[nt] = movmatrix_trans(float2_to_f16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; column qr)
-        }
-        // V rows past the valid tokens may hold anything (even NaN): zero them
-        const uint32_t klo = nvalid == kTileT ? 0xffffffffu
-                                              : (2 * qd < nvalid ? 0x0000ffffu : 0u) |
-                                                    (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t khi = nvalid == kTileT ? 0xffffffffu
-                                              : (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) |
-                                                    (9 + 2 * qd < nvalid ? 0xffff0000u : 0u);
-#pragma unroll
-        for (int kc2 = 0; kc2 < NC / 2; ++kc2) {
-            const int chunk = 2 * kc2 + a_ch;
-            uint32_t r0, r1, r2, r3;
-            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), r0, r1, r2, r3);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
-                // bytes (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0) and (t0 d1, t1 d1)
-                const uint32_t a0 = e4m3x2_to_f16x2(__byte_perm(rA, 0u, 0x4420)) & klo;
-                const uint32_t a1 = e4m3x2_to_f16x2(__byte_perm(rA, 0u, 0x4431)) & klo;
-                const uint32_t a2 = e4m3x2_to_f16x2(__byte_perm(rB, 0u, 0x4420)) & khi;
-                const uint32_t a3 = e4m3x2_to_f16x2(__byte_perm(rB, 0u, 0x4431)) & khi;
-                const int mc = 2 * kc2 + h;
-#pragma unroll
-                for (int nt = 0; nt < NTN; ++nt) mma_f16_16816(o[mc][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
-            }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
+    const int R = srow(h_lb, a_tok, 0, hps_lb, lb, 1);
+    int i = 0;
+    if constexpr (NTN == 1) {
+        for (; i + 1 < ntiles; i += 2)
+            swap8_stages<D, NTN, 2>(sm, d, i, gbase, qb, lim, o, m, l, ksc, R, a_ch, lane, abort);
     }
-    if (!active) return;
+    for (; i < ntiles; ++i) swap8_stages<D, NTN, 1>(sm, d, i, gbase, qb, lim, o, m, l, ksc, R, a_ch, lane, abort);
     const bool poisoned = sm.poison[si] != 0;  // final after the last stage's wait
     const float qnan = __int_as_float(0x7fc00000);
 #pragma unroll
