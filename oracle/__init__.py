@@ -61,6 +61,7 @@ def _load():
                 "oracle_e4m3_decode": [P, P, ctypes.c_int64],
                 "oracle_kv_append_fp8": [P, P, P, P, P, I, I, I, I, I, P, P],
                 "oracle_attention_fp8": [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, D],
+                "oracle_prefix_hash": [P, P, I, P, I, I, I, ctypes.c_uint64],
                 "oracle_num_threads": [],
             }
             for name, argt in sigs.items():
@@ -266,3 +267,70 @@ def spec_accept_greedy(logits, draft):
     am = np.empty((B, k1), np.int32)
     _load().oracle_spec_accept_greedy(_p(acc), _p(nxt), _p(am), _p(lg), _p(dr), B, k, V)
     return acc, nxt, am
+
+
+def prefix_hash(tokens, lens, block_size, max_blocks, salt=0):
+    """Chained 128-bit block hashes ("Inference at Scale" 05, prefix caching;
+    "Chapter 31 Serving Efficiency" 31.3).  tokens int32 [B][max_tokens],
+    lens int32 [B].  Returns uint64 [B][max_blocks][2] (zeros past the full
+    blocks of each sequence)."""
+    tk = _c(tokens, np.int32)
+    B, T = tk.shape
+    ln = _c(lens, np.int32).reshape(B)
+    out = np.zeros((B, max_blocks, 2), np.uint64)
+    _load().oracle_prefix_hash(_p(out), _p(tk), T, _p(ln), B, block_size, max_blocks, ctypes.c_uint64(salt & (2**64 - 1)))
+    return out
+
+
+class PrefixCache:
+    """The prefix cache's semantics, written plainly over a dict ("Inference at
+    Scale" 05: on a hash match a new request bumps the block's ref count and
+    skips that part of prefill; only a shared beginning counts, so the first
+    miss ends the match, "Chapter 31 Serving Efficiency" 31.3).
+
+    key (lane 0, lane 1) -> [block id, ref count]."""
+
+    def __init__(self):
+        self.d = {}
+
+    def lookup(self, hashes, lens, block_size, block_tables):
+        """For each sequence the longest run of leading full blocks found;
+        their ids go to block_tables[b][:n], each hit's ref count + 1.
+        Returns n per sequence."""
+        B = hashes.shape[0]
+        n = np.zeros(B, np.int32)
+        for b in range(B):
+            nfull = min(int(lens[b]) // block_size, hashes.shape[1])
+            j = 0
+            while j < nfull and (int(hashes[b, j, 0]), int(hashes[b, j, 1])) in self.d:
+                j += 1
+            for i in range(j):
+                e = self.d[(int(hashes[b, i, 0]), int(hashes[b, i, 1]))]
+                e[1] += 1
+                block_tables[b, i] = e[0]
+            n[b] = j
+        return n
+
+    def insert(self, hashes, block_tables, first, count):
+        """Register block_tables[b][j] under hashes[b][j] for j in
+        [first[b], first[b] + count[b]).  A key already present keeps its block
+        (the caller's block is a duplicate) and gains a reference; a key several
+        sequences insert in the same call goes to one of them.  Returns the
+        set of keys each (b, j) resolved to, for validation, and the ref counts."""
+        claims = {}
+        for b in range(hashes.shape[0]):
+            for j in range(int(first[b]), int(first[b]) + int(count[b])):
+                k = (int(hashes[b, j, 0]), int(hashes[b, j, 1]))
+                claims.setdefault(k, []).append((b, j, int(block_tables[b, j])))
+        for k, lst in claims.items():
+            if k in self.d:
+                self.d[k][1] += len(lst)
+            else:
+                self.d[k] = [None, len(lst)]   # block: any one of lst's (GPU: the first to claim)
+                self.d[k].append([c[2] for c in lst])
+        return claims
+
+    def release(self, hashes, n):
+        for b in range(hashes.shape[0]):
+            for j in range(int(n[b])):
+                self.d[(int(hashes[b, j, 0]), int(hashes[b, j, 1]))][1] -= 1
