@@ -70,6 +70,8 @@ extern "C" {
 #define PKV_STATUS_BAD_PAIR 64   /* a copy pair names a block outside the pool */
 #define PKV_STATUS_BAD_TOKEN 128 /* a draft token is outside [0, vocab) */
 #define PKV_STATUS_BAD_DIST 256  /* a sampling distribution has no positive weight */
+#define PKV_STATUS_TABLE_FULL 512  /* a prefix-cache insert found no free entry */
+#define PKV_STATUS_NOT_FOUND 1024  /* a prefix-cache release named a key not in the table */
 
 /* Attention flags. */
 #define PKV_ATTN_DECODE_CUDA_CORES 1 /* run q_len = 1 rows on the CUDA-core FMA path */
@@ -281,6 +283,77 @@ int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache
                                    int num_kv_heads, int head_dim, int block_size, int num_blocks,
                                    float scale, int partition_tokens, void* workspace,
                                    size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * Prefix-cache block lookup ([KVC] 05, "Prefix caching": every full block is
+ * identified by a hash of itself plus the hash of its parent block -- of the
+ * whole prefix up to it; a new request looks the hashes up and, on a match,
+ * bumps the block's ref count and skips that part of prefill.  [SE] 31.3:
+ * only a shared beginning counts, and the key must cover the computation
+ * version as well as the tokens).  The results feed the block tables the
+ * attention reads.
+ *
+ * Block hash (this library's definition; the pages fix none): 128 bits, two
+ * 64-bit lanes L = 0, 1, seeds S0 = 0x243F6A8885A308D3, S1 = 0x13198A2E03707344,
+ * arithmetic mod 2^64:
+ *   mix(x):  x ^= x >> 32; x *= M; x ^= x >> 29; x *= M; x ^= x >> 32,
+ *            M = 0xD6E8FEB86659FD93
+ *   content of block j:  c = S_L ^ salt;
+ *                        for i < block_size: c = mix(c + (uint32)tok[j*bs+i] + (i << 32))
+ *   chain:   h_-1 = S_L;  h_j = mix(h_{j-1} ^ mix(c_j + 0x9E3779B97F4A7C15))
+ * key_j = (h_j lane 0, h_j lane 1), except that a key with lane 1 == 0 and
+ * lane 0 < 2 takes lane 1 = 1 ((0, 0) and (1, 0) mark empty and removed
+ * entries).  salt is the caller's computation-version key (model, adapter,
+ * positional settings).  Only full blocks are hashed.
+ *
+ * Table: device memory of pkv_prefix_table_bytes(capacity) bytes (capacity a
+ * power of two, 16-byte aligned), caller-owned; entries are 32 bytes
+ * {uint64 key lane 0, uint64 key lane 1, int32 block id, int32 ref count},
+ * open addressing with linear probing from lane 0 mod capacity.  Calls on one
+ * table must be ordered (one stream).
+ */
+size_t pkv_prefix_table_bytes(int capacity);
+int pkv_prefix_table_init(void* table, int capacity, void* stream);
+
+/*
+ * hashes uint64 [num_seqs][max_blocks][2] out: keys of the full blocks
+ * j < lens[b] / block_size (entries past them untouched); tokens int32
+ * [num_seqs][max_tokens], max_tokens >= max_blocks * block_size.
+ */
+int pkv_prefix_hash(uint64_t* hashes, const int32_t* tokens, int max_tokens, const int32_t* lens,
+                    int num_seqs, int block_size, int max_blocks, uint64_t salt, void* stream);
+
+/*
+ * For each sequence, the longest run of leading full blocks whose keys are in
+ * the table: cached_blocks[b] = its length n, block_tables[b][j] (int32
+ * [num_seqs][max_blocks]) = the cached block of key j for j < n (other entries
+ * untouched), and each of those entries gains a reference.
+ */
+int pkv_prefix_lookup(void* table, int capacity, const uint64_t* hashes, const int32_t* lens,
+                      int num_seqs, int block_size, int max_blocks, int32_t* block_tables,
+                      int32_t* cached_blocks, void* stream);
+
+/*
+ * Register block_tables[b][j] under hashes[b][j] for j in [first[b],
+ * first[b] + count[b]), each registration taking a reference.  A key already
+ * in the table keeps its block; several sequences inserting one new key in
+ * the same call agree on one of their blocks.  resolved (int32
+ * [num_seqs][max_blocks], entries in range only) = the block the table holds
+ * for the key afterwards (the caller's own, or the one to share instead);
+ * -1 and PKV_STATUS_TABLE_FULL when no free entry was left.  Removed entries
+ * are not reused; re-initialise the table to reclaim them.
+ */
+int pkv_prefix_insert(void* table, int capacity, const uint64_t* hashes, const int32_t* block_tables,
+                      const int32_t* first, const int32_t* count, int num_seqs, int max_blocks,
+                      int32_t* resolved, int32_t* status, void* stream);
+
+/*
+ * Drop one reference of the blocks j < count[b] of each sequence (a finished
+ * request); a key not in the table sets PKV_STATUS_NOT_FOUND.  Entries whose
+ * count reaches 0 stay cached (evictable by the caller's policy).
+ */
+int pkv_prefix_release(void* table, int capacity, const uint64_t* hashes, const int32_t* count,
+                       int num_seqs, int max_blocks, int32_t* status, void* stream);
 
 /*
  * a9. Greedy speculative acceptance ([SI] 12.4; [KVC] 08: with greedy

@@ -32,6 +32,8 @@ PKV_STATUS_TIMEOUT = 32
 PKV_STATUS_BAD_PAIR = 64
 PKV_STATUS_BAD_TOKEN = 128
 PKV_STATUS_BAD_DIST = 256
+PKV_STATUS_TABLE_FULL = 512
+PKV_STATUS_NOT_FOUND = 1024
 PKV_ATTN_DECODE_CUDA_CORES = 1
 PKV_ERR_SCRATCH_LIMIT = -8
 
@@ -51,6 +53,12 @@ _SIGS = {
                                     ctypes.c_float, _I, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_spec_accept_greedy": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
     "pkv_spec_accept_sample": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+    "pkv_prefix_table_bytes": ([_I], ctypes.c_size_t),
+    "pkv_prefix_table_init": ([_P, _I, _P], _I),
+    "pkv_prefix_hash": ([_P, _P, _I, _P, _I, _I, _I, ctypes.c_uint64, _P], _I),
+    "pkv_prefix_lookup": ([_P, _I, _P, _P, _I, _I, _I, _P, _P, _P], _I),
+    "pkv_prefix_insert": ([_P, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P], _I),
+    "pkv_prefix_release": ([_P, _I, _P, _P, _I, _I, _P, _P], _I),
     "pkv_kv_append_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_copy_blocks_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_paged_attention_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -113,7 +121,7 @@ def _dev(t, name, dtype=None):
 
 
 def status_bits(code: int):
-    return [lib().pkv_status_string(1 << i).decode() for i in range(10) if code & (1 << i)]
+    return [lib().pkv_status_string(1 << i).decode() for i in range(12) if code & (1 << i)]
 
 
 def slot_mapping(slots, block_tables, seq_lens, append_lens, block_size, num_blocks, status=None, stream=None):
@@ -205,6 +213,67 @@ def spec_accept_greedy(logits, draft, argmax_out, accepted, next_token, stream=N
     rc = lib().pkv_spec_accept_greedy(_ptr(logits), _ptr(draft), B, k1 - 1, V, _ptr(argmax_out), _ptr(accepted),
                                       _ptr(next_token), _stream(stream))
     _check(rc, "pkv_spec_accept_greedy")
+
+
+class PrefixTable:
+    """A prefix-cache table in device memory (see pkv.h: chained 128-bit
+    block keys, open addressing, 32-byte entries)."""
+
+    def __init__(self, capacity: int, device="cuda", stream=None):
+        self.capacity = int(capacity)
+        nbytes = int(lib().pkv_prefix_table_bytes(self.capacity))
+        if nbytes == 0:
+            raise ValueError("capacity must be a power of two")
+        self.buf = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        _check(lib().pkv_prefix_table_init(_ptr(self.buf), self.capacity, _stream(stream)), "pkv_prefix_table_init")
+
+    def entries(self):
+        """(keys uint64 [cap][2], block int32 [cap], refs int32 [cap]) on the host."""
+        raw = self.buf.view(torch.int64).view(self.capacity, 4).cpu()
+        keys = raw[:, :2].numpy().view("uint64")
+        br = raw[:, 2:3].contiguous().view(torch.int32).view(self.capacity, 2).numpy()
+        return keys, br[:, 0], br[:, 1]
+
+
+def prefix_hash(hashes, tokens, lens, block_size, salt=0, stream=None):
+    """hashes uint64-as-int64 [B][max_blocks][2] out; tokens int32 [B][T]; lens int32 [B]."""
+    _dev(hashes, "hashes", torch.int64)
+    _dev(tokens, "tokens", torch.int32)
+    _dev(lens, "lens", torch.int32)
+    B, T = tokens.shape
+    rc = lib().pkv_prefix_hash(_ptr(hashes), _ptr(tokens), T, _ptr(lens), B, block_size, hashes.shape[1],
+                               ctypes.c_uint64(salt & (2 ** 64 - 1)), _stream(stream))
+    _check(rc, "pkv_prefix_hash")
+
+
+def prefix_lookup(table, hashes, lens, block_size, block_tables, cached_blocks, stream=None):
+    _dev(hashes, "hashes", torch.int64)
+    _dev(lens, "lens", torch.int32)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(cached_blocks, "cached_blocks", torch.int32)
+    B, MB, _ = hashes.shape
+    rc = lib().pkv_prefix_lookup(_ptr(table.buf), table.capacity, _ptr(hashes), _ptr(lens), B, block_size, MB,
+                                 _ptr(block_tables), _ptr(cached_blocks), _stream(stream))
+    _check(rc, "pkv_prefix_lookup")
+
+
+def prefix_insert(table, hashes, block_tables, first, count, resolved, status=None, stream=None):
+    for n, t in (("block_tables", block_tables), ("first", first), ("count", count), ("resolved", resolved)):
+        _dev(t, n, torch.int32)
+    _dev(hashes, "hashes", torch.int64)
+    B, MB, _ = hashes.shape
+    rc = lib().pkv_prefix_insert(_ptr(table.buf), table.capacity, _ptr(hashes), _ptr(block_tables), _ptr(first),
+                                 _ptr(count), B, MB, _ptr(resolved), _ptr(status), _stream(stream))
+    _check(rc, "pkv_prefix_insert")
+
+
+def prefix_release(table, hashes, count, status=None, stream=None):
+    _dev(hashes, "hashes", torch.int64)
+    _dev(count, "count", torch.int32)
+    B, MB, _ = hashes.shape
+    rc = lib().pkv_prefix_release(_ptr(table.buf), table.capacity, _ptr(hashes), _ptr(count), B, MB, _ptr(status),
+                                  _stream(stream))
+    _check(rc, "pkv_prefix_release")
 
 
 def kv_append_fp8(k_cache, v_cache, k_new, v_new, slots, k_scale, v_scale, status=None, stream=None):

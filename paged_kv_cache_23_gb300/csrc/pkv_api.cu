@@ -108,6 +108,8 @@ extern "C" const char* pkv_status_string(int bit) {
         case PKV_STATUS_BAD_PAIR: return "copy pair outside the pool";
         case PKV_STATUS_BAD_TOKEN: return "draft token outside the vocabulary";
         case PKV_STATUS_BAD_DIST: return "sampling distribution without positive weight";
+        case PKV_STATUS_TABLE_FULL: return "prefix-cache table full";
+        case PKV_STATUS_NOT_FOUND: return "prefix-cache key not found";
         default: return "unknown status bit";
     }
 }
