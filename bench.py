@@ -174,6 +174,10 @@ WORKLOADS = {
                     seq="log-normal median 1024", max_seq_len=32768, fp8=True),
     "decode_fp8": dict(desc="8B decode over an FP8 (e4m3) KV cache, " + SHAPE + ": batch 64, seq_len ~ U[512, 4096], "
                        "q_len 1", batch=64, seq="U[512, 4096]", max_seq_len=None, fp8=True),
+    "prefix": dict(desc="prefix-cache block lookup: batch 256 prompts, log-normal lengths (median 1024, sigma 1, "
+                   "clip [16, 32768]), half start with one 2048-token system prompt already cached; block_size 16; "
+                   "chained 128-bit block hashes of every full block + batched table lookup", batch=256,
+                   seq="log-normal median 1024", max_seq_len=None),
     "sample": dict(desc="stochastic speculative acceptance (modified rejection sampling): batch 32, k 5, "
                    "vocab 128256, p/q fp32 softmax rows, drafts drawn from q", batch=32, seq="n/a",
                    max_seq_len=None),
@@ -194,6 +198,8 @@ def make_workload(seed: int, name: str = "mix"):
         return wl.long_context(8, 131072, 512, 8192, 4096, seed)
     if name == "sample":
         return wl.spec_sample(B=32, k=5, vocab=128256, seed=seed)
+    if name == "prefix":
+        return wl.prompts(B=256, seed=seed)
     raise ValueError(name)
 
 
@@ -272,7 +278,22 @@ def run_reference(args):
     spec = WORKLOADS[args.workload]
     w = make_workload(0, args.workload)
     oracle.build()
-    if args.workload == "sample":
+    if args.workload == "prefix":
+        maxb = w.tokens.shape[1] // PREFIX_BS
+        h = oracle.prefix_hash(w.tokens, w.lens, PREFIX_BS, maxb)
+        sharer = int(w.meta["sharers"][np.argmax(w.lens[w.meta["sharers"]])])
+        nsys = min(int(w.lens[sharer]), w.meta["prefix"]) // PREFIX_BS
+        keys = {(int(h[sharer, j, 0]), int(h[sharer, j, 1])): j for j in range(nsys)}
+        _, n, _ = _prefix_oracle_step(w, keys)
+        nbytes = prefix_bytes(w, int(n.sum()))
+        t = []
+        for _ in range(max(0, args.warmup) + args.steps):
+            t0 = time.perf_counter()
+            _prefix_oracle_step(w, keys)
+            t.append(time.perf_counter() - t0)
+        t = t[max(0, args.warmup):]
+        sample = "the whole batch of 256 prompts per step (C hash + Python dict lookup)"
+    elif args.workload == "sample":
         acc, _, _ = oracle.spec_accept_sample(w.p, w.q, w.draft, w.r, w.s)
         nbytes = accounting.accept_sample_bytes(w, acc)
         oracle_sample_time(w, max(0, args.warmup))
@@ -306,6 +327,8 @@ def metric_of(name: str) -> str:
         return METRIC
     if name == "sample":
         return "stochastic speculative acceptance GB/s (% of GB300 HBM peak); sequences/s"
+    if name == "prefix":
+        return "prefix-cache hash + lookup GB/s (% of GB300 HBM peak); prompts/s"
     return f"paged attention KV GB/s (% of GB300 HBM peak); seq-steps/s, {name} workload"
 
 
@@ -471,6 +494,154 @@ def end_to_end(ds, w, args, stream, device, ws):
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}
 
 
+PREFIX_BS = 16
+PREFIX_CAPACITY = 1 << 20
+
+
+def prefix_bytes(x, nhit):
+    """Algorithmic bytes of hash + lookup: the tokens of every full block (4 B),
+    each block's key written and read back (16 B each), one 32-byte table
+    entry read per probe, and per hit a ref-count update (8 B) and a
+    block-table entry (4 B); plus lengths and hit counts."""
+    nb = (x.lens // PREFIX_BS).astype(np.int64)
+    blocks = int(nb.sum())
+    return int(blocks * PREFIX_BS * 4 + blocks * (16 + 16 + 32) + int(nhit) * 12 + len(x.lens) * 8)
+
+
+def _prefix_oracle_step(x, cache_keys):
+    import oracle
+    maxb = int(x.tokens.shape[1]) // PREFIX_BS
+    h = oracle.prefix_hash(x.tokens, x.lens, PREFIX_BS, maxb)
+    cache = oracle.PrefixCache()
+    for k, blk in cache_keys.items():
+        cache.d[k] = [blk, 1]
+    bt = np.full((len(x.lens), maxb), -1, np.int32)
+    n = cache.lookup(h, x.lens, PREFIX_BS, bt)
+    return h, n, bt
+
+
+def run_prefix(args):
+    """Prefix-cache hash + lookup for a batch of 256 prompts."""
+    import torch
+    ws, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the GPU arm needs a GB300)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    import paged_kv_cache_23_gb300 as pkv
+    spec = WORKLOADS["prefix"]
+    x = make_workload(rank, "prefix")
+    B, T = x.tokens.shape
+    maxb = T // PREFIX_BS
+    tok = torch.from_numpy(x.tokens).to(device)
+    lens = torch.from_numpy(x.lens).to(device)
+    hashes = torch.zeros((B, maxb, 2), dtype=torch.int64, device=device)
+    bt = torch.full((B, maxb), -1, dtype=torch.int32, device=device)
+    cached = torch.zeros(B, dtype=torch.int32, device=device)
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+    table = pkv.PrefixTable(PREFIX_CAPACITY, device=device)
+    # the system prompt is cached: insert the full blocks of the longest sharer
+    sharer = int(x.meta["sharers"][np.argmax(x.lens[x.meta["sharers"]])])
+    pkv.prefix_hash(hashes, tok, lens, PREFIX_BS)
+    nsys = min(int(x.lens[sharer]), x.meta["prefix"]) // PREFIX_BS
+    ids = torch.arange(B * maxb, dtype=torch.int32, device=device).view(B, maxb) + 5000
+    one = torch.zeros(B, dtype=torch.int32, device=device)
+    cnt = torch.zeros(B, dtype=torch.int32, device=device)
+    cnt[sharer] = nsys
+    res = torch.zeros((B, maxb), dtype=torch.int32, device=device)
+    pkv.prefix_insert(table, hashes, ids, one, cnt, res, status=st)
+    torch.cuda.synchronize()
+    keys = hashes[sharer, :nsys].cpu().numpy().view(np.uint64)
+    cache_keys = {(int(k[0]), int(k[1])): 5000 + sharer * maxb + j for j, k in enumerate(keys)}
+    flush_buf = torch.ones(64 << 20, dtype=torch.float32, device=device)
+    flush_sink = torch.empty(1, dtype=torch.float32, device=device)
+
+    def call():
+        pkv.prefix_hash(hashes, tok, lens, PREFIX_BS, stream=stream)
+        pkv.prefix_lookup(table, hashes, lens, PREFIX_BS, bt, cached, stream=stream)
+
+    parity = None
+    if rank == 0 and not args.no_check:
+        call()
+        torch.cuda.synchronize()
+        h_ref, n_ref, bt_ref = _prefix_oracle_step(x, cache_keys)
+        gh = hashes.cpu().numpy().view(np.uint64)
+        full = np.arange(maxb)[None, :] < (x.lens // PREFIX_BS)[:, None]
+        parity = {"hashes_bit_exact": bool(np.array_equal(gh[full], h_ref[full])),
+                  "hits_exact": bool(np.array_equal(cached.cpu().numpy(), n_ref)),
+                  "block_tables_exact": bool(np.array_equal(bt.cpu().numpy(), bt_ref)),
+                  "hits": int(n_ref.sum())}
+    for _ in range(max(3, args.warmup)):
+        torch.sum(flush_buf, dim=0, keepdim=True, out=flush_sink)
+        call()
+    torch.cuda.synchronize()
+    nhit = int(cached.sum().item())
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        torch.sum(flush_buf, dim=0, keepdim=True, out=flush_sink)
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    ms = aggregate_max(sum(a.elapsed_time(z) for a, z in ev) / args.steps, ws, device)
+    nbytes = prefix_bytes(x, nhit)
+    value = aggregate_sum(nbytes, ws, device) / (ms / 1e3) / 1e9
+    achieved = nbytes / (ms / 1e3) / 1e9
+    peak, peak_kind = load_peaks()
+    # end to end: the prompts' tokens and lengths come from pinned host memory
+    htok = torch.from_numpy(x.tokens).pin_memory()
+    hlen = torch.from_numpy(x.lens).pin_memory()
+    hout = torch.empty(B, dtype=torch.int32).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        tok.copy_(htok, non_blocking=True)
+        lens.copy_(hlen, non_blocking=True)
+        call()
+        hout.copy_(cached, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = aggregate_max(e0.elapsed_time(e1) / args.steps, ws, device)
+    if rank != 0:
+        return 0
+    line = {"metric": metric_of("prefix"), "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u64 hashes, i32 tokens", "data": "synthetic",
+            "config": {"workload": spec["desc"], "global_batch": B * ws, "seq_len": spec["seq"],
+                       "parallelism": "single GPU" if ws == 1 else f"replicas x{ws}",
+                       "l2": "L2 flushed before every call by reading a 256 MB buffer",
+                       "table_capacity": PREFIX_CAPACITY},
+            "prompts_per_s": B * ws / (ms / 1e3), "bytes_per_call": nbytes, "hits": nhit,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": None, "kernel": "prefix_hash_kernel + prefix_lookup_kernel",
+                         "peak_kind": peak_kind},
+            "clocks": clocks, "gpu_launches": 2 * args.steps, "status": int(st.item()), "parity": parity,
+            "e2e": {"value": nbytes / (ms_e2e / 1e3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": int(htok.numel() * 4 + hlen.numel() * 4), "d2h_bytes_per_step": B * 4,
+                    "ms_per_step": ms_e2e}}
+    t0 = time.perf_counter()
+    _prefix_oracle_step(x, cache_keys)
+    t_cpu = time.perf_counter() - t0
+    line["cpu_baseline"] = {"value": nbytes / t_cpu / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": "the whole batch of 256 prompts (C hash + Python dict lookup), one pass"}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def run_sample(args):
     """Stochastic speculative acceptance alone: batch 32, k 5, vocab 128256."""
     import torch
@@ -615,6 +786,8 @@ def main(argv=None):
         return run_reference(args)
     if args.workload == "sample":
         return run_sample(args)
+    if args.workload == "prefix":
+        return run_prefix(args)
     return run_gpu(args)
 
 

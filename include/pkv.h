@@ -295,16 +295,19 @@ int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache
  *
  * Block hash (this library's definition; the pages fix none): 128 bits, two
  * 64-bit lanes L = 0, 1, seeds S0 = 0x243F6A8885A308D3, S1 = 0x13198A2E03707344,
- * arithmetic mod 2^64:
+ * multipliers X0 = 0x0C3A5F1D2B4E6978, X1 = 0x15D3B7E9A1C4F286, P = 2^61 - 1:
  *   mix(x):  x ^= x >> 32; x *= M; x ^= x >> 29; x *= M; x ^= x >> 32,
- *            M = 0xD6E8FEB86659FD93
- *   content of block j:  c = S_L ^ salt;
- *                        for i < block_size: c = mix(c + (uint32)tok[j*bs+i] + (i << 32))
- *   chain:   h_-1 = S_L;  h_j = mix(h_{j-1} ^ mix(c_j + 0x9E3779B97F4A7C15))
- * key_j = (h_j lane 0, h_j lane 1), except that a key with lane 1 == 0 and
- * lane 0 < 2 takes lane 1 = 1 ((0, 0) and (1, 0) mark empty and removed
- * entries).  salt is the caller's computation-version key (model, adapter,
- * positional settings).  Only full blocks are hashed.
+ *            M = 0xD6E8FEB86659FD93 (mod 2^64)
+ *   digest of block j:  c = S_L ^ salt;
+ *                       for i < block_size: c = mix(c + (uint32)tok[j*bs+i] + (i << 32));
+ *                       d_j = mix(c + 0x9E3779B97F4A7C15) mod P
+ *   chain:   a_-1 = S_L mod P;  a_j = (a_{j-1} * X_L + d_j) mod P
+ *            (the parent's hash times X plus the block's own digest)
+ *   key_j:   lane L = mix(a_j); a key with lane 1 == 0 and lane 0 < 2 takes
+ *            lane 1 = 1 ((0, 0) and (1, 0) mark empty and removed entries).
+ * salt is the caller's computation-version key (model, adapter, positional
+ * settings).  Only full blocks are hashed.  The chain's affine steps compose
+ * associatively, so the GPU evaluates it as a parallel prefix scan.
  *
  * Table: device memory of pkv_prefix_table_bytes(capacity) bytes (capacity a
  * power of two, 16-byte aligned), caller-owned; entries are 32 bytes

@@ -660,16 +660,20 @@ int oracle_spec_accept_sample(int32_t *accepted, int32_t *next_token, const floa
  * content and the computation version, and only a shared beginning counts).
  *
  * The hash is this build's own definition (the pages fix none), 128 bits as two
- * 64-bit lanes L = 0, 1 with seeds S0 = 0x243F6A8885A308D3, S1 =
- * 0x13198A2E03707344, and salt = the caller's computation-version key:
+ * 64-bit lanes L = 0, 1; salt = the caller's computation-version key:
  *   mix(x):  x ^= x >> 32; x *= M; x ^= x >> 29; x *= M; x ^= x >> 32,
- *            M = 0xD6E8FEB86659FD93 (all arithmetic mod 2^64)
- *   content: c = S_L ^ salt; for i = 0..bs-1: c = mix(c + (uint32)tok_i + (i << 32))
- *   chain:   h_{-1} = S_L;  h_j = mix(h_{j-1} ^ mix(c_j + 0x9E3779B97F4A7C15))
- * and, so that (0, 0) and (1, 0) stay free as the table's empty and deleted
- * marks, a key whose lane 1 is 0 and lane 0 is 0 or 1 gets lane 1 = 1.
- * Only full blocks (j < len / bs) are hashed.  hashes: [num_seqs][max_blocks][2]
- * (lane 0, lane 1); entries past a sequence's full blocks are left alone.
+ *            M = 0xD6E8FEB86659FD93 (arithmetic mod 2^64)
+ *   content: c = S_L ^ salt; for i = 0..bs-1: c = mix(c + (uint32)tok_i + (i << 32));
+ *            d_j = mix(c + 0x9E3779B97F4A7C15) mod P
+ *   chain:   a_{-1} = S_L mod P;  a_j = (a_{j-1} * X_L + d_j) mod P,  P = 2^61 - 1
+ *            (the parent's hash times X_L plus the block's own digest)
+ *   key_j:   lane L = mix(a_j), except that a key whose lane 1 is 0 and lane 0
+ *            is 0 or 1 takes lane 1 = 1 ((0, 0) and (1, 0) mark the table's
+ *            empty and removed entries)
+ * with S0 = 0x243F6A8885A308D3, S1 = 0x13198A2E03707344, X0 =
+ * 0x0C3A5F1D2B4E6978, X1 = 0x15D3B7E9A1C4F286.  Only full blocks (j < len / bs)
+ * are hashed.  hashes: [num_seqs][max_blocks][2] (lane 0, lane 1); entries
+ * past a sequence's full blocks are left alone.
  */
 static uint64_t hmix(uint64_t x) {
     const uint64_t M = 0xD6E8FEB86659FD93ull;
@@ -681,26 +685,37 @@ static uint64_t hmix(uint64_t x) {
     return x;
 }
 
+static const uint64_t P61 = (1ull << 61) - 1;
+
+static uint64_t mulmod61(uint64_t a, uint64_t b) {
+    const unsigned __int128 p = (unsigned __int128)a * b;
+    uint64_t r = (uint64_t)(p % P61);
+    return r;
+}
+
 int oracle_prefix_hash(uint64_t *hashes, const int32_t *tokens, int max_tokens, const int32_t *lens, int num_seqs,
                        int block_size, int max_blocks, uint64_t salt) {
     const uint64_t seed[2] = {0x243F6A8885A308D3ull, 0x13198A2E03707344ull};
+    const uint64_t X[2] = {0x0C3A5F1D2B4E6978ull, 0x15D3B7E9A1C4F286ull};
     for (int b = 0; b < num_seqs; b++) {
         int nfull = lens[b] / block_size;
         if (nfull > max_blocks) nfull = max_blocks;
-        uint64_t h[2] = {seed[0], seed[1]};
+        uint64_t a[2] = {seed[0] % P61, seed[1] % P61};
         for (int j = 0; j < nfull; j++) {
+            uint64_t key[2];
             for (int L = 0; L < 2; L++) {
                 uint64_t c = seed[L] ^ salt;
                 for (int i = 0; i < block_size; i++) {
                     const uint32_t t = (uint32_t)tokens[(int64_t)b * max_tokens + (int64_t)j * block_size + i];
                     c = hmix(c + (uint64_t)t + ((uint64_t)i << 32));
                 }
-                h[L] = hmix(h[L] ^ hmix(c + 0x9E3779B97F4A7C15ull));
+                const uint64_t d = hmix(c + 0x9E3779B97F4A7C15ull) % P61;
+                a[L] = (mulmod61(a[L], X[L]) + d) % P61;
+                key[L] = hmix(a[L]);
             }
-            uint64_t k0 = h[0], k1 = h[1];
-            if (k1 == 0 && k0 < 2) k1 = 1;
-            hashes[((int64_t)b * max_blocks + j) * 2] = k0;
-            hashes[((int64_t)b * max_blocks + j) * 2 + 1] = k1;
+            if (key[1] == 0 && key[0] < 2) key[1] = 1;
+            hashes[((int64_t)b * max_blocks + j) * 2] = key[0];
+            hashes[((int64_t)b * max_blocks + j) * 2 + 1] = key[1];
         }
     }
     return 0;

@@ -9,7 +9,10 @@
 // computation version (the salt).
 //
 // Hash: this library's own 128-bit chained definition (two 64-bit lanes),
-// stated in pkv.h.  Table: open addressing in device memory, 32-byte entries
+// stated in pkv.h: a block's key is a mix of a_j = a_{j-1} X + d_j mod
+// 2^61 - 1 (the parent's value times X plus the block's own digest), whose
+// affine steps compose associatively, so a CTA computes a sequence's chain as
+// a parallel prefix scan rather than block after block.  Table: open addressing in device memory, 32-byte entries
 // {key lane 0, key lane 1, block id, ref count}; key (0, 0) = empty,
 // (1, 0) = removed; linear probing from lane 0 mod capacity.  Keys are claimed
 // with a 128-bit compare-and-swap, so concurrent inserts of one key in a batch
@@ -26,7 +29,10 @@ struct alignas(16) PrefixEntry {
 static_assert(sizeof(PrefixEntry) == 32, "32-byte entries");
 
 constexpr int kHashThreads = 256;
-constexpr int kHashChunk = 1024;  // blocks whose content hashes are staged in shared memory at a time
+constexpr int kHashPer = 4;                             // consecutive blocks per thread
+constexpr int kHashChunk = kHashThreads * kHashPer;     // blocks per pass of a CTA
+constexpr uint64_t kP61 = (1ull << 61) - 1;
+constexpr int kLookupBatch = 4;                         // probes a thread keeps in flight
 
 __device__ __forceinline__ uint64_t hmix(uint64_t x) {
     const uint64_t M = 0xD6E8FEB86659FD93ull;
@@ -38,49 +44,140 @@ __device__ __forceinline__ uint64_t hmix(uint64_t x) {
     return x;
 }
 
-__constant__ uint64_t kHashSeed[2] = {0x243F6A8885A308D3ull, 0x13198A2E03707344ull};
+// (a * b) mod 2^61 - 1 for a, b < 2^61 - 1 (2^61 = 1 mod P).
+__device__ __forceinline__ uint64_t mulmod61(uint64_t a, uint64_t b) {
+    const uint64_t lo = a * b, hi = __umul64hi(a, b);
+    uint64_t r = (lo & kP61) + ((hi << 3) | (lo >> 61));
+    r = (r & kP61) + (r >> 61);
+    return r >= kP61 ? r - kP61 : r;
+}
 
-// One CTA per sequence: content hashes of up to kHashChunk blocks in parallel
-// (thread per block and lane), then threads 0 and 1 run the two lanes' chains.
+__device__ __forceinline__ uint64_t addmod61(uint64_t a, uint64_t b) {
+    const uint64_t r = a + b;
+    return r >= kP61 ? r - kP61 : r;
+}
+
+// The chain a_j = a_{j-1} X + d_j is a product of affine maps v -> v A + V;
+// composing "first (A1, V1), then (A2, V2)" gives (A1 A2, V1 A2 + V2), an
+// associative operation, so the chain is a prefix scan.
+struct Aff {
+    uint64_t A, V;
+};
+
+__device__ __forceinline__ Aff compose(Aff f, Aff g) { return Aff{mulmod61(f.A, g.A), addmod61(mulmod61(f.V, g.A), g.V)}; }
+
+__device__ __forceinline__ Aff shfl_up_aff(Aff x, int o) {
+    return Aff{__shfl_up_sync(kFull, x.A, o), __shfl_up_sync(kFull, x.V, o)};
+}
+
+__constant__ uint64_t kHashSeed[2] = {0x243F6A8885A308D3ull, 0x13198A2E03707344ull};
+__constant__ uint64_t kHashX[2] = {0x0C3A5F1D2B4E6978ull, 0x15D3B7E9A1C4F286ull};
+
+// One CTA per sequence, kHashChunk blocks per pass: every block's digest in
+// parallel, each thread composes its 4 blocks' maps, a block-wide exclusive
+// scan of the composed maps gives every thread the map of all blocks before
+// its own, applied to the chain value carried from the previous pass.
 __global__ void __launch_bounds__(kHashThreads) prefix_hash_kernel(uint64_t* __restrict__ hashes,
                                                                    const int32_t* __restrict__ tokens,
                                                                    int max_tokens, const int32_t* __restrict__ lens,
                                                                    int num_seqs, int block_size, int max_blocks,
                                                                    uint64_t salt) {
-    __shared__ uint64_t content[kHashChunk][2];
+    __shared__ Aff warp_tot[2][kHashThreads / 32];
+    __shared__ uint64_t carry[2];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
     pdl_launch();
     for (int b = blockIdx.x; b < num_seqs; b += gridDim.x) {
         int nfull = lens[b] / block_size;
         if (nfull > max_blocks) nfull = max_blocks;
         if (nfull < 0) nfull = 0;
-        uint64_t h = threadIdx.x < 2 ? kHashSeed[threadIdx.x] : 0;
+        if (tid < 2) carry[tid] = kHashSeed[tid] % kP61;
+        __syncthreads();
         const int32_t* tk = tokens + (long long)b * max_tokens;
         for (int j0 = 0; j0 < nfull; j0 += kHashChunk) {
-            const int n = min(kHashChunk, nfull - j0);
-            for (int e = threadIdx.x; e < 2 * n; e += kHashThreads) {
-                const int j = j0 + (e >> 1), L = e & 1;
-                uint64_t c = kHashSeed[L] ^ salt;
-                const int32_t* blk = tk + (long long)j * block_size;
-                for (int i = 0; i < block_size; ++i)
-                    c = hmix(c + (uint64_t)(uint32_t)__ldg(blk + i) + ((uint64_t)i << 32));
-                content[e >> 1][L] = c;
+            const int jt = j0 + kHashPer * tid;  // this thread's first block
+            // digests: the 4 blocks x 2 lanes are 8 independent mix chains,
+            // interleaved token by token (one load per token feeds both lanes)
+            uint64_t d[2][kHashPer];
+            {
+                uint64_t c[kHashPer][2];
+                const int32_t* blk[kHashPer];
+#pragma unroll
+                for (int u = 0; u < kHashPer; ++u) {
+                    c[u][0] = kHashSeed[0] ^ salt;
+                    c[u][1] = kHashSeed[1] ^ salt;
+                    blk[u] = tk + (long long)min(jt + u, nfull - 1) * block_size;  // in range; unused past nfull
+                }
+                for (int i = 0; i < block_size; ++i) {
+                    uint32_t t[kHashPer];
+#pragma unroll
+                    for (int u = 0; u < kHashPer; ++u) t[u] = (uint32_t)__ldg(blk[u] + i);
+#pragma unroll
+                    for (int u = 0; u < kHashPer; ++u) {
+                        const uint64_t add = (uint64_t)t[u] + ((uint64_t)i << 32);
+                        c[u][0] = hmix(c[u][0] + add);
+                        c[u][1] = hmix(c[u][1] + add);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kHashPer; ++u)
+#pragma unroll
+                    for (int L = 0; L < 2; ++L) d[L][u] = hmix(c[u][L] + 0x9E3779B97F4A7C15ull) % kP61;
+            }
+            Aff mine[2];
+#pragma unroll
+            for (int L = 0; L < 2; ++L) {
+                mine[L] = Aff{1, 0};
+#pragma unroll
+                for (int u = 0; u < kHashPer; ++u)
+                    if (jt + u < nfull) mine[L] = compose(mine[L], Aff{kHashX[L], d[L][u]});
+            }
+            // exclusive scan of the threads' maps, in thread order
+            Aff pre[2];
+#pragma unroll
+            for (int L = 0; L < 2; ++L) {
+                Aff x = mine[L];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const Aff y = shfl_up_aff(x, o);
+                    if (lane >= o) x = compose(y, x);
+                }
+                if (lane == 31) warp_tot[L][warp] = x;
+                const Aff up = shfl_up_aff(x, 1);
+                pre[L] = lane ? up : Aff{1, 0};
             }
             __syncthreads();
-            if (threadIdx.x < 2) {
-                const int L = threadIdx.x;
-                for (int j = 0; j < n; ++j) {
-                    h = hmix(h ^ hmix(content[j][L] + 0x9E3779B97F4A7C15ull));
-                    hashes[((long long)b * max_blocks + j0 + j) * 2 + L] = h;
+#pragma unroll
+            for (int L = 0; L < 2; ++L) {
+                Aff w = Aff{1, 0};
+                for (int k = 0; k < warp; ++k) w = compose(w, warp_tot[L][k]);
+                pre[L] = compose(w, pre[L]);
+            }
+            // chain values of this thread's blocks
+            uint64_t a[2] = {carry[0], carry[1]};
+            __syncthreads();  // every thread has read the carry
+#pragma unroll
+            for (int L = 0; L < 2; ++L) a[L] = addmod61(mulmod61(a[L], pre[L].A), pre[L].V);
+#pragma unroll
+            for (int u = 0; u < kHashPer; ++u) {
+                const int j = jt + u;
+                if (j >= nfull) break;
+                uint64_t key[2];
+#pragma unroll
+                for (int L = 0; L < 2; ++L) {
+                    a[L] = addmod61(mulmod61(a[L], kHashX[L]), d[L][u]);
+                    key[L] = hmix(a[L]);
+                }
+                if (key[1] == 0 && key[0] < 2) key[1] = 1;
+                uint64_t* out = hashes + ((long long)b * max_blocks + j) * 2;
+                out[0] = key[0];
+                out[1] = key[1];
+                if (j == min(nfull, j0 + kHashChunk) - 1) {
+                    carry[0] = a[0];
+                    carry[1] = a[1];
                 }
             }
-            __syncthreads();
-        }
-        // the reserved keys (0, 0) and (1, 0): such a key takes lane 1 = 1
-        __syncthreads();
-        for (int j = threadIdx.x; j < nfull; j += kHashThreads) {
-            uint64_t* k = hashes + ((long long)b * max_blocks + j) * 2;
-            if (k[1] == 0 && k[0] < 2) k[1] = 1;
+            __syncthreads();  // the next pass reads the new carry
         }
         __syncthreads();
     }
@@ -116,9 +213,27 @@ __global__ void __launch_bounds__(kHashThreads) prefix_lookup_kernel(PrefixEntry
         if (nfull < 0) nfull = 0;
         if (threadIdx.x == 0) first_miss = nfull;
         __syncthreads();
-        for (int j = threadIdx.x; j < nfull; j += kHashThreads) {
-            const uint64_t* k = hashes + ((long long)b * max_blocks + j) * 2;
-            if (probe(table, mask, k[0], k[1]) < 0) atomicMin(&first_miss, j);
+        // kLookupBatch blocks per thread at a time: their keys and home slots
+        // are loaded together, so most probes cost one round trip
+        for (int j0 = 0; j0 < nfull; j0 += kHashThreads * kLookupBatch) {
+            ulonglong2 key[kLookupBatch], home[kLookupBatch];
+#pragma unroll
+            for (int u = 0; u < kLookupBatch; ++u) {
+                const int j = j0 + u * kHashThreads + threadIdx.x;
+                key[u] = j < nfull ? *reinterpret_cast<const ulonglong2*>(hashes + ((long long)b * max_blocks + j) * 2)
+                                   : make_ulonglong2(0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < kLookupBatch; ++u)
+                home[u] = *reinterpret_cast<const ulonglong2*>(&table[key[u].x & (uint64_t)mask]);
+#pragma unroll
+            for (int u = 0; u < kLookupBatch; ++u) {
+                const int j = j0 + u * kHashThreads + threadIdx.x;
+                if (j >= nfull) continue;
+                const bool hit = (home[u].x == key[u].x && home[u].y == key[u].y) ||
+                                 (!(home[u].x == 0 && home[u].y == 0) && probe(table, mask, key[u].x, key[u].y) >= 0);
+                if (!hit) atomicMin(&first_miss, j);
+            }
         }
         __syncthreads();
         const int n = first_miss;

@@ -333,6 +333,35 @@ def fp8_pools(w: Workload, seed: int = 0) -> Fp8Pools:
 
 
 @dataclass
+class Prompts:
+    """Token ids of a batch of prompts: tokens int32 [B][max_len] (0 past each
+    length), lens int32 [B]."""
+    tokens: np.ndarray
+    lens: np.ndarray
+    meta: dict = field(default_factory=dict)
+
+
+def prompts(B: int = 256, median: int = 1024, sigma: float = 1.0, clip=(16, 32768), share: float = 0.5,
+            prefix: int = 2048, vocab: int = 128256, seed: int = 0) -> Prompts:
+    """Prompt lengths as in the mix (log-normal, clipped); a random ``share`` of
+    the batch starts with one common ``prefix``-token system prompt (cut to
+    the prompt's length); token ids uniform over the vocabulary."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 31])))
+    lens = np.clip(np.rint(g.lognormal(math.log(median), sigma, size=B)), clip[0], clip[1]).astype(np.int32)
+    T = int(lens.max())
+    tokens = g.integers(0, vocab, size=(B, T), dtype=np.int32)
+    sys_prompt = g.integers(0, vocab, size=prefix, dtype=np.int32)
+    sharers = g.choice(B, size=int(round(share * B)), replace=False)
+    for b in sharers:
+        n = min(prefix, int(lens[b]), T)
+        tokens[b, :n] = sys_prompt[:n]
+    for b in range(B):
+        tokens[b, lens[b]:] = 0
+    return Prompts(tokens, lens, dict(B=B, median=median, sigma=sigma, share=share, prefix=prefix, seed=seed,
+                                      sharers=np.sort(sharers)))
+
+
+@dataclass
 class SampleInputs:
     """Inputs of stochastic speculative acceptance: target distributions
     p [B][k+1][V], draft distributions q [B][k][V] (fp32, each row sums to 1),
