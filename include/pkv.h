@@ -189,8 +189,8 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *                 or 0: automatic -- the planning kernel starts from
  *                 pkv_attention_auto_partition(...) and doubles it (up to
  *                 8192) while the batch would give more than 3 partitions
- *                 per SM (fewer, longer partitions cost fewer partial
- *                 results); the length used is the int at byte offset 8 of
+ *                 per SM (6 when multi-query rows make up most of the work;
+ *                 fewer, longer partitions cost fewer partial results); the length used is the int at byte offset 8 of
  *                 the workspace after the call
  *   flags         0, or PKV_ATTN_DECODE_CUDA_CORES (q_len = 1 rows on the
  *                 CUDA-core FMA path; by default every row uses the tensor

@@ -504,12 +504,16 @@ __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnPar
     const int hps_lb = d.hps << lb, h_lb = warp << lb;
     const int kvh = d.hg * d.hps + warp;
     const int qd = lane & 3, qr = lane >> 2;
-    // Q^T as B fragments: n = query head qr of the group, k = dims
+    // columns c < nq * G are (query c / G of the tile, q head c % G); a decode
+    // row is a tile of one query, columns = the g heads of the group
+    const int ncols = d.nq * G;
+    // Q^T as B fragments: n = column qr, k = dims
     uint32_t qb[NT][2];
     {
         const uint32_t* qrow =
-            (active && qr < G)
-                ? reinterpret_cast<const uint32_t*>(p.q + ((long long)d.q_row0 * p.n_q + (long long)kvh * G + qr) * D)
+            (active && qr < ncols)
+                ? reinterpret_cast<const uint32_t*>(
+                      p.q + ((long long)(d.q_row0 + qr / G) * p.n_q + (long long)kvh * G + qr % G) * D)
                 : nullptr;
 #pragma unroll
         for (int ks = 0; ks < NT; ++ks) {
@@ -520,7 +524,10 @@ __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnPar
     float o[NT][4];  // O^T tile mt: (dim 16mt + qr [+8], head 2qd [+1])
 #pragma unroll
     for (int mt = 0; mt < NT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // heads 2qd, 2qd + 1
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // columns 2qd, 2qd + 1
+    // last visible position of columns 2qd and 2qd + 1 (their query's causal limit)
+    const int lim0 = 2 * qd < ncols ? d.t_vis - d.nq + (2 * qd) / G : -1;
+    const int lim1 = 2 * qd + 1 < ncols ? d.t_vis - d.nq + (2 * qd + 1) / G : -1;
     const int mi = lane >> 3, mr = lane & 7;
     const int a_tok = ((mi & 1) << 3) + mr, a_hi = mi >> 1;   // K: (t0-7,lo) (t8-15,lo) (t0-7,hi) (t8-15,hi)
     const int v_tok = ((mi >> 1) << 3) + mr, v_hi = mi & 1;   // V: (t0-7,lo) (t0-7,hi) (t8-15,lo) (t8-15,hi)
@@ -548,12 +555,13 @@ __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnPar
             ldsm_x4(kb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
             mma_bf16_16816((ks & 1) ? cb : ca, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
         }
-        // (token qr, head 2qd), (qr, 2qd+1), (qr+8, 2qd), (qr+8, 2qd+1)
+        // (token qr, column 2qd), (qr, 2qd+1), (qr+8, 2qd), (qr+8, 2qd+1)
         const bool va = qr < nvalid, vb8 = qr + 8 < nvalid;
-        const float s0 = va ? (ca[0] + cb[0]) * p.scale_log2 : -INFINITY;
-        const float s1 = va ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;
-        const float s2 = vb8 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;
-        const float s3 = vb8 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;
+        const int ta = t0 + qr, tb8 = t0 + qr + 8;
+        const float s0 = va && ta <= lim0 ? (ca[0] + cb[0]) * p.scale_log2 : -INFINITY;
+        const float s1 = va && ta <= lim1 ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;
+        const float s2 = vb8 && tb8 <= lim0 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;
+        const float s3 = vb8 && tb8 <= lim1 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;
         // The reference maxima m0, m1 move only when a new score exceeds them
         // by more than kRescaleSlack (base-2 units), so most stages need no
         // max reduction and no rescale of O; probabilities stay <= 2^slack.
@@ -623,9 +631,9 @@ __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnPar
     const float mh[2] = {m0, m1}, lh[2] = {l0, l1};
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-        const int h = 2 * qd + j;
-        if (h >= G) continue;
-        const long long orow = (long long)d.q_row0 * p.n_q + (long long)kvh * G + h;
+        const int c = 2 * qd + j;
+        if (c >= ncols) continue;
+        const long long orow = (long long)(d.q_row0 + c / G) * p.n_q + (long long)kvh * G + c % G;
         if (d.nparts == 1) {
             const float inv = 1.0f / lh[j];
             __nv_bfloat16* dst = p.out + orow * D + qr;

@@ -118,19 +118,26 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         // while the batch would give more than kAutoItemsPerSM partitions per
         // SM -- fewer, longer items cost fewer partial results and item
         // switches, and the longest-first order keeps the queue balanced
-        long long tok = 0;
+        long long tok = 0, tok_mq = 0;
         for (int b = tid; b < n; b += kPlanThreads) {
             const int L = pp.seq_lens[b], ql = pp.q_lens[b];
             if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len) continue;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8);
             const bool multi = sh.kind == KIND_MQ || ql > 1;
-            tok += (long long)L * (pp.n_kv / sh.hps) * (multi ? ceil_div(ql, sh.qt) : 1);
+            const long long t = (long long)L * (pp.n_kv / sh.hps) * (multi ? ceil_div(ql, sh.qt) : 1);
+            tok += t;
+            if (multi) tok_mq += t;
         }
-        // block sum in units of 16 tokens (fits an int for any accepted batch)
-        int tot16;
-        block_exclusive_scan_1024((int)min(tok >> 4, (long long)(1 << 30) / kPlanThreads), tmp, &tot16);
+        // block sums in units of 16 tokens (fit an int for any accepted batch)
+        int tot16, mq16;
+        const int cap = (1 << 30) / kPlanThreads;
+        block_exclusive_scan_1024((int)min(tok >> 4, (long long)cap), tmp, &tot16);
+        block_exclusive_scan_1024((int)min(tok_mq >> 4, (long long)cap), tmp, &mq16);
         const long long T = (long long)tot16 << 4;
-        while (P < kAutoPMax && T > (long long)P * kAutoItemsPerSM * pp.sms) P <<= 1;
+        // multi-query items cost more compute per token: a batch made of them
+        // (speculative verification) balances better with twice the items
+        const int per_sm = 4 * (long long)mq16 > 3 * (long long)tot16 ? 2 * kAutoItemsPerSM : kAutoItemsPerSM;
+        while (P < kAutoPMax && T > (long long)P * per_sm * pp.sms) P <<= 1;
     }
     if (tid == 0) pp.hdr[2] = P;
     __syncthreads();
