@@ -240,6 +240,20 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
                                        void* stream);
 
 /*
+ * a1 + a2 in one launch: the slot mapping of pkv_slot_mapping (the new tokens
+ * of sequence b are its last append_lens[b] positions, [KVC] 05) fused with
+ * the append of pkv_kv_append ([KVC] 02).  Same arguments and status bits as
+ * the two calls; slots (int64 [num_tokens]) receives the slots as
+ * pkv_slot_mapping writes them.  Bit-exact with the two calls.  Batches of
+ * more than 2048 sequences run the two kernels.
+ */
+int pkv_kv_append_paged(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                        const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                        const int32_t* append_lens, int num_seqs, int num_tokens, int num_blocks,
+                        int block_size, int num_kv_heads, int head_dim, int64_t* slots,
+                        int32_t* status, void* stream);
+
+/*
  * FP8 KV cache ([KVC] 03, "KV cache quantization": store K and V in FP8, one
  * byte per value instead of two, halving the cache and the bytes decode
  * attention rereads; the formats are e4m3 and e5m2 -- these entry points use

@@ -59,6 +59,7 @@ _SIGS = {
     "pkv_prefix_lookup": ([_P, _I, _P, _P, _I, _I, _I, _P, _P, _P], _I),
     "pkv_prefix_insert": ([_P, _I, _P, _P, _P, _P, _I, _I, _P, _P, _P], _I),
     "pkv_prefix_release": ([_P, _I, _P, _P, _I, _I, _P, _P], _I),
+    "pkv_kv_append_paged": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P], _I),
     "pkv_kv_append_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_copy_blocks_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_paged_attention_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -145,6 +146,22 @@ def kv_append(k_cache, v_cache, k_new, v_new, slots, status=None, stream=None):
     rc = lib().pkv_kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(slots), slots.numel(), nb,
                              bs, nkv, d, _ptr(status), _stream(stream))
     _check(rc, "pkv_kv_append")
+
+
+def kv_append_paged(k_cache, v_cache, k_new, v_new, block_tables, seq_lens, append_lens, slots, status=None,
+                    stream=None):
+    """a1 + a2 in one launch: slot mapping fused with the append; slots receives the slots."""
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("k_new", k_new), ("v_new", v_new)):
+        _dev(t, n, torch.bfloat16)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(append_lens, "append_lens", torch.int32)
+    _dev(slots, "slots", torch.int64)
+    nb, nkv, bs, d = k_cache.shape
+    rc = lib().pkv_kv_append_paged(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), _ptr(block_tables),
+                                   block_tables.shape[1], _ptr(seq_lens), _ptr(append_lens), seq_lens.numel(),
+                                   slots.numel(), nb, bs, nkv, d, _ptr(slots), _ptr(status), _stream(stream))
+    _check(rc, "pkv_kv_append_paged")
 
 
 def copy_blocks(k_cache, v_cache, src_dst, status=None, stream=None):

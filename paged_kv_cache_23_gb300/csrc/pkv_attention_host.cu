@@ -108,9 +108,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     int* a_mq = small ? s_mq : pp.seq_mq;
     int* a_full = small ? s_full : pp.seq_full;
     if (tid < kTailBuckets) hist[tid] = 0;
-    // the previous kernel in the stream (e.g. the KV append, or the last
-    // step's combine that still reads this workspace) must be complete
-    pdl_wait();
+    // Programmatic launch: the previous kernel of the stream may still run
+    // while passes A and B1-B3 do.  They read only seq_lens and q_lens, which
+    // no kernel of this library writes, and write only work-list state the
+    // previous step's attention kernel read -- and that kernel has finished:
+    // this kernel starts no earlier than its predecessor's own wait, which
+    // completes everything before it.  The per-row counts and NaN output rows
+    // (read and written by a previous combine) wait for the predecessor, and
+    // so does this kernel's completion, which the attention kernel waits on.
     pdl_launch();
     int P = pp.P;
     if (pp.adapt_P) {
@@ -208,16 +213,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     // pass B1: one thread per sequence -- decode tails and invalid sequences
     for (int b = tid; b < n; b += kPlanThreads) {
         const int4 sq = pp.seqs[b];
-        const int L = sq.x, ql = sq.y, q0 = sq.z;
-        if (pp.seq_flag[b]) {
-            // rows of an invalid sequence are NaN (inside the q/out extent)
-            const int qlc = ql > 0 ? min(ql, pp.total_q) : 0;
-            const int rows = min(qlc, pp.total_q - q0);
-            const long long n16 = (long long)rows * pp.n_q * pp.D / 8;
-            uint4* o = reinterpret_cast<uint4*>(pp.out + (long long)q0 * pp.n_q * pp.D);
-            for (long long e = 0; e < n16; ++e) o[e] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-            continue;
-        }
+        const int L = sq.x, ql = sq.y;
+        if (pp.seq_flag[b]) continue;  // its rows are written NaN after the wait below
         if (ql != 1 || (sq.w & 15) == KIND_MQ) continue;  // multi-query tiles are counted in pass B2
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
         const int np = ceil_div(L, P);
@@ -252,6 +249,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             const int part = li / ngroups;
             pp.items[c_mq + it] = make_int4(b, part, 0, li - part * ngroups);
         }
+    }
+    pdl_wait();
+    // rows of an invalid sequence are NaN (inside the q/out extent)
+    for (int b = tid; b < n; b += kPlanThreads) {
+        if (!pp.seq_flag[b]) continue;
+        const int4 sq = pp.seqs[b];
+        const int ql = sq.y, q0 = sq.z;
+        const int qlc = ql > 0 ? min(ql, pp.total_q) : 0;
+        const int rows = min(qlc, pp.total_q - q0);
+        const long long n16 = (long long)rows * pp.n_q * pp.D / 8;
+        uint4* o = reinterpret_cast<uint4*>(pp.out + (long long)q0 * pp.n_q * pp.D);
+        for (long long e = 0; e < n16; ++e) o[e] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
     }
     // pass B4: partitions per query row (0 for rows of invalid sequences and
     // rows past the last sequence's queries: nothing to merge)
@@ -445,7 +454,11 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     const int rc2 = fp8                ? dispatch_attention_fp8_d128(tm, ap, w.max_items, st)
                     : head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st)
                                       : dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
-    if (rc2 != PKV_OK || w.np_max <= 1) return rc2;  // one partition per row: outputs are final
+    // The combine runs even when no row can span partitions (it then only
+    // waits and exits): it triggers the next kernel of the stream only after
+    // the attention grid has finished, which the next call's planning kernel
+    // relies on before it rewrites the work list.
+    if (rc2 != PKV_OK) return rc2;
     CombineParams cp{};
     cp.out = ap.out;
     cp.part_o = ap.part_o;

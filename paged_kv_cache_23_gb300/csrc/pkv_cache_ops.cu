@@ -123,6 +123,88 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
 }
 
 // ---------------------------------------------------------------------------
+// Slot mapping fused with the append: every 1024-thread CTA scans the
+// append lengths into shared memory (batches up to kFusedMaxSeqs sequences),
+// then each 16-byte chunk of a new row finds its sequence by binary search,
+// forms the slot (as slot_mapping_kernel) and is copied (as kv_append_kernel).
+// One launch instead of two.
+// ---------------------------------------------------------------------------
+constexpr int kFusedMaxSeqs = 2048;
+
+__global__ void __launch_bounds__(1024) kv_append_paged_kernel(
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const uint4* __restrict__ k_new,
+    const uint4* __restrict__ v_new, const int32_t* __restrict__ block_tables, int max_blocks,
+    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ append_lens, int num_seqs, int num_tokens,
+    int num_blocks, int block_size, int num_kv_heads, int chunks_per_row, int64_t* __restrict__ slots,
+    int32_t* status) {
+    __shared__ int start[kFusedMaxSeqs + 1];
+    __shared__ int bad[kFusedMaxSeqs];
+    __shared__ int tmp[32];
+    pdl_wait();
+    pdl_launch();
+    int bits = 0;
+    int carry = 0;
+    for (int base = 0; base < num_seqs; base += 1024) {
+        const int b = base + threadIdx.x;
+        int A = 0;
+        if (b < num_seqs) {
+            const int L = seq_lens[b];
+            const int a = append_lens[b];
+            int flag = 0;
+            if (L < 0 || (long long)L > (long long)max_blocks * block_size) flag |= PKV_STATUS_BAD_SEQLEN;
+            if (a < 0 || a > L) flag |= PKV_STATUS_BAD_QLEN;
+            bad[b] = flag;
+            if (blockIdx.x == 0) bits |= flag;
+            A = a > 0 ? min(a, num_tokens + 1) : 0;
+        }
+        int tot;
+        const int ex = block_exclusive_scan_1024(A, tmp, &tot);
+        if (b < num_seqs) start[b] = carry + ex;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) start[num_seqs] = carry;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && carry != num_tokens) bits |= PKV_STATUS_BAD_QLEN;
+    __syncthreads();
+    const int n = carry < num_tokens ? carry : num_tokens;
+    const long long cap = (long long)num_blocks * block_size;
+    const long long per_tok = (long long)num_kv_heads * chunks_per_row;
+    const long long total = (long long)num_tokens * per_tok;
+    for (long long i = blockIdx.x * 1024LL + threadIdx.x; i < total; i += (long long)gridDim.x * 1024) {
+        const int o = (int)(i / per_tok);
+        const long long rem = i - (long long)o * per_tok;
+        int64_t slot = -1;
+        if (o < n) {
+            int lo = 0, hi = num_seqs - 1;  // last b with start[b] <= o
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (start[mid] <= o) lo = mid; else hi = mid - 1;
+            }
+            const int b = lo;
+            if (!bad[b]) {
+                const int L = seq_lens[b];
+                const int pos = L - (start[b + 1] - start[b]) + (o - start[b]);
+                const int32_t blk = block_tables[(long long)b * max_blocks + pos / block_size];
+                if (blk < 0 || blk >= num_blocks) {
+                    if (rem == 0) bits |= PKV_STATUS_BAD_BLOCK;
+                } else {
+                    slot = (int64_t)blk * block_size + pos % block_size;
+                }
+            }
+        }
+        if (rem == 0) slots[o] = slot;
+        if (slot < 0 || slot >= cap) continue;
+        const int h = (int)(rem / chunks_per_row);
+        const int c = (int)(rem - (long long)h * chunks_per_row);
+        const long long blk = slot / block_size;
+        const int row = (int)(slot - blk * block_size);
+        const long long dst = ((blk * num_kv_heads + h) * block_size + row) * chunks_per_row + c;
+        k_cache[dst] = ld_nc_v4(k_new + i);
+        v_cache[dst] = ld_nc_v4(v_new + i);
+    }
+    if (bits) report(status, bits);
+}
+
+// ---------------------------------------------------------------------------
 // KV append into e4m3 pools ("Inference at Scale" section 03, KV cache
 // quantization): code = e4m3(x * (1 / scale[head])), the reciprocal and the
 // product rounded to fp32 (nearest even), the conversion rounding to nearest
@@ -292,6 +374,42 @@ extern "C" int pkv_kv_append(void* k_cache, void* v_cache, const void* k_new, co
                                            (uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new,
                                            (const uint4*)v_new, slots, num_tokens, num_blocks, block_size,
                                            num_kv_heads, cpr, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_kv_append_paged(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                                   const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                                   const int32_t* append_lens, int num_seqs, int num_tokens, int num_blocks,
+                                   int block_size, int num_kv_heads, int head_dim, int64_t* slots, int32_t* status,
+                                   void* stream) {
+    if (num_seqs < 0 || num_tokens < 0 || max_blocks < 1 || num_blocks < 1 || block_size < 1 || num_kv_heads < 1 ||
+        head_dim < 8)
+        return PKV_ERR_SIZE;
+    if (head_dim % 8) return PKV_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || num_tokens == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !block_tables || !seq_lens || !append_lens || !slots)
+        return PKV_ERR_NULL;
+    if (!host::aligned16(k_cache) || !host::aligned16(v_cache) || !host::aligned16(k_new) || !host::aligned16(v_new))
+        return PKV_ERR_ALIGN;
+    if (num_seqs > kFusedMaxSeqs) {
+        // larger batches: the two-kernel path
+        const int rc = pkv_slot_mapping(slots, block_tables, max_blocks, seq_lens, append_lens, num_seqs, num_tokens,
+                                        block_size, num_blocks, status, stream);
+        if (rc) return rc;
+        return pkv_kv_append(k_cache, v_cache, k_new, v_new, slots, num_tokens, num_blocks, block_size, num_kv_heads,
+                             head_dim, status, stream);
+    }
+    const int rc = host::check_device();
+    if (rc) return rc;
+    const int cpr = head_dim / 8;
+    const long long total = (long long)num_tokens * num_kv_heads * cpr;
+    const long long want = (total + 1023) / 1024;
+    const int grid = (int)(want < host::sm_count() * 2LL ? want : host::sm_count() * 2LL);
+    const cudaError_t e = host::launch_pdl(kv_append_paged_kernel, dim3(grid), dim3(1024), 0, (cudaStream_t)stream,
+                                           (uint4*)k_cache, (uint4*)v_cache, (const uint4*)k_new,
+                                           (const uint4*)v_new, block_tables, max_blocks, seq_lens, append_lens,
+                                           num_seqs, num_tokens, num_blocks, block_size, num_kv_heads, cpr, slots,
+                                           status);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -12,6 +12,7 @@ import numpy as np
 import torch
 
 from . import (attention_auto_partition, attention_workspace_bytes, copy_blocks, copy_blocks_fp8, kv_append_fp8,
+               kv_append_paged,
                paged_attention_decode_fp8, kv_append, paged_attention_decode, slot_mapping,
                spec_accept_greedy)
 
@@ -86,13 +87,11 @@ class DeviceStep:
             self.next_token = torch.empty(B, dtype=torch.int32, device=dev)
 
     def launches_per_step(self) -> int:
-        """Kernels one step() launches: copy_blocks, slot_mapping + kv_append,
-        plan + attention (+ combine when a row can span partitions), and the
-        two acceptance kernels."""
-        n = (1 if self.cow.numel() else 0) + (2 if self.n_slots else 0) + 2
-        np_max = -(-self.max_seq_len // max(self.partition_tokens or attention_auto_partition(
-            self.w.num_seqs, self.w.total_q, self.w.n_kv, self.max_seq_len), 1))
-        n += 1 if np_max > 1 else 0
+        """Kernels one step() launches: copy_blocks, the fused slot mapping + append
+        (two kernels for e4m3 pools),
+        plan + attention + combine, and the two acceptance kernels."""
+        n = (1 if self.cow.numel() else 0) + ((1 if self.fp8 is None else 2) if self.n_slots else 0) + 2
+        n += 1  # the combine kernel, launched on every call
         return n + (2 if self.spec else 0)
 
     def pinned_inputs(self) -> torch.Tensor:
@@ -121,12 +120,13 @@ class DeviceStep:
             (copy_blocks if self.fp8 is None else copy_blocks_fp8)(self.k_cache, self.v_cache, self.cow,
                                                                   status=self.status, stream=stream)
         if self.n_slots:
-            slot_mapping(self.slots, self.block_tables, self.seq_lens, self.append_lens, w.block_size, w.num_blocks,
-                         status=self.status, stream=stream)
             if self.fp8 is None:
-                kv_append(self.k_cache, self.v_cache, self.k_new, self.v_new, self.slots, status=self.status,
-                          stream=stream)
+                # slot mapping fused with the append (one launch)
+                kv_append_paged(self.k_cache, self.v_cache, self.k_new, self.v_new, self.block_tables,
+                                self.seq_lens, self.append_lens, self.slots, status=self.status, stream=stream)
             else:
+                slot_mapping(self.slots, self.block_tables, self.seq_lens, self.append_lens, w.block_size,
+                             w.num_blocks, status=self.status, stream=stream)
                 kv_append_fp8(self.k_cache, self.v_cache, self.k_new, self.v_new, self.slots, self.k_scale,
                               self.v_scale, status=self.status, stream=stream)
 
