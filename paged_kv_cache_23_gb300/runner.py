@@ -165,12 +165,14 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--flags", type=int, default=0)
+    ap.add_argument("--fp8", action="store_true", help="e4m3 KV pools (random codes, per-head scales)")
     a = ap.parse_args(argv)
     if a.workload == "mix" and a.batch:
         w = workloads.mix(B=a.batch)
     else:
         w = workloads.FULL[a.workload]()
-    ds = DeviceStep(w, partition_tokens=a.partition or None, flags=a.flags)
+    ds = DeviceStep(w, partition_tokens=a.partition or None, flags=a.flags,
+                    fp8=workloads.fp8_pools(w) if a.fp8 else None)
     for _ in range(a.steps):
         ds.cache_ops()
         ds.attention()
