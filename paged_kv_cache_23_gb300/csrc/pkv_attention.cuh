@@ -886,8 +886,9 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
-                const uint32_t a0 = e4m3x2_to_f16x2(rA), a2 = e4m3x2_to_f16x2(rA >> 16);
-                const uint32_t a1 = e4m3x2_to_f16x2(rB), a3 = e4m3x2_to_f16x2(rB >> 16);
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(rA, a0, a2);
+                e4m3x4_to_f16x2x2(rB, a1, a3);
                 const int kc = 2 * kc2 + h;
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt)
@@ -967,6 +968,9 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
         khi[u] = nv == kTileT ? 0xffffffffu
                               : (8 + 2 * qd < nv ? 0x0000ffffu : 0u) | (9 + 2 * qd < nv ? 0xffff0000u : 0u);
     }
+    bool partial = false;
+#pragma unroll
+    for (int u = 0; u < NS; ++u) partial = partial || nvalid[u] < kTileT;
 #pragma unroll
     for (int kc2 = 0; kc2 < NC / 2; ++kc2) {
         const int chunk = 2 * kc2 + a_ch;
@@ -977,11 +981,17 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
-                // bytes (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0) and (t0 d1, t1 d1)
-                const uint32_t a0 = e4m3x2_to_f16x2(__byte_perm(rA, 0u, 0x4420)) & klo[u];
-                const uint32_t a1 = e4m3x2_to_f16x2(__byte_perm(rA, 0u, 0x4431)) & klo[u];
-                const uint32_t a2 = e4m3x2_to_f16x2(__byte_perm(rB, 0u, 0x4420)) & khi[u];
-                const uint32_t a3 = e4m3x2_to_f16x2(__byte_perm(rB, 0u, 0x4431)) & khi[u];
+                // bytes (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0 | t0 d1, t1 d1): one
+                // permute, then each half converts to the f16 pair of one dim
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(__byte_perm(rA, 0u, 0x3120), a0, a1);
+                e4m3x4_to_f16x2x2(__byte_perm(rB, 0u, 0x3120), a2, a3);
+                if (partial) {
+                    a0 &= klo[u];
+                    a1 &= klo[u];
+                    a2 &= khi[u];
+                    a3 &= khi[u];
+                }
                 const int mc = 2 * kc2 + h;
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt) mma_f16_16816(o[mc][nt], a0, a1, a2, a3, pb0[u][nt], pb1[u][nt]);

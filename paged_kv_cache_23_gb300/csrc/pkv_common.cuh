@@ -146,6 +146,15 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two) {
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// Four e4m3 codes in one register -> (codes 0, 1) and (codes 2, 3) as two
+// f16x2 (exact), the halves split without extra instructions.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\tcvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(four));
+}
+
 // Two fp32 -> two e4m3 codes (round to nearest even, saturate to +-448, NaN
 // kept), lo in the lower byte.
 __device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float lo, float hi) {
