@@ -746,13 +746,28 @@ __device__ __forceinline__ void mq_item(Smem<D, false>& sm, const AttnParams& p,
                 sf[nt][j] = v;
                 if (j < 2) mxA = fmaxf(mxA, v); else mxB = fmaxf(mxB, v);
             }
-        mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, 1));
-        mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, 2));
-        mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, 1));
-        mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, 2));
-        const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
-        const float uA = nA == -INFINITY ? 0.f : nA, uB = nB == -INFINITY ? 0.f : nB;
-        const float cA = exp2f(mA - uA), cB = exp2f(mB - uB);
+        // lazy reference maxima (as in decode_tc_item): rows move theirs only
+        // when a score exceeds it by more than kRescaleSlack
+        if (!__all_sync(kFull, mxA <= mA + kRescaleSlack && mxB <= mB + kRescaleSlack)) {
+            mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, 1));
+            mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, 2));
+            mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, 1));
+            mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, 2));
+            const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
+            const float cA = nA == -INFINITY ? 1.f : exp2f(mA - nA), cB = nB == -INFINITY ? 1.f : exp2f(mB - nB);
+            lA *= cA;
+            lB *= cB;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                o[nt][0] *= cA;
+                o[nt][1] *= cA;
+                o[nt][2] *= cB;
+                o[nt][3] *= cB;
+            }
+            mA = nA;
+            mB = nB;
+        }
+        const float uA = mA == -INFINITY ? 0.f : mA, uB = mB == -INFINITY ? 0.f : mB;
         float sA = 0.f, sB = 0.f;
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
@@ -763,42 +778,46 @@ __device__ __forceinline__ void mq_item(Smem<D, false>& sm, const AttnParams& p,
             sA += sf[nt][0] + sf[nt][1];
             sB += sf[nt][2] + sf[nt][3];
         }
-        sA += __shfl_xor_sync(kFull, sA, 1);
-        sA += __shfl_xor_sync(kFull, sA, 2);
-        sB += __shfl_xor_sync(kFull, sB, 1);
-        sB += __shfl_xor_sync(kFull, sB, 2);
-        lA = lA * cA + sA;
-        lB = lB * cB + sB;
-        mA = nA;
-        mB = nB;
-#pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) {
-            o[nt][0] *= cA;
-            o[nt][1] *= cA;
-            o[nt][2] *= cB;
-            o[nt][3] *= cB;
-        }
+        // l stays a per-lane partial sum (this lane's tokens); reduced once at the end
+        lA += sA;
+        lB += sB;
         const uint32_t pa0 = float2_to_bf16x2(sf[0][0], sf[0][1]);
         const uint32_t pa1 = float2_to_bf16x2(sf[0][2], sf[0][3]);
         const uint32_t pa2 = float2_to_bf16x2(sf[1][0], sf[1][1]);
         const uint32_t pa3 = float2_to_bf16x2(sf[1][2], sf[1][3]);
-        // V rows past the valid tokens may hold anything (even NaN): zero them
-        const uint32_t keep0 = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
-        const uint32_t keep1 =
-            (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (8 + 2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+        if (nvalid == kTileT) {
 #pragma unroll
-        for (int dp = 0; dp < D / 16; ++dp) {
-            const int chunk = 2 * dp + v_hi;
-            const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
-            mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0 & keep0, b1 & keep1);
-            mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & keep0, b3 & keep1);
+            for (int dp = 0; dp < D / 16; ++dp) {
+                const int chunk = 2 * dp + v_hi;
+                const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
+                mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+            }
+        } else {
+            // V rows past the valid tokens may hold anything (even NaN): zero them
+            const uint32_t keep0 = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+            const uint32_t keep1 =
+                (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (8 + 2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int dp = 0; dp < D / 16; ++dp) {
+                const int chunk = 2 * dp + v_hi;
+                const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
+                mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0 & keep0, b1 & keep1);
+                mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & keep0, b3 & keep1);
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
     }
     if (!active) return;
+    lA += __shfl_xor_sync(kFull, lA, 1);
+    lA += __shfl_xor_sync(kFull, lA, 2);
+    lB += __shfl_xor_sync(kFull, lB, 1);
+    lB += __shfl_xor_sync(kFull, lB, 2);
     const bool poisoned = sm.poison[si] != 0;  // final after the last stage's wait
     // finish from registers: rows rA, rB of kv head kvh
     const float qnan = __int_as_float(0x7fc00000);
