@@ -75,6 +75,7 @@ extern "C" {
 
 /* Attention flags. */
 #define PKV_ATTN_DECODE_CUDA_CORES 1 /* run q_len = 1 rows on the CUDA-core FMA path */
+#define PKV_ATTN_NO_TCGEN05 2        /* run every multi-query tile on mma.sync (no tcgen05 tiles) */
 
 /* Library version, 100 * major + minor. */
 int pkv_version(void);
@@ -192,9 +193,15 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *                 per SM (6 when multi-query rows make up most of the work;
  *                 fewer, longer partitions cost fewer partial results); the length used is the int at byte offset 8 of
  *                 the workspace after the call
- *   flags         0, or PKV_ATTN_DECODE_CUDA_CORES (q_len = 1 rows on the
- *                 CUDA-core FMA path; by default every row uses the tensor
- *                 cores, measured faster on GB300)
+ *   flags         0, or an OR of PKV_ATTN_DECODE_CUDA_CORES (q_len = 1 rows
+ *                 on the CUDA-core FMA path; by default every row uses the
+ *                 tensor cores, measured faster on GB300) and
+ *                 PKV_ATTN_NO_TCGEN05.  By default (head_dim 128, block_size
+ *                 >= 16, partition length a multiple of 128) a sequence with
+ *                 q_len * g >= 128 runs as tiles of 128 (query, q head) rows
+ *                 of one kv head on the tcgen05 tensor cores (accumulators in
+ *                 tensor memory, 128-token stages); PKV_ATTN_NO_TCGEN05 keeps
+ *                 it on the mma.sync multi-query path
  *   workspace     >= pkv_attention_workspace_bytes(...) bytes, 256-byte
  *                 aligned; scratch, contents need not be initialised
  * Rows of a sequence with a bad length, or that read a bad block id, are

@@ -35,6 +35,7 @@ PKV_STATUS_BAD_DIST = 256
 PKV_STATUS_TABLE_FULL = 512
 PKV_STATUS_NOT_FOUND = 1024
 PKV_ATTN_DECODE_CUDA_CORES = 1
+PKV_ATTN_NO_TCGEN05 = 2  # multi-query tiles on mma.sync instead of tcgen05
 PKV_ERR_SCRATCH_LIMIT = -8
 
 _P = ctypes.c_void_p

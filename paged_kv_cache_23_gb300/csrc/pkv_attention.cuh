@@ -57,8 +57,18 @@ constexpr int kMaxParts = 1024;             // partitions per sequence
 constexpr int kPlanThreads = 1024;
 constexpr int kTailBuckets = 256;           // tail-length classes of the longest-first ordering
 
-// KIND_DEC: q_len = 1 rows on tensor cores; KIND_DECF: on CUDA cores; KIND_MQ: q_len > 1.
-enum { KIND_END = -1, KIND_DEC = 0, KIND_MQ = 1, KIND_DECF = 2 };
+// tcgen05 chunk tiles: 128 rows = (query, q head) pairs of one kv head, stages
+// of 128 tokens, tensor-memory columns [S0 | S1 | O | P0 | P1].
+constexpr int kTcT = 128;                   // tokens per stage
+constexpr int kTcRows = 128;                // tile rows (the MMA's M)
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0, kTmemO = 256, kTmemP = 384;
+
+// KIND_DEC: q_len = 1 rows on tensor cores; KIND_DECF: on CUDA cores; KIND_MQ:
+// q_len > 1 on mma.sync; KIND_TC: query tiles of 128 rows on tcgen05.
+enum { KIND_END = -1, KIND_DEC = 0, KIND_MQ = 1, KIND_DECF = 2, KIND_TC = 3 };
+
+__host__ __device__ constexpr bool multi_query_kind(int kind) { return kind == KIND_MQ || kind == KIND_TC; }
 
 struct Desc {
     int b, part, nparts, hg;        // sequence, partition, partitions of the group, head group
@@ -71,6 +81,7 @@ struct Desc {
 struct TMaps {
     CUtensorMap k[4];
     CUtensorMap v[4];
+    CUtensorMap k_tc, v_tc;  // one 64-column slab of min(bs, 128) rows of one kv head
 };
 
 struct AttnParams {
@@ -86,6 +97,7 @@ struct AttnParams {
     const float* k_scale;  // e4m3 pools: dequantisation scale per kv head (null for bf16)
     const float* v_scale;
     int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, row_bytes;
+    int tc;              // tcgen05 tiles possible: tensor memory is allocated when the plan made some
     float scale_log2;    // scale * log2(e): scores live in base-2 units
 };
 
@@ -104,13 +116,26 @@ struct Geo {
 template <int D, bool F8 = false>
 struct Smem {
     using G = Geo<D, F8>;
+    static constexpr bool kTC = D == 128 && !F8;             // the pool shape with tcgen05 tiles
     uint8_t kv[G::kSlots][2][G::kHalf];                      // [slot][K,V][rows of 128 B], swizzled
-    float pbuf[kCWarps][kTileT * 8];                         // decode: p[token][head]
+    union {
+        float pbuf[kCWarps][kTileT * 8];                     // decode on CUDA cores: p[token][head]
+        uint8_t qbuf[kTC ? kTcRows * D * 2 : 16];            // tcgen05 tile: Q, K-major, 128-byte swizzle
+    };
     Desc desc[kSlots];
     int poison[kSlots];
     int abort;
     uint64_t full[G::kSlots], empty[G::kSlots], ifull[kSlots], iempty[kSlots];
+    // tcgen05 tiles: S ready, PV done (per buffer), P written, half-row
+    // exchange, tile entry, Q written, final drain, warps done with tensor memory
+    uint64_t sbar[2], obar[2], pready, xbar, ebar, qbar, tdone, dbar;
+    uint32_t tmem;
+    float red[kTC ? 2 : 1][2][kTcRows];                       // [exchange parity][half][row]
 };
+// the tcgen05 operands (ring slabs, Q) start on 1024-byte swizzle atoms
+using SmemTc = Smem<128, false>;
+static_assert(sizeof(SmemTc::kv) % 1024 == 0, "ring size");
+static_assert(offsetof(SmemTc, qbuf) == sizeof(SmemTc::kv), "Q follows the ring");
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -165,6 +190,75 @@ __device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, int P) {
 }
 
 // ---------------------------------------------------------------------------
+// Stages of a tcgen05 tile: 128 tokens of one kv head, K then V, each as two
+// 64-column slabs of 128 rows ([slab][token][128 B], 128-byte swizzle) -- the
+// K-major B operand of S = Q K^T and the MN-major B operand of O += P V.  One
+// TMA box per (tensor, slab, block): lane l copies tensor l & 1, slab
+// (l >> 1) & 1 of the stage's block l >> 2.  Blocks that start past the
+// item's last position are not fetched (the consumers zero those V rows).
+// Returns false when the pipeline was aborted.
+// ---------------------------------------------------------------------------
+template <int D, bool F8>
+__device__ __forceinline__ bool produce_tc(Smem<D, F8>& sm, const TMaps* tm, const AttnParams& p, const Desc& d,
+                                           int si, int lane, uint32_t& g, int& next) {
+    if constexpr (!Smem<D, F8>::kTC) {
+        return false;
+    } else {
+        constexpr int RS = Geo<D, F8>::kSlots;
+        volatile int* abort = &sm.abort;
+        const int rows = p.bs < kTcT ? p.bs : kTcT;  // rows per box
+        const int nblk = kTcT / rows;                // blocks per stage (<= 8)
+        const uint32_t box_bytes = (uint32_t)rows * 128;
+        const int tv = lane & 1, x = (lane >> 1) & 1, j = lane >> 2;
+        const int tb = d.t_begin / kTcT, te = (d.t_end + kTcT - 1) / kTcT;
+        const int32_t* bt = p.block_tables + (long long)d.b * p.max_blocks;
+        const int e_lim = (d.t_end + p.bs - 1) / p.bs;
+        int tab_base = tb * kTcT / p.bs;
+        int tab = tab_base + lane < e_lim ? __ldg(bt + tab_base + lane) : 0;
+        int tab_next = tab_base + 32 + lane < e_lim ? __ldg(bt + tab_base + 32 + lane) : 0;
+        const int i_claim = max(tb, te - kClaimAhead);
+        for (int i = tb; i < te; ++i, ++g) {
+            if (i == i_claim && lane == 0) next = atomicAdd(&p.hdr[1], 1);
+            const int t0 = i * kTcT;
+            const int e0 = t0 / p.bs;
+            if (e0 >= tab_base + 32) {
+                tab = tab_next;
+                tab_base += 32;
+                const int en = tab_base + 32 + lane;
+                tab_next = en < e_lim ? __ldg(bt + en) : 0;
+            }
+            const int off = e0 - tab_base + j;  // in [0, 40)
+            const int lo = __shfl_sync(kFull, tab, off & 31);
+            const int hi = __shfl_sync(kFull, tab_next, off & 31);
+            int my = off < 32 ? lo : hi;
+            const int nvb = min(nblk, (d.t_end - t0 + rows - 1) / rows);  // blocks holding positions < t_end
+            const bool in = j < nvb;
+            const bool okb = !in || (my >= 0 && my < p.num_blocks);
+            if (!okb) my = 0;
+            const unsigned badmask = __ballot_sync(kFull, !okb);
+            const int s = (int)(g % RS);
+            bool got = true;
+            if (lane == 0) {
+                if (badmask) {
+                    sm.poison[si] = 1;
+                    report(p.status, PKV_STATUS_BAD_BLOCK);
+                }
+                got = mbar_wait(&sm.empty[s], ((g / RS) & 1) ^ 1, abort);
+                if (got) mbar_arrive_expect_tx(&sm.full[s], 4u * nvb * box_bytes);
+            }
+            if (!__shfl_sync(kFull, got, 0)) return false;  // never arm a barrier whose previous phase is open
+            if (in) {
+                const int row0 = p.bs > kTcT ? (t0 % p.bs) : 0;
+                tma_load_5d(&sm.kv[s][tv][x * (kTcT * 128) + j * box_bytes], tv ? &tm->v_tc : &tm->k_tc, 0, x, row0,
+                            d.hg, my, &sm.full[s]);
+            }
+            __syncwarp();
+        }
+        return true;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Producer warp: item queue, block-table reads, TMA stage stream.
 // ---------------------------------------------------------------------------
 template <int D, bool F8>
@@ -204,6 +298,11 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
             mbar_arrive(&sm.ifull[si]);
         }
         if (end) break;
+        if (d.kind == KIND_TC) {
+            if (!produce_tc<D, F8>(sm, tm, p, d, si, lane, g, next)) break;
+            next = __shfl_sync(kFull, next, 0);
+            continue;
+        }
         const CUtensorMap* mk = &tm->k[log2i(d.hps)];
         const CUtensorMap* mv = &tm->v[log2i(d.hps)];
         const uint32_t op_bytes = (uint32_t)d.hps * bsr * Geo<D, F8>::kRow;
@@ -849,6 +948,263 @@ __device__ __forceinline__ void mq_item(Smem<D, false>& sm, const AttnParams& p,
 }
 
 // ---------------------------------------------------------------------------
+// Query tile on the 5th-generation tensor cores (tcgen05, accumulators in
+// tensor memory): the FlashAttention block loop of "Inference at Scale"
+// section 07 for 128 rows = (query, q head) pairs of one kv head.
+//   S_k  = Q K_k^T        (M 128, N 128 tokens, K = D): A = Q (shared memory,
+//                          K-major), B = the stage's K slabs (K-major)
+//   O   += P_k V_k         (M 128, N = D, K 128 tokens): A = P (tensor memory,
+//                          bf16), B = the stage's V slabs (MN-major)
+// Thread (warp w, lane l) owns row r = 32 (w % 4) + l -- the tensor-memory
+// lane its warp may access -- and the column half h = w / 4 of S and of O.
+// One elected thread (consumer warp 0, lane 0) issues the MMAs: S_{k+1} as
+// soon as its stage has landed (it overlaps the softmax of stage k), PV_k once
+// every warp has written P_k.  The PV commit releases the ring slot.  The two
+// halves of a row exchange their maxima (and at the end their sums) through
+// shared memory.  Every wait is a bounded mbarrier wait: a stalled warp can
+// make the tile time out, never hang it.
+// Reference maxima are lazy as in the other items (kRescaleSlack): a row
+// rescales its O half in tensor memory only when its maximum moves.
+// ---------------------------------------------------------------------------
+struct TcState {
+    uint32_t tmem;   // tensor-memory base
+    uint32_t k;      // tcgen05 stages processed by this CTA (S, P, O buffer parity)
+    uint32_t x;      // half-row exchanges done
+    uint32_t tiles;  // tcgen05 tiles processed (entry / Q barrier parity)
+};
+
+// Wait bounded by time only (teardown: must not be cut short by an abort).
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u && global_ns() - t0 > kWaitNs) return false;
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void tc_item(Smem<D, false>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
+                                        uint32_t gbase, int ntiles, int si, TcState& st, volatile int* abort) {
+    static_assert(D == 128, "tcgen05 tiles are built for head_dim 128");
+    constexpr uint32_t kIdS = umma_idesc_bf16(kTcRows, kTcT, false);
+    constexpr uint32_t kIdPV = umma_idesc_bf16(kTcRows, D, true);
+    constexpr int kSlab = kTcT * 128;  // bytes of one 64-column slab of a stage
+    const int G = p.G;
+    const int quarter = warp & 3, hh = warp >> 2;
+    const int r = quarter * 32 + lane;
+    const int qi = r / G, hq = r - qi * G;
+    const uint32_t tl = st.tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lanes
+    const bool issuer = warp == 0 && lane == 0;
+    const uint32_t tpar = st.tiles & 1;
+    // every consumer warp has left its previous item (qbuf aliases pbuf)
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.ebar);
+    mbar_wait(&sm.ebar, tpar, abort);
+    // Q tile -> qbuf: 16-byte chunk j of row rr (slab x) at rr * 128 + ((j ^ (rr & 7)) << 4)
+    for (int c = warp * 32 + lane; c < kTcRows * 16; c += kCThreads) {
+        const int rr = c >> 4, c16 = c & 15, xs = c16 >> 3, jj = c16 & 7;
+        const int qq = rr / G, h2 = rr - qq * G;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (qq < d.nq) v = ld_nc_v4(p.q + ((long long)(d.q_row0 + qq) * p.n_q + (long long)d.hg * G + h2) * D + c16 * 8);
+        *reinterpret_cast<uint4*>(sm.qbuf + xs * kSlab + rr * 128 + ((jj ^ (rr & 7)) << 4)) = v;
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.qbar);
+
+    const int tb = d.t_begin / kTcT;
+    const uint32_t qa = smem_u32(sm.qbuf);
+    // S_i = Q K_i^T into S buffer (k + i) & 1
+    auto issue_s = [&](int i) {
+        const uint32_t gi = gbase + i;
+        const int s = (int)(gi % kRingSlots);
+        if (!mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort)) return;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
+        const uint32_t dst = st.tmem + kTmemS + ((st.k + i) & 1) * kTcT;
+#pragma unroll
+        for (int xs = 0; xs < 2; ++xs)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma_ss(dst, umma_desc_sw128(qa + xs * kSlab + kk * 32, 0), umma_desc_sw128(kb + xs * kSlab + kk * 32, 0),
+                        kIdS, (xs | kk) != 0);
+        umma_commit(&sm.sbar[(st.k + i) & 1]);
+    };
+    if (issuer) {
+        if (mbar_wait(&sm.qbar, tpar, abort)) issue_s(0);
+    }
+    __syncwarp();
+
+    // last visible position of this row (rows past the tile's queries take the last query's)
+    const int lim = d.t_vis - d.nq + min(qi, d.nq - 1);
+    const int last = min(lim, d.t_end - 1);
+    float m_ref = -INFINITY, l = 0.f;
+    bool poisoned = false;
+    for (int i = 0; i < ntiles; ++i) {
+        const uint32_t k = st.k + i;
+        const int b = (int)(k & 1);
+        const uint32_t gi = gbase + i;
+        const int s = (int)(gi % kRingSlots);
+        if (issuer && i + 1 < ntiles) issue_s(i + 1);
+        __syncwarp();
+        // scores of this row half: columns t0 + j, visible iff j <= nv
+        mbar_wait(&sm.sbar[b], (k >> 1) & 1, abort);
+        __syncwarp();  // tcgen05.ld/st are warp-collective: reconverge after the polling wait
+        tc_fence_after();
+        // one 64-register array: raw scores, then scaled scores (as bits), then packed P
+        uint32_t sv[64];
+        tmem_ld32(tl + kTmemS + b * kTcT + hh * 64, sv);
+        tmem_ld32(tl + kTmemS + b * kTcT + hh * 64 + 32, sv + 32);
+        tmem_wait_ld();
+        float mx = -INFINITY;
+        {
+            const int nv = last - ((tb + i) * kTcT + hh * 64);
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                const float v = j <= nv ? __uint_as_float(sv[j]) * p.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, v);
+                sv[j] = __float_as_uint(v);
+            }
+        }
+        // exchange the half maxima of each row (the S reads above are done first:
+        // the issuer refills this S buffer after the exchange)
+        sm.red[st.x & 1][hh][r] = mx;
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.xbar);
+        mbar_wait(&sm.xbar, st.x & 1, abort);
+        const float row_mx = fmaxf(mx, sm.red[st.x & 1][hh ^ 1][r]);
+        ++st.x;
+        // O and l are relative to m_ref.  A row whose maximum moved rescales its
+        // half of O once PV_{k-1} is done; the tensor-memory accesses are
+        // warp-collective, so the whole warp takes the path (factor 1, exact,
+        // for the rows that keep their reference)
+        const bool move = row_mx > m_ref + kRescaleSlack;
+        const float c = move && m_ref != -INFINITY ? exp2f(m_ref - row_mx) : 1.f;
+        if (__any_sync(kFull, c != 1.f)) {
+            const uint32_t kp = k - 1;  // i >= 1 here: a finite m_ref was set by an earlier stage
+            mbar_wait(&sm.obar[kp & 1], (kp >> 1) & 1, abort);
+            __syncwarp();
+            tc_fence_after();
+#pragma unroll 1
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t ov[32];
+                tmem_ld32(tl + kTmemO + hh * 64 + cc * 32, ov);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * c);
+                tmem_st32(tl + kTmemO + hh * 64 + cc * 32, ov);
+            }
+            tmem_wait_st();
+        }
+        if (move) {
+            l *= c;
+            m_ref = row_mx;  // (while m_ref was -inf every p was 0, so O and l are 0)
+        }
+        const float u = m_ref == -INFINITY ? 0.f : m_ref;
+        float ls = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {  // pair j overwrites sv[j], already consumed
+            const float p0 = exp2f(__uint_as_float(sv[2 * j]) - u), p1 = exp2f(__uint_as_float(sv[2 * j + 1]) - u);
+            ls += p0 + p1;
+            sv[j] = float2_to_bf16x2(p0, p1);
+        }
+        l += ls;
+        // P buffer b was last read by PV_{k-2}
+        if (k >= 2) {
+            mbar_wait(&sm.obar[b], ((k - 2) >> 1) & 1, abort);
+            __syncwarp();
+            tc_fence_after();
+        }
+        tmem_st32(tl + kTmemP + b * 64 + hh * 32, sv);
+        tmem_wait_st();
+        if (i == ntiles - 1) {
+            // the stage has landed (its slot is released only by PV_k): the
+            // item's block checks are final, and V rows past the item's last
+            // position -- unfetched, or stale, possibly NaN -- are zeroed
+            mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort);
+            poisoned = sm.poison[si] != 0;
+            const int nvalid = d.t_end - (tb + i) * kTcT;
+            if (nvalid < kTcT) {
+                uint8_t* vz = &sm.kv[s][1][0];
+                for (int c = warp * 32 + lane; c < (kTcT - nvalid) * 16; c += kCThreads) {
+                    const int row = nvalid + (c >> 4), xs = (c >> 3) & 1, ch = c & 7;
+                    *reinterpret_cast<uint4*>(vz + xs * kSlab + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.pready);
+        if (issuer) {
+            if (mbar_wait(&sm.pready, k & 1, abort)) {
+                tc_fence_after();
+                const uint32_t vb = smem_u32(&sm.kv[s][1][0]);
+#pragma unroll
+                for (int kk = 0; kk < kTcT / 16; ++kk)
+                    umma_ts(st.tmem + kTmemO, st.tmem + kTmemP + b * 64 + kk * 8,
+                            umma_desc_sw128(vb + kk * 2048, kSlab), kIdPV, i > 0 || kk > 0);
+                umma_commit(&sm.obar[b]);
+                mbar_arrive(&sm.empty[s], kCWarps - 1);
+                umma_commit(&sm.empty[s]);  // the slot's last arrival: when PV_k has read V
+            }
+        }
+        __syncwarp();
+    }
+    st.k += ntiles;
+    ++st.tiles;
+    // row sum = the two halves' partial sums
+    sm.red[st.x & 1][hh][r] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.xbar);
+    mbar_wait(&sm.xbar, st.x & 1, abort);
+    const float lrow = l + sm.red[st.x & 1][hh ^ 1][r];
+    ++st.x;
+    const uint32_t kl = st.k - 1;
+    mbar_wait(&sm.obar[kl & 1], (kl >> 1) & 1, abort);
+    __syncwarp();
+    tc_fence_after();
+    const bool row_ok = qi < d.nq;
+    const long long orow = (long long)(d.q_row0 + min(qi, d.nq - 1)) * p.n_q + (long long)d.hg * G + hq;
+    const float inv = 1.0f / lrow;
+    const float qnan = __int_as_float(0x7fc00000);
+    // O half-row in two 32-column pieces (fewer live registers)
+#pragma unroll 1
+    for (int cc = 0; cc < 2; ++cc) {
+        uint32_t ov[32];
+        tmem_ld32(tl + kTmemO + hh * 64 + cc * 32, ov);
+        tmem_wait_ld();
+        if (!row_ok) continue;
+        const int col0 = hh * 64 + cc * 32;
+        if (d.nparts == 1) {
+            uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + col0);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint4 w;
+                w.x = float2_to_bf16x2(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
+                w.y = float2_to_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
+                w.z = float2_to_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
+                w.w = float2_to_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
+                if (poisoned) w = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
+                dst[c] = w;
+            }
+        } else {
+            float4* dst = reinterpret_cast<float4*>(p.part_o + (orow * p.np_max + d.part) * D + col0);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 v = poisoned ? make_float4(qnan, qnan, qnan, qnan)
+                                          : make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
+                                                        __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
+                __stcg(dst + c, v);
+            }
+        }
+    }
+    tc_fence_before();  // the next tile's first PV overwrites O after these reads
+    if (row_ok && d.nparts > 1 && hh == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(m_ref, lrow));
+}
+
+// ---------------------------------------------------------------------------
 // Item over an e4m3 pool ("Inference at Scale" section 03, KV cache
 // quantization), any query tile of nq <= 8 * NTN / g queries: warp w < hps owns
 // kv head hg * hps + w, in the transposed form of decode_tc_item with the
@@ -1234,7 +1590,7 @@ int launch_combine(const CombineParams& c, cudaStream_t st) {
 // Consumer warps
 // ---------------------------------------------------------------------------
 template <int D, int GD, bool F8>
-__device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, int warp, int lane) {
+__device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, int warp, int lane, TcState& tc) {
     volatile int* abort = &sm.abort;
     uint32_t g = 0;
     for (int islot = 0;; ++islot) {
@@ -1242,8 +1598,11 @@ __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, i
         if (!mbar_wait(&sm.ifull[si], (islot / kSlots) & 1, abort)) break;  // timed out: abort is set
         const Desc d = sm.desc[si];
         if (d.kind == KIND_END) break;
-        const int ntiles = (d.t_end + kTileT - 1) / kTileT - d.t_begin / kTileT;
-        if constexpr (F8) {
+        const int T = d.kind == KIND_TC ? kTcT : kTileT;  // tokens per stage
+        const int ntiles = (d.t_end + T - 1) / T - d.t_begin / T;
+        if (d.kind == KIND_TC) {
+            if constexpr (Smem<D, F8>::kTC) tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, tc, abort);
+        } else if constexpr (F8) {
             if (d.nq * p.G > 8) swap8_item<D, 2>(sm, p, d, warp, lane, g, ntiles, si, abort);
             else swap8_item<D, 1>(sm, p, d, warp, lane, g, ntiles, si, abort);
         } else {
@@ -1261,13 +1620,25 @@ __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, i
     }
 }
 
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+    uint32_t n;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+    return n;
+}
+
 template <int D, int GD, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_attention_kernel(const __grid_constant__ TMaps tm, const __grid_constant__ AttnParams p) {
-    extern __shared__ uint8_t smem_raw[];
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     using SM = Smem<D, F8>;
     constexpr int RS = Geo<D, F8>::kSlots;
-    SM& sm = *reinterpret_cast<SM*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023);
+    if (base - reinterpret_cast<uintptr_t>(smem_raw) + sizeof(SM) > dynamic_smem_bytes()) {
+        // the shared window is not 1024-byte aligned and the launch left no slack
+        if (threadIdx.x == 0) report(p.status, PKV_STATUS_TIMEOUT);
+        return;
+    }
+    SM& sm = *reinterpret_cast<SM*>(base);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < RS; ++s) {
@@ -1278,6 +1649,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.ifull[i], 1);
             mbar_init(&sm.iempty[i], kCWarps);
         }
+        if constexpr (SM::kTC) {
+            mbar_init(&sm.sbar[0], 1);
+            mbar_init(&sm.sbar[1], 1);
+            mbar_init(&sm.obar[0], 1);
+            mbar_init(&sm.obar[1], 1);
+            mbar_init(&sm.pready, kCWarps);
+            mbar_init(&sm.xbar, kCWarps);
+            mbar_init(&sm.ebar, kCWarps);
+            mbar_init(&sm.qbar, kCWarps);
+            mbar_init(&sm.tdone, 1);
+            mbar_init(&sm.dbar, kCWarps);
+        }
         sm.abort = 0;
         fence_mbar_init();
     }
@@ -1287,7 +1670,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kCWarps) {
         producer<D, F8>(sm, &tm, p, lane);
     } else {
-        consumer<D, GD, F8>(sm, p, warp, lane);
+        TcState tc{0u, 0u, 0u, 0u};
+        bool use_tc = false;
+        if constexpr (SM::kTC) {
+            // tensor memory only when the plan made tcgen05 tiles (one CTA per
+            // SM, so the allocation never waits)
+            use_tc = p.tc != 0 && p.hdr[3] != 0;
+            if (use_tc) {
+                if (warp == 0) tmem_alloc(&sm.tmem, kTmemCols);
+                tc_fence_before();
+                named_bar(1, kCThreads);
+                tc_fence_after();
+                tc.tmem = sm.tmem;
+            }
+        }
+        consumer<D, GD, F8>(sm, p, warp, lane, tc);
+        if constexpr (SM::kTC) {
+            if (use_tc) {
+                // every MMA has completed and every warp is done with tensor memory
+                // (bounded by time alone: an abort must not skip the release)
+                if (warp == 0 && lane == 0) {
+                    umma_commit(&sm.tdone);
+                    if (!mbar_wait_ns(&sm.tdone, 0)) sm.abort = 1;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.dbar);
+                if (warp == 0) {
+                    if (!mbar_wait_ns(&sm.dbar, 0)) sm.abort = 1;
+                    __syncwarp();
+                    tc_fence_after();
+                    tmem_dealloc(tc.tmem, kTmemCols);
+                }
+            }
+        }
     }
     if (threadIdx.x == 0 && sm.abort) report(p.status, PKV_STATUS_TIMEOUT);
 }
@@ -1297,7 +1713,11 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    const size_t smem = sizeof(Smem<D, F8>) + 1024;
+    // 1 KB of slack aligns the ring to 1024 bytes where the budget allows; the
+    // shared window itself is 1024-byte aligned, which the kernel checks
+    constexpr size_t kMaxSmem = 227 * 1024;
+    const size_t smem = sizeof(Smem<D, F8>) + 1024 <= kMaxSmem ? sizeof(Smem<D, F8>) + 1024 : sizeof(Smem<D, F8>);
+    static_assert(sizeof(Smem<D, F8>) <= kMaxSmem, "shared-memory budget");
     if (dev < 0 || dev >= 64) return PKV_ERR_CUDA;
     if (!configured[dev]) {
         if (cudaFuncSetAttribute(paged_attention_kernel<D, GD, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -1,5 +1,7 @@
 // pkv_attention_host.cu -- planning kernel, workspace layout and the C entry
 // points of the paged attention (kernels in pkv_attention.cuh).
+#include <string.h>
+
 #include "pkv_attention.cuh"
 
 namespace pkv {
@@ -19,6 +21,7 @@ struct PlanParams {
     int32_t* status;
     int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, decode_ok;
     int fp8;         // e4m3 pool: every row on the transposed tensor-core item
+    int tc;          // tcgen05 tiles allowed (head_dim 128, bf16, block_size >= 16, P % 128 == 0)
     int adapt_P;     // 1: P is a floor; the planning kernel may double it
     int sms;         // SM count (persistent CTAs of the attention kernel)
 };
@@ -37,8 +40,17 @@ struct SeqShape {
 
 // decode_fma: run q_len = 1 rows on the CUDA-core path (else tensor cores).
 // fp8: e4m3 pool -- tiles of up to 16 (query, q head) columns per kv head.
-__device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_fma, int fp8 = 0) {
+// tc: a sequence with at least 128 (query, q head) rows per kv head runs as
+// tcgen05 tiles of 128 rows (128 / G queries), one kv head each.
+__device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_fma, int fp8, int tc) {
     SeqShape s;
+    if (tc && ql * G >= kTcRows && kTcRows % G == 0) {
+        s.kind = KIND_TC;
+        s.hps = 1;
+        s.wph = kCWarps;
+        s.qt = kTcRows / G;
+        return s;
+    }
     if (fp8) {
         s.kind = KIND_DEC;
         s.hps = gcd_pow2(n_kv, kMaxHPS);
@@ -127,8 +139,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         for (int b = tid; b < n; b += kPlanThreads) {
             const int L = pp.seq_lens[b], ql = pp.q_lens[b];
             if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len) continue;
-            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8);
-            const bool multi = sh.kind == KIND_MQ || ql > 1;
+            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
+            const bool multi = multi_query_kind(sh.kind) || ql > 1;
             const long long t = (long long)L * (pp.n_kv / sh.hps) * (multi ? ceil_div(ql, sh.qt) : 1);
             tok += t;
             if (multi) tok_mq += t;
@@ -146,7 +158,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     }
     if (tid == 0) pp.hdr[2] = P;
     __syncthreads();
-    int bits = 0;
+    int bits = 0, any_tc = 0;
     // pass A
     long long carry = 0;
     int c_mq = 0, c_full = 0;
@@ -170,10 +182,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             if (q0l + qlc > pp.total_q) flag |= PKV_STATUS_BAD_QLEN;  // rows would overflow q/out
             q0 = (int)(q0l < pp.total_q ? q0l : pp.total_q);
             bits |= flag;
-            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8);
+            const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
             const int ngroups = pp.n_kv / sh.hps;
             if (flag == 0) {
-                if (sh.kind != KIND_MQ && ql == 1) {
+                if (sh.kind == KIND_TC) any_tc = 1;
+                if (!multi_query_kind(sh.kind) && ql == 1) {
                     const int np = ceil_div(L, P);
                     nfull = (np - 1) * ngroups;
                     const int tl = L - (np - 1) * P;  // in [1, P]
@@ -198,7 +211,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         c_full += tf;
     }
     // tail buckets -> first slot of each bucket (exclusive scan)
-    __syncthreads();
+    any_tc = __syncthreads_or(any_tc);
     int c_tail;
     {
         const int v = tid < kTailBuckets ? hist[tid] : 0;
@@ -208,6 +221,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     if (tid == 0) {
         pp.hdr[0] = c_mq + c_full + c_tail;
         pp.hdr[1] = 0;
+        pp.hdr[3] = any_tc;  // the attention kernel allocates tensor memory only then
     }
     __syncthreads();
     // pass B1: one thread per sequence -- decode tails and invalid sequences
@@ -215,7 +229,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         const int4 sq = pp.seqs[b];
         const int L = sq.x, ql = sq.y;
         if (pp.seq_flag[b]) continue;  // its rows are written NaN after the wait below
-        if (ql != 1 || (sq.w & 15) == KIND_MQ) continue;  // multi-query tiles are counted in pass B2
+        if (ql != 1 || multi_query_kind(sq.w & 15)) continue;  // multi-query tiles are counted in pass B2
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
         const int np = ceil_div(L, P);
         const int tl = L - (np - 1) * P;
@@ -356,7 +370,7 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     if (G > 64) return PKV_ERR_UNSUPPORTED;
     if ((block_size & (block_size - 1)) || block_size > 256) return PKV_ERR_UNSUPPORTED;
     if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31)) return PKV_ERR_SIZE;
-    if (flags & ~PKV_ATTN_DECODE_CUDA_CORES) return PKV_ERR_SIZE;
+    if (flags & ~(PKV_ATTN_DECODE_CUDA_CORES | PKV_ATTN_NO_TCGEN05)) return PKV_ERR_SIZE;
     if (fp8 && (head_dim != 128 || G > 16)) return PKV_ERR_UNSUPPORTED;
     if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
     if (num_seqs == 0 || total_q == 0) return PKV_OK;
@@ -395,6 +409,24 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
         }
     }
 
+    // tcgen05 tiles: bf16 head_dim 128, boxes of >= 16 rows, partitions made of
+    // whole 128-token stages, and a batch with at least one 128-row tile
+    const bool tc = !fp8 && head_dim == 128 && block_size >= 16 && P % kTcT == 0 &&
+                    !(flags & PKV_ATTN_NO_TCGEN05) && (long long)total_q * G >= kTcRows;
+    if (tc) {
+        // [num_blocks][n_kv][bs][2 slabs][64] with one slab of min(bs, 128) rows per box
+        const uint64_t row = 256;
+        const uint64_t dims[5] = {64, 2, (uint64_t)block_size, (uint64_t)num_kv_heads, (uint64_t)num_blocks};
+        const uint64_t strides[4] = {128, row, (uint64_t)block_size * row, (uint64_t)num_kv_heads * block_size * row};
+        const uint32_t box[5] = {64, 1, (uint32_t)(block_size < kTcT ? block_size : kTcT), 1, 1};
+        if (host::encode_tiled(&tm.k_tc, k_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+            host::encode_tiled(&tm.v_tc, v_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+            return PKV_ERR_CUDA;
+    } else {
+        memset(&tm.k_tc, 0, sizeof(tm.k_tc));
+        memset(&tm.v_tc, 0, sizeof(tm.v_tc));
+    }
+
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* aux = reinterpret_cast<int*>(ws + w.seqaux);
     const int GD = (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
@@ -426,6 +458,7 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     pp.decode_ok = decode_fma ? 1 : 0;
     pp.adapt_P = partition_tokens == 0 ? 1 : 0;
     pp.fp8 = fp8 ? 1 : 0;
+    pp.tc = tc ? 1 : 0;
     pp.sms = host::sm_count();
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (host::launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess) return PKV_ERR_CUDA;
@@ -451,6 +484,7 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     ap.scale_log2 = scale * 1.4426950408889634f;
     ap.k_scale = k_scale;
     ap.v_scale = v_scale;
+    ap.tc = tc ? 1 : 0;
     const int rc2 = fp8                ? dispatch_attention_fp8_d128(tm, ap, w.max_items, st)
                     : head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st)
                                       : dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
