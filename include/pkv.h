@@ -64,7 +64,7 @@ extern "C" {
 
 #define PKV_STATUS_BAD_BLOCK 1   /* a needed block id is outside [0, num_blocks) */
 #define PKV_STATUS_BAD_SEQLEN 2  /* a seq_len is < 0, > max_blocks*block_size or > max_seq_len */
-#define PKV_STATUS_BAD_QLEN 4    /* a q_len/append_len is < 0 or > seq_len, or rows overflow */
+#define PKV_STATUS_BAD_QLEN 4    /* a q_len/append_len is < 0, > seq_len or > max_q_len, or rows overflow */
 #define PKV_STATUS_BAD_SLOT 8    /* a slot is >= num_blocks*block_size */
 #define PKV_STATUS_TIMEOUT 32    /* a bounded device wait ran out (library bug) */
 #define PKV_STATUS_BAD_PAIR 64   /* a copy pair names a block outside the pool */
@@ -183,6 +183,8 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *                 already be in the cache (pkv_kv_append)
  *   q_lens        int32 [num_seqs]: 1 = decode, k > 1 = speculative verify
  *                 or a prefill chunk, 0 = no rows
+ *   max_q_len     host bound on every q_len (a larger q_len is BAD_QLEN);
+ *                 the tcgen05 tile code runs only when max_q_len * g >= 128
  *   max_seq_len   host bound on every seq_len (sizes the workspace)
  *   head_dim      64 or 128; block_size a power of two in [1, 256];
  *                 g = num_q_heads / num_kv_heads an integer in [1, 64]
@@ -197,8 +199,9 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *                 on the CUDA-core FMA path; by default every row uses the
  *                 tensor cores, measured faster on GB300) and
  *                 PKV_ATTN_NO_TCGEN05.  By default (head_dim 128, block_size
- *                 >= 16, partition length a multiple of 128) a sequence with
- *                 q_len * g >= 128 runs as tiles of 128 (query, q head) rows
+ *                 >= 16, partition length a multiple of 128, decode rows on
+ *                 tensor cores) a sequence with q_len * g >= 128 runs as
+ *                 tiles of 128 (query, q head) rows
  *                 of one kv head on the tcgen05 tensor cores (accumulators in
  *                 tensor memory, 128-token stages); PKV_ATTN_NO_TCGEN05 keeps
  *                 it on the mma.sync multi-query path
@@ -210,10 +213,10 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  */
 int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                                const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
-                               const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
-                               int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                               int num_blocks, float scale, int partition_tokens, int flags,
-                               void* workspace, size_t workspace_bytes, int32_t* status,
+                               const int32_t* q_lens, int num_seqs, int total_q, int max_q_len,
+                               int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, float scale, int partition_tokens,
+                               int flags, void* workspace, size_t workspace_bytes, int32_t* status,
                                void* stream);
 
 /*
@@ -241,7 +244,7 @@ int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_c
                                        const void* v_cache, const int32_t* block_tables,
                                        int max_blocks, const int32_t* seq_lens,
                                        const int32_t* q_lens, int num_seqs, int total_q,
-                                       int max_seq_len, int num_q_heads, int num_kv_heads,
+                                       int max_q_len, int max_seq_len, int num_q_heads, int num_kv_heads,
                                        int head_dim, int block_size, int num_blocks, float scale,
                                        int partition_tokens, int flags, int32_t* status,
                                        void* stream);
@@ -300,8 +303,8 @@ int pkv_copy_blocks_fp8(void* k_cache, void* v_cache, const int32_t* src_dst, in
 int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
                                    int max_blocks, const int32_t* seq_lens, const int32_t* q_lens,
-                                   int num_seqs, int total_q, int max_seq_len, int num_q_heads,
-                                   int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                   int num_seqs, int total_q, int max_q_len, int max_seq_len,
+                                   int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
                                    float scale, int partition_tokens, void* workspace,
                                    size_t workspace_bytes, int32_t* status, void* stream);
 

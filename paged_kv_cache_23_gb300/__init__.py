@@ -50,7 +50,7 @@ _SIGS = {
     "pkv_gather_kv": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_attention_auto_partition": ([_I, _I, _I, _I], _I),
     "pkv_attention_workspace_bytes": ([_I, _I, _I, _I, _I, _I, _I], ctypes.c_size_t),
-    "pkv_paged_attention_decode": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+    "pkv_paged_attention_decode": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                     ctypes.c_float, _I, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_spec_accept_greedy": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
     "pkv_spec_accept_sample": ([_P, _P, _P, _P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
@@ -64,9 +64,9 @@ _SIGS = {
     "pkv_kv_append_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_copy_blocks_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_paged_attention_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
-                                        ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P], _I),
+                                        _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_noalloc_scratch_bytes": ([], ctypes.c_size_t),
-    "pkv_paged_attention_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+    "pkv_paged_attention_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                             ctypes.c_float, _I, _I, _P, _P], _I),
 }
 
@@ -200,9 +200,14 @@ def attention_workspace_bytes(num_seqs, total_q, num_q_heads, num_kv_heads, head
                                                    max_seq_len, partition_tokens))
 
 
+def _max_q(max_q_len, total_q) -> int:
+    return int(total_q if max_q_len is None else max_q_len)
+
+
 def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, q_lens, max_seq_len, scale,
-                           workspace, partition_tokens=0, flags=0, status=None, stream=None):
-    """a4-a8: paged attention (decode, speculative verify, prefill chunks) into out [total_q][n_q][d]."""
+                           workspace, partition_tokens=0, flags=0, status=None, stream=None, max_q_len=None):
+    """a4-a8: paged attention (decode, speculative verify, prefill chunks) into out [total_q][n_q][d].
+    max_q_len: host bound on every q_len (default total_q, always valid)."""
     for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
         _dev(t, n, torch.bfloat16)
     _dev(block_tables, "block_tables", torch.int32)
@@ -213,8 +218,8 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, q_l
     total_q, nq, _ = q.shape
     rc = lib().pkv_paged_attention_decode(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
                                           block_tables.shape[1], _ptr(seq_lens), _ptr(q_lens), seq_lens.numel(),
-                                          total_q, int(max_seq_len), nq, nkv, d, bs, nb, float(scale),
-                                          int(partition_tokens), int(flags), _ptr(workspace),
+                                          total_q, _max_q(max_q_len, total_q), int(max_seq_len), nq, nkv, d, bs,
+                                          nb, float(scale), int(partition_tokens), int(flags), _ptr(workspace),
                                           workspace.numel() * workspace.element_size(), _ptr(status),
                                           _stream(stream))
     _check(rc, "pkv_paged_attention_decode")
@@ -320,7 +325,8 @@ def copy_blocks_fp8(k_cache, v_cache, src_dst, status=None, stream=None):
 
 
 def paged_attention_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, q_lens,
-                               max_seq_len, scale, workspace, partition_tokens=0, status=None, stream=None):
+                               max_seq_len, scale, workspace, partition_tokens=0, status=None, stream=None,
+                               max_q_len=None):
     """Paged attention over e4m3 pools (uint8 [nb][n_kv][bs][d]) with per-kv-head scales."""
     _dev(out, "out", torch.bfloat16)
     _dev(q, "q", torch.bfloat16)
@@ -337,7 +343,8 @@ def paged_attention_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block
     rc = lib().pkv_paged_attention_decode_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                               _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
                                               _ptr(seq_lens), _ptr(q_lens), seq_lens.numel(), total_q,
-                                              int(max_seq_len), nq, nkv, d, bs, nb, float(scale),
+                                              _max_q(max_q_len, total_q), int(max_seq_len), nq, nkv, d, bs, nb,
+                                              float(scale),
                                               int(partition_tokens), _ptr(workspace),
                                               workspace.numel() * workspace.element_size(), _ptr(status),
                                               _stream(stream))
@@ -363,7 +370,7 @@ def spec_accept_sample(p, q, draft, r, s, accepted, next_token, status=None, str
 
 
 def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, q_lens, max_seq_len, scale,
-                                   partition_tokens=0, flags=0, status=None, stream=None):
+                                   partition_tokens=0, flags=0, status=None, stream=None, max_q_len=None):
     """paged_attention_decode without a workspace: for callers that cannot
     allocate device memory; the scratch is the library's fixed device array
     (noalloc_scratch_bytes()).  Calls overlapping on the GPU race on it."""
@@ -376,7 +383,8 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_l
     total_q, nq, _ = q.shape
     rc = lib().pkv_paged_attention_decode_noalloc(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
                                                   _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens),
-                                                  _ptr(q_lens), seq_lens.numel(), total_q, int(max_seq_len), nq, nkv,
+                                                  _ptr(q_lens), seq_lens.numel(), total_q,
+                                                  _max_q(max_q_len, total_q), int(max_seq_len), nq, nkv,
                                                   d, bs, nb, float(scale), int(partition_tokens), int(flags),
                                                   _ptr(status), _stream(stream))
     _check(rc, "pkv_paged_attention_decode_noalloc")

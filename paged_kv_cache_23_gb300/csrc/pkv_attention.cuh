@@ -1589,7 +1589,7 @@ int launch_combine(const CombineParams& c, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // Consumer warps
 // ---------------------------------------------------------------------------
-template <int D, int GD, bool F8>
+template <int D, int GD, bool F8, bool TC>
 __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, int warp, int lane, TcState& tc) {
     volatile int* abort = &sm.abort;
     uint32_t g = 0;
@@ -1601,7 +1601,7 @@ __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, i
         const int T = d.kind == KIND_TC ? kTcT : kTileT;  // tokens per stage
         const int ntiles = (d.t_end + T - 1) / T - d.t_begin / T;
         if (d.kind == KIND_TC) {
-            if constexpr (Smem<D, F8>::kTC) tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, tc, abort);
+            if constexpr (TC) tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, tc, abort);
         } else if constexpr (F8) {
             if (d.nq * p.G > 8) swap8_item<D, 2>(sm, p, d, warp, lane, g, ntiles, si, abort);
             else swap8_item<D, 1>(sm, p, d, warp, lane, g, ntiles, si, abort);
@@ -1626,9 +1626,13 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
     return n;
 }
 
-template <int D, int GD, bool F8>
+// TC: the variant with tcgen05 tiles (head_dim 128, bf16), launched only for
+// batches that may hold a 128-row tile -- the other variant's item code keeps
+// its register allocation free of the tile's.
+template <int D, int GD, bool F8, bool TC>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_attention_kernel(const __grid_constant__ TMaps tm, const __grid_constant__ AttnParams p) {
+    static_assert(!TC || Smem<D, F8>::kTC, "tcgen05 tiles need the head_dim 128 bf16 layout");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     using SM = Smem<D, F8>;
     constexpr int RS = Geo<D, F8>::kSlots;
@@ -1649,7 +1653,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.ifull[i], 1);
             mbar_init(&sm.iempty[i], kCWarps);
         }
-        if constexpr (SM::kTC) {
+        if constexpr (TC) {
             mbar_init(&sm.sbar[0], 1);
             mbar_init(&sm.sbar[1], 1);
             mbar_init(&sm.obar[0], 1);
@@ -1672,7 +1676,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         TcState tc{0u, 0u, 0u, 0u};
         bool use_tc = false;
-        if constexpr (SM::kTC) {
+        if constexpr (TC) {
             // tensor memory only when the plan made tcgen05 tiles (one CTA per
             // SM, so the allocation never waits)
             use_tc = p.tc != 0 && p.hdr[3] != 0;
@@ -1684,8 +1688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc.tmem = sm.tmem;
             }
         }
-        consumer<D, GD, F8>(sm, p, warp, lane, tc);
-        if constexpr (SM::kTC) {
+        consumer<D, GD, F8, TC>(sm, p, warp, lane, tc);
+        if constexpr (TC) {
             if (use_tc) {
                 // every MMA has completed and every warp is done with tensor memory
                 // (bounded by time alone: an abort must not skip the release)
@@ -1708,7 +1712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0 && sm.abort) report(p.status, PKV_STATUS_TIMEOUT);
 }
 
-template <int D, int GD, bool F8 = false>
+template <int D, int GD, bool F8 = false, bool TC = false>
 int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, cudaStream_t st) {
     static int configured[64] = {0};
     int dev = 0;
@@ -1720,7 +1724,7 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     static_assert(sizeof(Smem<D, F8>) <= kMaxSmem, "shared-memory budget");
     if (dev < 0 || dev >= 64) return PKV_ERR_CUDA;
     if (!configured[dev]) {
-        if (cudaFuncSetAttribute(paged_attention_kernel<D, GD, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(paged_attention_kernel<D, GD, F8, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured[dev] = 1;
@@ -1729,7 +1733,7 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
     const cudaError_t e =
-        host::launch_pdl(paged_attention_kernel<D, GD, F8>, dim3((unsigned)grid), dim3(kThreads), smem, st, tm, p);
+        host::launch_pdl(paged_attention_kernel<D, GD, F8, TC>, dim3((unsigned)grid), dim3(kThreads), smem, st, tm, p);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -1745,7 +1749,7 @@ int dispatch_g(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaS
 }
 
 int dispatch_attention_d64(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
-int dispatch_attention_d128(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
+int dispatch_attention_d128(int GD, bool tc, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
 int combine_d64(const CombineParams& c, cudaStream_t st);
 int dispatch_attention_fp8_d128(const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
 int combine_d128(const CombineParams& c, cudaStream_t st);

@@ -2,7 +2,8 @@
 #include "pkv_attention.cuh"
 
 namespace pkv {
-int dispatch_attention_d128(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st) {
+int dispatch_attention_d128(int GD, bool tc, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st) {
+    if (tc) return launch_attention<128, 0, false, true>(tm, p, mi, st);
     return dispatch_g<128>(GD, tm, p, mi, st);
 }
 int combine_d128(const CombineParams& c, cudaStream_t st) { return launch_combine<128>(c, st); }

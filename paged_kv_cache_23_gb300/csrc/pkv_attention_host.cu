@@ -19,7 +19,7 @@ struct PlanParams {
     int* row_np;     // [total_q] partitions of each query row
     __nv_bfloat16* out;
     int32_t* status;
-    int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, decode_ok;
+    int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, max_q_len, decode_ok;
     int fp8;         // e4m3 pool: every row on the transposed tensor-core item
     int tc;          // tcgen05 tiles allowed (head_dim 128, bf16, block_size >= 16, P % 128 == 0)
     int adapt_P;     // 1: P is a floor; the planning kernel may double it
@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         long long tok = 0, tok_mq = 0;
         for (int b = tid; b < n; b += kPlanThreads) {
             const int L = pp.seq_lens[b], ql = pp.q_lens[b];
-            if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len) continue;
+            if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len || ql > pp.max_q_len) continue;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
             const bool multi = multi_query_kind(sh.kind) || ql > 1;
             const long long t = (long long)L * (pp.n_kv / sh.hps) * (multi ? ceil_div(ql, sh.qt) : 1);
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             ql = pp.q_lens[b];
             if (L < 0 || (long long)L > (long long)pp.max_blocks * pp.bs || L > pp.max_seq_len)
                 flag |= PKV_STATUS_BAD_SEQLEN;
-            if (ql < 0 || ql > L) flag |= PKV_STATUS_BAD_QLEN;
+            if (ql < 0 || ql > L || ql > pp.max_q_len) flag |= PKV_STATUS_BAD_QLEN;
             // clamp so the scan cannot overflow (total_q <= 2^20 is checked on the host)
             qlc = ql > 0 ? min(ql, pp.total_q + 1) : 0;
         }
@@ -357,12 +357,12 @@ namespace {
 // per-kv-head dequantisation scales.
 int run_attention(void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
                   const float* v_scale, bool fp8, const int32_t* block_tables, int max_blocks,
-                  const int32_t* seq_lens, const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
-                  int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, float scale,
-                  int partition_tokens, int flags, void* workspace, size_t workspace_bytes, int32_t* status,
-                  void* stream) {
-    if (num_seqs < 0 || total_q < 0 || max_blocks < 1 || max_seq_len < 0 || num_q_heads < 1 || num_kv_heads < 1 ||
-        num_blocks < 1 || block_size < 1)
+                  const int32_t* seq_lens, const int32_t* q_lens, int num_seqs, int total_q, int max_q_len,
+                  int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                  float scale, int partition_tokens, int flags, void* workspace, size_t workspace_bytes,
+                  int32_t* status, void* stream) {
+    if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_blocks < 1 || max_seq_len < 0 || num_q_heads < 1 ||
+        num_kv_heads < 1 || num_blocks < 1 || block_size < 1)
         return PKV_ERR_SIZE;
     if (head_dim != 64 && head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (num_q_heads % num_kv_heads) return PKV_ERR_UNSUPPORTED;
@@ -410,9 +410,13 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     }
 
     // tcgen05 tiles: bf16 head_dim 128, boxes of >= 16 rows, partitions made of
-    // whole 128-token stages, and a batch with at least one 128-row tile
-    const bool tc = !fp8 && head_dim == 128 && block_size >= 16 && P % kTcT == 0 &&
-                    !(flags & PKV_ATTN_NO_TCGEN05) && (long long)total_q * G >= kTcRows;
+    // whole 128-token stages, decode rows on tensor cores, and a batch that may
+    // hold a 128-row tile (max_q_len * g >= 128); otherwise the variant
+    // without tile code runs
+    const int GD = (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
+    const bool decode_fma = !fp8 && GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
+    const bool tc = !fp8 && head_dim == 128 && block_size >= 16 && P % kTcT == 0 && !decode_fma &&
+                    !(flags & PKV_ATTN_NO_TCGEN05) && (long long)max_q_len * G >= kTcRows;
     if (tc) {
         // [num_blocks][n_kv][bs][2 slabs][64] with one slab of min(bs, 128) rows per box
         const uint64_t row = 256;
@@ -429,8 +433,6 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     int* aux = reinterpret_cast<int*>(ws + w.seqaux);
-    const int GD = (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
-    const bool decode_fma = !fp8 && GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
 
     PlanParams pp{};
     pp.seq_lens = seq_lens;
@@ -455,6 +457,7 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     pp.max_blocks = max_blocks;
     pp.bs = block_size;
     pp.max_seq_len = max_seq_len;
+    pp.max_q_len = max_q_len;
     pp.decode_ok = decode_fma ? 1 : 0;
     pp.adapt_P = partition_tokens == 0 ? 1 : 0;
     pp.fp8 = fp8 ? 1 : 0;
@@ -486,7 +489,7 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     ap.v_scale = v_scale;
     ap.tc = tc ? 1 : 0;
     const int rc2 = fp8                ? dispatch_attention_fp8_d128(tm, ap, w.max_items, st)
-                    : head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tm, ap, w.max_items, st)
+                    : head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tc, tm, ap, w.max_items, st)
                                       : dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
     // The combine runs even when no row can span partitions (it then only
     // waits and exits): it triggers the next kernel of the stream only after
@@ -508,23 +511,27 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
 
 extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
                                           const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
-                                          const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
-                                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                                          int num_blocks, float scale, int partition_tokens, int flags,
-                                          void* workspace, size_t workspace_bytes, int32_t* status, void* stream) {
+                                          const int32_t* q_lens, int num_seqs, int total_q, int max_q_len,
+                                          int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_blocks, float scale, int partition_tokens,
+                                          int flags, void* workspace, size_t workspace_bytes, int32_t* status,
+                                          void* stream) {
     return run_attention(out, q, k_cache, v_cache, nullptr, nullptr, false, block_tables, max_blocks, seq_lens,
-                         q_lens, num_seqs, total_q, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                         num_blocks, scale, partition_tokens, flags, workspace, workspace_bytes, status, stream);
+                         q_lens, num_seqs, total_q, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                         block_size, num_blocks, scale, partition_tokens, flags, workspace, workspace_bytes, status,
+                         stream);
 }
 
 extern "C" int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
                                               const float* k_scale, const float* v_scale,
                                               const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
-                                              const int32_t* q_lens, int num_seqs, int total_q, int max_seq_len,
-                                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                                              int num_blocks, float scale, int partition_tokens, void* workspace,
-                                              size_t workspace_bytes, int32_t* status, void* stream) {
+                                              const int32_t* q_lens, int num_seqs, int total_q, int max_q_len,
+                                              int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                              int block_size, int num_blocks, float scale, int partition_tokens,
+                                              void* workspace, size_t workspace_bytes, int32_t* status,
+                                              void* stream) {
     return run_attention(out, q, k_cache, v_cache, k_scale, v_scale, true, block_tables, max_blocks, seq_lens,
-                         q_lens, num_seqs, total_q, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
-                         num_blocks, scale, partition_tokens, 0, workspace, workspace_bytes, status, stream);
+                         q_lens, num_seqs, total_q, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                         block_size, num_blocks, scale, partition_tokens, 0, workspace, workspace_bytes, status,
+                         stream);
 }

@@ -53,7 +53,8 @@ extern "C" size_t pkv_noalloc_scratch_bytes(void) { return pkv::kScratchBytes; }
 extern "C" int pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
                                                   const int32_t* block_tables, int max_blocks,
                                                   const int32_t* seq_lens, const int32_t* q_lens, int num_seqs,
-                                                  int total_q, int max_seq_len, int num_q_heads, int num_kv_heads,
+                                                  int total_q, int max_q_len, int max_seq_len, int num_q_heads,
+                                                  int num_kv_heads,
                                                   int head_dim, int block_size, int num_blocks, float scale,
                                                   int partition_tokens, int flags, int32_t* status, void* stream) {
     const size_t need = pkv_attention_workspace_bytes(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim,
@@ -63,7 +64,7 @@ extern "C" int pkv_paged_attention_decode_noalloc(void* out, const void* q, cons
     void* ws = pkv::scratch_address();
     if (ws == nullptr) return PKV_ERR_CUDA;
     return pkv_paged_attention_decode(out, q, k_cache, v_cache, block_tables, max_blocks, seq_lens, q_lens, num_seqs,
-                                      total_q, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                                      total_q, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
                                       num_blocks, scale, partition_tokens, flags, ws, pkv::kScratchBytes, status,
                                       stream);
 }

@@ -72,6 +72,7 @@ class DeviceStep:
         self.out = torch.empty((w.total_q, w.n_q, w.head_dim), dtype=torch.bfloat16, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.max_seq_len = int(max_seq_len if max_seq_len is not None else max(1, int(w.seq_lens.max())))
+        self.max_q_len = max(1, int(w.q_lens.max())) if w.num_seqs else 1  # host bound on every q_len
         self.partition_tokens = int(partition_tokens if partition_tokens is not None else w.partition_tokens)
         self.flags = int(flags)
         nbytes = attention_workspace_bytes(w.num_seqs, w.total_q, w.n_q, w.n_kv, w.head_dim, self.max_seq_len,
@@ -135,12 +136,12 @@ class DeviceStep:
             paged_attention_decode_fp8(self.out, self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                                        self.block_tables, self.seq_lens, self.q_lens, self.max_seq_len, self.w.scale,
                                        self.workspace, partition_tokens=self.partition_tokens, status=self.status,
-                                       stream=stream)
+                                       stream=stream, max_q_len=self.max_q_len)
             return
         paged_attention_decode(self.out, self.q, self.k_cache, self.v_cache, self.block_tables, self.seq_lens,
                                self.q_lens, self.max_seq_len, self.w.scale, self.workspace,
                                partition_tokens=self.partition_tokens, flags=self.flags, status=self.status,
-                               stream=stream)
+                               stream=stream, max_q_len=self.max_q_len)
 
     def accept(self, stream=None):
         if self.spec:

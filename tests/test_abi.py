@@ -52,13 +52,13 @@ def test_host_side_argument_checks(lib):
     f = lib.pkv_paged_attention_decode
     nullp = None
     args = dict(out=nullp, q=nullp, k=nullp, v=nullp, bt=nullp, max_blocks=4, sl=nullp, ql=nullp, num_seqs=2,
-                total_q=2, max_seq_len=64, n_q=32, n_kv=8, d=128, bs=16, nb=10, scale=0.1, P=0, flags=0,
+                total_q=2, max_q_len=1, max_seq_len=64, n_q=32, n_kv=8, d=128, bs=16, nb=10, scale=0.1, P=0, flags=0,
                 ws=nullp, wsb=0, st=nullp, stream=nullp)
 
     def call(**kw):
         a = dict(args, **kw)
         return f(a["out"], a["q"], a["k"], a["v"], a["bt"], a["max_blocks"], a["sl"], a["ql"], a["num_seqs"],
-                 a["total_q"], a["max_seq_len"], a["n_q"], a["n_kv"], a["d"], a["bs"], a["nb"], a["scale"], a["P"],
+                 a["total_q"], a["max_q_len"], a["max_seq_len"], a["n_q"], a["n_kv"], a["d"], a["bs"], a["nb"], a["scale"], a["P"],
                  a["flags"], a["ws"], a["wsb"], a["st"], a["stream"])
 
     assert call(d=96) == -3                 # head_dim
@@ -66,6 +66,7 @@ def test_host_side_argument_checks(lib):
     assert call(bs=24) == -3                # block_size not a power of two
     assert call(P=24) == -2                 # partition not a multiple of 16
     assert call(num_seqs=-1) == -2
+    assert call(max_q_len=-1) == -2
     assert call(flags=8) == -2
     assert call() == -1                     # NULL pointers
     assert call(num_seqs=0) == 0            # nothing to do

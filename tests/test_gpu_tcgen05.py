@@ -131,3 +131,19 @@ def test_bad_block_in_a_tile_gives_nan_rows():
     oracle.kv_append(k, v, w.k_new, w.v_new, slots)
     ref, _ = oracle.attention(w.q, k, v, w.block_tables, w.seq_lens, w.q_lens, w.scale)
     assert_close(bf16_to_bits(ds.out)[:q0], ref[:q0], "decode rows")
+
+
+def test_q_len_above_the_host_bound_is_flagged():
+    # max_q_len is a host bound: a longer q_len gives NaN rows and BAD_QLEN
+    w = chunk(32, 8, 40, prefix=300, decodes=2, ctx=200, seed=6)
+    ds = DeviceStep(w, partition_tokens=256)
+    ds.cache_ops()
+    ds.max_q_len = 39
+    ds.status.zero_()
+    ds.attention()
+    torch.cuda.synchronize()
+    st = int(ds.status.item())
+    assert st & pkv.PKV_STATUS_BAD_QLEN
+    out = wl.bf16_bits_to_f32(bf16_to_bits(ds.out))
+    q0 = int(w.q_lens[:-1].sum())
+    assert np.isnan(out[q0:]).all() and np.isfinite(out[:q0]).all()

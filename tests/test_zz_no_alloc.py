@@ -24,7 +24,7 @@ def _noalloc_call(ds, out, status):
     p = lambda t: ctypes.c_void_p(t.data_ptr())
     return L.pkv_paged_attention_decode_noalloc(
         p(out), p(ds.q), p(ds.k_cache), p(ds.v_cache), p(ds.block_tables), w.max_blocks, p(ds.seq_lens),
-        p(ds.q_lens), w.num_seqs, w.total_q, ds.max_seq_len, w.n_q, w.n_kv, w.head_dim, w.block_size,
+        p(ds.q_lens), w.num_seqs, w.total_q, ds.max_q_len, ds.max_seq_len, w.n_q, w.n_kv, w.head_dim, w.block_size,
         w.num_blocks, ctypes.c_float(w.scale), ds.partition_tokens, ds.flags, p(status),
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
 
@@ -68,7 +68,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
     p = lambda t: ctypes.c_void_p(t.data_ptr())
     rc = L.pkv_paged_attention_decode_noalloc(
         p(out), p(ds.q), p(ds.k_cache), p(ds.v_cache), p(ds.block_tables), ds.w.max_blocks, p(ds.seq_lens),
-        p(ds.q_lens), 4096, 4096, big, 32, 8, 128, 16, ds.w.num_blocks, ctypes.c_float(0.1), 512, 0, None,
+        p(ds.q_lens), 4096, 4096, 1, big, 32, 8, 128, 16, ds.w.num_blocks, ctypes.c_float(0.1), 512, 0, None,
         ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert rc == pkv.PKV_ERR_SCRATCH_LIMIT
     assert b"scratch" in L.pkv_error_string(rc)
