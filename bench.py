@@ -495,8 +495,7 @@ def end_to_end(ds, w, args, stream, device, ws):
     z.record(stream)
     torch.cuda.synchronize()
     ms = aggregate_max(a.elapsed_time(z), ws, device) / steps
-    from paged_kv_cache_23_gb300 import accounting
-    b = accounting.step_bytes(w)
+    b = step_bytes_of(w, ds.fp8 is not None)  # the same bytes as the device-timed value
     bytes_all = aggregate_sum(b["step_unique"], ws, device)
     return {"value": bytes_all / (ms / 1e3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": int(h2d),
             "d2h_bytes_per_step": int(d2h), "ms_per_step": ms}

@@ -58,11 +58,11 @@ constexpr int kPlanThreads = 1024;
 constexpr int kTailBuckets = 256;           // tail-length classes of the longest-first ordering
 
 // tcgen05 chunk tiles: 128 rows = (query, q head) pairs of one kv head, stages
-// of 128 tokens, tensor-memory columns [S0 | S1 | O | P0 | P1].
+// of 128 tokens, tensor-memory columns [S0 | S1 | O_0 | O_1] (P over S).
 constexpr int kTcT = 128;                   // tokens per stage
 constexpr int kTcRows = 128;                // tile rows (the MMA's M)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0, kTmemO = 256, kTmemP = 384;
+constexpr uint32_t kTmemS = 0, kTmemO = 256;
 
 // KIND_DEC: q_len = 1 rows on tensor cores; KIND_DECF: on CUDA cores; KIND_MQ:
 // q_len > 1 on mma.sync; KIND_TC: query tiles of 128 rows on tcgen05.
@@ -81,7 +81,7 @@ struct Desc {
 struct TMaps {
     CUtensorMap k[4];
     CUtensorMap v[4];
-    CUtensorMap k_tc, v_tc;  // one 64-column slab of min(bs, 128) rows of one kv head
+    CUtensorMap k_tc, v_tc;  // tcgen05 stages: see produce_tc
 };
 
 struct AttnParams {
@@ -98,6 +98,7 @@ struct AttnParams {
     const float* v_scale;
     int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, row_bytes;
     int tc;              // tcgen05 tiles possible: tensor memory is allocated when the plan made some
+    int tc_pair;         // tcgen05 stages of block_size 16: one V box holds both slabs of a block
     float scale_log2;    // scale * log2(e): scores live in base-2 units
 };
 
@@ -126,11 +127,12 @@ struct Smem {
     int poison[kSlots];
     int abort;
     uint64_t full[G::kSlots], empty[G::kSlots], ifull[kSlots], iempty[kSlots];
-    // tcgen05 tiles: S ready, PV done (per buffer), P written, half-row
-    // exchange, tile entry, Q written, final drain, warps done with tensor memory
-    uint64_t sbar[2], obar[2], pready, xbar, ebar, qbar, tdone, dbar;
+    // tcgen05 tiles: S ready, PV done (per buffer), P written (per half),
+    // half-row merge, tile entry, Q written, final drain, warps done with
+    // tensor memory
+    uint64_t sbar[2], obar[2], pready[2], xbar, ebar, qbar, tdone, dbar;
     uint32_t tmem;
-    float red[kTC ? 2 : 1][2][kTcRows];                       // [exchange parity][half][row]
+    float red[kTC ? 2 : 1][2][kTcRows];                       // [m, l][half][row]
 };
 // the tcgen05 operands (ring slabs, Q) start on 1024-byte swizzle atoms
 using SmemTc = Smem<128, false>;
@@ -190,17 +192,29 @@ __device__ __forceinline__ Desc make_desc(const int4 it, const int4 sq, int P) {
 }
 
 // ---------------------------------------------------------------------------
-// Stages of a tcgen05 tile: 128 tokens of one kv head, K then V, each as two
-// 64-column slabs of 128 rows ([slab][token][128 B], 128-byte swizzle) -- the
-// K-major B operand of S = Q K^T and the MN-major B operand of O += P V.  One
-// TMA box per (tensor, slab, block): lane l copies tensor l & 1, slab
-// (l >> 1) & 1 of the stage's block l >> 2.  Blocks that start past the
-// item's last position are not fetched (the consumers zero those V rows).
+// Ring slots of a tcgen05 tile.  A stage is 128 tokens of one kv head; K and V
+// each take 32 KB of 128-byte rows (128-byte swizzle): the K-major B operand of
+// S = Q K^T and the MN-major B operand of O += P V.  The slots are skewed: slot
+// j holds K of stage j and V of stage j - 1 (n + 1 slots for n stages), so a
+// slot is free once S_j and PV_{j-1} have run -- one stage earlier than with
+// K_j and V_j together, which doubles how far ahead the ring can fetch.
+// A TMA copy costs the issuing warp about the same time whatever its size, so
+// the stage is fetched in as few boxes as the paged layout and the MMA
+// operands allow.  K: one box per (slab, block), [slab][token] -- slab x at
+// x * 16 KB, rows contiguous, 8-row groups 1 KB apart, so S is one N = 128
+// MMA chain.  V: the same with block_size >= 32; with block_size 16 one 4 KB
+// box per block holds both slabs of its 16 rows, [slab][row], block b of the
+// stage at b * 4 KB (the MN-major operand of a 16-token k-step is one block:
+// slabs 2 KB apart, its two 8-row groups 1 KB apart).  Two warps issue the
+// copies of a slot in parallel, half each (12 copies apiece with block_size
+// 16): the producer and the helper warp.
+// Blocks that start past the item's last position are not fetched (the
+// consumers zero those V rows).
 // Returns false when the pipeline was aborted.
 // ---------------------------------------------------------------------------
 template <int D, bool F8>
 __device__ __forceinline__ bool produce_tc(Smem<D, F8>& sm, const TMaps* tm, const AttnParams& p, const Desc& d,
-                                           int si, int lane, uint32_t& g, int& next) {
+                                           int si, int lane, uint32_t& g, int& next, bool helper) {
     if constexpr (!Smem<D, F8>::kTC) {
         return false;
     } else {
@@ -208,49 +222,78 @@ __device__ __forceinline__ bool produce_tc(Smem<D, F8>& sm, const TMaps* tm, con
         volatile int* abort = &sm.abort;
         const int rows = p.bs < kTcT ? p.bs : kTcT;  // rows per box
         const int nblk = kTcT / rows;                // blocks per stage (<= 8)
-        const uint32_t box_bytes = (uint32_t)rows * 128;
-        const int tv = lane & 1, x = (lane >> 1) & 1, j = lane >> 2;
+        const bool pair = p.tc_pair != 0;  // block_size 16: one V box = both slabs of a block
+        // two warps split every slot: warp w (0 = producer, 1 = helper) copies
+        // slab w of K for every block (lanes l < nblk: block l), then half of V:
+        // paired boxes of blocks [w nblk / 2, (w + 1) nblk / 2), or slab w of
+        // every block -- K first, since S_j needs it before PV_{j-1} needs V
+        const int w = helper ? 1 : 0;
+        int tv = 0, x = w, jb = lane;
+        bool lane_ok = lane < nblk;
+        if (lane >= nblk) {
+            const int l2 = lane - nblk;
+            tv = 1;
+            x = pair ? 0 : w;
+            jb = pair ? l2 + w * (nblk / 2) : l2;
+            lane_ok = l2 < (pair ? nblk / 2 : nblk);
+        }
+        const bool pv = pair && tv;                  // this lane copies a paired V box
+        const uint32_t slab_bytes = (uint32_t)rows * 128;
         const int tb = d.t_begin / kTcT, te = (d.t_end + kTcT - 1) / kTcT;
+        const int n = te - tb;
         const int32_t* bt = p.block_tables + (long long)d.b * p.max_blocks;
         const int e_lim = (d.t_end + p.bs - 1) / p.bs;
         int tab_base = tb * kTcT / p.bs;
         int tab = tab_base + lane < e_lim ? __ldg(bt + tab_base + lane) : 0;
         int tab_next = tab_base + 32 + lane < e_lim ? __ldg(bt + tab_base + 32 + lane) : 0;
-        const int i_claim = max(tb, te - kClaimAhead);
-        for (int i = tb; i < te; ++i, ++g) {
-            if (i == i_claim && lane == 0) next = atomicAdd(&p.hdr[1], 1);
-            const int t0 = i * kTcT;
-            const int e0 = t0 / p.bs;
-            if (e0 >= tab_base + 32) {
+        const int j_claim = max(0, n + 1 - kClaimAhead);
+        for (int j = 0; j <= n; ++j, ++g) {
+            if (!helper && j == j_claim && lane == 0) next = atomicAdd(&p.hdr[1], 1);
+            // V (stage j - 1) trails K (stage j) by one stage: the table window
+            // follows V's first entry; K's entries are at most 8 further
+            const int tk = (tb + j) * kTcT, tvv = tk - kTcT;
+            const int e_lo = (j > 0 ? tvv : tk) / p.bs;
+            if (e_lo >= tab_base + 32) {
                 tab = tab_next;
                 tab_base += 32;
                 const int en = tab_base + 32 + lane;
                 tab_next = en < e_lim ? __ldg(bt + en) : 0;
             }
-            const int off = e0 - tab_base + j;  // in [0, 40)
+            const int t0 = tv ? tvv : tk;          // this lane's stage
+            const bool has = tv ? j > 0 : j < n;   // slot j holds that stage
+            const int nvb_k = j < n ? min(nblk, (d.t_end - tk + rows - 1) / rows) : 0;
+            const int nvb_v = j > 0 ? min(nblk, (d.t_end - tvv + rows - 1) / rows) : 0;
+            const int off = (has ? t0 / p.bs : e_lo) - tab_base + jb;  // in [0, 48)
             const int lo = __shfl_sync(kFull, tab, off & 31);
             const int hi = __shfl_sync(kFull, tab_next, off & 31);
             int my = off < 32 ? lo : hi;
-            const int nvb = min(nblk, (d.t_end - t0 + rows - 1) / rows);  // blocks holding positions < t_end
-            const bool in = j < nvb;
+            const bool in = lane_ok && has && jb < (tv ? nvb_v : nvb_k) && jb < nblk;
             const bool okb = !in || (my >= 0 && my < p.num_blocks);
             if (!okb) my = 0;
             const unsigned badmask = __ballot_sync(kFull, !okb);
             const int s = (int)(g % RS);
             bool got = true;
             if (lane == 0) {
-                if (badmask) {
+                // every block of the stage has a producer lane (slab 0 of K; V
+                // stage j - 1 reads the blocks K stage j - 1 was checked on): the
+                // producer alone reports, and alone arms the slot's barrier with
+                // both warps' bytes (the helper's copies may land first: the
+                // phase cannot complete before this arrival)
+                if (badmask && !helper) {
                     sm.poison[si] = 1;
                     report(p.status, PKV_STATUS_BAD_BLOCK);
                 }
                 got = mbar_wait(&sm.empty[s], ((g / RS) & 1) ^ 1, abort);
-                if (got) mbar_arrive_expect_tx(&sm.full[s], 4u * nvb * box_bytes);
+                if (got && !helper) mbar_arrive_expect_tx(&sm.full[s], 2u * (nvb_k + nvb_v) * slab_bytes);
             }
             if (!__shfl_sync(kFull, got, 0)) return false;  // never arm a barrier whose previous phase is open
             if (in) {
                 const int row0 = p.bs > kTcT ? (t0 % p.bs) : 0;
-                tma_load_5d(&sm.kv[s][tv][x * (kTcT * 128) + j * box_bytes], tv ? &tm->v_tc : &tm->k_tc, 0, x, row0,
-                            d.hg, my, &sm.full[s]);
+                if (pv)  // view {64, bs, slab, n_kv, nb}: [slab][16 rows] of block my, 4 KB at 4 KB steps
+                    tma_load_5d(&sm.kv[s][1][jb * 4096], &tm->v_tc, 0, 0, 0, d.hg, my, &sm.full[s]);
+                else     // view {64, slab, bs, n_kv, nb}: one slab of `rows` rows
+                    tma_load_5d(&sm.kv[s][tv][x * (kTcT * 128) + jb * slab_bytes], tv ? &tm->v_tc : &tm->k_tc, 0, x,
+                                row0, d.hg, my, &sm.full[s]);
             }
             __syncwarp();
         }
@@ -299,7 +342,7 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
         }
         if (end) break;
         if (d.kind == KIND_TC) {
-            if (!produce_tc<D, F8>(sm, tm, p, d, si, lane, g, next)) break;
+            if (!produce_tc<D, F8>(sm, tm, p, d, si, lane, g, next, false)) break;
             next = __shfl_sync(kFull, next, 0);
             continue;
         }
@@ -951,24 +994,30 @@ __device__ __forceinline__ void mq_item(Smem<D, false>& sm, const AttnParams& p,
 // Query tile on the 5th-generation tensor cores (tcgen05, accumulators in
 // tensor memory): the FlashAttention block loop of "Inference at Scale"
 // section 07 for 128 rows = (query, q head) pairs of one kv head.
-//   S_k  = Q K_k^T        (M 128, N 128 tokens, K = D): A = Q (shared memory,
-//                          K-major), B = the stage's K slabs (K-major)
-//   O   += P_k V_k         (M 128, N = D, K 128 tokens): A = P (tensor memory,
-//                          bf16), B = the stage's V slabs (MN-major)
-// Thread (warp w, lane l) owns row r = 32 (w % 4) + l -- the tensor-memory
-// lane its warp may access -- and the column half h = w / 4 of S and of O.
-// One elected thread (consumer warp 0, lane 0) issues the MMAs: S_{k+1} as
-// soon as its stage has landed (it overlaps the softmax of stage k), PV_k once
-// every warp has written P_k.  The PV commit releases the ring slot.  The two
-// halves of a row exchange their maxima (and at the end their sums) through
-// shared memory.  Every wait is a bounded mbarrier wait: a stalled warp can
-// make the tile time out, never hang it.
-// Reference maxima are lazy as in the other items (kRescaleSlack): a row
-// rescales its O half in tensor memory only when its maximum moves.
+//   S_k  = Q K_k^T      (M 128, N 128 tokens, K = D): A = Q (shared memory,
+//                        K-major), B = the stage's K slabs (K-major)
+//   O_h += P_h V_k,h     (M 128, N = D, K 64 tokens): A = P (tensor memory,
+//                        bf16), B = the stage's V slabs (MN-major)
+// The two warpgroups split every stage's 128 tokens: warpgroup h (warps 4h ..
+// 4h + 3) takes tokens [64 h, 64 h + 64) of each stage with its own running
+// maximum, sum and accumulator O_h -- two independent online softmaxes over
+// interleaved halves of the keys, merged once at the end with the same
+// log-sum-exp rescaling as split-KV partitions (section 07, Flash-Decoding).
+// So a stage needs no exchange between warps.  Thread (warp w, lane l) owns
+// row r = 32 (w % 4) + l, the tensor-memory lane its warp may access.  It
+// reads its 64 scores of S_k, writes its 64 probabilities (bf16) over the
+// first 32 of those columns, and rescales its O_h only when its maximum moves
+// by more than kRescaleSlack (lazy reference maximum, as in the other items).
+// A dedicated MMA warp issues every tcgen05.mma (tc_mma): S_{k+1} once PV_{k-1}
+// has read the S buffer it reuses, PV_k per half once that half's P is
+// written; the PV commit releases the ring slot.  Every wait is a bounded
+// mbarrier wait: a stalled warp can make the tile time out, never hang it.
+// Tensor-memory columns: S0 [0, 128), S1 [128, 256), O_0 [256, 384),
+// O_1 [384, 512).
 // ---------------------------------------------------------------------------
 struct TcState {
     uint32_t tmem;   // tensor-memory base
-    uint32_t k;      // tcgen05 stages processed by this CTA (S, P, O buffer parity)
+    uint32_t k;      // tcgen05 stages processed by this CTA (S / O buffer parity)
     uint32_t x;      // half-row exchanges done
     uint32_t tiles;  // tcgen05 tiles processed (entry / Q barrier parity)
 };
@@ -982,21 +1031,28 @@ __device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// 2^x by the hardware approximation (MUFU), subnormal results flushed to 0:
+// a probability below 2^-126 of the row maximum is 0 in the bf16 P anyway.
+__device__ __forceinline__ float ex2_fast(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Softmax side of a tile (the eight consumer warps).
 template <int D>
 __device__ __forceinline__ void tc_item(Smem<D, false>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
                                         uint32_t gbase, int ntiles, int si, TcState& st, volatile int* abort) {
     static_assert(D == 128, "tcgen05 tiles are built for head_dim 128");
-    constexpr uint32_t kIdS = umma_idesc_bf16(kTcRows, kTcT, false);
-    constexpr uint32_t kIdPV = umma_idesc_bf16(kTcRows, D, true);
     constexpr int kSlab = kTcT * 128;  // bytes of one 64-column slab of a stage
     const int G = p.G;
     const int quarter = warp & 3, hh = warp >> 2;
     const int r = quarter * 32 + lane;
     const int qi = r / G, hq = r - qi * G;
     const uint32_t tl = st.tmem + ((uint32_t)(quarter * 32) << 16);  // this warp's lanes
-    const bool issuer = warp == 0 && lane == 0;
     const uint32_t tpar = st.tiles & 1;
-    // every consumer warp has left its previous item (qbuf aliases pbuf)
+    // every consumer warp has left its previous item (qbuf aliases pbuf, and
+    // the previous tile's output reads are done)
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.ebar);
     mbar_wait(&sm.ebar, tpar, abort);
@@ -1013,154 +1069,141 @@ __device__ __forceinline__ void tc_item(Smem<D, false>& sm, const AttnParams& p,
     if (lane == 0) mbar_arrive(&sm.qbar);
 
     const int tb = d.t_begin / kTcT;
-    const uint32_t qa = smem_u32(sm.qbuf);
-    // S_i = Q K_i^T into S buffer (k + i) & 1
-    auto issue_s = [&](int i) {
-        const uint32_t gi = gbase + i;
-        const int s = (int)(gi % kRingSlots);
-        if (!mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort)) return;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
-        const uint32_t dst = st.tmem + kTmemS + ((st.k + i) & 1) * kTcT;
-#pragma unroll
-        for (int xs = 0; xs < 2; ++xs)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                umma_ss(dst, umma_desc_sw128(qa + xs * kSlab + kk * 32, 0), umma_desc_sw128(kb + xs * kSlab + kk * 32, 0),
-                        kIdS, (xs | kk) != 0);
-        umma_commit(&sm.sbar[(st.k + i) & 1]);
-    };
-    if (issuer) {
-        if (mbar_wait(&sm.qbar, tpar, abort)) issue_s(0);
-    }
-    __syncwarp();
-
     // last visible position of this row (rows past the tile's queries take the last query's)
     const int lim = d.t_vis - d.nq + min(qi, d.nq - 1);
     const int last = min(lim, d.t_end - 1);
-    float m_ref = -INFINITY, l = 0.f;
+    const float sl2 = p.scale_log2;
+    const bool pair = p.tc_pair != 0;
+    const uint32_t ocol = kTmemO + (uint32_t)hh * D;  // this half's accumulator
+    float m_ref = -INFINITY, l = 0.f;                 // this half's reference maximum and sum
     bool poisoned = false;
     for (int i = 0; i < ntiles; ++i) {
         const uint32_t k = st.k + i;
         const int b = (int)(k & 1);
-        const uint32_t gi = gbase + i;
-        const int s = (int)(gi % kRingSlots);
-        if (issuer && i + 1 < ntiles) issue_s(i + 1);
-        __syncwarp();
-        // scores of this row half: columns t0 + j, visible iff j <= nv
+        const uint32_t scol = kTmemS + (uint32_t)b * kTcT + (uint32_t)hh * 64;
         mbar_wait(&sm.sbar[b], (k >> 1) & 1, abort);
         __syncwarp();  // tcgen05.ld/st are warp-collective: reconverge after the polling wait
         tc_fence_after();
-        // one 64-register array: raw scores, then scaled scores (as bits), then packed P
         uint32_t sv[64];
-        tmem_ld32(tl + kTmemS + b * kTcT + hh * 64, sv);
-        tmem_ld32(tl + kTmemS + b * kTcT + hh * 64 + 32, sv + 32);
+        tmem_ld32(tl + scol, sv);
+        tmem_ld32(tl + scol + 32, sv + 32);
         tmem_wait_ld();
+        // column j of this half holds stage token 64 hh + j, visible iff 64 hh + j <= lr
+        const int lr = last - (tb + i) * kTcT;
+        const bool full = lr >= 64 * hh + 63;
         float mx = -INFINITY;
-        {
-            const int nv = last - ((tb + i) * kTcT + hh * 64);
+        if (full) {
+            // max of the scaled scores from the raw ones (the scale's sign picks max or min)
+            float a = __uint_as_float(sv[0]);
+            if (sl2 >= 0.f) {
+#pragma unroll
+                for (int j = 1; j < 64; ++j) a = fmaxf(a, __uint_as_float(sv[j]));
+            } else {
+#pragma unroll
+                for (int j = 1; j < 64; ++j) a = fminf(a, __uint_as_float(sv[j]));
+            }
+            mx = a * sl2;
+        } else {
 #pragma unroll
             for (int j = 0; j < 64; ++j) {
-                const float v = j <= nv ? __uint_as_float(sv[j]) * p.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, v);
+                const float v = 64 * hh + j <= lr ? __uint_as_float(sv[j]) * sl2 : -INFINITY;
                 sv[j] = __float_as_uint(v);
+                mx = fmaxf(mx, v);
             }
         }
-        // exchange the half maxima of each row (the S reads above are done first:
-        // the issuer refills this S buffer after the exchange)
-        sm.red[st.x & 1][hh][r] = mx;
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.xbar);
-        mbar_wait(&sm.xbar, st.x & 1, abort);
-        const float row_mx = fmaxf(mx, sm.red[st.x & 1][hh ^ 1][r]);
-        ++st.x;
-        // O and l are relative to m_ref.  A row whose maximum moved rescales its
-        // half of O once PV_{k-1} is done; the tensor-memory accesses are
+        // O_h and l are relative to m_ref.  A row whose maximum moved rescales
+        // its O_h once PV_{k-1} is done; the tensor-memory accesses are
         // warp-collective, so the whole warp takes the path (factor 1, exact,
         // for the rows that keep their reference)
-        const bool move = row_mx > m_ref + kRescaleSlack;
-        const float c = move && m_ref != -INFINITY ? exp2f(m_ref - row_mx) : 1.f;
+        const bool move = mx > m_ref + kRescaleSlack;
+        const float c = move && m_ref != -INFINITY ? ex2_fast(m_ref - mx) : 1.f;
         if (__any_sync(kFull, c != 1.f)) {
             const uint32_t kp = k - 1;  // i >= 1 here: a finite m_ref was set by an earlier stage
             mbar_wait(&sm.obar[kp & 1], (kp >> 1) & 1, abort);
             __syncwarp();
             tc_fence_after();
 #pragma unroll 1
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t ov[32];
-                tmem_ld32(tl + kTmemO + hh * 64 + cc * 32, ov);
+                tmem_ld32(tl + ocol + cc * 32, ov);
                 tmem_wait_ld();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * c);
-                tmem_st32(tl + kTmemO + hh * 64 + cc * 32, ov);
+                tmem_st32(tl + ocol + cc * 32, ov);
             }
             tmem_wait_st();
         }
         if (move) {
             l *= c;
-            m_ref = row_mx;  // (while m_ref was -inf every p was 0, so O and l are 0)
+            m_ref = mx;  // (while m_ref was -inf every p was 0, so O_h and l are 0)
         }
         const float u = m_ref == -INFINITY ? 0.f : m_ref;
         float ls = 0.f;
+        if (full) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {  // pair j overwrites sv[j], already consumed
-            const float p0 = exp2f(__uint_as_float(sv[2 * j]) - u), p1 = exp2f(__uint_as_float(sv[2 * j + 1]) - u);
-            ls += p0 + p1;
-            sv[j] = float2_to_bf16x2(p0, p1);
+            for (int j = 0; j < 32; ++j) {  // pair j overwrites sv[j], already consumed
+                const float p0 = ex2_fast(fmaf(__uint_as_float(sv[2 * j]), sl2, -u));
+                const float p1 = ex2_fast(fmaf(__uint_as_float(sv[2 * j + 1]), sl2, -u));
+                ls += p0 + p1;
+                sv[j] = float2_to_bf16x2(p0, p1);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = ex2_fast(__uint_as_float(sv[2 * j]) - u);
+                const float p1 = ex2_fast(__uint_as_float(sv[2 * j + 1]) - u);
+                ls += p0 + p1;
+                sv[j] = float2_to_bf16x2(p0, p1);
+            }
         }
         l += ls;
-        // P buffer b was last read by PV_{k-2}
-        if (k >= 2) {
-            mbar_wait(&sm.obar[b], ((k - 2) >> 1) & 1, abort);
-            __syncwarp();
-            tc_fence_after();
-        }
-        tmem_st32(tl + kTmemP + b * 64 + hh * 32, sv);
+        // P over the first 32 of this half's S columns (this thread has read them;
+        // the MMA warp refills the buffer only after PV_k)
+        tmem_st32(tl + scol, sv);
         tmem_wait_st();
         if (i == ntiles - 1) {
-            // the stage has landed (its slot is released only by PV_k): the
-            // item's block checks are final, and V rows past the item's last
-            // position -- unfetched, or stale, possibly NaN -- are zeroed
-            mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort);
+            // the last V stage has landed (its slot is released only by PV_k):
+            // the item's block checks are final, and this half's V rows past
+            // the item's last position -- unfetched, or stale, possibly NaN --
+            // are zeroed
+            const uint32_t gv = gbase + i + 1;
+            const int sv_ = (int)(gv % kRingSlots);
+            mbar_wait(&sm.full[sv_], (gv / kRingSlots) & 1, abort);
             poisoned = sm.poison[si] != 0;
             const int nvalid = d.t_end - (tb + i) * kTcT;
             if (nvalid < kTcT) {
-                uint8_t* vz = &sm.kv[s][1][0];
-                for (int c = warp * 32 + lane; c < (kTcT - nvalid) * 16; c += kCThreads) {
-                    const int row = nvalid + (c >> 4), xs = (c >> 3) & 1, ch = c & 7;
-                    *reinterpret_cast<uint4*>(vz + xs * kSlab + row * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                uint8_t* vz = &sm.kv[sv_][1][0];
+                // this half's 64 tokens x (2 slabs x 8 chunks of 16 B)
+                for (int cz = quarter * 32 + lane; cz < 64 * 16; cz += 128) {
+                    const int j = cz >> 4, xs = (cz >> 3) & 1, ch = cz & 7;
+                    const int tok = 64 * hh + j;
+                    if (tok < nvalid) continue;
+                    const int off = pair ? (tok >> 4) * 4096 + xs * 2048 + (tok & 15) * 128 : xs * kSlab + tok * 128;
+                    *reinterpret_cast<uint4*>(vz + off + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async_smem();
             }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.pready);
-        if (issuer) {
-            if (mbar_wait(&sm.pready, k & 1, abort)) {
-                tc_fence_after();
-                const uint32_t vb = smem_u32(&sm.kv[s][1][0]);
-#pragma unroll
-                for (int kk = 0; kk < kTcT / 16; ++kk)
-                    umma_ts(st.tmem + kTmemO, st.tmem + kTmemP + b * 64 + kk * 8,
-                            umma_desc_sw128(vb + kk * 2048, kSlab), kIdPV, i > 0 || kk > 0);
-                umma_commit(&sm.obar[b]);
-                mbar_arrive(&sm.empty[s], kCWarps - 1);
-                umma_commit(&sm.empty[s]);  // the slot's last arrival: when PV_k has read V
-            }
-        }
-        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.pready[hh]);
     }
     st.k += ntiles;
     ++st.tiles;
-    // row sum = the two halves' partial sums
-    sm.red[st.x & 1][hh][r] = l;
+    // merge the two halves of each row: (m, l) through shared memory, then
+    // O = O_0 c_0 + O_1 c_1 with c_h = 2^(m_h - m), l = l_0 c_0 + l_1 c_1
+    sm.red[0][hh][r] = m_ref;
+    sm.red[1][hh][r] = l;
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.xbar);
     mbar_wait(&sm.xbar, st.x & 1, abort);
-    const float lrow = l + sm.red[st.x & 1][hh ^ 1][r];
     ++st.x;
+    const float m_o = sm.red[0][hh ^ 1][r], l_o = sm.red[1][hh ^ 1][r];
+    const float m0 = hh == 0 ? m_ref : m_o, m1 = hh == 0 ? m_o : m_ref;
+    const float l0 = hh == 0 ? l : l_o, l1 = hh == 0 ? l_o : l;
+    const float m = fmaxf(m0, m1);
+    const float c0 = m0 == -INFINITY ? 0.f : ex2_fast(m0 - m), c1 = m1 == -INFINITY ? 0.f : ex2_fast(m1 - m);
+    const float lrow = l0 * c0 + l1 * c1;
     const uint32_t kl = st.k - 1;
     mbar_wait(&sm.obar[kl & 1], (kl >> 1) & 1, abort);
     __syncwarp();
@@ -1169,39 +1212,165 @@ __device__ __forceinline__ void tc_item(Smem<D, false>& sm, const AttnParams& p,
     const long long orow = (long long)(d.q_row0 + min(qi, d.nq - 1)) * p.n_q + (long long)d.hg * G + hq;
     const float inv = 1.0f / lrow;
     const float qnan = __int_as_float(0x7fc00000);
-    // O half-row in two 32-column pieces (fewer live registers)
+    // this thread writes output columns [64 hh, 64 hh + 64), in 32-column pieces
 #pragma unroll 1
     for (int cc = 0; cc < 2; ++cc) {
-        uint32_t ov[32];
-        tmem_ld32(tl + kTmemO + hh * 64 + cc * 32, ov);
+        const int col0 = hh * 64 + cc * 32;
+        uint32_t oa[32], ob[32];
+        tmem_ld32(tl + kTmemO + col0, oa);
+        tmem_ld32(tl + kTmemO + D + col0, ob);
         tmem_wait_ld();
         if (!row_ok) continue;
-        const int col0 = hh * 64 + cc * 32;
+        float o[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = __uint_as_float(oa[j]) * c0 + __uint_as_float(ob[j]) * c1;
         if (d.nparts == 1) {
             uint4* dst = reinterpret_cast<uint4*>(p.out + orow * D + col0);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int q4 = 0; q4 < 4; ++q4) {
                 uint4 w;
-                w.x = float2_to_bf16x2(__uint_as_float(ov[8 * c + 0]) * inv, __uint_as_float(ov[8 * c + 1]) * inv);
-                w.y = float2_to_bf16x2(__uint_as_float(ov[8 * c + 2]) * inv, __uint_as_float(ov[8 * c + 3]) * inv);
-                w.z = float2_to_bf16x2(__uint_as_float(ov[8 * c + 4]) * inv, __uint_as_float(ov[8 * c + 5]) * inv);
-                w.w = float2_to_bf16x2(__uint_as_float(ov[8 * c + 6]) * inv, __uint_as_float(ov[8 * c + 7]) * inv);
+                w.x = float2_to_bf16x2(o[8 * q4 + 0] * inv, o[8 * q4 + 1] * inv);
+                w.y = float2_to_bf16x2(o[8 * q4 + 2] * inv, o[8 * q4 + 3] * inv);
+                w.z = float2_to_bf16x2(o[8 * q4 + 4] * inv, o[8 * q4 + 5] * inv);
+                w.w = float2_to_bf16x2(o[8 * q4 + 6] * inv, o[8 * q4 + 7] * inv);
                 if (poisoned) w = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-                dst[c] = w;
+                dst[q4] = w;
             }
         } else {
             float4* dst = reinterpret_cast<float4*>(p.part_o + (orow * p.np_max + d.part) * D + col0);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
+            for (int q4 = 0; q4 < 8; ++q4) {
                 const float4 v = poisoned ? make_float4(qnan, qnan, qnan, qnan)
-                                          : make_float4(__uint_as_float(ov[4 * c]), __uint_as_float(ov[4 * c + 1]),
-                                                        __uint_as_float(ov[4 * c + 2]), __uint_as_float(ov[4 * c + 3]));
-                __stcg(dst + c, v);
+                                          : make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+                __stcg(dst + q4, v);
             }
         }
     }
     tc_fence_before();  // the next tile's first PV overwrites O after these reads
-    if (row_ok && d.nparts > 1 && hh == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(m_ref, lrow));
+    if (row_ok && d.nparts > 1 && hh == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(m, lrow));
+}
+
+// MMA side of a tile (the MMA warp; lane 0 issues).  K_i is in ring slot
+// gbase + i, V_i in slot gbase + i + 1 (skewed slots, see produce_tc).
+template <int D>
+__device__ __forceinline__ void tc_mma(Smem<D, false>& sm, const Desc& d, int lane, uint32_t gbase, int ntiles,
+                                       TcState& st, volatile int* abort, bool pair) {
+    constexpr uint32_t kIdS = umma_idesc_bf16(kTcRows, kTcT, false);
+    constexpr uint32_t kIdPV = umma_idesc_bf16(kTcRows, D, true);
+    constexpr int kSlab = kTcT * 128;
+    if (lane == 0) {
+        const uint32_t qa = smem_u32(sm.qbuf);
+        // S_i = Q K_i^T into S buffer (k + i) & 1
+        auto issue_s = [&](int i) -> bool {
+            const uint32_t gi = gbase + i;
+            const int s = (int)(gi % kRingSlots);
+            if (!mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort)) return false;
+            tc_fence_after();
+            const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
+            const uint32_t dst = st.tmem + kTmemS + ((st.k + i) & 1) * kTcT;
+#pragma unroll
+            for (int xs = 0; xs < 2; ++xs)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    umma_ss(dst, umma_desc_sw128(qa + xs * kSlab + kk * 32, 0),
+                            umma_desc_sw128(kb + xs * kSlab + kk * 32, 0), kIdS, (xs | kk) != 0);
+            umma_commit(&sm.sbar[(st.k + i) & 1]);
+            return true;
+        };
+        // Q written; the previous tile's last PV (which read the S buffer S_0
+        // reuses) completed before the softmax warps wrote this Q
+        bool ok = mbar_wait(&sm.qbar, st.tiles & 1, abort) && issue_s(0);
+        if (ok) {
+            // slot gbase holds K_0 alone: free once S_0 has read it
+            const int s0 = (int)(gbase % kRingSlots);
+            mbar_arrive(&sm.empty[s0], kCWarps - 1);
+            umma_commit(&sm.empty[s0]);
+        }
+        for (int i = 0; ok && i < ntiles; ++i) {
+            const uint32_t k = st.k + i;
+            const int b = (int)(k & 1);
+            if (i + 1 < ntiles) {
+                // S_{k+1} reuses the buffer whose P_{k-1} PV_{k-1} reads
+                if (i >= 1) ok = mbar_wait(&sm.obar[(k - 1) & 1], ((k - 1) >> 1) & 1, abort);
+                ok = ok && issue_s(i + 1);
+            }
+            const uint32_t gv = gbase + i + 1;
+            const int sv = (int)(gv % kRingSlots);
+            ok = ok && mbar_wait(&sm.full[sv], (gv / kRingSlots) & 1, abort);
+            if (!ok) break;
+            const uint32_t vb = smem_u32(&sm.kv[sv][1][0]);
+            // PV_k, each half once its four warps have written P
+            for (int h = 0; h < 2; ++h) {
+                ok = mbar_wait(&sm.pready[h], k & 1, abort);
+                if (!ok) break;
+                tc_fence_after();
+                // k-step kk of half h: tokens 64 h + 16 kk .. + 15 -- block
+                // 4 h + kk of a paired V stage ([slab][16 rows] at 4 KB steps)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t bd = pair ? umma_desc_sw128(vb + (4 * h + kk) * 4096, 2048)
+                                             : umma_desc_sw128(vb + (64 * h + 16 * kk) * 128, kSlab);
+                    umma_ts(st.tmem + kTmemO + h * D, st.tmem + kTmemS + b * kTcT + 64 * h + 8 * kk, bd, kIdPV,
+                            i > 0 || kk > 0);
+                }
+            }
+            if (!ok) break;
+            umma_commit(&sm.obar[b]);
+            // the slot's last arrival: once PV_k has read V_k (S_{k+1}, issued
+            // earlier, has read K_{k+1})
+            mbar_arrive(&sm.empty[sv], kCWarps - 1);
+            umma_commit(&sm.empty[sv]);
+        }
+    }
+    st.k += ntiles;
+    ++st.tiles;
+    __syncwarp();
+}
+
+// The MMA warp's item loop: it follows the item sequence (and the ring's
+// stage count) and serves the tcgen05 tiles.
+template <int D, bool F8>
+__device__ __forceinline__ void mma_warp(Smem<D, F8>& sm, const AttnParams& p, int lane, TcState& tc) {
+    volatile int* abort = &sm.abort;
+    uint32_t g = 0;
+    for (int islot = 0;; ++islot) {
+        const int si = islot % kSlots;
+        if (!mbar_wait(&sm.ifull[si], (islot / kSlots) & 1, abort)) break;
+        const Desc d = sm.desc[si];
+        if (d.kind == KIND_END) break;
+        const int T = d.kind == KIND_TC ? kTcT : kTileT;
+        const int ntiles = (d.t_end + T - 1) / T - d.t_begin / T;
+        if constexpr (!F8) {
+            if (d.kind == KIND_TC) tc_mma<D>(sm, d, lane, g, ntiles, tc, abort, p.tc_pair != 0);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.iempty[si]);
+        g += (uint32_t)(d.kind == KIND_TC ? ntiles + 1 : ntiles);
+    }
+}
+
+// The helper TMA warp's item loop: it follows the item sequence (and the
+// ring's stage count) and issues the V copies of the tcgen05 tiles.
+template <int D, bool F8>
+__device__ __forceinline__ void helper_warp(Smem<D, F8>& sm, const TMaps* tm, const AttnParams& p, int lane) {
+    volatile int* abort = &sm.abort;
+    uint32_t g = 0;
+    int unused = 0;
+    for (int islot = 0;; ++islot) {
+        const int si = islot % kSlots;
+        if (!mbar_wait(&sm.ifull[si], (islot / kSlots) & 1, abort)) break;
+        const Desc d = sm.desc[si];
+        if (d.kind == KIND_END) break;
+        const int T = d.kind == KIND_TC ? kTcT : kTileT;
+        const int ntiles = (d.t_end + T - 1) / T - d.t_begin / T;
+        if (d.kind == KIND_TC) {
+            uint32_t gg = g;
+            produce_tc<D, F8>(sm, tm, p, d, si, lane, gg, unused, true);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.iempty[si]);
+        g += (uint32_t)(d.kind == KIND_TC ? ntiles + 1 : ntiles);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1600,6 +1769,7 @@ __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, i
         if (d.kind == KIND_END) break;
         const int T = d.kind == KIND_TC ? kTcT : kTileT;  // tokens per stage
         const int ntiles = (d.t_end + T - 1) / T - d.t_begin / T;
+        const int nslots = d.kind == KIND_TC ? ntiles + 1 : ntiles;  // tcgen05 tiles: skewed K/V slots
         if (d.kind == KIND_TC) {
             if constexpr (TC) tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, tc, abort);
         } else if constexpr (F8) {
@@ -1616,7 +1786,7 @@ __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, i
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.iempty[si]);  // this warp is done with the descriptor
-        g += (uint32_t)ntiles;
+        g += (uint32_t)nslots;
     }
 }
 
@@ -1629,8 +1799,13 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
 // TC: the variant with tcgen05 tiles (head_dim 128, bf16), launched only for
 // batches that may hold a 128-row tile -- the other variant's item code keeps
 // its register allocation free of the tile's.
+// Threads of a CTA: eight consumer warps, the producer warp, and in the
+// variant with tcgen05 tiles the MMA warp and the helper TMA warp.
+template <bool TC>
+constexpr int kThreadsOf = TC ? kThreads + 64 : kThreads;
+
 template <int D, int GD, bool F8, bool TC>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreadsOf<TC>, 1)
     paged_attention_kernel(const __grid_constant__ TMaps tm, const __grid_constant__ AttnParams p) {
     static_assert(!TC || Smem<D, F8>::kTC, "tcgen05 tiles need the head_dim 128 bf16 layout");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1651,19 +1826,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&sm.ifull[i], 1);
-            mbar_init(&sm.iempty[i], kCWarps);
+            mbar_init(&sm.iempty[i], kCWarps + (TC ? 2 : 0));  // + the MMA and helper warps
         }
         if constexpr (TC) {
             mbar_init(&sm.sbar[0], 1);
             mbar_init(&sm.sbar[1], 1);
             mbar_init(&sm.obar[0], 1);
             mbar_init(&sm.obar[1], 1);
-            mbar_init(&sm.pready, kCWarps);
+            mbar_init(&sm.pready[0], kCWarps / 2);
+            mbar_init(&sm.pready[1], kCWarps / 2);
             mbar_init(&sm.xbar, kCWarps);
             mbar_init(&sm.ebar, kCWarps);
             mbar_init(&sm.qbar, kCWarps);
             mbar_init(&sm.tdone, 1);
-            mbar_init(&sm.dbar, kCWarps);
+            mbar_init(&sm.dbar, kCWarps + 1);
         }
         sm.abort = 0;
         fence_mbar_init();
@@ -1673,7 +1849,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_launch();  // the combine kernel may be scheduled; it waits for this grid to finish
     if (warp == kCWarps) {
         producer<D, F8>(sm, &tm, p, lane);
+    } else if (TC && warp == kCWarps + 2) {
+        if constexpr (TC) helper_warp<D, F8>(sm, &tm, p, lane);
     } else {
+        // consumer warps 0-7 and (tcgen05 variant) the MMA warp kCWarps + 1
+        const bool mma = TC && warp == kCWarps + 1;
         TcState tc{0u, 0u, 0u, 0u};
         bool use_tc = false;
         if constexpr (TC) {
@@ -1683,17 +1863,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (use_tc) {
                 if (warp == 0) tmem_alloc(&sm.tmem, kTmemCols);
                 tc_fence_before();
-                named_bar(1, kCThreads);
+                named_bar(1, kCThreads + 32);  // consumers + the MMA warp, once
                 tc_fence_after();
                 tc.tmem = sm.tmem;
             }
         }
-        consumer<D, GD, F8, TC>(sm, p, warp, lane, tc);
+        if (mma) {
+            if constexpr (TC) mma_warp<D, F8>(sm, p, lane, tc);
+        } else {
+            consumer<D, GD, F8, TC>(sm, p, warp, lane, tc);
+        }
         if constexpr (TC) {
             if (use_tc) {
                 // every MMA has completed and every warp is done with tensor memory
                 // (bounded by time alone: an abort must not skip the release)
-                if (warp == 0 && lane == 0) {
+                if (mma && lane == 0) {
                     umma_commit(&sm.tdone);
                     if (!mbar_wait_ns(&sm.tdone, 0)) sm.abort = 1;
                 }
@@ -1733,7 +1917,8 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
     const cudaError_t e =
-        host::launch_pdl(paged_attention_kernel<D, GD, F8, TC>, dim3((unsigned)grid), dim3(kThreads), smem, st, tm, p);
+        host::launch_pdl(paged_attention_kernel<D, GD, F8, TC>, dim3((unsigned)grid), dim3(kThreadsOf<TC>), smem, st,
+                         tm, p);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -417,15 +417,32 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     const bool decode_fma = !fp8 && GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
     const bool tc = !fp8 && head_dim == 128 && block_size >= 16 && P % kTcT == 0 && !decode_fma &&
                     !(flags & PKV_ATTN_NO_TCGEN05) && (long long)max_q_len * G >= kTcRows;
+    bool tc_pair = false;
     if (tc) {
-        // [num_blocks][n_kv][bs][2 slabs][64] with one slab of min(bs, 128) rows per box
         const uint64_t row = 256;
-        const uint64_t dims[5] = {64, 2, (uint64_t)block_size, (uint64_t)num_kv_heads, (uint64_t)num_blocks};
-        const uint64_t strides[4] = {128, row, (uint64_t)block_size * row, (uint64_t)num_kv_heads * block_size * row};
-        const uint32_t box[5] = {64, 1, (uint32_t)(block_size < kTcT ? block_size : kTcT), 1, 1};
-        if (host::encode_tiled(&tm.k_tc, k_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
-            host::encode_tiled(&tm.v_tc, v_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-            return PKV_ERR_CUDA;
+        const uint64_t blk = (uint64_t)block_size * row, head = (uint64_t)num_kv_heads * blk;
+        // K (and V unless paired): [num_blocks][n_kv][bs][2 slabs][64], one slab
+        // of min(bs, 128) rows per box
+        {
+            const uint64_t dims[5] = {64, 2, (uint64_t)block_size, (uint64_t)num_kv_heads, (uint64_t)num_blocks};
+            const uint64_t strides[4] = {128, row, blk, head};
+            const uint32_t box[5] = {64, 1, (uint32_t)(block_size < kTcT ? block_size : kTcT), 1, 1};
+            if (host::encode_tiled(&tm.k_tc, k_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) ||
+                host::encode_tiled(&tm.v_tc, v_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+                return PKV_ERR_CUDA;
+        }
+        // V with block_size 16: the view [num_blocks][n_kv][2 slabs][bs][64]
+        // (the slab outside the row), one box = both slabs of a block
+        if (block_size == 16) {
+            const uint64_t dims[5] = {64, 16, 2, (uint64_t)num_kv_heads, (uint64_t)num_blocks};
+            const uint64_t strides[4] = {row, 128, blk, head};
+            const uint32_t box[5] = {64, 16, 2, 1, 1};
+            CUtensorMap v2;
+            if (host::encode_tiled(&v2, v_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B) == 0) {
+                tm.v_tc = v2;
+                tc_pair = true;
+            }
+        }
     } else {
         memset(&tm.k_tc, 0, sizeof(tm.k_tc));
         memset(&tm.v_tc, 0, sizeof(tm.v_tc));
@@ -488,6 +505,7 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     ap.k_scale = k_scale;
     ap.v_scale = v_scale;
     ap.tc = tc ? 1 : 0;
+    ap.tc_pair = tc_pair ? 1 : 0;
     const int rc2 = fp8                ? dispatch_attention_fp8_d128(tm, ap, w.max_items, st)
                     : head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tc, tm, ap, w.max_items, st)
                                       : dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);

@@ -139,16 +139,17 @@ __device__ __forceinline__ void mma_f16_16816(float* c, uint32_t a0, uint32_t a1
 }
 
 // ---- 5th-generation tensor cores (tcgen05, accumulators in tensor memory) ----
-// Shared-memory matrix descriptor, 128-byte swizzle, rows of 128 bytes, 8-row
-// groups 1024 bytes apart (stride byte offset); descriptor version 1 (bits
-// 46-48), swizzle mode 2 (bits 61-63).
+// Shared-memory matrix descriptor, 128-byte swizzle, rows of 128 bytes in
+// 1024-byte 8-row groups (swizzle atoms) whose starts are `sbo` bytes apart
+// (stride byte offset); descriptor version 1 (bits 46-48), swizzle mode 2
+// (bits 61-63).
 //   K-major operand: one 64-element (bf16) slab of K per 128-byte row; the
 //     leading byte offset is unused.  A k-step of 16 advances the start by 32 B.
 //   MN-major operand: 64 MN-elements per 128-byte row, 8 K-rows per group;
 //     `lbo` is the byte distance between 64-wide MN slabs.
-__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo) {
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo = 1024) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-           ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) | (2ull << 61);
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), bf16 A

@@ -167,9 +167,12 @@ def main(argv=None):
     ap.add_argument("--partition", type=int, default=0)
     ap.add_argument("--flags", type=int, default=0)
     ap.add_argument("--fp8", action="store_true", help="e4m3 KV pools (random codes, per-head scales)")
+    ap.add_argument("--ctx", type=int, default=0, help="decode context of the long workload (0 = 131072)")
     a = ap.parse_args(argv)
     if a.workload == "mix" and a.batch:
         w = workloads.mix(B=a.batch)
+    elif a.workload == "long" and a.ctx:
+        w = workloads.long_context(ctx=a.ctx)
     else:
         w = workloads.FULL[a.workload]()
     ds = DeviceStep(w, partition_tokens=a.partition or None, flags=a.flags,
