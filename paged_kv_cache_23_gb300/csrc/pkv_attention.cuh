@@ -130,7 +130,10 @@ struct Smem {
     // tcgen05 tiles: S ready, PV done (per buffer), P written (per half),
     // half-row merge, tile entry, Q written, final drain, warps done with
     // tensor memory
-    uint64_t sbar[2], obar[2], pready[2], xbar, ebar, qbar, tdone, dbar;
+    // P ready is double-buffered by stage parity: the softmax warps may finish
+    // stages k and k + 1 before the MMA warp waits for stage k's phase (it
+    // issues S_{k+1} first), and one barrier would then have moved on twice
+    uint64_t sbar[2], obar[2], pready[2][2], xbar, ebar, qbar, tdone, dbar;
     uint32_t tmem;
     float red[kTC ? 2 : 1][2][kTcRows];                       // [m, l][half][row]
 };
@@ -1186,7 +1189,7 @@ __device__ __forceinline__ void tc_item(Smem<D, false>& sm, const AttnParams& p,
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.pready[hh]);
+        if (lane == 0) mbar_arrive(&sm.pready[hh][k & 1]);
     }
     st.k += ntiles;
     ++st.tiles;
@@ -1301,7 +1304,7 @@ __device__ __forceinline__ void tc_mma(Smem<D, false>& sm, const Desc& d, int la
             const uint32_t vb = smem_u32(&sm.kv[sv][1][0]);
             // PV_k, each half once its four warps have written P
             for (int h = 0; h < 2; ++h) {
-                ok = mbar_wait(&sm.pready[h], k & 1, abort);
+                ok = mbar_wait(&sm.pready[h][k & 1], (k >> 1) & 1, abort);
                 if (!ok) break;
                 tc_fence_after();
                 // k-step kk of half h: tokens 64 h + 16 kk .. + 15 -- block
@@ -1833,8 +1836,8 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
             mbar_init(&sm.sbar[1], 1);
             mbar_init(&sm.obar[0], 1);
             mbar_init(&sm.obar[1], 1);
-            mbar_init(&sm.pready[0], kCWarps / 2);
-            mbar_init(&sm.pready[1], kCWarps / 2);
+            for (int h = 0; h < 2; ++h)
+                for (int e = 0; e < 2; ++e) mbar_init(&sm.pready[h][e], kCWarps / 2);
             mbar_init(&sm.xbar, kCWarps);
             mbar_init(&sm.ebar, kCWarps);
             mbar_init(&sm.qbar, kCWarps);

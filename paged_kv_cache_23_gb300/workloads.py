@@ -429,6 +429,27 @@ def long_context(B: int = 8, ctx: int = 131072, chunk: int = 512, chunk_prefix: 
                    meta=dict(seed=seed, ctx=ctx, chunk=chunk, chunk_prefix=chunk_prefix))
 
 
+def concat(a: Workload, b: Workload) -> Workload:
+    """One batch holding a's sequences then b's, over one pool (b's blocks
+    after a's); same head shape and block size.  Acceptance inputs are
+    dropped (their shapes differ between workloads)."""
+    assert (a.n_q, a.n_kv, a.head_dim, a.block_size) == (b.n_q, b.n_kv, b.head_dim, b.block_size)
+    nb = a.num_blocks
+    mb = max(a.max_blocks, b.max_blocks)
+    bt = np.full((a.num_seqs + b.num_seqs, mb), -1, np.int32)
+    bt[: a.num_seqs, : a.max_blocks] = a.block_tables
+    bt[a.num_seqs:, : b.max_blocks] = np.where(b.block_tables >= 0, b.block_tables + nb, -1)
+    cow = np.concatenate([a.cow.reshape(-1, 2), b.cow.reshape(-1, 2) + nb]).astype(np.int32)
+    return Workload(name=f"{a.name}+{b.name}", n_q=a.n_q, n_kv=a.n_kv, head_dim=a.head_dim, block_size=a.block_size,
+                    k_cache=np.concatenate([a.k_cache, b.k_cache]), v_cache=np.concatenate([a.v_cache, b.v_cache]),
+                    block_tables=bt, seq_lens=np.concatenate([a.seq_lens, b.seq_lens]),
+                    q_lens=np.concatenate([a.q_lens, b.q_lens]),
+                    append_lens=np.concatenate([a.append_lens, b.append_lens]),
+                    k_new=np.concatenate([a.k_new, b.k_new]), v_new=np.concatenate([a.v_new, b.v_new]), cow=cow,
+                    q=np.concatenate([a.q, b.q]), scale=a.scale, partition_tokens=a.partition_tokens,
+                    meta=dict(parts=[a.name, b.name]))
+
+
 # The five workloads at full size, by name.
 FULL = {
     "tiny": lambda: tiny(0),

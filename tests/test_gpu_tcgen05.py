@@ -147,3 +147,32 @@ def test_q_len_above_the_host_bound_is_flagged():
     out = wl.bf16_bits_to_f32(bf16_to_bits(ds.out))
     q0 = int(w.q_lens[:-1].sum())
     assert np.isnan(out[q0:]).all() and np.isfinite(out[:q0]).all()
+
+
+def spec_w(n_q, n_kv, k, lo=200, hi=1500, B=4, bs=16, seed=0):
+    return wl.spec(B=B, lo=lo, hi=hi, k=k, vocab=97, seed=seed, n_q=n_q, n_kv=n_kv, d=128, bs=bs)
+
+
+def test_mixed_batch_of_row_kinds():
+    # decode rows, speculative rows (mma.sync) and 128-row tcgen05 tiles in one launch
+    a = wl.long_context(B=3, ctx=700, chunk=70, chunk_prefix=600, partition_tokens=256, seed=12, n_q=32, n_kv=8,
+                        d=128, bs=16)
+    b = spec_w(32, 8, 5, lo=100, hi=900, B=3, seed=13)
+    # concatenate the two workloads' sequences over one pool
+    ds, _, _ = run_and_check(wl.concat(a, b))
+    assert tiles_used(ds) == 1
+
+
+def test_back_to_back_tile_launches_never_time_out():
+    # hundreds of launches with many short tile items per CTA: the MMA warp's
+    # barriers must never see a phase run ahead of it (a bounded wait would
+    # give up and set PKV_STATUS_TIMEOUT)
+    w = chunk(32, 8, 256, prefix=3000, decodes=8, ctx=4000, seed=15)
+    ds = DeviceStep(w, partition_tokens=128)
+    ds.cache_ops()
+    ds.status.zero_()
+    for _ in range(300):
+        ds.attention()
+    torch.cuda.synchronize()
+    assert tiles_used(ds) == 1
+    assert int(ds.status.item()) == 0, pkv.status_bits(int(ds.status.item()))
