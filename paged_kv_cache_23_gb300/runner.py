@@ -99,6 +99,18 @@ class DeviceStep:
         """The step's inputs as one pinned host buffer in the arena layout."""
         return self._host_arena.pin_memory()
 
+    def arena_views(self, arena: torch.Tensor) -> dict:
+        """The per-step input tensors as views of `arena` (a device buffer of
+        arena_bytes in the same layout), for double-buffered inputs."""
+        return {name: arena[o:o + nbytes].view(dt).view(shape) for name, o, nbytes, shape, dt in self._layout}
+
+    def bind(self, views: dict, out: torch.Tensor | None = None):
+        """Point the step's inputs (and optionally its output) at other buffers."""
+        for name, t in views.items():
+            setattr(self, name, t)
+        if out is not None:
+            self.out = out
+
     def upload(self, host: torch.Tensor, stream=None):
         """One host -> device copy of every per-step input (q, new K/V rows,
         block tables, lengths, copy-on-write pairs)."""
