@@ -95,7 +95,46 @@ __device__ __forceinline__ int last_le(const int* a, int n, int x) {
     return lo;
 }
 
-constexpr int kPlanSmemSeqs = 2048;  // batches up to this size search shared-memory copies
+constexpr int kPlanSmemSeqs = 1024;  // batches up to this size keep their records in shared memory
+
+// Block-wide exclusive scans of K ints per thread at once (blockDim.x ==
+// 1024): one pair of barriers for all K.  `tmp` holds 32 * K ints; v is
+// replaced by its exclusive prefixes and tot receives the block sums.
+template <int K>
+__device__ __forceinline__ void block_scan_k(int (&v)[K], int (&tot)[K], int* tmp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        x[k] = v[k];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, x[k], o);
+            if (lane >= o) x[k] += y;
+        }
+        if (lane == 31) tmp[warp * K + k] = x[k];
+    }
+    __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            int w = tmp[lane * K + k];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, w, o);
+                if (lane >= o) w += y;
+            }
+            tmp[lane * K + k] = w;  // inclusive prefix over warps
+        }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+        tot[k] = tmp[31 * K + k];
+        v[k] = (warp > 0 ? tmp[(warp - 1) * K + k] : 0) + x[k] - v[k];
+    }
+    __syncthreads();
+}
 constexpr int kAutoPMax = 8192;       // automatic partition length: upper bound
 constexpr int kAutoItemsPerSM = 3;    // automatic partition length: target partitions per SM
 
@@ -110,15 +149,20 @@ constexpr int kAutoItemsPerSM = 3;    // automatic partition length: target part
 //           by binary search in the prefix sums -- consecutive threads write
 //           consecutive 16-byte items, so the stores coalesce.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams pp) {
-    __shared__ int tmp[32];
+    __shared__ int tmp[32 * 2];
     __shared__ int hist[kTailBuckets];
-    __shared__ int s_q0[kPlanSmemSeqs], s_mq[kPlanSmemSeqs], s_full[kPlanSmemSeqs];
+    __shared__ int s_q0[kPlanSmemSeqs], s_mq[kPlanSmemSeqs], s_full[kPlanSmemSeqs], s_flag[kPlanSmemSeqs];
+    __shared__ int4 s_seq[kPlanSmemSeqs];
     const int tid = threadIdx.x;
     const int n = pp.num_seqs;
     const bool small = n <= kPlanSmemSeqs;
     int* a_q0 = small ? s_q0 : pp.seq_q0;
     int* a_mq = small ? s_mq : pp.seq_mq;
     int* a_full = small ? s_full : pp.seq_full;
+    int* a_flag = small ? s_flag : pp.seq_flag;
+    const int4* a_seq = small ? s_seq : pp.seqs;  // per-sequence records of pass A (global copy always written)
+    // this thread's first sequence, read once for the partition choice and pass A
+    const int L0 = tid < n ? pp.seq_lens[tid] : 0, ql0 = tid < n ? pp.q_lens[tid] : 0;
     if (tid < kTailBuckets) hist[tid] = 0;
     // Programmatic launch: the previous kernel of the stream may still run
     // while passes A and B1-B3 do.  They read only seq_lens and q_lens, which
@@ -137,7 +181,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         // switches, and the longest-first order keeps the queue balanced
         long long tok = 0, tok_mq = 0;
         for (int b = tid; b < n; b += kPlanThreads) {
-            const int L = pp.seq_lens[b], ql = pp.q_lens[b];
+            const int L = b == tid ? L0 : pp.seq_lens[b], ql = b == tid ? ql0 : pp.q_lens[b];
             if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len || ql > pp.max_q_len) continue;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
             const bool multi = multi_query_kind(sh.kind) || ql > 1;
@@ -146,10 +190,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             if (multi) tok_mq += t;
         }
         // block sums in units of 16 tokens (fit an int for any accepted batch)
-        int tot16, mq16;
         const int cap = (1 << 30) / kPlanThreads;
-        block_exclusive_scan_1024((int)min(tok >> 4, (long long)cap), tmp, &tot16);
-        block_exclusive_scan_1024((int)min(tok_mq >> 4, (long long)cap), tmp, &mq16);
+        int v2[2] = {(int)min(tok >> 4, (long long)cap), (int)min(tok_mq >> 4, (long long)cap)}, t2[2];
+        block_scan_k<2>(v2, t2, tmp);
+        const int tot16 = t2[0], mq16 = t2[1];
         const long long T = (long long)tot16 << 4;
         // multi-query items cost more compute per token: a batch made of them
         // (speculative verification) balances better with twice the items
@@ -166,8 +210,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         const int b = base + tid;
         int qlc = 0, flag = 0, L = 0, ql = 0;
         if (b < n) {
-            L = pp.seq_lens[b];
-            ql = pp.q_lens[b];
+            L = b == tid ? L0 : pp.seq_lens[b];
+            ql = b == tid ? ql0 : pp.q_lens[b];
             if (L < 0 || (long long)L > (long long)pp.max_blocks * pp.bs || L > pp.max_seq_len)
                 flag |= PKV_STATUS_BAD_SEQLEN;
             if (ql < 0 || ql > L || ql > pp.max_q_len) flag |= PKV_STATUS_BAD_QLEN;
@@ -195,20 +239,21 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
                     nmq = mq_parts_of(L, ql, sh.qt, P) * ngroups;
                 }
             }
-            pp.seqs[b] = make_int4(L, ql, q0, sh.kind | (sh.hps << 4) | (sh.wph << 8) | (sh.qt << 12));
-            pp.seq_flag[b] = flag;
+            const int4 rec = make_int4(L, ql, q0, sh.kind | (sh.hps << 4) | (sh.wph << 8) | (sh.qt << 12));
+            pp.seqs[b] = rec;
+            if (small) s_seq[b] = rec;
+            a_flag[b] = flag;
         }
         carry += tot;
-        int tm, tf;
-        const int exm = block_exclusive_scan_1024(nmq, tmp, &tm);
-        const int exf = block_exclusive_scan_1024(nfull, tmp, &tf);
+        int v2[2] = {nmq, nfull}, t2[2];
+        block_scan_k<2>(v2, t2, tmp);
         if (b < n) {
             a_q0[b] = q0;
-            a_mq[b] = c_mq + exm;
-            a_full[b] = c_full + exf;
+            a_mq[b] = c_mq + v2[0];
+            a_full[b] = c_full + v2[1];
         }
-        c_mq += tm;
-        c_full += tf;
+        c_mq += t2[0];
+        c_full += t2[1];
     }
     // tail buckets -> first slot of each bucket (exclusive scan)
     any_tc = __syncthreads_or(any_tc);
@@ -226,9 +271,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     __syncthreads();
     // pass B1: one thread per sequence -- decode tails and invalid sequences
     for (int b = tid; b < n; b += kPlanThreads) {
-        const int4 sq = pp.seqs[b];
+        const int4 sq = a_seq[b];
         const int L = sq.x, ql = sq.y;
-        if (pp.seq_flag[b]) continue;  // its rows are written NaN after the wait below
+        if (a_flag[b]) continue;  // its rows are written NaN after the wait below
         if (ql != 1 || multi_query_kind(sq.w & 15)) continue;  // multi-query tiles are counted in pass B2
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
         const int np = ceil_div(L, P);
@@ -240,7 +285,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     for (int it = tid; it < c_mq; it += kPlanThreads) {
         const int b = last_le(a_mq, n, it);
         int li = it - a_mq[b];
-        const int4 sq = pp.seqs[b];
+        const int4 sq = a_seq[b];
         const int L = sq.x, ql = sq.y, QT = (sq.w >> 12) & 4095;
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
         for (int qt = 0; qt * QT < ql; ++qt) {
@@ -267,8 +312,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     pdl_wait();
     // rows of an invalid sequence are NaN (inside the q/out extent)
     for (int b = tid; b < n; b += kPlanThreads) {
-        if (!pp.seq_flag[b]) continue;
-        const int4 sq = pp.seqs[b];
+        if (!a_flag[b]) continue;
+        const int4 sq = a_seq[b];
         const int ql = sq.y, q0 = sq.z;
         const int qlc = ql > 0 ? min(ql, pp.total_q) : 0;
         const int rows = min(qlc, pp.total_q - q0);
@@ -282,9 +327,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         int np = 0;
         if (r < carry) {
             const int b = last_le(a_q0, n, r);
-            const int4 sq = pp.seqs[b];
+            const int4 sq = a_seq[b];
             const int L = sq.x, ql = sq.y, q0 = sq.z;
-            if (pp.seq_flag[b] == 0 && r - q0 < ql) {
+            if (a_flag[b] == 0 && r - q0 < ql) {
                 // query tile of row r; a decode row is a tile of one query
                 const int QT = (sq.w >> 12) & 4095;
                 const int qt = (r - q0) / QT;
