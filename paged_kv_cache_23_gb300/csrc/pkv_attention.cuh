@@ -1683,9 +1683,34 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
         if (np <= 1) continue;
         const float2* ml = c.part_ml + orow * c.np_max;
         const float* src = c.part_o + orow * c.np_max * D + lane * V;
-        // statistics: lane j holds partitions j, j + 32, ...
-        float M = -INFINITY;
-        for (int pp = lane; pp < np; pp += 32) M = fmaxf(M, __ldcg(&ml[pp].x));
+        // the first U partitions' outputs are loaded together with the
+        // statistics (they do not depend on them): two dependent rounds of
+        // loads for rows of up to U partitions
+        float a[U][V];
+        auto load_o = [&](int p0) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (p0 + u < np) {
+                    const float* sp = src + (long long)(p0 + u) * D;
+                    if constexpr (V == 4) {
+                        const float4 t = __ldcg(reinterpret_cast<const float4*>(sp));
+                        a[u][0] = t.x;
+                        a[u][1] = t.y;
+                        a[u][2] = t.z;
+                        a[u][3] = t.w;
+                    } else {
+                        const float2 t = __ldcg(reinterpret_cast<const float2*>(sp));
+                        a[u][0] = t.x;
+                        a[u][1] = t.y;
+                    }
+                }
+            }
+        };
+        // statistics: lane j holds partitions j, j + 32, ... (the first 32 kept in registers)
+        const float2 s0 = lane < np ? __ldcg(ml + lane) : make_float2(-INFINITY, 0.f);
+        load_o(0);
+        float M = s0.x;
+        for (int pp = lane + 32; pp < np; pp += 32) M = fmaxf(M, __ldcg(&ml[pp].x));
 #pragma unroll
         for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, o));
         const float mu = M == -INFINITY ? 0.f : M;
@@ -1696,31 +1721,13 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
         for (int p0 = 0; p0 < np; p0 += 32) {
             float w = 0.f;
             if (p0 + lane < np) {
-                const float2 s = __ldcg(ml + p0 + lane);
+                const float2 s = p0 == 0 ? s0 : __ldcg(ml + p0 + lane);
                 w = exp2f(s.x - mu);
                 L += s.y * w;
             }
             const int n = min(32, np - p0);
             for (int u0 = 0; u0 < n; u0 += U) {
-                // U partitions' loads in flight before any of them is used
-                float a[U][V];
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    if (u0 + u < n) {
-                        const float* sp = src + (long long)(p0 + u0 + u) * D;
-                        if constexpr (V == 4) {
-                            const float4 t = __ldcg(reinterpret_cast<const float4*>(sp));
-                            a[u][0] = t.x;
-                            a[u][1] = t.y;
-                            a[u][2] = t.z;
-                            a[u][3] = t.w;
-                        } else {
-                            const float2 t = __ldcg(reinterpret_cast<const float2*>(sp));
-                            a[u][0] = t.x;
-                            a[u][1] = t.y;
-                        }
-                    }
-                }
+                if (p0 + u0 > 0) load_o(p0 + u0);  // (the first batch is in flight already)
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const float wu = __shfl_sync(kFull, w, (u0 + u) & 31);
