@@ -167,7 +167,8 @@ WORKLOADS = {
                  "greedy acceptance over logits [32, 6, 128256] fp32", batch=32, seq="U[2048, 8192]",
                  max_seq_len=None),
     "long": dict(desc="long context + chunk, " + SHAPE + ": 8 decodes of 131072 tokens + one 512-query chunk "
-                 "over 8192 + 512, in one call", batch=9, seq="131072 (x8) and 8704", max_seq_len=None),
+                 "over 8192 + 512, in one call, split-KV partitions of 4096 tokens", batch=9,
+                 seq="131072 (x8) and 8704", max_seq_len=None, partition=4096),
     "mix_fp8": dict(desc="continuous-batching mix over an FP8 (e4m3) KV cache with per-kv-head scales, "
                     + SHAPE + ": batch 256, log-normal ctx (median 1024, sigma 1, clip [16, 32768]), 50% share a "
                     "2048-token prefix (CoW), q_len 1, 1 appended token/seq", batch=256,
@@ -351,7 +352,9 @@ def run_gpu(args):
     from paged_kv_cache_23_gb300 import workloads as wl
     pools = wl.fp8_pools(w, rank) if spec.get("fp8") else None
     b = step_bytes_of(w, pools is not None)
-    ds = DeviceStep(w, device=device, max_seq_len=spec["max_seq_len"], partition_tokens=args.partition,
+    # the workload's own partition length where its definition fixes one (--partition overrides)
+    part = args.partition or spec.get("partition", 0)
+    ds = DeviceStep(w, device=device, max_seq_len=spec["max_seq_len"], partition_tokens=part,
                     flags=args.flags, fp8=pools)
     stream = torch.cuda.current_stream(device)
 
