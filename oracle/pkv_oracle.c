@@ -420,7 +420,7 @@ int oracle_spec_accept_greedy(int32_t *accepted, int32_t *next_token, int32_t *a
 
 /*
  * FP8 KV cache ([KVC] 03 "KV cache quantization": store K and V in FP8,
- * 1 byte per value, formats e4m3 and e5m2; this build takes e4m3).
+ * 1 byte per value, formats e4m3 and e5m2; this library takes e4m3).
  *
  * e4m3 (the "fn" variant: no infinities): sign bit, 4 exponent bits with bias
  * 7, 3 mantissa bits; exponent field 0 holds subnormals m * 2^-9; code
@@ -659,7 +659,7 @@ int oracle_spec_accept_sample(int32_t *accepted, int32_t *next_token, const floa
  * whole prefix up to that block; [SE] 31.3: the key must cover the token
  * content and the computation version, and only a shared beginning counts).
  *
- * The hash is this build's own definition (the pages fix none), 128 bits as two
+ * The hash is this library's own definition (the pages fix none), 128 bits as two
  * 64-bit lanes L = 0, 1; salt = the caller's computation-version key:
  *   mix(x):  x ^= x >> 32; x *= M; x ^= x >> 29; x *= M; x ^= x >> 32,
  *            M = 0xD6E8FEB86659FD93 (arithmetic mod 2^64)

@@ -2,7 +2,7 @@
 
 Bit-exact for slot mapping, KV append, copy-on-write copies, gather and the
 acceptance integers; attention outputs within |gpu - ref| <= 1e-2 + 1e-2*|ref|
-(bf16 in, fp32 accumulate, bf16 out), the tolerance the benchmark spec states.
+(bf16 in, fp32 accumulate, bf16 out), the stated tolerance of the attention outputs.
 """
 import math
 

@@ -99,7 +99,7 @@ def test_scenario_against_oracle():
     table = pkv.PrefixTable(1024)
     cache = oracle.PrefixCache()
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    # round 1: the first half inserts all of its full blocks (many shared keys)
+    # phase 1: the first half inserts all of its full blocks (many shared keys)
     half = B // 2
     blocks = (np.arange(B * maxb, dtype=np.int32) + 1000).reshape(B, maxb)
     first = np.zeros(B, np.int32)
@@ -116,7 +116,7 @@ def test_scenario_against_oracle():
         assert all(r[b, j] == blk for b, j, _ in lst)
         cache.d[k][0] = blk
     assert len(gt) == len(cache.d) and int(st.item()) == 0
-    # round 2: everyone looks up; hits stop at the first miss
+    # phase 2: everyone looks up; hits stop at the first miss
     bt_gpu = t32(np.full((B, maxb), -1))
     cached = t32(np.zeros(B))
     pkv.prefix_lookup(table, h_dev, t32(lens), bs, bt_gpu, cached)
