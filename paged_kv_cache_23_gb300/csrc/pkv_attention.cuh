@@ -154,11 +154,15 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 // Index of the 128-byte shared-memory row that holds (head h of the stage,
-// token r of the tile, 64-column box x): the TMA boxes of one stage are
-// [op][head][rows of the op][box], one op per block when block_size < 16.
-// Rows per op are a power of two, 1 << lb; hps_lb = hps << lb, h_lb = h << lb.
+// token r of the tile, 128-byte box x of the token's row): the TMA boxes of one
+// stage are [op][head][box][rows of the op], one op per block when
+// block_size < 16.  Rows per op are a power of two, 1 << lb; hps_lb =
+// hps << lb, h_lb = h << lb.  With the box outside the rows, the 8 consecutive
+// tokens an ldmatrix reads for one box sit in 8 consecutive 128-byte rows, so
+// the 128-byte swizzle spreads them over all banks (rows [token][box] would
+// put tokens r and r + 4 on the same banks).
 __device__ __forceinline__ int srow(int h_lb, int r, int x, int hps_lb, int lb, int nb) {
-    return (((r >> lb) * hps_lb + h_lb + (r & ((1 << lb) - 1))) * nb) + x;
+    return ((r >> lb) * hps_lb + h_lb) * nb + (x << lb) + (r & ((1 << lb) - 1));
 }
 
 __device__ __forceinline__ void tma_load_5d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
@@ -402,8 +406,14 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
             if (in) {
                 const int row0 = p.bs > kTileT ? (t0 % p.bs) : 0;
                 const int v = lane & 1;
-                tma_load_5d(&sm.kv[s][v][(lane >> 1) * op_bytes], v ? mv : mk, 0, 0, row0, d.hg * d.hps, my,
-                            &sm.full[s]);
+                // map dimensions {column of a 128-byte box, row, box, kv head,
+                // block}; rows of a single box: {column, box, row, ...}
+                if constexpr (Geo<D, F8>::kNB > 1)
+                    tma_load_5d(&sm.kv[s][v][(lane >> 1) * op_bytes], v ? mv : mk, 0, row0, 0, d.hg * d.hps, my,
+                                &sm.full[s]);
+                else
+                    tma_load_5d(&sm.kv[s][v][(lane >> 1) * op_bytes], v ? mv : mk, 0, 0, row0, d.hg * d.hps, my,
+                                &sm.full[s]);
             }
             __syncwarp();
         }
@@ -799,6 +809,111 @@ __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnPar
     }
 }
 
+// Per-lane constants of a multi-query warp: causal limits of its rows A and
+// B, shared-memory row indexing of the stage, ldmatrix lane roles.
+struct MqLanes {
+    int limA, limB, h_lb, hps_lb, lb, k_tok, k_hi, v_tok, v_hi, qd;
+};
+
+// One 16-token stage of a multi-query item (K at kb, V at vb, tokens t0 ..
+// t0 + 15; positions at or past t_end are not part of the item): S = Q K^T,
+// causal / tail mask, lazy reference maxima, O += P V.
+template <int D>
+__device__ __forceinline__ void mq_stage(uint32_t kb, uint32_t vb, int t0, int t_end, float scale_log2,
+                                         const uint32_t (&qf)[D / 16][4], float (&o)[D / 8][4], float& mA, float& mB,
+                                         float& lA, float& lB, const MqLanes& ml) {
+    constexpr int NB = D / 64;
+    const int qd = ml.qd;
+    float sf[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const int chunk = 2 * ks + ml.k_hi;
+        const int R = srow(ml.h_lb, ml.k_tok, chunk >> 3, ml.hps_lb, ml.lb, NB);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
+        mma_bf16_16816(sf[0], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
+        mma_bf16_16816(sf[1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+    }
+    // scale, causal / tail mask
+    float mxA = -INFINITY, mxB = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int t = t0 + 8 * nt + 2 * qd + (j & 1);
+            const int lim = j < 2 ? ml.limA : ml.limB;
+            const bool vis = t < t_end && t <= lim;
+            const float v = vis ? sf[nt][j] * scale_log2 : -INFINITY;
+            sf[nt][j] = v;
+            if (j < 2) mxA = fmaxf(mxA, v); else mxB = fmaxf(mxB, v);
+        }
+    // lazy reference maxima (as in decode_tc_item): rows move theirs only when
+    // a score exceeds it by more than kRescaleSlack
+    if (!__all_sync(kFull, mxA <= mA + kRescaleSlack && mxB <= mB + kRescaleSlack)) {
+        mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, 1));
+        mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, 2));
+        mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, 1));
+        mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, 2));
+        const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
+        const float cA = nA == -INFINITY ? 1.f : exp2f(mA - nA), cB = nB == -INFINITY ? 1.f : exp2f(mB - nB);
+        lA *= cA;
+        lB *= cB;
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+            o[nt][0] *= cA;
+            o[nt][1] *= cA;
+            o[nt][2] *= cB;
+            o[nt][3] *= cB;
+        }
+        mA = nA;
+        mB = nB;
+    }
+    const float uA = mA == -INFINITY ? 0.f : mA, uB = mB == -INFINITY ? 0.f : mB;
+    float sA = 0.f, sB = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        sf[nt][0] = exp2f(sf[nt][0] - uA);
+        sf[nt][1] = exp2f(sf[nt][1] - uA);
+        sf[nt][2] = exp2f(sf[nt][2] - uB);
+        sf[nt][3] = exp2f(sf[nt][3] - uB);
+        sA += sf[nt][0] + sf[nt][1];
+        sB += sf[nt][2] + sf[nt][3];
+    }
+    // l stays a per-lane partial sum (this lane's tokens); reduced once at the end
+    lA += sA;
+    lB += sB;
+    const uint32_t pa0 = float2_to_bf16x2(sf[0][0], sf[0][1]);
+    const uint32_t pa1 = float2_to_bf16x2(sf[0][2], sf[0][3]);
+    const uint32_t pa2 = float2_to_bf16x2(sf[1][0], sf[1][1]);
+    const uint32_t pa3 = float2_to_bf16x2(sf[1][2], sf[1][3]);
+    if (t0 + kTileT <= t_end) {
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+            const int chunk = 2 * dp + ml.v_hi;
+            const int R = srow(ml.h_lb, ml.v_tok, chunk >> 3, ml.hps_lb, ml.lb, NB);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
+            mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
+        }
+    } else {
+        // V rows past the valid tokens may hold anything (even NaN): zero them
+        const int nvalid = t_end - t0;
+        const uint32_t keep0 = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+        const uint32_t keep1 =
+            (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (8 + 2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+            const int chunk = 2 * dp + ml.v_hi;
+            const int R = srow(ml.h_lb, ml.v_tok, chunk >> 3, ml.hps_lb, ml.lb, NB);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
+            mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0 & keep0, b1 & keep1);
+            mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & keep0, b3 & keep1);
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Multi-query item on tensor cores (mma.sync m16n8k16, bf16 in, fp32 acc).
 // Warp w serves kv head hw = w / wph of the group and its rows
@@ -808,7 +923,6 @@ __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnPar
 template <int D>
 __device__ __forceinline__ void mq_item(Smem<D, false>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
                                         uint32_t gbase, int ntiles, int si, volatile int* abort) {
-    constexpr int NB = D / 64;
     const int G = p.G;
     const int per = d.nq * G;                      // rows per kv head in this tile
     const int hw = warp / d.wph, rw = warp - hw * d.wph;
@@ -855,106 +969,14 @@ __device__ __forceinline__ void mq_item(Smem<D, false>& sm, const AttnParams& p,
     const int k_hi = mi & 1;
     const int v_tok = ((mi & 1) << 3) + mrow;   // V: (tok 0-7, d lo), (tok 8-15, d lo), (tok 0-7, d hi), ...
     const int v_hi = mi >> 1;
+    const MqLanes ml{limA, limB, h_lb, hps_lb, lb, k_tok, k_hi, v_tok, v_hi, qd};
     for (int i = 0; i < ntiles; ++i) {
         const uint32_t gi = gbase + i;
         const int s = (int)(gi % kRingSlots);
         mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort);
-        if (!active) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[s]);
-            continue;
-        }
-        const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
-        const uint32_t vb = smem_u32(&sm.kv[s][1][0]);
-        const int t0 = (tb + i) * kTileT;
-        const int nvalid = min(kTileT, d.t_end - t0);
-        float sf[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const int chunk = 2 * ks + k_hi;
-            const int R = srow(h_lb, k_tok, chunk >> 3, hps_lb, lb, NB);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
-            mma_bf16_16816(sf[0], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-            mma_bf16_16816(sf[1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
-        }
-        // scale, causal / tail mask
-        float mxA = -INFINITY, mxB = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int tl = 8 * nt + 2 * qd + (j & 1);
-                const int lim = j < 2 ? limA : limB;
-                const bool vis = tl < nvalid && t0 + tl <= lim;
-                const float v = vis ? sf[nt][j] * p.scale_log2 : -INFINITY;
-                sf[nt][j] = v;
-                if (j < 2) mxA = fmaxf(mxA, v); else mxB = fmaxf(mxB, v);
-            }
-        // lazy reference maxima (as in decode_tc_item): rows move theirs only
-        // when a score exceeds it by more than kRescaleSlack
-        if (!__all_sync(kFull, mxA <= mA + kRescaleSlack && mxB <= mB + kRescaleSlack)) {
-            mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, 1));
-            mxA = fmaxf(mxA, __shfl_xor_sync(kFull, mxA, 2));
-            mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, 1));
-            mxB = fmaxf(mxB, __shfl_xor_sync(kFull, mxB, 2));
-            const float nA = fmaxf(mA, mxA), nB = fmaxf(mB, mxB);
-            const float cA = nA == -INFINITY ? 1.f : exp2f(mA - nA), cB = nB == -INFINITY ? 1.f : exp2f(mB - nB);
-            lA *= cA;
-            lB *= cB;
-#pragma unroll
-            for (int nt = 0; nt < D / 8; ++nt) {
-                o[nt][0] *= cA;
-                o[nt][1] *= cA;
-                o[nt][2] *= cB;
-                o[nt][3] *= cB;
-            }
-            mA = nA;
-            mB = nB;
-        }
-        const float uA = mA == -INFINITY ? 0.f : mA, uB = mB == -INFINITY ? 0.f : mB;
-        float sA = 0.f, sB = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            sf[nt][0] = exp2f(sf[nt][0] - uA);
-            sf[nt][1] = exp2f(sf[nt][1] - uA);
-            sf[nt][2] = exp2f(sf[nt][2] - uB);
-            sf[nt][3] = exp2f(sf[nt][3] - uB);
-            sA += sf[nt][0] + sf[nt][1];
-            sB += sf[nt][2] + sf[nt][3];
-        }
-        // l stays a per-lane partial sum (this lane's tokens); reduced once at the end
-        lA += sA;
-        lB += sB;
-        const uint32_t pa0 = float2_to_bf16x2(sf[0][0], sf[0][1]);
-        const uint32_t pa1 = float2_to_bf16x2(sf[0][2], sf[0][3]);
-        const uint32_t pa2 = float2_to_bf16x2(sf[1][0], sf[1][1]);
-        const uint32_t pa3 = float2_to_bf16x2(sf[1][2], sf[1][3]);
-        if (nvalid == kTileT) {
-#pragma unroll
-            for (int dp = 0; dp < D / 16; ++dp) {
-                const int chunk = 2 * dp + v_hi;
-                const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0, b1);
-                mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2, b3);
-            }
-        } else {
-            // V rows past the valid tokens may hold anything (even NaN): zero them
-            const uint32_t keep0 = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
-            const uint32_t keep1 =
-                (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (8 + 2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
-#pragma unroll
-            for (int dp = 0; dp < D / 16; ++dp) {
-                const int chunk = 2 * dp + v_hi;
-                const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), b0, b1, b2, b3);
-                mma_bf16_16816(o[2 * dp], pa0, pa1, pa2, pa3, b0 & keep0, b1 & keep1);
-                mma_bf16_16816(o[2 * dp + 1], pa0, pa1, pa2, pa3, b2 & keep0, b3 & keep1);
-            }
-        }
+        if (active)
+            mq_stage<D>(smem_u32(&sm.kv[s][0][0]), smem_u32(&sm.kv[s][1][0]), (tb + i) * kTileT, d.t_end,
+                        p.scale_log2, qf, o, mA, mB, lA, lB, ml);
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
     }

@@ -434,20 +434,28 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     const int rc = host::check_device();
     if (rc) return rc;
 
-    // 5-D views [num_blocks][n_kv][bs][row / 128 B][128 B] of each pool, one per
-    // box height in kv heads (a row is D values of 2 bytes, or of 1 byte in e4m3)
+    // 5-D views of each pool, one per box height in kv heads (a row is D values
+    // of 2 bytes, or of 1 byte in e4m3).  Rows of more than 128 bytes are
+    // viewed as [num_blocks][n_kv][row / 128 B][bs][128 B] (the 128-byte box
+    // outside the row, a non-monotonic stride), so a box lands in shared memory
+    // as [head][box][row]: consecutive tokens of one box in consecutive
+    // 128-byte lines, which the 128-byte swizzle maps to distinct banks.
     TMaps tm;
     {
         const uint64_t row = (uint64_t)head_dim * (fp8 ? 1 : 2);
         const uint64_t inner = fp8 ? 128 : 64;  // elements per 128-byte box
+        const uint64_t nb = row / 128;
         const uint32_t box_rows = block_size < kTileT ? (uint32_t)block_size : (uint32_t)kTileT;
-        const uint64_t dims[5] = {inner, row / 128, (uint64_t)block_size, (uint64_t)num_kv_heads,
-                                  (uint64_t)num_blocks};
-        const uint64_t strides[4] = {128, row, (uint64_t)block_size * row, (uint64_t)num_kv_heads * block_size * row};
+        const uint64_t blk = (uint64_t)block_size * row, head = (uint64_t)num_kv_heads * blk;
+        const bool split = nb > 1;
+        const uint64_t dims[5] = {inner, split ? (uint64_t)block_size : nb, split ? nb : (uint64_t)block_size,
+                                  (uint64_t)num_kv_heads, (uint64_t)num_blocks};
+        const uint64_t strides[4] = {split ? row : 128, split ? 128 : row, blk, head};
         for (int i = 0; i < 4; ++i) {
             uint32_t hb = 1u << i;
             if (hb > (uint32_t)num_kv_heads) hb = (uint32_t)num_kv_heads;
-            const uint32_t box[5] = {(uint32_t)inner, (uint32_t)(row / 128), box_rows, hb, 1};
+            const uint32_t box[5] = {(uint32_t)inner, split ? box_rows : (uint32_t)nb, split ? (uint32_t)nb : box_rows,
+                                     hb, 1};
             if (host::encode_tiled(&tm.k[i], k_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, fp8) ||
                 host::encode_tiled(&tm.v[i], v_cache, 5, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, fp8))
                 return PKV_ERR_CUDA;
