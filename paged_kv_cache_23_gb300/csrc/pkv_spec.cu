@@ -219,7 +219,9 @@ __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSample
     // partial sums per (chunk, warp) in token order: segment i covers tokens
     // lo + (i / W) * chunk + (i % W) * 128 ... + 127
     __shared__ uint64_t seg[kSampleMaxSegs];
+    __shared__ uint64_t wsum[kSampleWarps];
     __shared__ uint64_t slice_total;
+    __shared__ uint64_t s_tot[3];  // total, before this slice, this slice
     __shared__ int s_rej, s_bad, s_seg;
     __shared__ uint64_t s_run;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -281,23 +283,29 @@ __global__ void __cluster_dims__(kSampleCluster, 1, 1) __launch_bounds__(kSample
                 if (lane == 0) seg[c * kSampleWarps + warp] = sw;
                 acc += sw;
             }
+            if (lane == 0) wsum[warp] = acc;
             __syncthreads();
-            if (tid == 0) {
-                uint64_t t = 0;
-                for (int i = 0; i < nchunks * kSampleWarps; ++i) t += seg[i];
-                slice_total = t;
+            if (warp == 0) {
+                uint64_t t = lane < kSampleWarps ? wsum[lane] : 0;
+                t = warp_sum_u64(t);
+                if (lane == 0) slice_total = t;
             }
             cluster.sync();
-            total = 0;
-            before = 0;
-            for (int c = 0; c < kSampleCluster; ++c) {
-                const uint64_t t = *cluster.map_shared_rank(&slice_total, c);
-                if (c < rank) before += t;
-                if (c == rank) mine = t;
-                total += t;
+            // lanes 0-7 of warp 0 read the slice totals of the cluster once
+            if (warp == 0) {
+                const uint64_t t = lane < kSampleCluster ? *cluster.map_shared_rank(&slice_total, lane) : 0;
+                const uint64_t tot = warp_sum_u64(t);
+                const uint64_t bef = warp_sum_u64(lane < rank ? t : 0);
+                if (lane == 0) {
+                    s_tot[0] = tot;
+                    s_tot[1] = bef;
+                }
+                if (lane == rank) s_tot[2] = t;
             }
-            cluster.sync();  // slice_total is rewritten by a second pass
-            (void)acc;
+            cluster.sync();  // slice_total is rewritten by a second pass; s_tot is complete
+            total = s_tot[0];
+            before = s_tot[1];
+            mine = s_tot[2];
             if (total == 0 && residual) {
                 residual = 0;  // no positive residual: draw from p itself
                 continue;
