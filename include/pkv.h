@@ -190,11 +190,12 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *                 g = num_q_heads / num_kv_heads an integer in [1, 64]
  *   partition_tokens  multiple of 16, at most 1024 partitions per sequence;
  *                 or 0: automatic -- the planning kernel starts from
- *                 pkv_attention_auto_partition(...) and doubles it (up to
- *                 8192) while the batch would give more than 3 partitions
- *                 per SM (6 when multi-query rows make up most of the work;
- *                 fewer, longer partitions cost fewer partial results); the length used is the int at byte offset 8 of
- *                 the workspace after the call
+ *                 P0 = pkv_attention_auto_partition(...) and raises it along
+ *                 P0, 3P0/2, 2P0, 3P0, 4P0, ... (up to 8192) while the batch
+ *                 would give more than 2 partitions per SM (3 when
+ *                 multi-query rows make up most of the work; fewer, longer
+ *                 partitions cost fewer partial results); the length used is
+ *                 the int at byte offset 8 of the workspace after the call
  *   flags         0, or an OR of PKV_ATTN_DECODE_CUDA_CORES (q_len = 1 rows
  *                 on the CUDA-core FMA path; by default every row uses the
  *                 tensor cores, measured faster on GB300) and
