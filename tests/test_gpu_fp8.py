@@ -59,7 +59,7 @@ def test_small_workloads(name):
     run_and_check(wl.SMALL[name]())
 
 
-@pytest.mark.parametrize("P", [16, 48, 512, 0])
+@pytest.mark.parametrize("P", [16, 48, 512, 768, 0])
 def test_partitions(P):
     run_and_check(wl.SMALL["mix"](), partition_tokens=P)
 

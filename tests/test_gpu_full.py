@@ -34,11 +34,19 @@ def _sampled(w, out_bits, k, v, seqs):
     assert np.all(err <= 1e-2 + 1e-2 * np.abs(ref)), f"max err {err.max():.3e}"
 
 
+# partition lengths the automatic mode may pick from a floor of 512
+AUTO_LADDER = {512, 768, 1024, 1536, 2048, 3072, 4096, 6144, 8192}
+
+
 def _run(w, **kw):
     ds = DeviceStep(w, **kw)
     ds.step()
     torch.cuda.synchronize()
     assert int(ds.status.item()) == 0, pkv.status_bits(int(ds.status.item()))
+    if ds.partition_tokens in (None, 0):
+        # the length the planning kernel used is the int at byte offset 8 of the workspace
+        used = int(ds.workspace[8:12].view(torch.int32).item())
+        assert used in AUTO_LADDER, used
     return ds
 
 

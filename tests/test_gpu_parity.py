@@ -77,7 +77,7 @@ def test_decode_rows_on_cuda_cores_match_oracle(name):
     run_and_check(wl.SMALL[name](), flags=pkv.PKV_ATTN_DECODE_CUDA_CORES)
 
 
-@pytest.mark.parametrize("P", [16, 32, 48, 160, 4096])
+@pytest.mark.parametrize("P", [16, 32, 48, 160, 768, 1536, 4096])
 def test_partition_sizes(P):
     # many partitions per sequence exercise the split-KV merge; 16 tokens with
     # long sequences takes the many-partition merge path

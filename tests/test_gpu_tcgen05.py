@@ -48,9 +48,10 @@ def test_head_groupings_on_tcgen05(n_q, n_kv, q_len):
     assert tiles_used(ds) == 1
 
 
-@pytest.mark.parametrize("P", [128, 256, 640, 0])
+@pytest.mark.parametrize("P", [128, 256, 640, 768, 0])
 def test_partitions_of_tiles(P):
-    # P = 128: one stage per partition; 640: partitions of five stages; 0: automatic
+    # P = 128: one stage per partition; 640, 768: partitions of five and six
+    # stages (768 is a step of the automatic ladder); 0: automatic
     w = chunk(32, 8, 70, prefix=1000, decodes=2, ctx=900, P=P, seed=P)
     ds, _, _ = run_and_check(w)
     assert tiles_used(ds) == 1
