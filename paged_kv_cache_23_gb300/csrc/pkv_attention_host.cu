@@ -22,7 +22,7 @@ struct PlanParams {
     int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, max_q_len, decode_ok;
     int fp8;         // e4m3 pool: every row on the transposed tensor-core item
     int tc;          // tcgen05 tiles allowed (head_dim 128, bf16, block_size >= 16, P % 128 == 0)
-    int adapt_P;     // 1: P is a floor; the planning kernel may double it
+    int adapt_P;     // 1: P is a floor; the planning kernel may raise it
     int sms;         // SM count (persistent CTAs of the attention kernel)
 };
 
