@@ -434,6 +434,19 @@ int pkv_spec_accept_sample(const float* p, const float* q, const int32_t* draft,
                            const float* s, int num_seqs, int k, int vocab, int32_t* accepted,
                            int32_t* next_token, int32_t* status, void* stream);
 
+/*
+ * Self-test of the library's failure detection (no counterpart on the pages):
+ * one warp waits, through the same bounded device wait every attention kernel
+ * uses, on an mbarrier phase that nothing ever completes.  The wait gives up
+ * after limit_ns nanoseconds of %globaltimer (1 ns .. 10 s), ORs
+ * PKV_STATUS_TIMEOUT into *status (device int32, required) and the kernel
+ * returns normally, so the context stays usable -- which is what a caller
+ * relies on when a real wait inside an attention call runs out.
+ * Returns PKV_ERR_SIZE for a limit outside the range, PKV_ERR_NULL for a null
+ * status.
+ */
+int pkv_wait_selftest(long long limit_ns, int32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -66,6 +66,7 @@ _SIGS = {
     "pkv_paged_attention_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                         _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_noalloc_scratch_bytes": ([], ctypes.c_size_t),
+    "pkv_wait_selftest": ([ctypes.c_longlong, _P, _P], _I),
     "pkv_paged_attention_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                             ctypes.c_float, _I, _I, _P, _P], _I),
 }
@@ -392,3 +393,10 @@ def paged_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_l
 
 def noalloc_scratch_bytes() -> int:
     return int(lib().pkv_noalloc_scratch_bytes())
+
+
+def wait_selftest(limit_ns: int, status, stream=None):
+    """Failure-detection self-test: a device wait on a flag that nothing sets
+    must give up after limit_ns and set PKV_STATUS_TIMEOUT in status."""
+    _dev(status, "status", torch.int32)
+    _check(lib().pkv_wait_selftest(int(limit_ns), _ptr(status), _stream(stream)), "pkv_wait_selftest")

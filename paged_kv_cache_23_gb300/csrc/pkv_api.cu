@@ -4,6 +4,7 @@
 #include <mutex>
 
 #include "pkv.h"
+#include "pkv_common.cuh"
 #include "pkv_host.h"
 
 namespace pkv {
@@ -112,4 +113,37 @@ extern "C" const char* pkv_status_string(int bit) {
         case PKV_STATUS_NOT_FOUND: return "prefix-cache key not found";
         default: return "unknown status bit";
     }
+}
+
+// ---------------------------------------------------------------------------
+// Self-test of the bounded device wait: one warp waits, with mbar_wait (the
+// wait every attention kernel uses), on an mbarrier phase that nothing
+// completes.  The wait must give up after limit_ns of %globaltimer, report
+// PKV_STATUS_TIMEOUT and let the kernel return, leaving the context usable.
+// ---------------------------------------------------------------------------
+namespace pkv {
+namespace {
+__global__ void wait_selftest_kernel(unsigned long long limit_ns, int32_t* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);  // one arrival completes phase 0; none ever comes
+        abort = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    bool ok = true;
+    if (threadIdx.x == 0) ok = mbar_wait(&bar, 0, &abort, limit_ns);
+    if (threadIdx.x == 0 && !ok) report(status, PKV_STATUS_TIMEOUT);
+}
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_wait_selftest(long long limit_ns, int32_t* status, void* stream) {
+    if (limit_ns < 1 || limit_ns > 10000000000LL) return PKV_ERR_SIZE;
+    if (!status) return PKV_ERR_NULL;
+    const int rc = pkv::host::check_device();
+    if (rc) return rc;
+    pkv::wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((unsigned long long)limit_ns, status);
+    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

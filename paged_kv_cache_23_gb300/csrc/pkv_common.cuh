@@ -65,16 +65,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Returns false (and
-// sets *abort) if it did not within kWaitNs, or at once if *abort is already
+// sets *abort) if it did not within limit_ns (kWaitNs unless a caller, such as
+// the wait self-test, gives another bound), or at once if *abort is already
 // set by another warp of the CTA.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          unsigned long long limit_ns = kWaitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 63u) == 0u) {
             if (*abort) return false;
-            if (global_ns() - t0 > kWaitNs) {
+            if (global_ns() - t0 > limit_ns) {
                 *abort = 1;
                 return false;
             }

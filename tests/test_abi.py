@@ -72,6 +72,9 @@ def test_host_side_argument_checks(lib):
     assert call(num_seqs=0) == 0            # nothing to do
     assert lib.pkv_kv_append(None, None, None, None, None, 3, 4, 16, 8, 100, None, None) == -3
     assert lib.pkv_spec_accept_greedy(None, None, 2, 0, 10, None, None, None, None) == -2
+    assert lib.pkv_wait_selftest(0, None, None) == -2                  # limit out of range
+    assert lib.pkv_wait_selftest(20_000_000_000, None, None) == -2
+    assert lib.pkv_wait_selftest(1000, None, None) == -1               # status is required
 
 
 def test_workspace_bytes_grow_with_partitions(lib):
