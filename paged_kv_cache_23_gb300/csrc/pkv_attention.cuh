@@ -834,19 +834,31 @@ __device__ __forceinline__ void mq_stage(uint32_t kb, uint32_t vb, int t0, int t
         mma_bf16_16816(sf[0], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
         mma_bf16_16816(sf[1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
     }
-    // scale, causal / tail mask
+    // scale, causal / tail mask (a stage whose 16 tokens every row of the warp
+    // sees needs no mask: all stages but a partition's last ones)
     float mxA = -INFINITY, mxB = -INFINITY;
+    if (__all_sync(kFull, t0 + kTileT <= t_end && t0 + kTileT - 1 <= min(ml.limA, ml.limB))) {
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int t = t0 + 8 * nt + 2 * qd + (j & 1);
-            const int lim = j < 2 ? ml.limA : ml.limB;
-            const bool vis = t < t_end && t <= lim;
-            const float v = vis ? sf[nt][j] * scale_log2 : -INFINITY;
-            sf[nt][j] = v;
-            if (j < 2) mxA = fmaxf(mxA, v); else mxB = fmaxf(mxB, v);
-        }
+            for (int j = 0; j < 4; ++j) {
+                const float v = sf[nt][j] * scale_log2;
+                sf[nt][j] = v;
+                if (j < 2) mxA = fmaxf(mxA, v); else mxB = fmaxf(mxB, v);
+            }
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int t = t0 + 8 * nt + 2 * qd + (j & 1);
+                const int lim = j < 2 ? ml.limA : ml.limB;
+                const bool vis = t < t_end && t <= lim;
+                const float v = vis ? sf[nt][j] * scale_log2 : -INFINITY;
+                sf[nt][j] = v;
+                if (j < 2) mxA = fmaxf(mxA, v); else mxB = fmaxf(mxB, v);
+            }
+    }
     // lazy reference maxima (as in decode_tc_item): rows move theirs only when
     // a score exceeds it by more than kRescaleSlack
     if (!__all_sync(kFull, mxA <= mA + kRescaleSlack && mxB <= mB + kRescaleSlack)) {
