@@ -68,6 +68,8 @@ def _load():
                 f = getattr(lib, name)
                 f.argtypes = argt
                 f.restype = ctypes.c_int
+            lib.oracle_set_num_threads.argtypes = [I]
+            lib.oracle_set_num_threads.restype = None
             _lib = lib
     return _lib
 
@@ -83,6 +85,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (timing only)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def slot_mapping(block_tables, seq_lens, append_lens, block_size, num_blocks):

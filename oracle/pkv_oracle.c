@@ -721,6 +721,16 @@ int oracle_prefix_hash(uint64_t *hashes, const int32_t *tokens, int max_tokens, 
     return 0;
 }
 
+/* Threads for the oracle's parallel loops from now on (no effect without
+ * OpenMP); the CPU-baseline timing runs the same step on all cores and on one. */
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Number of threads the oracle's parallel loops use (1 without OpenMP). */
 int oracle_num_threads(void) {
 #ifdef _OPENMP
