@@ -62,12 +62,19 @@ def _load():
                 "oracle_kv_append_fp8": [P, P, P, P, P, I, I, I, I, I, P, P],
                 "oracle_attention_fp8": [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, D],
                 "oracle_prefix_hash": [P, P, I, P, I, I, I, ctypes.c_uint64],
+                "oracle_fp8_encode": [P, P, ctypes.c_int64, I],
+                "oracle_fp8_decode": [P, P, ctypes.c_int64, I],
+                "oracle_kv_append_fp8_ex": [P, P, P, P, P, P, P, I, I, I, I, I, I, I],
+                "oracle_copy_blocks_fp8": [P, P, P, P, P, I, I, I, I, I, I],
+                "oracle_attention_fp8_ex": [P, P, P, P, P, P, P, I, P, P, I, I, I, I, I, I, D, I, I],
                 "oracle_num_threads": [],
             }
             for name, argt in sigs.items():
                 f = getattr(lib, name)
                 f.argtypes = argt
                 f.restype = ctypes.c_int
+            lib.oracle_block_scale.argtypes = [P, I, I]
+            lib.oracle_block_scale.restype = ctypes.c_float
             lib.oracle_set_num_threads.argtypes = [I]
             lib.oracle_set_num_threads.restype = None
             _lib = lib
@@ -237,6 +244,77 @@ def attention_fp8(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_len
     st = _load().oracle_attention_fp8(_p(out), _p(qq), _p(_c(k_cache8, np.uint8)), _p(_c(v_cache8, np.uint8)),
                                       _p(_c(k_scale, np.float32)), _p(_c(v_scale, np.float32)), _p(bt), bt.shape[1],
                                       _p(sl), _p(ql), len(sl), n_q, nkv, d, bs, nb, float(scale))
+    return out, st
+
+
+E4M3, E5M2 = 0, 1
+
+
+def fp8_encode(x, fmt=E4M3):
+    """fp32 -> e4m3 or e5m2 codes (round to nearest even, saturate to the
+    largest finite value, NaN kept as 0x7f)."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load().oracle_fp8_encode(_p(out), _p(x), x.size, int(fmt))
+    return out
+
+
+def fp8_decode(codes, fmt=E4M3):
+    """e4m3 / e5m2 codes -> exact fp64 values."""
+    c = _c(codes, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().oracle_fp8_decode(_p(out), _p(c), c.size, int(fmt))
+    return out
+
+
+def block_scale(row, fmt=E4M3):
+    """Scale a block's opening row sets for one kv head: the smallest power of
+    two s with max|row| <= s * FMAX / 2 (1 for an all-zero or infinite row)."""
+    r = _c(row, np.float32).reshape(-1)
+    return float(_load().oracle_block_scale(_p(r), r.size, int(fmt)))
+
+
+def kv_append_fp8_ex(k_cache8, v_cache8, k_new, v_new, slots, k_scale, v_scale, fmt=E4M3, per_block=False):
+    """Append bf16 rows into FP8 pools in place ("Inference at Scale" 03, KV
+    cache quantization), either format; per_block: scales [num_blocks][n_kv]
+    (updated in place: a block's row 0 sets its scales), else [n_kv].
+    Returns status."""
+    nb, nkv, bs, d = k_cache8.shape
+    assert k_cache8.dtype == np.uint8 and v_cache8.dtype == np.uint8
+    assert k_scale.dtype == np.float32 and k_scale.flags.c_contiguous and v_scale.flags.c_contiguous
+    kn = _c(k_new, np.uint16)
+    vn = _c(v_new, np.uint16)
+    sl = _c(slots, np.int64)
+    return _load().oracle_kv_append_fp8_ex(_p(k_cache8), _p(v_cache8), _p(k_scale), _p(v_scale), _p(kn), _p(vn),
+                                           _p(sl), len(sl), nb, bs, nkv, d, int(fmt), int(bool(per_block)))
+
+
+def copy_blocks_fp8(k_cache8, v_cache8, k_scale, v_scale, src_dst, per_block=False):
+    """Copy-on-write block copies in FP8 pools, in place (and the blocks'
+    scales with per_block).  Returns status."""
+    nb, nkv, bs, d = k_cache8.shape
+    sd = _c(src_dst, np.int32).reshape(-1, 2)
+    return _load().oracle_copy_blocks_fp8(_p(k_cache8), _p(v_cache8), _p(k_scale), _p(v_scale), _p(sd),
+                                          sd.shape[0], nb, bs, nkv, d, int(bool(per_block)))
+
+
+def attention_fp8_ex(q, k_cache8, v_cache8, k_scale, v_scale, block_tables, seq_lens, q_lens, scale, fmt=E4M3,
+                     per_block=False):
+    """attention() over FP8 pools of either format: K = fp8(K) * scale of the
+    kv head (or of the (block, kv head) tile with per_block), V likewise."""
+    qq = _c(q, np.uint16)
+    T, n_q, d = qq.shape
+    nb, nkv, bs, d2 = k_cache8.shape
+    if d2 != d or n_q % nkv or T < int(np.maximum(np.asarray(q_lens), 0).sum()):
+        raise ValueError("q must be [sum q_lens][n_q][head_dim] with n_q a multiple of n_kv")
+    bt = _c(block_tables, np.int32)
+    sl = _c(seq_lens, np.int32)
+    ql = _c(q_lens, np.int32)
+    out = np.zeros((T, n_q, d), np.float64)
+    st = _load().oracle_attention_fp8_ex(_p(out), _p(qq), _p(_c(k_cache8, np.uint8)), _p(_c(v_cache8, np.uint8)),
+                                         _p(_c(k_scale, np.float32)), _p(_c(v_scale, np.float32)), _p(bt),
+                                         bt.shape[1], _p(sl), _p(ql), len(sl), n_q, nkv, d, bs, nb, float(scale),
+                                         int(fmt), int(bool(per_block)))
     return out, st
 
 

@@ -493,6 +493,219 @@ int oracle_kv_append_fp8(uint8_t *k_cache, uint8_t *v_cache, const uint16_t *k_n
 }
 
 /*
+ * The second FP8 format of [KVC] 03, e5m2: sign bit, 5 exponent bits with bias
+ * 15, 2 mantissa bits; exponent field 0 holds subnormals m * 2^-16; field 31
+ * holds the infinities (m = 0) and NaN (m != 0); the largest finite magnitude
+ * is 1.75 * 2^15 = 57344.  Encoding rounds to the nearest representable value,
+ * ties to the even code, and saturates magnitudes above 57344 (infinities
+ * included) to 57344; NaN is stored as 0x7f.
+ */
+static double e5m2_value(uint8_t c) {
+    const int s = c >> 7, e = (c >> 2) & 31, m = c & 3;
+    double v;
+    if (e == 31) v = m ? NAN : INFINITY;
+    else v = e == 0 ? ldexp((double)m, -16) : ldexp((double)(4 + m), e - 17);
+    return s ? -v : v;
+}
+
+static uint8_t e5m2_encode(float x) {
+    if (isnan(x)) return 0x7f;
+    const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    const double a = fabs((double)x);
+    if (a >= 57344.0) return sign | 0x7b;
+    int c = 0;
+    while (c < 0x7b && e5m2_value((uint8_t)(c + 1)) <= a) c++;
+    if (c < 0x7b) {
+        const double lo = e5m2_value((uint8_t)c), hi = e5m2_value((uint8_t)(c + 1));
+        if (a - lo > hi - a || (a - lo == hi - a && (c & 1))) c++;
+    }
+    return sign | (uint8_t)c;
+}
+
+/* fmt 0 = e4m3, 1 = e5m2 */
+static double fp8_value(uint8_t c, int fmt) { return fmt ? e5m2_value(c) : e4m3_value(c); }
+static uint8_t fp8_encode(float x, int fmt) { return fmt ? e5m2_encode(x) : e4m3_encode(x); }
+
+int oracle_fp8_encode(uint8_t *out, const float *in, int64_t n, int fmt) {
+    for (int64_t i = 0; i < n; i++) out[i] = fp8_encode(in[i], fmt);
+    return 0;
+}
+
+int oracle_fp8_decode(double *out, const uint8_t *in, int64_t n, int fmt) {
+    for (int64_t i = 0; i < n; i++) out[i] = fp8_value(in[i], fmt);
+    return 0;
+}
+
+/*
+ * Scale of one (block, kv head) tile of an FP8 pool with per-block scales (a
+ * reading: [KVC] 03 fixes no scaling).  It is set when the block is opened --
+ * by the append that writes the block's row 0 -- from that row's values x of
+ * the head: the smallest power of two s = 2^e (e in [-120, 120]) with
+ *   amax <= s * FMAX / 2,   amax = max |x| over the row's non-NaN values,
+ * FMAX the format's largest finite value (448 for e4m3, 57344 for e5m2).  The
+ * opening row then uses at most half of the format's range, and the rows
+ * appended after it may grow to twice its magnitude before they saturate.
+ * s = 1 when amax is 0 (or every value is NaN) or infinite.  A power of two
+ * makes 1 / s and x * (1 / s) exact in fp32.
+ */
+float oracle_block_scale(const float *row, int d, int fmt) {
+    double amax = 0.0;
+    for (int c = 0; c < d; c++)
+        if (!isnan(row[c]) && fabs((double)row[c]) > amax) amax = fabs((double)row[c]);
+    if (amax == 0.0 || isinf(amax)) return 1.0f;
+    const double half = fmt ? 28672.0 : 224.0;
+    int e = -120;
+    while (e < 120 && ldexp(half, e) < amax) e++;
+    return (float)ldexp(1.0, e);
+}
+
+/*
+ * KV append into an FP8 pool of either format.  per_block = 0: one scale per
+ * kv head, k_scale[n_kv] (read only), as oracle_kv_append_fp8.  per_block = 1:
+ * k_scale and v_scale are [num_blocks][n_kv]; first every appended token whose
+ * slot is row 0 of its block sets that block's scales from its own row
+ * (oracle_block_scale), then every token is stored with its block's scales --
+ * so rows appended in the same call as their block's row 0 use the scale that
+ * row set.  Each value x is stored as fp8(x * (1 / scale)), the reciprocal and
+ * the product rounded to fp32.
+ */
+int oracle_kv_append_fp8_ex(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale, const uint16_t *k_new,
+                            const uint16_t *v_new, const int64_t *slots, int num_tokens, int num_blocks,
+                            int block_size, int n_kv, int d, int fmt, int per_block) {
+    int status = 0;
+    float *row = (float *)malloc(sizeof(float) * (d > 0 ? d : 1));
+    if (per_block) {
+        for (int t = 0; t < num_tokens; t++) {
+            int64_t s = slots[t];
+            if (s < 0 || s >= (int64_t)num_blocks * block_size || s % block_size != 0) continue;
+            int64_t blk = s / block_size;
+            for (int h = 0; h < n_kv; h++) {
+                for (int c = 0; c < d; c++) row[c] = (float)widen_bf16(k_new[((int64_t)t * n_kv + h) * d + c]);
+                k_scale[blk * n_kv + h] = oracle_block_scale(row, d, fmt);
+                for (int c = 0; c < d; c++) row[c] = (float)widen_bf16(v_new[((int64_t)t * n_kv + h) * d + c]);
+                v_scale[blk * n_kv + h] = oracle_block_scale(row, d, fmt);
+            }
+        }
+    }
+    for (int t = 0; t < num_tokens; t++) {
+        int64_t s = slots[t];
+        if (s < 0) continue;
+        if (s >= (int64_t)num_blocks * block_size) { status |= ST_BAD_SLOT; continue; }
+        int64_t blk = s / block_size;
+        int r = (int)(s % block_size);
+        for (int h = 0; h < n_kv; h++) {
+            const int64_t si = per_block ? blk * n_kv + h : h;
+            const float ik = 1.0f / k_scale[si], iv = 1.0f / v_scale[si];
+            for (int c = 0; c < d; c++) {
+                int64_t dst = cache_offset(blk, h, r, n_kv, block_size, d) + c;
+                int64_t src = ((int64_t)t * n_kv + h) * d + c;
+                const float xk = (float)widen_bf16(k_new[src]) * ik;
+                const float xv = (float)widen_bf16(v_new[src]) * iv;
+                k_cache[dst] = fp8_encode(xk, fmt);
+                v_cache[dst] = fp8_encode(xv, fmt);
+            }
+        }
+    }
+    free(row);
+    return status;
+}
+
+/*
+ * Copy-on-write block copy in an FP8 pool ([SE] 31.3; [KVC] 05): every byte of
+ * K and V of block src to block dst, and with per-block scales the block's
+ * scales too.  A pair outside the pool sets ST_BAD_PAIR and is skipped.
+ */
+int oracle_copy_blocks_fp8(uint8_t *k_cache, uint8_t *v_cache, float *k_scale, float *v_scale,
+                           const int32_t *src_dst, int n, int num_blocks, int block_size, int n_kv, int d,
+                           int per_block) {
+    int status = 0;
+    const int64_t blk_bytes = (int64_t)n_kv * block_size * d;
+    for (int i = 0; i < n; i++) {
+        int32_t sb = src_dst[2 * i], tb = src_dst[2 * i + 1];
+        if (sb < 0 || sb >= num_blocks || tb < 0 || tb >= num_blocks) { status |= ST_BAD_PAIR; continue; }
+        for (int64_t e = 0; e < blk_bytes; e++) {
+            k_cache[(int64_t)tb * blk_bytes + e] = k_cache[(int64_t)sb * blk_bytes + e];
+            v_cache[(int64_t)tb * blk_bytes + e] = v_cache[(int64_t)sb * blk_bytes + e];
+        }
+        if (per_block)
+            for (int h = 0; h < n_kv; h++) {
+                k_scale[(int64_t)tb * n_kv + h] = k_scale[(int64_t)sb * n_kv + h];
+                v_scale[(int64_t)tb * n_kv + h] = v_scale[(int64_t)sb * n_kv + h];
+            }
+    }
+    return status;
+}
+
+/*
+ * Attention over an FP8 pool of either format and scale granularity:
+ * oracle_attention with K_t = fp8(K) * k_scale and V_t = fp8(V) * v_scale,
+ * the scale of kv head j (per_block = 0) or of the (block of t, j) tile
+ * (per_block = 1).
+ */
+int oracle_attention_fp8_ex(double *out, const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                            const float *k_scale, const float *v_scale, const int32_t *block_tables, int max_blocks,
+                            const int32_t *seq_lens, const int32_t *q_lens, int num_seqs, int n_q, int n_kv, int d,
+                            int block_size, int num_blocks, double scale, int fmt, int per_block) {
+    int status = 0;
+    int g = n_q / n_kv;
+    double val[256]; /* value of every code, looked up below */
+    for (int c = 0; c < 256; c++) val[c] = fp8_value((uint8_t)c, fmt);
+    int64_t *row0 = (int64_t *)malloc(sizeof(int64_t) * (num_seqs + 1));
+    row0[0] = 0;
+    for (int b = 0; b < num_seqs; b++) row0[b + 1] = row0[b] + (q_lens[b] > 0 ? q_lens[b] : 0);
+    for (int b = 0; b < num_seqs; b++) status |= check_seq(seq_lens[b], q_lens[b], max_blocks, block_size);
+
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : status)
+    for (int b = 0; b < num_seqs; b++) {
+        int L = seq_lens[b], ql = q_lens[b];
+        if (ql <= 0) continue;
+        int seq_bad = check_seq(L, ql, max_blocks, block_size);
+        double *s = (double *)malloc(sizeof(double) * (L > 0 ? L : 1));
+        for (int i = 0; i < ql; i++) {
+            int64_t r = row0[b] + i;
+            int p = L - ql + i;
+            for (int h = 0; h < n_q; h++) {
+                double *o = out + (r * n_q + h) * d;
+                const uint16_t *qv = q + (r * n_q + h) * d;
+                int j = h / g;
+                int bad = seq_bad;
+                for (int t = 0; t <= p && !bad; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    if (blk < 0 || blk >= num_blocks) { bad = 1; status |= ST_BAD_BLOCK; }
+                }
+                if (bad) {
+                    for (int c = 0; c < d; c++) o[c] = NAN;
+                    continue;
+                }
+                for (int t = 0; t <= p; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    const uint8_t *kt = k_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                    const double ks = per_block ? (double)k_scale[(int64_t)blk * n_kv + j] : (double)k_scale[j];
+                    double acc = 0.0;
+                    for (int c = 0; c < d; c++) acc += widen_bf16(qv[c]) * (val[kt[c]] * ks);
+                    s[t] = scale * acc;
+                }
+                double M = -INFINITY;
+                for (int t = 0; t <= p; t++) if (s[t] > M) M = s[t];
+                double den = 0.0;
+                for (int t = 0; t <= p; t++) { s[t] = exp(s[t] - M); den += s[t]; }
+                for (int c = 0; c < d; c++) o[c] = 0.0;
+                for (int t = 0; t <= p; t++) {
+                    int32_t blk = block_tables[(int64_t)b * max_blocks + t / block_size];
+                    const uint8_t *vt = v_cache + cache_offset(blk, j, t % block_size, n_kv, block_size, d);
+                    const double vs = per_block ? (double)v_scale[(int64_t)blk * n_kv + j] : (double)v_scale[j];
+                    for (int c = 0; c < d; c++) o[c] += s[t] * (val[vt[c]] * vs);
+                }
+                for (int c = 0; c < d; c++) o[c] /= den;
+            }
+        }
+        free(s);
+    }
+    free(row0);
+    return status;
+}
+
+/*
  * Attention over an e4m3 pool: oracle_attention with K_t = e4m3(K) * k_scale[j]
  * and V_t = e4m3(V) * v_scale[j] for kv head j.
  */

@@ -274,13 +274,16 @@ def mix(B: int = 256, median: int = 1024, sigma: float = 1.0, clip=(16, 32768), 
 
 
 def spec(B: int = 32, lo: int = 2048, hi: int = 8192, k: int = 5, vocab: int = 128256,
-         alpha: float = 0.7, seed: int = 0, **kw) -> Workload:
-    """Speculative verification: seq_len ~ U[lo, hi] including k drafted
-    tokens, q_len = k (causal within the draft), k appended tokens per
-    sequence; target logits [B][k+1][vocab] fp32 N(0,1); draft[b][j] equals
-    the row argmax (numpy's, first index on ties) with probability alpha,
-    independently per position, else a uniform pick among the other ids."""
-    w = _uniform_decode(f"spec_b{B}_k{k}", B, lo, hi, k, seed, **kw)
+         alpha: float = 0.7, seed: int = 0, q_len: int | None = None, **kw) -> Workload:
+    """Speculative verification: seq_len ~ U[lo, hi] including the new tokens,
+    q_len = k by default (the k drafted tokens, causal within the draft) or
+    q_len = k + 1 (the last accepted token and the k drafts: one pass yields
+    the k + 1 distributions), q_len appended tokens per sequence; target
+    logits [B][k+1][vocab] fp32 N(0,1); draft[b][j] equals the row argmax
+    (numpy's, first index on ties) with probability alpha, independently per
+    position, else a uniform pick among the other ids."""
+    ql = k if q_len is None else int(q_len)
+    w = _uniform_decode(f"spec_b{B}_k{k}" + ("" if ql == k else f"_q{ql}"), B, lo, hi, ql, seed, **kw)
     ss = np.random.SeedSequence(seed)
     s_logit = ss.spawn(5)[4]
     kids = s_logit.spawn(2)
@@ -304,32 +307,43 @@ def spec(B: int = 32, lo: int = 2048, hi: int = 8192, k: int = 5, vocab: int = 1
 
 @dataclass
 class Fp8Pools:
-    """An e4m3 KV cache holding the same structure as a bf16 workload's pools:
-    uint8 codes [num_blocks][n_kv][bs][d] and one fp32 dequantisation scale per
-    kv head for K and for V."""
+    """An FP8 KV cache holding the same structure as a bf16 workload's pools:
+    uint8 codes [num_blocks][n_kv][bs][d] of format fmt (0 = e4m3, 1 = e5m2)
+    and fp32 dequantisation scales for K and for V: one per kv head
+    ([n_kv]), or one per (block, kv head) tile ([num_blocks][n_kv]) when
+    per_block."""
     k_cache: np.ndarray
     v_cache: np.ndarray
     k_scale: np.ndarray
     v_scale: np.ndarray
+    fmt: int = 0
+    per_block: bool = False
 
 
-def fp8_pools(w: Workload, seed: int = 0) -> Fp8Pools:
-    """Random e4m3 contents for the rows the bf16 workload holds (sign random,
-    exponent field 4..10 -- magnitudes 2^-3..15 --, mantissa random; no
-    encoding step), e4m3 NaN (0x7f) wherever the bf16 pool is NaN (unused
-    rows and spare blocks), and per-head scales 2^-3 * U[0.5, 1.5]."""
-    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 8])))
+def fp8_pools(w: Workload, seed: int = 0, fmt: int = 0, per_block: bool = False) -> Fp8Pools:
+    """Random FP8 contents for the rows the bf16 workload holds (sign random,
+    exponent field 4..10 for e4m3 or 12..18 for e5m2 -- magnitudes 2^-3..15
+    --, mantissa random; no encoding step), the format's NaN (0x7f) wherever
+    the bf16 pool is NaN (unused rows and spare blocks), and scales
+    2^-3 * U[0.5, 1.5] per kv head, or per (block, kv head) with per_block."""
+    g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, 8] if fmt == 0 and not per_block
+                                                                   else [seed, 8, fmt, int(per_block)])))
     out = []
     for pool in (w.k_cache, w.v_cache):
         sign = g.integers(0, 2, size=pool.shape, dtype=np.uint8) << 7
-        expo = g.integers(4, 11, size=pool.shape, dtype=np.uint8) << 3
-        mant = g.integers(0, 8, size=pool.shape, dtype=np.uint8)
+        if fmt == 0:
+            expo = g.integers(4, 11, size=pool.shape, dtype=np.uint8) << 3
+            mant = g.integers(0, 8, size=pool.shape, dtype=np.uint8)
+        else:
+            expo = g.integers(12, 19, size=pool.shape, dtype=np.uint8) << 2
+            mant = g.integers(0, 4, size=pool.shape, dtype=np.uint8)
         codes = sign | expo | mant
         codes[(pool & 0x7FFF) > 0x7F80] = 0x7F
         out.append(codes)
-    ks = (0.125 * g.uniform(0.5, 1.5, size=w.n_kv)).astype(np.float32)
-    vs = (0.125 * g.uniform(0.5, 1.5, size=w.n_kv)).astype(np.float32)
-    return Fp8Pools(out[0], out[1], ks, vs)
+    shape = (w.num_blocks, w.n_kv) if per_block else (w.n_kv,)
+    ks = (0.125 * g.uniform(0.5, 1.5, size=shape)).astype(np.float32)
+    vs = (0.125 * g.uniform(0.5, 1.5, size=shape)).astype(np.float32)
+    return Fp8Pools(out[0], out[1], ks, vs, int(fmt), bool(per_block))
 
 
 @dataclass
