@@ -72,10 +72,12 @@ extern "C" {
 #define PKV_STATUS_BAD_DIST 256  /* a sampling distribution has no positive weight */
 #define PKV_STATUS_TABLE_FULL 512  /* a prefix-cache insert found no free entry */
 #define PKV_STATUS_NOT_FOUND 1024  /* a prefix-cache release named a key not in the table */
+#define PKV_STATUS_BAD_PLAN 2048   /* an attention run found no plan for its shape in the workspace */
 
 /* Attention flags. */
 #define PKV_ATTN_DECODE_CUDA_CORES 1 /* run q_len = 1 rows on the CUDA-core FMA path */
 #define PKV_ATTN_NO_TCGEN05 2        /* run every multi-query tile on mma.sync (no tcgen05 tiles) */
+#define PKV_ATTN_PLAN_FP8 4          /* pkv_attention_plan only: the runs are over e4m3 pools */
 
 /* Library version, 100 * major + minor. */
 int pkv_version(void);
@@ -221,6 +223,52 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, co
                                void* stream);
 
 /*
+ * The two halves of pkv_paged_attention_decode, so that one plan serves many
+ * calls.  A model calls attention once per layer over the same block tables
+ * and lengths ([KVC] 03: the KV bytes a decode step reads are summed over
+ * every layer; [KVC] 05: the block table is per sequence, not per layer), so
+ * the work list -- which depends only on seq_lens and q_lens -- is built once
+ * per decode step and each layer runs over it.
+ *
+ * pkv_attention_plan: the planning part (one small kernel): validates the
+ * lengths (PKV_STATUS_BAD_SEQLEN / BAD_QLEN bits into *status, may be NULL),
+ * picks the partition length and writes the work list into the workspace.
+ * Arguments as in pkv_paged_attention_decode; flags may add
+ * PKV_ATTN_PLAN_FP8 when the runs will be pkv_paged_attention_run_fp8 (then
+ * no other flag).  The workspace (pkv_attention_workspace_bytes, 256-byte
+ * aligned) then holds the plan until the next plan written into it.
+ *
+ * pkv_paged_attention_run / pkv_paged_attention_run_fp8: the attention over
+ * a planned workspace (the attention and combine kernels): the same
+ * computation, outputs and error behaviour as pkv_paged_attention_decode /
+ * pkv_paged_attention_decode_fp8_ex (kv_format, scale_mode as there) for the
+ * lengths the plan was made from.
+ * Every size and flag argument must equal the plan's (num_blocks, scale,
+ * the pools, block tables, q and out are the run's own); a workspace planned
+ * for another shape makes the run write every output row NaN and set
+ * PKV_STATUS_BAD_PLAN (the check is a key of the sizes the plan leaves in the
+ * workspace, so it catches a mismatch, not a changed length array).  Runs and
+ * the plan must be ordered on one stream; the lengths must not change between
+ * the plan and its runs.  Any number of runs may follow one plan: each run
+ * leaves the plan as it found it.
+ */
+int pkv_attention_plan(const int32_t* seq_lens, const int32_t* q_lens, int num_seqs, int total_q,
+                       int max_q_len, int max_seq_len, int max_blocks, int num_q_heads, int num_kv_heads,
+                       int head_dim, int block_size, int partition_tokens, int flags, void* workspace,
+                       size_t workspace_bytes, int32_t* status, void* stream);
+int pkv_paged_attention_run(void* out, const void* q, const void* k_cache, const void* v_cache,
+                            const int32_t* block_tables, int max_blocks, int num_seqs, int total_q,
+                            int max_q_len, int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int num_blocks, float scale, int partition_tokens, int flags,
+                            void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
+int pkv_paged_attention_run_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const float* k_scale, const float* v_scale, int kv_format, int scale_mode,
+                                const int32_t* block_tables, int max_blocks, int num_seqs, int total_q,
+                                int max_q_len, int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                int block_size, int num_blocks, float scale, int partition_tokens, void* workspace,
+                                size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
  * No-allocation variant of pkv_paged_attention_decode.  The source pages have
  * no counterpart to this entry point; it exists for callers that cannot
  * allocate device memory on the call path -- code running inside another
@@ -236,6 +284,10 @@ int pkv_paged_attention_decode(void* out, const void* q, const void* k_cache, co
  *   pkv_attention_workspace_bytes(...) for these sizes exceeds that array.
  * - The first call on a device (with that device current) looks up the
  *   array's device address; make that first call before any stream capture.
+ *   The address is cached per device and per CUDA context (its unique id):
+ *   after cudaDeviceReset, or any other destruction and re-creation of the
+ *   device's context, the next call looks it up again and is then a first
+ *   call in this sense.
  * - All calls share the array.  Calls that overlap on the GPU (other streams,
  *   unordered host threads) race on it and give wrong results; calls ordered
  *   on one stream are safe (each call re-initialises what it uses).
@@ -308,6 +360,63 @@ int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache
                                    int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
                                    float scale, int partition_tokens, void* workspace,
                                    size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * FP8 pools of either format and scale granularity ([KVC] 03, "KV cache
+ * quantization": FP8 as fp8_e4m3 or fp8_e5m2; the pages fix no scaling).
+ *   kv_format   PKV_FP8_E4M3 (as above) or PKV_FP8_E5M2: sign, 5 exponent bits
+ *               (bias 15), 2 mantissa bits, subnormals m * 2^-16, infinities
+ *               and NaN in exponent field 31, largest finite 57344; encoding
+ *               rounds to nearest even and saturates to +-57344 (infinities
+ *               too), NaN is stored as 0x7f
+ *   scale_mode  PKV_FP8_SCALE_PER_HEAD: k_scale, v_scale fp32 [num_kv_heads],
+ *               read only (as the e4m3 entry points above);
+ *               PKV_FP8_SCALE_PER_BLOCK: fp32 [num_blocks][num_kv_heads], one
+ *               scale per (block, kv head) tile.  A block's scales are set when
+ *               the block is opened -- by the append that writes its row 0 --
+ *               from that row's values of each kv head: the smallest power of
+ *               two s = 2^e, e in [-120, 120], with max|x| <= s * FMAX / 2
+ *               (FMAX = 448 for e4m3, 57344 for e5m2; NaN values ignored;
+ *               s = 1 for an all-zero or infinite row).  The opening row then
+ *               uses at most half of the format's range; later rows of the
+ *               block are stored with the same scale and saturate only beyond
+ *               twice its magnitude.  Rows appended in the same call as their
+ *               block's row 0 use the scale that row sets (the call runs a
+ *               small scale kernel first).  The caller initialises the scales
+ *               of blocks that hold data before their row 0 is appended here.
+ *               With per-block V scales the kernel multiplies each token's
+ *               probability (<= 2^8) by its V scale in f16: V scales up to 2^7
+ *               are safe.
+ * pkv_kv_append_fp8_ex: as pkv_kv_append_fp8, in the given format; with
+ *   per-block scales it sets the opened blocks' scales (k_scale, v_scale are
+ *   then written) and stores every row with its block's scales.
+ * pkv_copy_blocks_fp8_ex: as pkv_copy_blocks_fp8; with per-block scales the
+ *   copied blocks' scales are copied too.
+ * pkv_paged_attention_decode_fp8_ex: the attention of
+ *   pkv_paged_attention_decode_fp8 with K_t = fp8(code) * (scale of t's kv
+ *   head, or of t's (block, kv head) tile), V likewise.  e5m2 -> f16 is exact
+ *   (an e5m2 code is the upper byte of its f16).
+ * Every other argument, the workspace and the error behaviour as in the e4m3
+ * entry points; an unknown kv_format or scale_mode is PKV_ERR_UNSUPPORTED.
+ */
+#define PKV_FP8_E4M3 0
+#define PKV_FP8_E5M2 1
+#define PKV_FP8_SCALE_PER_HEAD 0
+#define PKV_FP8_SCALE_PER_BLOCK 1
+int pkv_kv_append_fp8_ex(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const void* k_new,
+                         const void* v_new, const int64_t* slots, int num_tokens, int num_blocks, int block_size,
+                         int num_kv_heads, int head_dim, int kv_format, int scale_mode, int32_t* status,
+                         void* stream);
+int pkv_copy_blocks_fp8_ex(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src_dst,
+                           int num_pairs, int num_blocks, int block_size, int num_kv_heads, int head_dim,
+                           int scale_mode, int32_t* status, void* stream);
+int pkv_paged_attention_decode_fp8_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                      const float* k_scale, const float* v_scale, int kv_format, int scale_mode,
+                                      const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                                      const int32_t* q_lens, int num_seqs, int total_q, int max_q_len,
+                                      int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int num_blocks, float scale, int partition_tokens,
+                                      void* workspace, size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
  * Prefix-cache block lookup ([KVC] 05, "Prefix caching": every full block is

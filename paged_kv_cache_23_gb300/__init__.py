@@ -7,9 +7,11 @@ CUDA kernels.  There is no CPU fallback: if the library is missing or the
 device is not a GB300, calls raise.
 
 Entry points (same names as the C ABI without the ``pkv_`` prefix):
-    slot_mapping, kv_append, copy_blocks, gather_kv,
+    slot_mapping, kv_append, kv_append_paged, copy_blocks, gather_kv,
     attention_auto_partition, attention_workspace_bytes,
-    paged_attention_decode, spec_accept_greedy
+    paged_attention_decode, attention_plan, paged_attention_run,
+    spec_accept_greedy, spec_accept_sample, the e4m3 variants, the prefix
+    cache and the no-allocation attention
 """
 from __future__ import annotations
 
@@ -34,8 +36,12 @@ PKV_STATUS_BAD_TOKEN = 128
 PKV_STATUS_BAD_DIST = 256
 PKV_STATUS_TABLE_FULL = 512
 PKV_STATUS_NOT_FOUND = 1024
+PKV_STATUS_BAD_PLAN = 2048
 PKV_ATTN_DECODE_CUDA_CORES = 1
 PKV_ATTN_NO_TCGEN05 = 2  # multi-query tiles on mma.sync instead of tcgen05
+PKV_ATTN_PLAN_FP8 = 4    # attention_plan only: the runs are over FP8 pools
+PKV_FP8_E4M3, PKV_FP8_E5M2 = 0, 1
+PKV_FP8_SCALE_PER_HEAD, PKV_FP8_SCALE_PER_BLOCK = 0, 1
 PKV_ERR_SCRATCH_LIMIT = -8
 
 _P = ctypes.c_void_p
@@ -65,6 +71,15 @@ _SIGS = {
     "pkv_copy_blocks_fp8": ([_P, _P, _P, _I, _I, _I, _I, _I, _P, _P], _I),
     "pkv_paged_attention_decode_fp8": ([_P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                         _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P], _I),
+    "pkv_attention_plan": ([_P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P, _P], _I),
+    "pkv_paged_attention_run": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.c_float, _I, _I,
+                                 _P, ctypes.c_size_t, _P, _P], _I),
+    "pkv_paged_attention_run_fp8": ([_P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                     ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P], _I),
+    "pkv_kv_append_fp8_ex": ([_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_copy_blocks_fp8_ex": ([_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P], _I),
+    "pkv_paged_attention_decode_fp8_ex": ([_P, _P, _P, _P, _P, _P, _I, _I, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I,
+                                           _I, _I, _I, ctypes.c_float, _I, _P, ctypes.c_size_t, _P, _P], _I),
     "pkv_noalloc_scratch_bytes": ([], ctypes.c_size_t),
     "pkv_wait_selftest": ([ctypes.c_longlong, _P, _P], _I),
     "pkv_paged_attention_decode_noalloc": ([_P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _I,
@@ -226,6 +241,62 @@ def paged_attention_decode(out, q, k_cache, v_cache, block_tables, seq_lens, q_l
     _check(rc, "pkv_paged_attention_decode")
 
 
+def attention_plan(seq_lens, q_lens, total_q, max_blocks, num_q_heads, num_kv_heads, head_dim, block_size,
+                   max_seq_len, workspace, partition_tokens=0, flags=0, status=None, stream=None, max_q_len=None):
+    """The planning half of paged_attention_decode: the work list for these
+    lengths, written into workspace, for any number of paged_attention_run calls."""
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(q_lens, "q_lens", torch.int32)
+    _dev(workspace, "workspace")
+    rc = lib().pkv_attention_plan(_ptr(seq_lens), _ptr(q_lens), seq_lens.numel(), int(total_q),
+                                  _max_q(max_q_len, total_q), int(max_seq_len), int(max_blocks), int(num_q_heads),
+                                  int(num_kv_heads), int(head_dim), int(block_size), int(partition_tokens),
+                                  int(flags), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _ptr(status), _stream(stream))
+    _check(rc, "pkv_attention_plan")
+
+
+def paged_attention_run(out, q, k_cache, v_cache, block_tables, num_seqs, max_seq_len, scale, workspace,
+                        partition_tokens=0, flags=0, status=None, stream=None, max_q_len=None):
+    """The attention half of paged_attention_decode over a planned workspace."""
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _dev(t, n, torch.bfloat16)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(workspace, "workspace")
+    nb, nkv, bs, d = k_cache.shape
+    total_q, nq, _ = q.shape
+    rc = lib().pkv_paged_attention_run(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                       block_tables.shape[1], int(num_seqs), total_q, _max_q(max_q_len, total_q),
+                                       int(max_seq_len), nq, nkv, d, bs, nb, float(scale), int(partition_tokens),
+                                       int(flags), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _ptr(status), _stream(stream))
+    _check(rc, "pkv_paged_attention_run")
+
+
+def paged_attention_run_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, num_seqs, max_seq_len, scale,
+                            workspace, partition_tokens=0, status=None, stream=None, max_q_len=None,
+                            kv_format=PKV_FP8_E4M3, scale_mode=PKV_FP8_SCALE_PER_HEAD):
+    """paged_attention_run over FP8 pools (plan made with PKV_ATTN_PLAN_FP8)."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_cache, "k_cache", torch.uint8)
+    _dev(v_cache, "v_cache", torch.uint8)
+    _dev(k_scale, "k_scale", torch.float32)
+    _dev(v_scale, "v_scale", torch.float32)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(workspace, "workspace")
+    nb, nkv, bs, d = k_cache.shape
+    total_q, nq, _ = q.shape
+    rc = lib().pkv_paged_attention_run_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                           _ptr(v_scale), int(kv_format), int(scale_mode), _ptr(block_tables),
+                                           block_tables.shape[1], int(num_seqs),
+                                           total_q, _max_q(max_q_len, total_q), int(max_seq_len), nq, nkv, d, bs, nb,
+                                           float(scale), int(partition_tokens), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _ptr(status),
+                                           _stream(stream))
+    _check(rc, "pkv_paged_attention_run_fp8")
+
+
 def spec_accept_greedy(logits, draft, argmax_out, accepted, next_token, stream=None):
     """a9: greedy acceptance; logits fp32 [B][k+1][V], draft int32 [B][k]."""
     _dev(logits, "logits", torch.float32)
@@ -350,6 +421,65 @@ def paged_attention_decode_fp8(out, q, k_cache, v_cache, k_scale, v_scale, block
                                               workspace.numel() * workspace.element_size(), _ptr(status),
                                               _stream(stream))
     _check(rc, "pkv_paged_attention_decode_fp8")
+
+
+def _fp8_args(k_cache, v_cache, k_scale, v_scale):
+    _dev(k_cache, "k_cache", torch.uint8)
+    _dev(v_cache, "v_cache", torch.uint8)
+    _dev(k_scale, "k_scale", torch.float32)
+    _dev(v_scale, "v_scale", torch.float32)
+
+
+def kv_append_fp8_ex(k_cache, v_cache, k_scale, v_scale, k_new, v_new, slots, kv_format=PKV_FP8_E4M3,
+                     scale_mode=PKV_FP8_SCALE_PER_HEAD, status=None, stream=None):
+    """Quantising append into FP8 pools of either format; with per-block scales
+    ([num_blocks][n_kv]) the blocks this call opens get their scales set."""
+    _fp8_args(k_cache, v_cache, k_scale, v_scale)
+    _dev(k_new, "k_new", torch.bfloat16)
+    _dev(v_new, "v_new", torch.bfloat16)
+    _dev(slots, "slots", torch.int64)
+    nb, nkv, bs, d = k_cache.shape
+    rc = lib().pkv_kv_append_fp8_ex(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(k_new),
+                                    _ptr(v_new), _ptr(slots), slots.numel(), nb, bs, nkv, d, int(kv_format),
+                                    int(scale_mode), _ptr(status), _stream(stream))
+    _check(rc, "pkv_kv_append_fp8_ex")
+
+
+def copy_blocks_fp8_ex(k_cache, v_cache, k_scale, v_scale, src_dst, scale_mode=PKV_FP8_SCALE_PER_HEAD, status=None,
+                       stream=None):
+    """Copy-on-write block copies in FP8 pools (and the blocks' scales with per-block scales)."""
+    _fp8_args(k_cache, v_cache, k_scale, v_scale)
+    _dev(src_dst, "src_dst", torch.int32)
+    nb, nkv, bs, d = k_cache.shape
+    rc = lib().pkv_copy_blocks_fp8_ex(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(src_dst),
+                                      src_dst.shape[0], nb, bs, nkv, d, int(scale_mode), _ptr(status),
+                                      _stream(stream))
+    _check(rc, "pkv_copy_blocks_fp8_ex")
+
+
+def paged_attention_decode_fp8_ex(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, q_lens,
+                                  max_seq_len, scale, workspace, kv_format=PKV_FP8_E4M3,
+                                  scale_mode=PKV_FP8_SCALE_PER_HEAD, partition_tokens=0, status=None, stream=None,
+                                  max_q_len=None):
+    """Paged attention over FP8 pools of either format and scale granularity."""
+    _dev(out, "out", torch.bfloat16)
+    _dev(q, "q", torch.bfloat16)
+    _fp8_args(k_cache, v_cache, k_scale, v_scale)
+    _dev(block_tables, "block_tables", torch.int32)
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(q_lens, "q_lens", torch.int32)
+    _dev(workspace, "workspace")
+    nb, nkv, bs, d = k_cache.shape
+    total_q, nq, _ = q.shape
+    rc = lib().pkv_paged_attention_decode_fp8_ex(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                                 _ptr(v_scale), int(kv_format), int(scale_mode), _ptr(block_tables),
+                                                 block_tables.shape[1], _ptr(seq_lens), _ptr(q_lens),
+                                                 seq_lens.numel(), total_q, _max_q(max_q_len, total_q),
+                                                 int(max_seq_len), nq, nkv, d, bs, nb, float(scale),
+                                                 int(partition_tokens), _ptr(workspace),
+                                                 workspace.numel() * workspace.element_size(), _ptr(status),
+                                                 _stream(stream))
+    _check(rc, "pkv_paged_attention_decode_fp8_ex")
 
 
 def spec_accept_sample(p, q, draft, r, s, accepted, next_token, status=None, stream=None):

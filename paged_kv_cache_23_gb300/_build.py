@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
 SOURCES = ["pkv_api.cu", "pkv_cache_ops.cu", "pkv_spec.cu", "pkv_prefix.cu", "pkv_attention_d64.cu", "pkv_attention_d128.cu",
-           "pkv_attention_host.cu", "pkv_noalloc.cu"]
+           "pkv_attention_fp8.cu", "pkv_attention_host.cu", "pkv_noalloc.cu"]
 HEADERS = ["pkv_common.cuh", "pkv_host.h", "pkv_attention.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr", "-I", INCLUDE,

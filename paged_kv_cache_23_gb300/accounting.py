@@ -19,11 +19,13 @@ def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, bytes_
     return 2 * num_layers * num_kv_heads * head_dim * bytes_per_value
 
 
-def step_bytes(w, bytes_per_value: int = 2, kv_bytes: int | None = None) -> dict:
+def step_bytes(w, bytes_per_value: int = 2, kv_bytes: int | None = None, block_scales: bool = False) -> dict:
     """Algorithmic bytes of one step over workload ``w`` (one layer).
 
-    kv_bytes: bytes per cached K/V value (1 for an e4m3 pool, section 03 "KV
+    kv_bytes: bytes per cached K/V value (1 for an FP8 pool, section 03 "KV
     cache quantization"); queries, outputs and appended rows stay bf16.
+    block_scales: the FP8 pool has a K and a V scale (fp32) per (block, kv
+    head) tile, read with the block.
 
     kv_logical  every sequence's visible K/V, counted once per sequence (the
                 query heads of a group share one read)
@@ -53,8 +55,10 @@ def step_bytes(w, bytes_per_value: int = 2, kv_bytes: int | None = None) -> dict
         first = np.ones(len(r), bool)
         first[1:] = r[1:, 0] != r[:-1, 0]
         kv_unique = int(r[first, 1].sum()) * per_row
+        n_unique_blocks = int(first.sum())
     else:
         kv_unique = 0
+        n_unique_blocks = 0
     q_bytes = w.total_q * w.n_q * w.head_dim * bytes_per_value
     o_bytes = q_bytes
     tables = int(sum(-(-int(n) // bs) for n in L)) * 4 + 2 * 4 * w.num_seqs
@@ -62,11 +66,22 @@ def step_bytes(w, bytes_per_value: int = 2, kv_bytes: int | None = None) -> dict
     new_row = w.n_kv * w.head_dim * bytes_per_value * 2
     append = t_new * (new_row + per_row) + t_new * 8  # read new rows, write them (cache format), read slots
     cow = int(w.cow.shape[0]) * 2 * (w.n_kv * bs * w.head_dim * kvb * 2)
-    attn_unique = kv_unique + q_bytes + o_bytes + tables
-    attn_logical = kv_logical + q_bytes + o_bytes + tables
+    scales_unique = scales_logical = 0
+    if block_scales:
+        per_blk = w.n_kv * 8                                     # K and V scale, fp32, every kv head
+        scales_unique = n_unique_blocks * per_blk
+        scales_logical = int(sum(-(-int(n) // bs) for n in L)) * per_blk
+        cow += int(w.cow.shape[0]) * 2 * per_blk
+        # the append sets the scales of the blocks it opens (positions at a block's row 0)
+        A = w.append_lens.astype(np.int64)
+        opened = sum(len(range(-(-(int(L[b]) - int(A[b])) // bs) * bs, int(L[b]), bs)) for b in range(w.num_seqs))
+        append += int(opened) * per_blk
+    attn_unique = kv_unique + q_bytes + o_bytes + tables + scales_unique
+    attn_logical = kv_logical + q_bytes + o_bytes + tables + scales_logical
     return dict(kv_logical=kv_logical, kv_unique=kv_unique, q=q_bytes, o=o_bytes, tables=tables,
-                append=append, cow=cow, attention_unique=attn_unique, attention_logical=attn_logical,
-                step_unique=attn_unique + append + cow, step_logical=attn_logical + append + cow)
+                append=append, cow=cow, scales=scales_unique, attention_unique=attn_unique,
+                attention_logical=attn_logical, step_unique=attn_unique + append + cow,
+                step_logical=attn_logical + append + cow)
 
 
 def accept_greedy_bytes(w) -> int:

@@ -111,6 +111,7 @@ extern "C" const char* pkv_status_string(int bit) {
         case PKV_STATUS_BAD_DIST: return "sampling distribution without positive weight";
         case PKV_STATUS_TABLE_FULL: return "prefix-cache table full";
         case PKV_STATUS_NOT_FOUND: return "prefix-cache key not found";
+        case PKV_STATUS_BAD_PLAN: return "no attention plan for this shape in the workspace";
         default: return "unknown status bit";
     }
 }

@@ -49,6 +49,8 @@ constexpr int kCWarps = 8;                  // consumer warps
 constexpr int kCThreads = kCWarps * 32;
 constexpr int kThreads = kCThreads + 32;    // + producer warp
 constexpr int kMaxHPS = 8;                  // kv heads per stage
+constexpr int kDecCols = 16;                // (query, q head) columns of a transposed tensor-core tile
+constexpr int kTcMinCols = 8;               // multi-query rows of more columns run as tcgen05 tiles (when enabled)
 constexpr int kRingSlots = 3;
 constexpr int kSlots = 4;                   // item descriptors in flight
 constexpr int kClaimAhead = 6;              // stages before an item's end at which the next is claimed
@@ -94,13 +96,21 @@ struct AttnParams {
     float* part_o;       // [(row * n_q + h) * np_max + part][D]
     float2* part_ml;     // [(row * n_q + h) * np_max + part] = (m in log2 units, l)
     int32_t* status;
-    const float* k_scale;  // e4m3 pools: dequantisation scale per kv head (null for bf16)
+    const float* k_scale;  // FP8 pools: dequantisation scales per kv head, or [num_blocks][n_kv] (null for bf16)
     const float* v_scale;
+    int scale_pb;          // FP8 pools: 1 = a scale per (block, kv head) tile
     int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, row_bytes;
     int tc;              // tcgen05 tiles possible: tensor memory is allocated when the plan made some
     int tc_pair;         // tcgen05 stages of block_size 16: one V box holds both slabs of a block
+    int plan_key;        // shape key the workspace's plan must carry (hdr[4]); else nothing runs
     float scale_log2;    // scale * log2(e): scores live in base-2 units
 };
+
+// Workspace header (ints): [0] item count, [1] queue head (reset to 0 by the
+// planning kernel and again by each call's combine kernel, so one plan serves
+// any number of calls), [2] partition length, [3] tcgen05 tiles present,
+// [4] key of the shape the plan was made for.
+enum { HDR_ITEMS = 0, HDR_HEAD = 1, HDR_P = 2, HDR_TC = 3, HDR_KEY = 4 };
 
 // Stage geometry of a pool: bf16 (2-byte values, 3 ring slots of 64 KB at the
 // 8B shape) or e4m3 (1-byte values, 6 ring slots of 32 KB -- the same 192 KB
@@ -123,6 +133,9 @@ struct Smem {
         float pbuf[kCWarps][kTileT * 8];                     // decode on CUDA cores: p[token][head]
         uint8_t qbuf[kTC ? kTcRows * D * 2 : 16];            // tcgen05 tile: Q, K-major, 128-byte swizzle
     };
+    // FP8 pools with per-block scales: the K and V scales of each block of a
+    // stage for its kv heads, [slot][K,V][block of the stage][head of the stage]
+    float scl[F8 ? G::kSlots : 1][2][F8 ? kTileT : 1][kMaxHPS];
     Desc desc[kSlots];
     int poison[kSlots];
     int abort;
@@ -255,7 +268,7 @@ __device__ __forceinline__ bool produce_tc(Smem<D, F8>& sm, const TMaps* tm, con
         int tab_next = tab_base + 32 + lane < e_lim ? __ldg(bt + tab_base + 32 + lane) : 0;
         const int j_claim = max(0, n + 1 - kClaimAhead);
         for (int j = 0; j <= n; ++j, ++g) {
-            if (!helper && j == j_claim && lane == 0) next = atomicAdd(&p.hdr[1], 1);
+            if (!helper && j == j_claim && lane == 0) next = atomicAdd(&p.hdr[HDR_HEAD], 1);
             // V (stage j - 1) trails K (stage j) by one stage: the table window
             // follows V's first entry; K's entries are at most 8 further
             const int tk = (tb + j) * kTcT, tvv = tk - kTcT;
@@ -319,11 +332,13 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
         prefetch_tmap(&tm->k[lane]);
         prefetch_tmap(&tm->v[lane]);
     }
-    const int num_items = p.hdr[0];
-    const int P = p.hdr[2];  // partition length the planning kernel chose
+    // a workspace whose plan was made for another shape runs nothing (the
+    // combine kernel then writes every output row NaN and reports it)
+    const int num_items = p.hdr[HDR_KEY] == p.plan_key ? p.hdr[HDR_ITEMS] : 0;
+    const int P = p.hdr[HDR_P];  // partition length the planning kernel chose
     const int bsr = p.bs < kTileT ? p.bs : kTileT;
     int next = 0;
-    if (lane == 0) next = atomicAdd(&p.hdr[1], 1);
+    if (lane == 0) next = atomicAdd(&p.hdr[HDR_HEAD], 1);
     next = __shfl_sync(kFull, next, 0);
     uint32_t g = 0;
     for (int islot = 0;; ++islot) {
@@ -367,7 +382,7 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
         // CTA never holds a second item for long and the queue balances finely
         const int i_claim = max(tb, te - kClaimAhead);
         for (int i = tb; i < te; ++i, ++g) {
-            if (i == i_claim && lane == 0) next = atomicAdd(&p.hdr[1], 1);
+            if (i == i_claim && lane == 0) next = atomicAdd(&p.hdr[HDR_HEAD], 1);
             const int t0 = i * kTileT;
             const int tvalid = min(kTileT, d.t_end - t0);
             const int e0 = t0 / p.bs;
@@ -389,6 +404,18 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
             if (!okb) my = 0;
             const unsigned badmask = __ballot_sync(kFull, !okb);
             const int s = (int)(g % RS);
+            // FP8 pools with per-block scales: lane 2e + v loads the K (v = 0)
+            // or V (v = 1) scales of the stage's block e for the group's kv
+            // heads now, and stores them into the slot's scale rows once the
+            // slot is free -- before the barrier is armed, so the consumers'
+            // wait on it orders them
+            float scv[kMaxHPS];
+            const bool pbs = F8 && p.scale_pb != 0;
+            if (pbs && in) {
+                const float* src = ((lane & 1) ? p.v_scale : p.k_scale) + (long long)my * p.n_kv + d.hg * d.hps;
+#pragma unroll
+                for (int h = 0; h < kMaxHPS; ++h) scv[h] = h < d.hps ? __ldg(src + h) : 0.f;
+            }
             bool got = true;
             if (lane == 0) {
                 if (badmask) {
@@ -396,12 +423,20 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
                     report(p.status, PKV_STATUS_BAD_BLOCK);
                 }
                 got = mbar_wait(&sm.empty[s], ((g / RS) & 1) ^ 1, abort);
-                if (got) mbar_arrive_expect_tx(&sm.full[s], 2u * ne * op_bytes);
             }
             if (!__shfl_sync(kFull, got, 0)) {
                 stopped = true;  // never arm a barrier whose previous phase is still open
                 break;
             }
+            if (pbs) {
+                if (in) {
+#pragma unroll
+                    for (int h = 0; h < kMaxHPS; ++h)
+                        if (h < d.hps) sm.scl[s][lane & 1][lane >> 1][h] = scv[h];
+                }
+                __syncwarp();
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], 2u * ne * op_bytes);
             // one box per tensor and block: every head of the group, 16 (or block_size) rows
             if (in) {
                 const int row0 = p.bs > kTileT ? (t0 % p.bs) : 0;
@@ -420,14 +455,10 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
         if (stopped) break;
         next = __shfl_sync(kFull, next, 0);
     }
-    // drain: wait (bounded) until every issued stage has landed
-    if (lane == 0) {
-        for (int s = 0; s < RS; ++s) {
-            if (g <= (uint32_t)s) continue;
-            const uint32_t last = g - 1 - ((g - 1 - s) % RS);
-            mbar_wait(&sm.full[s], (last / RS) & 1, abort);
-        }
-    }
+    // drain: wait until every issued stage has landed, bounded by time only --
+    // an abort must not cut it short, or the CTA could exit with copies still
+    // landing in its shared memory
+    if (lane == 0) drain_ring<RS>(sm.full, g);
 }
 
 // ---------------------------------------------------------------------------
@@ -640,15 +671,23 @@ __device__ __forceinline__ void decode_item(Smem<D, false>& sm, const AttnParams
 }
 
 // ---------------------------------------------------------------------------
-// Decode item on tensor cores (q_len = 1): warp w < hps owns kv head
-// hg * hps + w.  The product is taken transposed, tokens on the M axis and the
-// G <= 8 query heads of the group on N:
-//   S^T[16 x 8]  = K_tile[16 x D] . Q^T[D x 8]          (D/16 mma m16n8k16)
-//   O^T[D x 8]  += V_tile^T[D x 16] . P^T[16 x 8]       (D/16 mma)
-// so half of N is padding at G = 4 instead of three quarters of M.  P^T's
-// B fragments are the S^T accumulators transposed in registers (movmatrix).
+// Decode and short multi-query items on tensor cores: warp w < hps owns kv
+// head hg * hps + w.  The product is taken transposed, tokens on the M axis
+// and the columns -- (query, q head) pairs of the query tile, 8 per n-tile,
+// NTN n-tiles -- on N:
+//   S^T[16 x 8 NTN]  = K_tile[16 x D] . Q^T[D x 8 NTN]      (NTN D/16 mma m16n8k16)
+//   O^T[D x 8 NTN]  += V_tile^T[D x 16] . P^T[16 x 8 NTN]   (NTN D/16 mma)
+// A decode row (q_len = 1) is a tile of one query: its g <= 8 heads fill one
+// n-tile, so g = 4 pads half of N instead of three quarters of M.  A short
+// multi-query row of q_len <= 16 / g queries is one tile of two n-tiles, so
+// every kv head of a block still shares one stage (32 KB copies of K and of V
+// at the 8B shape) and each column applies its query's causal limit.  (Three
+// n-tiles were measured: the accumulators and query fragments of 24 columns
+// do not fit the warp's 168 registers, and the spills made a speculative
+// verification twice as slow as on mma.sync row tiles.)  P^T's B fragments
+// are the S^T accumulators transposed in registers (movmatrix).
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, int NTN>
 __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
                                                uint32_t gbase, int ntiles, int si, volatile int* abort) {
     constexpr int NB = D / 64;
@@ -659,30 +698,41 @@ __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnPar
     const int hps_lb = d.hps << lb, h_lb = warp << lb;
     const int kvh = d.hg * d.hps + warp;
     const int qd = lane & 3, qr = lane >> 2;
-    // columns c < nq * G are (query c / G of the tile, q head c % G); a decode
-    // row is a tile of one query, columns = the g heads of the group
+    // columns c < nq * G are (query c / G of the tile, q head c % G)
     const int ncols = d.nq * G;
-    // Q^T as B fragments: n = column qr, k = dims
-    uint32_t qb[NT][2];
-    {
+    // Q^T as B fragments: n = column 8 nt + qr, k = dims
+    uint32_t qb[NTN][NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt) {
+        const int c = 8 * nt + qr;
         const uint32_t* qrow =
-            (active && qr < ncols)
+            (active && c < ncols)
                 ? reinterpret_cast<const uint32_t*>(
-                      p.q + ((long long)(d.q_row0 + qr / G) * p.n_q + (long long)kvh * G + qr % G) * D)
+                      p.q + ((long long)(d.q_row0 + c / G) * p.n_q + (long long)kvh * G + c % G) * D)
                 : nullptr;
 #pragma unroll
         for (int ks = 0; ks < NT; ++ks) {
-            qb[ks][0] = qrow ? qrow[8 * ks + qd] : 0u;
-            qb[ks][1] = qrow ? qrow[8 * ks + 4 + qd] : 0u;
+            qb[nt][ks][0] = qrow ? qrow[8 * ks + qd] : 0u;
+            qb[nt][ks][1] = qrow ? qrow[8 * ks + 4 + qd] : 0u;
         }
     }
-    float o[NT][4];  // O^T tile mt: (dim 16mt + qr [+8], head 2qd [+1])
+    float o[NT][NTN][4];  // O^T tile (mt, nt): (dim 16 mt + qr [+8], column 8 nt + 2 qd [+1])
 #pragma unroll
-    for (int mt = 0; mt < NT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // columns 2qd, 2qd + 1
-    // last visible position of columns 2qd and 2qd + 1 (their query's causal limit)
-    const int lim0 = 2 * qd < ncols ? d.t_vis - d.nq + (2 * qd) / G : -1;
-    const int lim1 = 2 * qd + 1 < ncols ? d.t_vis - d.nq + (2 * qd + 1) / G : -1;
+    for (int mt = 0; mt < NT; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+    // per column (8 nt + 2 qd + j): reference maximum, partial sum, last visible position
+    float m[NTN][2], l[NTN][2];
+    int lim[NTN][2];
+#pragma unroll
+    for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c = 8 * nt + 2 * qd + j;
+            m[nt][j] = -INFINITY;
+            l[nt][j] = 0.f;
+            lim[nt][j] = c < ncols ? d.t_vis - d.nq + c / G : -1;
+        }
     const int mi = lane >> 3, mr = lane & 7;
     const int a_tok = ((mi & 1) << 3) + mr, a_hi = mi >> 1;   // K: (t0-7,lo) (t8-15,lo) (t0-7,hi) (t8-15,hi)
     const int v_tok = ((mi >> 1) << 3) + mr, v_hi = mi & 1;   // V: (t0-7,lo) (t0-7,hi) (t8-15,lo) (t8-15,hi)
@@ -700,111 +750,137 @@ __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnPar
         const uint32_t vb = smem_u32(&sm.kv[s][1][0]);
         const int t0 = (tb + i) * kTileT;
         const int nvalid = min(kTileT, d.t_end - t0);
-        // S^T, two accumulators to halve the dependent mma chain
-        float ca[4] = {0.f, 0.f, 0.f, 0.f}, cb[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T; with one n-tile, two accumulators halve the dependent mma chain
+        float ca[NTN][4], cb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) ca[nt][0] = ca[nt][1] = ca[nt][2] = ca[nt][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < NT; ++ks) {
             const int chunk = 2 * ks + a_hi;
             const int R = srow(h_lb, a_tok, chunk >> 3, hps_lb, lb, NB);
             uint32_t a0, a1, a2, a3;
             ldsm_x4(kb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
-            mma_bf16_16816((ks & 1) ? cb : ca, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+            if constexpr (NTN == 1) {
+                mma_bf16_16816((ks & 1) ? cb : ca[0], a0, a1, a2, a3, qb[0][ks][0], qb[0][ks][1]);
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < NTN; ++nt) mma_bf16_16816(ca[nt], a0, a1, a2, a3, qb[nt][ks][0], qb[nt][ks][1]);
+            }
         }
-        // (token qr, column 2qd), (qr, 2qd+1), (qr+8, 2qd), (qr+8, 2qd+1)
+        if constexpr (NTN == 1) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) ca[0][j] += cb[j];
+        }
+        // (token qr, column 2qd), (qr, 2qd+1), (qr+8, 2qd), (qr+8, 2qd+1) of each n-tile
         const bool va = qr < nvalid, vb8 = qr + 8 < nvalid;
         const int ta = t0 + qr, tb8 = t0 + qr + 8;
-        const float s0 = va && ta <= lim0 ? (ca[0] + cb[0]) * p.scale_log2 : -INFINITY;
-        const float s1 = va && ta <= lim1 ? (ca[1] + cb[1]) * p.scale_log2 : -INFINITY;
-        const float s2 = vb8 && tb8 <= lim0 ? (ca[2] + cb[2]) * p.scale_log2 : -INFINITY;
-        const float s3 = vb8 && tb8 <= lim1 ? (ca[3] + cb[3]) * p.scale_log2 : -INFINITY;
-        // The reference maxima m0, m1 move only when a new score exceeds them
-        // by more than kRescaleSlack (base-2 units), so most stages need no
-        // max reduction and no rescale of O; probabilities stay <= 2^slack.
-        // The softmax is unchanged: O and l are relative to the same m.
-        const bool fits = __all_sync(kFull, fmaxf(s0, s2) <= m0 + kRescaleSlack && fmaxf(s1, s3) <= m1 + kRescaleSlack);
-        if (!fits) {
-            float x0 = fmaxf(s0, s2), x1 = fmaxf(s1, s3);
+        float sv[NTN][4];
+        bool fits = true;
 #pragma unroll
-            for (int o8 = 4; o8 < 32; o8 <<= 1) {
-                x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, o8));
-                x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, o8));
-            }
-            const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-            const float c0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0), c1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
-            l0 *= c0;
-            l1 *= c1;
-#pragma unroll
-            for (int mt = 0; mt < NT; ++mt) {
-                o[mt][0] *= c0;
-                o[mt][1] *= c1;
-                o[mt][2] *= c0;
-                o[mt][3] *= c1;
-            }
-            m0 = n0;
-            m1 = n1;
+        for (int nt = 0; nt < NTN; ++nt) {
+            sv[nt][0] = va && ta <= lim[nt][0] ? ca[nt][0] * p.scale_log2 : -INFINITY;
+            sv[nt][1] = va && ta <= lim[nt][1] ? ca[nt][1] * p.scale_log2 : -INFINITY;
+            sv[nt][2] = vb8 && tb8 <= lim[nt][0] ? ca[nt][2] * p.scale_log2 : -INFINITY;
+            sv[nt][3] = vb8 && tb8 <= lim[nt][1] ? ca[nt][3] * p.scale_log2 : -INFINITY;
+            fits = fits && fmaxf(sv[nt][0], sv[nt][2]) <= m[nt][0] + kRescaleSlack &&
+                   fmaxf(sv[nt][1], sv[nt][3]) <= m[nt][1] + kRescaleSlack;
         }
-        const float u0 = m0 == -INFINITY ? 0.f : m0, u1 = m1 == -INFINITY ? 0.f : m1;
-        const float p0 = exp2f(s0 - u0), p1 = exp2f(s1 - u1), p2 = exp2f(s2 - u0), p3 = exp2f(s3 - u1);
-        // l stays a per-lane partial sum (this lane's tokens); reduced once at the end
-        l0 += p0 + p2;
-        l1 += p1 + p3;
-        const uint32_t pb0 = movmatrix_trans(float2_to_bf16x2(p0, p1));  // (tokens 2qd, 2qd+1; head qr)
-        const uint32_t pb1 = movmatrix_trans(float2_to_bf16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; head qr)
-        if (nvalid == kTileT) {
+        // The reference maxima move only when a new score exceeds them by more
+        // than kRescaleSlack (base-2 units), so most stages need no max
+        // reduction and no rescale of O; probabilities stay <= 2^slack.  The
+        // softmax is unchanged: O and l are relative to the same m.
+        if (!__all_sync(kFull, fits)) {
 #pragma unroll
-            for (int mt = 0; mt < NT; ++mt) {
-                const int chunk = 2 * mt + v_hi;
-                const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
-                mma_bf16_16816(o[mt], a0, a1, a2, a3, pb0, pb1);
-            }
-        } else {
-            // V rows past the valid tokens may hold anything (even NaN): zero them
-            const uint32_t klo = (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u);
-            const uint32_t khi = (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (9 + 2 * qd < nvalid ? 0xffff0000u : 0u);
+            for (int nt = 0; nt < NTN; ++nt) {
+                float x0 = fmaxf(sv[nt][0], sv[nt][2]), x1 = fmaxf(sv[nt][1], sv[nt][3]);
 #pragma unroll
-            for (int mt = 0; mt < NT; ++mt) {
-                const int chunk = 2 * mt + v_hi;
-                const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
-                mma_bf16_16816(o[mt], a0 & klo, a1 & klo, a2 & khi, a3 & khi, pb0, pb1);
+                for (int o8 = 4; o8 < 32; o8 <<= 1) {
+                    x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, o8));
+                    x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, o8));
+                }
+                const float n0 = fmaxf(m[nt][0], x0), n1 = fmaxf(m[nt][1], x1);
+                const float c0 = n0 == -INFINITY ? 1.f : exp2f(m[nt][0] - n0);
+                const float c1 = n1 == -INFINITY ? 1.f : exp2f(m[nt][1] - n1);
+                l[nt][0] *= c0;
+                l[nt][1] *= c1;
+#pragma unroll
+                for (int mt = 0; mt < NT; ++mt) {
+                    o[mt][nt][0] *= c0;
+                    o[mt][nt][1] *= c1;
+                    o[mt][nt][2] *= c0;
+                    o[mt][nt][3] *= c1;
+                }
+                m[nt][0] = n0;
+                m[nt][1] = n1;
             }
+        }
+        uint32_t pb0[NTN], pb1[NTN];
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt) {
+            const float u0 = m[nt][0] == -INFINITY ? 0.f : m[nt][0], u1 = m[nt][1] == -INFINITY ? 0.f : m[nt][1];
+            const float p0 = exp2f(sv[nt][0] - u0), p1 = exp2f(sv[nt][1] - u1);
+            const float p2 = exp2f(sv[nt][2] - u0), p3 = exp2f(sv[nt][3] - u1);
+            // l stays a per-lane partial sum (this lane's tokens); reduced once at the end
+            l[nt][0] += p0 + p2;
+            l[nt][1] += p1 + p3;
+            pb0[nt] = movmatrix_trans(float2_to_bf16x2(p0, p1));  // (tokens 2qd, 2qd+1; column qr)
+            pb1[nt] = movmatrix_trans(float2_to_bf16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; column qr)
+        }
+        // V rows past the valid tokens may hold anything (even NaN): zero them
+        const bool part = nvalid < kTileT;
+        const uint32_t klo =
+            part ? (2 * qd < nvalid ? 0x0000ffffu : 0u) | (2 * qd + 1 < nvalid ? 0xffff0000u : 0u) : 0xffffffffu;
+        const uint32_t khi =
+            part ? (8 + 2 * qd < nvalid ? 0x0000ffffu : 0u) | (9 + 2 * qd < nvalid ? 0xffff0000u : 0u) : 0xffffffffu;
+#pragma unroll
+        for (int mt = 0; mt < NT; ++mt) {
+            const int chunk = 2 * mt + v_hi;
+            const int R = srow(h_lb, v_tok, chunk >> 3, hps_lb, lb, NB);
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_t(vb + R * 128 + (((chunk & 7) ^ (R & 7)) << 4), a0, a1, a2, a3);
+            if (part) {
+                a0 &= klo;
+                a1 &= klo;
+                a2 &= khi;
+                a3 &= khi;
+            }
+#pragma unroll
+            for (int nt = 0; nt < NTN; ++nt) mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, pb0[nt], pb1[nt]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[s]);  // one arrival per consumer warp and stage
     }
     if (!active) return;
-#pragma unroll
-    for (int o8 = 4; o8 < 32; o8 <<= 1) {
-        l0 += __shfl_xor_sync(kFull, l0, o8);
-        l1 += __shfl_xor_sync(kFull, l1, o8);
-    }
     const bool poisoned = sm.poison[si] != 0;  // final after the last stage's wait
     const float qnan = __int_as_float(0x7fc00000);
-    const float mh[2] = {m0, m1}, lh[2] = {l0, l1};
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        const int c = 2 * qd + j;
-        if (c >= ncols) continue;
-        const long long orow = (long long)(d.q_row0 + c / G) * p.n_q + (long long)kvh * G + c % G;
-        if (d.nparts == 1) {
-            const float inv = 1.0f / lh[j];
-            __nv_bfloat16* dst = p.out + orow * D + qr;
+    for (int nt = 0; nt < NTN; ++nt) {
 #pragma unroll
-            for (int mt = 0; mt < NT; ++mt) {
-                dst[16 * mt] = poisoned ? __float2bfloat16_rn(qnan) : __float2bfloat16_rn(o[mt][j] * inv);
-                dst[16 * mt + 8] = poisoned ? __float2bfloat16_rn(qnan) : __float2bfloat16_rn(o[mt][2 + j] * inv);
+        for (int j = 0; j < 2; ++j) {
+            float lj = l[nt][j];
+#pragma unroll
+            for (int o8 = 4; o8 < 32; o8 <<= 1) lj += __shfl_xor_sync(kFull, lj, o8);
+            const int c = 8 * nt + 2 * qd + j;
+            if (c >= ncols) continue;
+            const long long orow = (long long)(d.q_row0 + c / G) * p.n_q + (long long)kvh * G + c % G;
+            if (d.nparts == 1) {
+                const float inv = 1.0f / lj;
+                __nv_bfloat16* dst = p.out + orow * D + qr;
+#pragma unroll
+                for (int mt = 0; mt < NT; ++mt) {
+                    dst[16 * mt] = poisoned ? __float2bfloat16_rn(qnan) : __float2bfloat16_rn(o[mt][nt][j] * inv);
+                    dst[16 * mt + 8] =
+                        poisoned ? __float2bfloat16_rn(qnan) : __float2bfloat16_rn(o[mt][nt][2 + j] * inv);
+                }
+            } else {
+                float* dst = p.part_o + (orow * p.np_max + d.part) * D + qr;
+#pragma unroll
+                for (int mt = 0; mt < NT; ++mt) {
+                    __stcg(dst + 16 * mt, poisoned ? qnan : o[mt][nt][j]);
+                    __stcg(dst + 16 * mt + 8, poisoned ? qnan : o[mt][nt][2 + j]);
+                }
+                if (qr == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(m[nt][j], lj));
             }
-        } else {
-            float* dst = p.part_o + (orow * p.np_max + d.part) * D + qr;
-#pragma unroll
-            for (int mt = 0; mt < NT; ++mt) {
-                __stcg(dst + 16 * mt, poisoned ? qnan : o[mt][j]);
-                __stcg(dst + 16 * mt + 8, poisoned ? qnan : o[mt][2 + j]);
-            }
-            if (qr == 0) __stcg(p.part_ml + orow * p.np_max + d.part, make_float2(mh[j], lh[j]));
         }
     }
 }
@@ -1058,15 +1134,6 @@ struct TcState {
     uint32_t x;      // half-row exchanges done
     uint32_t tiles;  // tcgen05 tiles processed (entry / Q barrier parity)
 };
-
-// Wait bounded by time only (teardown: must not be cut short by an abort).
-__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity) {
-    const unsigned long long t0 = global_ns();
-    for (uint32_t it = 0;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 63u && global_ns() - t0 > kWaitNs) return false;
-    }
-}
 
 // 2^x by the hardware approximation (MUFU), subnormal results flushed to 0:
 // a probability below 2^-126 of the row maximum is 0 in the bf16 P anyway.
@@ -1393,20 +1460,61 @@ __device__ __forceinline__ void helper_warp(Smem<D, F8>& sm, const TMaps* tm, co
     volatile int* abort = &sm.abort;
     uint32_t g = 0;
     int unused = 0;
+    bool aborted = false;
     for (int islot = 0;; ++islot) {
         const int si = islot % kSlots;
-        if (!mbar_wait(&sm.ifull[si], (islot / kSlots) & 1, abort)) break;
+        if (!mbar_wait(&sm.ifull[si], (islot / kSlots) & 1, abort)) {
+            aborted = true;
+            break;
+        }
         const Desc d = sm.desc[si];
         if (d.kind == KIND_END) break;
         const int T = d.kind == KIND_TC ? kTcT : kTileT;
         const int ntiles = (d.t_end + T - 1) / T - d.t_begin / T;
         if (d.kind == KIND_TC) {
             uint32_t gg = g;
-            produce_tc<D, F8>(sm, tm, p, d, si, lane, gg, unused, true);
+            if (!produce_tc<D, F8>(sm, tm, p, d, si, lane, gg, unused, true)) {
+                g = gg;  // stages up to the last one this warp copied into
+                aborted = true;
+                break;
+            }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.iempty[si]);
         g += (uint32_t)(d.kind == KIND_TC ? ntiles + 1 : ntiles);
+    }
+    // This warp's copies land on the producer's barriers.  After the last item
+    // g is the producer's own stage count, so the drain waits for the latest
+    // phase of every slot -- the one the producer's drain waits for too (an
+    // older phase of a slot could alias the parity of a newer one).  After an
+    // abort it waits for the stages this warp copied into, bounded by time
+    // only: the producer may never have armed the last of them, and the wait
+    // then gives up after the time limit, by which the copies have landed.
+    if (lane == 0 && (aborted || g > 0)) drain_ring<Geo<D, F8>::kSlots>(sm.full, g);
+}
+
+// Four FP8 codes of one register -> (codes 0, 1) and (codes 2, 3) as f16x2
+// (exact): e4m3 through the conversion instruction; an e5m2 code is the upper
+// byte of the f16 of the same value, so e5m2 needs only a byte permute.
+template <int FMT>
+__device__ __forceinline__ void fp8x4_to_f16x2x2(uint32_t four, uint32_t& lo, uint32_t& hi) {
+    if constexpr (FMT == 0) {
+        e4m3x4_to_f16x2x2(four, lo, hi);
+    } else {
+        lo = __byte_perm(four, 0u, 0x1404);
+        hi = __byte_perm(four, 0u, 0x3424);
+    }
+}
+
+// V rows: bytes (t0 d0, t0 d1, t1 d0, t1 d1) of ldmatrix.trans -> the f16x2
+// (t0 d0, t1 d0) and (t0 d1, t1 d1).
+template <int FMT>
+__device__ __forceinline__ void fp8x4_v_to_f16x2x2(uint32_t four, uint32_t& d0, uint32_t& d1) {
+    if constexpr (FMT == 0) {
+        e4m3x4_to_f16x2x2(__byte_perm(four, 0u, 0x3120), d0, d1);
+    } else {
+        d0 = __byte_perm(four, 0u, 0x2404);
+        d1 = __byte_perm(four, 0u, 0x3414);
     }
 }
 
@@ -1431,11 +1539,17 @@ __device__ __forceinline__ void helper_warp(Smem<D, F8>& sm, const TMaps* tm, co
 // NS consecutive stages (i0, i0 + 1, ...) of a swap8 item: their S products
 // are independent, so a warp running two at once hides more of the ldmatrix
 // and MMA latency.
-template <int D, int NTN, int NS>
+// FQ: bit 0 = e5m2 codes (else e4m3), bit 1 = a scale per (block, kv head)
+// tile, read from the stage's scale rows (token qr's block and token qr + 8's;
+// else the item's kv-head scale ksc, with V's applied at the end).
+template <int D, int NTN, int NS, int FQ>
 __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, int i0, uint32_t gbase,
                                              const uint32_t (&qb)[NTN][D / 16][2], const int (&lim)[NTN][2],
                                              float (&o)[D / 16][NTN][4], float (&m)[NTN][2], float (&l)[NTN][2],
-                                             float ksc, int R, int a_ch, int lane, volatile int* abort) {
+                                             float ksc, int R, int a_ch, int lane, volatile int* abort, int warp,
+                                             int lb, float sl2) {
+    constexpr int FMT = FQ & 1;
+    constexpr bool PB = (FQ & 2) != 0;
     constexpr int RS = Geo<D, true>::kSlots;
     constexpr int NC = D / 16;
     const int qd = lane & 3, qr = lane >> 2;
@@ -1468,8 +1582,8 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
             for (int h = 0; h < 2; ++h) {
                 const uint32_t rA = h ? r2 : r0, rB = h ? r3 : r1;
                 uint32_t a0, a1, a2, a3;
-                e4m3x4_to_f16x2x2(rA, a0, a2);
-                e4m3x4_to_f16x2x2(rB, a1, a3);
+                fp8x4_to_f16x2x2<FMT>(rA, a0, a2);
+                fp8x4_to_f16x2x2<FMT>(rB, a1, a3);
                 const int kc = 2 * kc2 + h;
 #pragma unroll
                 for (int nt = 0; nt < NTN; ++nt)
@@ -1480,6 +1594,21 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
     // scores (token qr / qr + 8, column 2 qd / 2 qd + 1) with the partition end
     // and each column's causal limit; lazy reference maxima as in decode_tc_item
     float sv[NS][NTN][4];
+    // per-block scales of this lane's two tokens (qr, qr + 8) in each stage
+    float kA[NS], kB[NS], vA[NS], vB[NS];
+#pragma unroll
+    for (int u = 0; u < NS; ++u) {
+        if constexpr (PB) {
+            const int eA = qr >> lb, eB = (qr + 8) >> lb;  // the tokens' blocks within the stage
+            kA[u] = sm.scl[slot[u]][0][eA][warp] * sl2;
+            kB[u] = sm.scl[slot[u]][0][eB][warp] * sl2;
+            vA[u] = sm.scl[slot[u]][1][eA][warp];
+            vB[u] = sm.scl[slot[u]][1][eB][warp];
+        } else {
+            kA[u] = kB[u] = ksc;
+            vA[u] = vB[u] = 1.0f;
+        }
+    }
     bool fits = true;
 #pragma unroll
     for (int u = 0; u < NS; ++u) {
@@ -1487,10 +1616,10 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
         const bool in_a = qr < nvalid[u], in_b = qr + 8 < nvalid[u];
 #pragma unroll
         for (int nt = 0; nt < NTN; ++nt) {
-            sv[u][nt][0] = in_a && ta <= lim[nt][0] ? (sc[u][0][nt][0] + sc[u][1][nt][0]) * ksc : -INFINITY;
-            sv[u][nt][1] = in_a && ta <= lim[nt][1] ? (sc[u][0][nt][1] + sc[u][1][nt][1]) * ksc : -INFINITY;
-            sv[u][nt][2] = in_b && tb8 <= lim[nt][0] ? (sc[u][0][nt][2] + sc[u][1][nt][2]) * ksc : -INFINITY;
-            sv[u][nt][3] = in_b && tb8 <= lim[nt][1] ? (sc[u][0][nt][3] + sc[u][1][nt][3]) * ksc : -INFINITY;
+            sv[u][nt][0] = in_a && ta <= lim[nt][0] ? (sc[u][0][nt][0] + sc[u][1][nt][0]) * kA[u] : -INFINITY;
+            sv[u][nt][1] = in_a && ta <= lim[nt][1] ? (sc[u][0][nt][1] + sc[u][1][nt][1]) * kA[u] : -INFINITY;
+            sv[u][nt][2] = in_b && tb8 <= lim[nt][0] ? (sc[u][0][nt][2] + sc[u][1][nt][2]) * kB[u] : -INFINITY;
+            sv[u][nt][3] = in_b && tb8 <= lim[nt][1] ? (sc[u][0][nt][3] + sc[u][1][nt][3]) * kB[u] : -INFINITY;
             fits = fits && fmaxf(sv[u][nt][0], sv[u][nt][2]) <= m[nt][0] + kRescaleSlack &&
                    fmaxf(sv[u][nt][1], sv[u][nt][3]) <= m[nt][1] + kRescaleSlack;
         }
@@ -1535,8 +1664,15 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
             const float p2 = exp2f(sv[u][nt][2] - u0), p3 = exp2f(sv[u][nt][3] - u1);
             l[nt][0] += p0 + p2;
             l[nt][1] += p1 + p3;
-            pb0[u][nt] = movmatrix_trans(float2_to_f16x2(p0, p1));  // (tokens 2qd, 2qd+1; column qr)
-            pb1[u][nt] = movmatrix_trans(float2_to_f16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; column qr)
+            // with per-block scales each token's V scale rides on its
+            // probability in the P V product (the sum l stays unscaled)
+            if constexpr (PB) {
+                pb0[u][nt] = movmatrix_trans(float2_to_f16x2(p0 * vA[u], p1 * vA[u]));
+                pb1[u][nt] = movmatrix_trans(float2_to_f16x2(p2 * vB[u], p3 * vB[u]));
+            } else {
+                pb0[u][nt] = movmatrix_trans(float2_to_f16x2(p0, p1));  // (tokens 2qd, 2qd+1; column qr)
+                pb1[u][nt] = movmatrix_trans(float2_to_f16x2(p2, p3));  // (tokens 8+2qd, 9+2qd; column qr)
+            }
         }
     }
     // V rows past the valid tokens may hold anything (even NaN): zero them
@@ -1565,8 +1701,8 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
                 // bytes (t0 d0, t0 d1, t1 d0, t1 d1) -> (t0 d0, t1 d0 | t0 d1, t1 d1): one
                 // permute, then each half converts to the f16 pair of one dim
                 uint32_t a0, a1, a2, a3;
-                e4m3x4_to_f16x2x2(__byte_perm(rA, 0u, 0x3120), a0, a1);
-                e4m3x4_to_f16x2x2(__byte_perm(rB, 0u, 0x3120), a2, a3);
+                fp8x4_v_to_f16x2x2<FMT>(rA, a0, a1);
+                fp8x4_v_to_f16x2x2<FMT>(rB, a2, a3);
                 if (partial) {
                     a0 &= klo[u];
                     a1 &= klo[u];
@@ -1586,9 +1722,10 @@ __device__ __forceinline__ void swap8_stages(Smem<D, true>& sm, const Desc& d, i
     }
 }
 
-template <int D, int NTN>
+template <int D, int NTN, int FQ>
 __device__ __forceinline__ void swap8_item(Smem<D, true>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
                                            uint32_t gbase, int ntiles, int si, volatile int* abort) {
+    constexpr bool PB = (FQ & 2) != 0;
     constexpr int RS = Geo<D, true>::kSlots;
     constexpr int NC = D / 16;  // 16-code chunks per row: k-steps of S, m-tiles of O
     static_assert(Geo<D, true>::kNB == 1, "e4m3 rows are one 128-byte box");
@@ -1623,8 +1760,10 @@ __device__ __forceinline__ void swap8_item(Smem<D, true>& sm, const AttnParams& 
             qb[nt][kc][1] = float2_to_f16x2(x23.x, x23.y);
         }
     }
-    const float ksc = __ldg(p.k_scale + kvh) * p.scale_log2;
-    const float vsc = __ldg(p.v_scale + kvh);
+    // a scale per kv head: folded into the scores (K) and the output (V); per
+    // block: read with each stage (swap8_stages)
+    const float ksc = PB ? p.scale_log2 : __ldg(p.k_scale + kvh) * p.scale_log2;
+    const float vsc = PB ? 1.0f : __ldg(p.v_scale + kvh);
     // last visible position of the two columns (2 qd, 2 qd + 1) of each n-tile
     int lim[NTN][2];
 #pragma unroll
@@ -1648,9 +1787,12 @@ __device__ __forceinline__ void swap8_item(Smem<D, true>& sm, const AttnParams& 
     int i = 0;
     if constexpr (NTN == 1) {
         for (; i + 1 < ntiles; i += 2)
-            swap8_stages<D, NTN, 2>(sm, d, i, gbase, qb, lim, o, m, l, ksc, R, a_ch, lane, abort);
+            swap8_stages<D, NTN, 2, FQ>(sm, d, i, gbase, qb, lim, o, m, l, ksc, R, a_ch, lane, abort, warp, lb,
+                                        p.scale_log2);
     }
-    for (; i < ntiles; ++i) swap8_stages<D, NTN, 1>(sm, d, i, gbase, qb, lim, o, m, l, ksc, R, a_ch, lane, abort);
+    for (; i < ntiles; ++i)
+        swap8_stages<D, NTN, 1, FQ>(sm, d, i, gbase, qb, lim, o, m, l, ksc, R, a_ch, lane, abort, warp, lb,
+                                    p.scale_log2);
     const bool poisoned = sm.poison[si] != 0;  // final after the last stage's wait
     const float qnan = __int_as_float(0x7fc00000);
 #pragma unroll
@@ -1696,8 +1838,11 @@ struct CombineParams {
     __nv_bfloat16* out;
     const float* part_o;
     const float2* part_ml;
-    const int* row_np;   // [total_q] partitions of each query row (0 or 1: nothing to merge)
-    int total_q, n_q, np_max;
+    const int* row_np;   // [total_q] partitions of each query row (0 or 1: nothing to merge; -1: invalid
+                         // sequence, the row is written NaN)
+    int* hdr;            // workspace header: key check, queue head reset
+    int32_t* status;
+    int total_q, n_q, np_max, plan_key;
 };
 
 constexpr int kCombineThreads = 128;
@@ -1711,9 +1856,21 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const __grid_c
     const int lane = threadIdx.x & 31;
     const long long nwarps = (long long)gridDim.x * (kCombineThreads / 32);
     const long long rows = (long long)c.total_q * c.n_q;
+    const bool planned = c.hdr[HDR_KEY] == c.plan_key;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (planned) c.hdr[HDR_HEAD] = 0;  // the next call over this plan starts its queue at 0
+        else report(c.status, PKV_STATUS_BAD_PLAN);
+    }
     for (long long orow = (long long)blockIdx.x * (kCombineThreads / 32) + (threadIdx.x >> 5); orow < rows;
          orow += nwarps) {
-        const int np = __ldg(c.row_np + orow / c.n_q);
+        const int np = planned ? __ldg(c.row_np + orow / c.n_q) : -1;
+        if (np < 0) {
+            // a row of an invalid sequence, or a workspace without a plan for this shape
+            __nv_bfloat16* dst = c.out + orow * D + lane * V;
+            if constexpr (V == 4) *reinterpret_cast<uint2*>(dst) = make_uint2(0x7fc07fc0u, 0x7fc07fc0u);
+            else *reinterpret_cast<uint32_t*>(dst) = 0x7fc07fc0u;
+            continue;
+        }
         if (np <= 1) continue;
         const float2* ml = c.part_ml + orow * c.np_max;
         const float* src = c.part_o + orow * c.np_max * D + lane * V;
@@ -1802,7 +1959,11 @@ int launch_combine(const CombineParams& c, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // Consumer warps
 // ---------------------------------------------------------------------------
-template <int D, int GD, bool F8, bool TC>
+// NTN: most n-tiles (8 columns each) of the transposed tensor-core items this
+// kernel variant holds code for; a variant built for decode batches alone
+// (NTN = 1) keeps its register allocation free of the wider items'.
+// FQ (FP8 pools): bit 0 = e5m2 codes, bit 1 = per-block scales.
+template <int D, int GD, bool F8, bool TC, int NTN, int FQ>
 __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, int warp, int lane, TcState& tc) {
     volatile int* abort = &sm.abort;
     uint32_t g = 0;
@@ -1817,11 +1978,14 @@ __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, i
         if (d.kind == KIND_TC) {
             if constexpr (TC) tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, tc, abort);
         } else if constexpr (F8) {
-            if (d.nq * p.G > 8) swap8_item<D, 2>(sm, p, d, warp, lane, g, ntiles, si, abort);
-            else swap8_item<D, 1>(sm, p, d, warp, lane, g, ntiles, si, abort);
+            if (d.nq * p.G > 8) swap8_item<D, 2, FQ>(sm, p, d, warp, lane, g, ntiles, si, abort);
+            else swap8_item<D, 1, FQ>(sm, p, d, warp, lane, g, ntiles, si, abort);
         } else {
             if (d.kind == KIND_DEC) {
-                decode_tc_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
+                // columns of the tile: g heads of each of its nq queries, 8 per n-tile
+                const int ncols = d.nq * p.G;
+                if (NTN == 1 || ncols <= 8) decode_tc_item<D, 1>(sm, p, d, warp, lane, g, ntiles, si, abort);
+                else if constexpr (NTN > 1) decode_tc_item<D, 2>(sm, p, d, warp, lane, g, ntiles, si, abort);
             } else if (d.kind == KIND_MQ) {
                 mq_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
             } else {
@@ -1848,7 +2012,7 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
 template <bool TC>
 constexpr int kThreadsOf = TC ? kThreads + 64 : kThreads;
 
-template <int D, int GD, bool F8, bool TC>
+template <int D, int GD, bool F8, bool TC, int NTN, int FQ>
 __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
     paged_attention_kernel(const __grid_constant__ TMaps tm, const __grid_constant__ AttnParams p) {
     static_assert(!TC || Smem<D, F8>::kTC, "tcgen05 tiles need the head_dim 128 bf16 layout");
@@ -1903,7 +2067,7 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
         if constexpr (TC) {
             // tensor memory only when the plan made tcgen05 tiles (one CTA per
             // SM, so the allocation never waits)
-            use_tc = p.tc != 0 && p.hdr[3] != 0;
+            use_tc = p.tc != 0 && p.hdr[HDR_TC] != 0 && p.hdr[HDR_KEY] == p.plan_key;
             if (use_tc) {
                 if (warp == 0) tmem_alloc(&sm.tmem, kTmemCols);
                 tc_fence_before();
@@ -1915,7 +2079,7 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
         if (mma) {
             if constexpr (TC) mma_warp<D, F8>(sm, p, lane, tc);
         } else {
-            consumer<D, GD, F8, TC>(sm, p, warp, lane, tc);
+            consumer<D, GD, F8, TC, NTN, FQ>(sm, p, warp, lane, tc);
         }
         if constexpr (TC) {
             if (use_tc) {
@@ -1940,7 +2104,7 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
     if (threadIdx.x == 0 && sm.abort) report(p.status, PKV_STATUS_TIMEOUT);
 }
 
-template <int D, int GD, bool F8 = false, bool TC = false>
+template <int D, int GD, bool F8 = false, bool TC = false, int NTN = 2, int FQ = 0>
 int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, cudaStream_t st) {
     static int configured[64] = {0};
     int dev = 0;
@@ -1952,7 +2116,7 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     static_assert(sizeof(Smem<D, F8>) <= kMaxSmem, "shared-memory budget");
     if (dev < 0 || dev >= 64) return PKV_ERR_CUDA;
     if (!configured[dev]) {
-        if (cudaFuncSetAttribute(paged_attention_kernel<D, GD, F8, TC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(paged_attention_kernel<D, GD, F8, TC, NTN, FQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
             return PKV_ERR_CUDA;
         configured[dev] = 1;
@@ -1961,26 +2125,31 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
     const cudaError_t e =
-        host::launch_pdl(paged_attention_kernel<D, GD, F8, TC>, dim3((unsigned)grid), dim3(kThreadsOf<TC>), smem, st,
+        host::launch_pdl(paged_attention_kernel<D, GD, F8, TC, NTN, FQ>, dim3((unsigned)grid), dim3(kThreadsOf<TC>), smem, st,
                          tm, p);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+// wide: the batch may hold transposed items of more than 8 columns (q_len * g
+// > 8, at most kDecCols); otherwise the variant with decode items only runs.
 template <int D>
-int dispatch_g(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st) {
+int dispatch_g(int GD, bool wide, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st) {
     switch (GD) {
         case 1: return launch_attention<D, 1>(tm, p, mi, st);
         case 2: return launch_attention<D, 2>(tm, p, mi, st);
         case 4: return launch_attention<D, 4>(tm, p, mi, st);
         case 8: return launch_attention<D, 8>(tm, p, mi, st);
-        default: return launch_attention<D, 0>(tm, p, mi, st);
+        default:
+            return wide ? launch_attention<D, 0, false, false, 2>(tm, p, mi, st)
+                        : launch_attention<D, 0, false, false, 1>(tm, p, mi, st);
     }
 }
 
-int dispatch_attention_d64(int GD, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
-int dispatch_attention_d128(int GD, bool tc, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
+int dispatch_attention_d64(int GD, bool wide, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
+int dispatch_attention_d128(int GD, bool tc, bool wide, const TMaps& tm, const AttnParams& p, long long mi,
+                            cudaStream_t st);
 int combine_d64(const CombineParams& c, cudaStream_t st);
-int dispatch_attention_fp8_d128(const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
+int dispatch_attention_fp8_d128(int fq, const TMaps& tm, const AttnParams& p, long long mi, cudaStream_t st);
 int combine_d128(const CombineParams& c, cudaStream_t st);
 
 }  // namespace pkv

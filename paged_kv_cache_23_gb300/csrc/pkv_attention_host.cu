@@ -16,14 +16,14 @@ struct PlanParams {
     int* seq_flag;   // PKV_STATUS_* bits of the sequence (0 = valid)
     int* seq_mq;     // exclusive prefix of multi-query item counts
     int* seq_full;   // exclusive prefix of full decode-partition item counts
-    int* row_np;     // [total_q] partitions of each query row
-    __nv_bfloat16* out;
+    int* row_np;     // [total_q] partitions of each query row (-1: row of an invalid sequence)
     int32_t* status;
     int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, max_q_len, decode_ok;
     int fp8;         // e4m3 pool: every row on the transposed tensor-core item
     int tc;          // tcgen05 tiles allowed (head_dim 128, bf16, block_size >= 16, P % 128 == 0)
     int adapt_P;     // 1: P is a floor; the planning kernel may raise it
     int sms;         // SM count (persistent CTAs of the attention kernel)
+    int plan_key;    // key of the shape this plan is made for (header int 4)
 };
 
 __host__ __device__ inline int gcd_pow2(int n, int m) {  // largest power of two <= m dividing n (m a power of 2)
@@ -40,11 +40,17 @@ struct SeqShape {
 
 // decode_fma: run q_len = 1 rows on the CUDA-core path (else tensor cores).
 // fp8: e4m3 pool -- tiles of up to 16 (query, q head) columns per kv head.
-// tc: a sequence with at least 128 (query, q head) rows per kv head runs as
-// tcgen05 tiles of 128 rows (128 / G queries), one kv head each.
+// bf16 q_len * g <= kDecCols: one tile of q_len queries on the transposed
+// tensor-core item (decode_tc_item); longer multi-query rows on mma.sync
+// row tiles (mq_item).
+// tc: a sequence with more than kTcMinCols (query, q head) rows per kv head
+// runs as tcgen05 tiles of 128 rows (128 / G queries), one kv head each --
+// a speculative verification's 20 rows fill a sixth of a tile, but the
+// accumulators live in tensor memory, so the item costs no registers and
+// streams 128-token stages.
 __device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_fma, int fp8, int tc) {
     SeqShape s;
-    if (tc && ql * G >= kTcRows && kTcRows % G == 0) {
+    if (tc && ql * G > kTcMinCols && kTcRows % G == 0) {
         s.kind = KIND_TC;
         s.hps = 1;
         s.wph = kCWarps;
@@ -58,11 +64,22 @@ __device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decod
         s.qt = G <= 16 ? 16 / G : 1;
         return s;
     }
-    if (ql == 1 && G <= 8) {
-        s.kind = decode_fma ? KIND_DECF : KIND_DEC;
+    if (ql <= 1 && G <= 8 && decode_fma) {
+        s.kind = KIND_DECF;
         s.hps = gcd_pow2(n_kv, kMaxHPS);
         s.wph = 1;
         s.qt = 1;
+        return s;
+    }
+    if (ql * G <= kDecCols) {
+        // decode rows and short verifications: one query tile of up to 16
+        // (query, q head) columns per kv head, one warp per kv head, so every
+        // kv head of a block shares a stage (with tcgen05 tiles enabled, rows
+        // of more than 8 columns are tiles instead)
+        s.kind = KIND_DEC;
+        s.hps = gcd_pow2(n_kv, kMaxHPS);
+        s.wph = 1;
+        s.qt = ql > 1 ? ql : 1;
         return s;
     }
     s.kind = KIND_MQ;
@@ -140,10 +157,11 @@ constexpr int kAutoPMax = 8192;       // automatic partition length: upper bound
 // multi-query-heavy batches)
 constexpr int kAutoItemsPerSM = 2, kAutoItemsPerSMMQ = 3;
 
-// Work list for one call: multi-query items first (the compute-heavy tiles
+// Work list for a batch: multi-query items first (the compute-heavy tiles
 // start early), then every full decode partition, then the decode partition
 // tails ordered longest first (counting sort over kTailBuckets length
-// classes), so the dynamic queue ends on the shortest items.
+// classes), so the dynamic queue ends on the shortest items.  The list depends
+// only on the lengths, so one plan serves every layer of a decode step.
 //   pass A  one thread per sequence: validity, query rows, item counts and
 //           their prefix sums, tail-length histogram;
 //   pass B  items and per-row partition counts written over the item (row)
@@ -163,18 +181,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     int* a_full = small ? s_full : pp.seq_full;
     int* a_flag = small ? s_flag : pp.seq_flag;
     const int4* a_seq = small ? s_seq : pp.seqs;  // per-sequence records of pass A (global copy always written)
+    if (tid < kTailBuckets) hist[tid] = 0;
+    // Programmatic launch: the attention kernel may be scheduled at once (it
+    // waits for this grid to complete before it reads the plan), but this
+    // kernel reads nothing before the previous kernel of the stream has
+    // completed and its writes are visible -- seq_lens and q_lens may be the
+    // output of that very kernel (a caller advancing its lengths on the GPU),
+    // and the work list may still be read by a previous call's kernels.
+    pdl_launch();
+    pdl_wait();
     // this thread's first sequence, read once for the partition choice and pass A
     const int L0 = tid < n ? pp.seq_lens[tid] : 0, ql0 = tid < n ? pp.q_lens[tid] : 0;
-    if (tid < kTailBuckets) hist[tid] = 0;
-    // Programmatic launch: the previous kernel of the stream may still run
-    // while passes A and B1-B3 do.  They read only seq_lens and q_lens, which
-    // no kernel of this library writes, and write only work-list state the
-    // previous step's attention kernel read -- and that kernel has finished:
-    // this kernel starts no earlier than its predecessor's own wait, which
-    // completes everything before it.  The per-row counts and NaN output rows
-    // (read and written by a previous combine) wait for the predecessor, and
-    // so does this kernel's completion, which the attention kernel waits on.
-    pdl_launch();
     int P = pp.P;
     if (pp.adapt_P) {
         // automatic partition length: the floor P, raised along the ladder
@@ -204,7 +221,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         const int per_sm = 4 * (long long)mq16 > 3 * (long long)tot16 ? kAutoItemsPerSMMQ : kAutoItemsPerSM;
         while (P < kAutoPMax && T > (long long)P * per_sm * pp.sms) P = (P & (P - 1)) == 0 ? P + P / 2 : P + P / 3;
     }
-    if (tid == 0) pp.hdr[2] = P;
+    if (tid == 0) pp.hdr[HDR_P] = P;
     __syncthreads();
     int bits = 0, any_tc = 0;
     // pass A
@@ -268,9 +285,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         if (tid < kTailBuckets) hist[tid] = c_mq + c_full + ex;
     }
     if (tid == 0) {
-        pp.hdr[0] = c_mq + c_full + c_tail;
-        pp.hdr[1] = 0;
-        pp.hdr[3] = any_tc;  // the attention kernel allocates tensor memory only then
+        pp.hdr[HDR_ITEMS] = c_mq + c_full + c_tail;
+        pp.hdr[HDR_HEAD] = 0;
+        pp.hdr[HDR_TC] = any_tc;  // the attention kernel allocates tensor memory only then
+        pp.hdr[HDR_KEY] = pp.plan_key;
     }
     __syncthreads();
     // pass B1: one thread per sequence -- decode tails and invalid sequences
@@ -313,27 +331,19 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             pp.items[c_mq + it] = make_int4(b, part, 0, li - part * ngroups);
         }
     }
-    pdl_wait();
-    // rows of an invalid sequence are NaN (inside the q/out extent)
-    for (int b = tid; b < n; b += kPlanThreads) {
-        if (!a_flag[b]) continue;
-        const int4 sq = a_seq[b];
-        const int ql = sq.y, q0 = sq.z;
-        const int qlc = ql > 0 ? min(ql, pp.total_q) : 0;
-        const int rows = min(qlc, pp.total_q - q0);
-        const long long n16 = (long long)rows * pp.n_q * pp.D / 8;
-        uint4* o = reinterpret_cast<uint4*>(pp.out + (long long)q0 * pp.n_q * pp.D);
-        for (long long e = 0; e < n16; ++e) o[e] = make_uint4(0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u, 0x7fc07fc0u);
-    }
-    // pass B4: partitions per query row (0 for rows of invalid sequences and
-    // rows past the last sequence's queries: nothing to merge)
+    // pass B4: partitions per query row; -1 for the rows of an invalid
+    // sequence (inside the q/out extent), which each call's combine kernel
+    // writes NaN; 0 for rows past the last sequence's queries
     for (int r = tid; r < pp.total_q; r += kPlanThreads) {
         int np = 0;
         if (r < carry) {
             const int b = last_le(a_q0, n, r);
             const int4 sq = a_seq[b];
             const int L = sq.x, ql = sq.y, q0 = sq.z;
-            if (a_flag[b] == 0 && r - q0 < ql) {
+            if (a_flag[b] != 0) {
+                const int qlc = ql > 0 ? min(ql, pp.total_q) : 0;
+                if (r - q0 < qlc) np = -1;
+            } else if (r - q0 < ql) {
                 // query tile of row r; a decode row is a tile of one query
                 const int QT = (sq.w >> 12) & 4095;
                 const int qt = (r - q0) / QT;
@@ -402,14 +412,37 @@ extern "C" size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int n
 
 namespace {
 
-// Both entry points: bf16 pools (k_scale == nullptr) or e4m3 pools with
-// per-kv-head dequantisation scales.
-int run_attention(void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
-                  const float* v_scale, bool fp8, const int32_t* block_tables, int max_blocks,
-                  const int32_t* seq_lens, const int32_t* q_lens, int num_seqs, int total_q, int max_q_len,
-                  int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
-                  float scale, int partition_tokens, int flags, void* workspace, size_t workspace_bytes,
-                  int32_t* status, void* stream) {
+// Everything the host derives from one call's sizes and flags: checked once,
+// shared by the plan and the run, and condensed into the key the plan leaves
+// in the workspace header (a run over a workspace planned for another shape
+// does nothing and reports PKV_STATUS_BAD_PLAN).
+struct Shape {
+    int num_seqs, total_q, max_q_len, max_seq_len, max_blocks, n_q, n_kv, D, bs, flags;
+    int G, GD, P, adapt;
+    bool fp8, decode_fma, tc, empty;
+    WsLayout w;
+    int key;
+};
+
+// FNV-1a over the fields that decide the work list and the workspace layout,
+// folded to a positive nonzero int.
+int shape_key(const Shape& s) {
+    const long long f[] = {s.num_seqs, s.total_q, s.max_q_len, s.max_seq_len, s.max_blocks, s.n_q, s.n_kv, s.D,
+                           s.bs, s.P, s.adapt, s.fp8, s.decode_fma, s.tc, s.w.np_max};
+    uint32_t h = 2166136261u;
+    for (long long v : f)
+        for (int k = 0; k < 8; ++k) {
+            h ^= (uint32_t)((unsigned long long)v >> (8 * k)) & 0xffu;
+            h *= 16777619u;
+        }
+    return (int)((h & 0x7fffffffu) | 1u);
+}
+
+// Host checks of a call's sizes (no pointers); PKV_OK and a filled Shape, or
+// an error code.  fp8: e4m3 pools.
+int check_shape(Shape& s, bool fp8, int num_seqs, int total_q, int max_q_len, int max_seq_len, int max_blocks,
+                int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks, int partition_tokens,
+                int flags) {
     if (num_seqs < 0 || total_q < 0 || max_q_len < 0 || max_blocks < 1 || max_seq_len < 0 || num_q_heads < 1 ||
         num_kv_heads < 1 || num_blocks < 1 || block_size < 1)
         return PKV_ERR_SIZE;
@@ -421,29 +454,100 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31)) return PKV_ERR_SIZE;
     if (flags & ~(PKV_ATTN_DECODE_CUDA_CORES | PKV_ATTN_NO_TCGEN05)) return PKV_ERR_SIZE;
     if (fp8 && (head_dim != 128 || G > 16)) return PKV_ERR_UNSUPPORTED;
-    if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
-    if (num_seqs == 0 || total_q == 0) return PKV_OK;
+    s = Shape{};
+    s.empty = num_seqs == 0 || total_q == 0;
+    if (s.empty) return PKV_OK;
     if (num_seqs > (1 << 24) || total_q > (1 << 20)) return PKV_ERR_SIZE;
     int P = partition_tokens;
     if (P == 0) P = pkv_attention_auto_partition(num_seqs, total_q, num_kv_heads, max_seq_len);
     if (P < kTileT || P % kTileT) return PKV_ERR_SIZE;
-    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_lens) return PKV_ERR_NULL;
-    if (!host::aligned16(out) || !host::aligned16(q) || !host::aligned16(k_cache) || !host::aligned16(v_cache))
-        return PKV_ERR_ALIGN;
-    const WsLayout w = ws_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, max_seq_len, P);
-    if (w.np_max > kMaxParts) return PKV_ERR_SIZE;
-    if (!workspace || workspace_bytes < w.total) return PKV_ERR_WORKSPACE;
-    if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_ALIGN;
-    if (w.max_items > 0x7fffffffLL) return PKV_ERR_SIZE;
-    const int rc = host::check_device();
-    if (rc) return rc;
+    s.w = ws_layout(num_seqs, total_q, num_q_heads, num_kv_heads, head_dim, max_seq_len, P);
+    if (s.w.np_max > kMaxParts) return PKV_ERR_SIZE;
+    if (s.w.max_items > 0x7fffffffLL) return PKV_ERR_SIZE;
+    s.num_seqs = num_seqs;
+    s.total_q = total_q;
+    s.max_q_len = max_q_len;
+    s.max_seq_len = max_seq_len;
+    s.max_blocks = max_blocks;
+    s.n_q = num_q_heads;
+    s.n_kv = num_kv_heads;
+    s.D = head_dim;
+    s.bs = block_size;
+    s.flags = flags;
+    s.G = G;
+    s.GD = (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
+    s.P = P;
+    s.adapt = partition_tokens == 0 ? 1 : 0;
+    s.fp8 = fp8;
+    s.decode_fma = !fp8 && s.GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
+    // tcgen05 tiles: bf16 head_dim 128, boxes of >= 16 rows, partitions made of
+    // whole 128-token stages (every automatic length is one), decode rows on
+    // tensor cores, and a batch that may hold a multi-query row of more than
+    // kTcMinCols (query, q head) pairs; otherwise the variant without tile
+    // code runs
+    s.tc = !fp8 && head_dim == 128 && block_size >= 16 && P % kTcT == 0 && !s.decode_fma &&
+           !(flags & PKV_ATTN_NO_TCGEN05) && (long long)max_q_len * G > kTcMinCols && kTcRows % G == 0;
+    s.key = shape_key(s);
+    return PKV_OK;
+}
 
+int check_workspace(const Shape& s, const void* workspace, size_t workspace_bytes) {
+    if (!workspace || workspace_bytes < s.w.total) return PKV_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) & 255) return PKV_ERR_ALIGN;
+    return PKV_OK;
+}
+
+// The planning kernel over the lengths (one CTA).
+int launch_plan(const Shape& s, const int32_t* seq_lens, const int32_t* q_lens, void* workspace, int32_t* status,
+                cudaStream_t st) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    int* aux = reinterpret_cast<int*>(ws + s.w.seqaux);
+    PlanParams pp{};
+    pp.seq_lens = seq_lens;
+    pp.q_lens = q_lens;
+    pp.items = reinterpret_cast<int4*>(ws + s.w.items);
+    pp.seqs = reinterpret_cast<int4*>(ws + s.w.seqs);
+    pp.hdr = reinterpret_cast<int*>(ws + s.w.hdr);
+    pp.seq_q0 = aux;
+    pp.seq_flag = aux + s.num_seqs;
+    pp.seq_mq = aux + 2 * s.num_seqs;
+    pp.seq_full = aux + 3 * s.num_seqs;
+    pp.row_np = reinterpret_cast<int*>(ws + s.w.rownp);
+    pp.status = status;
+    pp.num_seqs = s.num_seqs;
+    pp.total_q = s.total_q;
+    pp.n_q = s.n_q;
+    pp.n_kv = s.n_kv;
+    pp.G = s.G;
+    pp.D = s.D;
+    pp.P = s.P;
+    pp.max_blocks = s.max_blocks;
+    pp.bs = s.bs;
+    pp.max_seq_len = s.max_seq_len;
+    pp.max_q_len = s.max_q_len;
+    pp.decode_ok = s.decode_fma ? 1 : 0;
+    pp.adapt_P = s.adapt;
+    pp.fp8 = s.fp8 ? 1 : 0;
+    pp.tc = s.tc ? 1 : 0;
+    pp.sms = host::sm_count();
+    pp.plan_key = s.key;
+    return host::launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) == cudaSuccess ? PKV_OK
+                                                                                                  : PKV_ERR_CUDA;
+}
+
+// The attention kernel and the combine kernel over a planned workspace.  fq
+// (FP8 pools): bit 0 = e5m2 codes, bit 1 = per-block scales.
+int launch_run(const Shape& s, void* out, const void* q, const void* k_cache, const void* v_cache,
+               const float* k_scale, const float* v_scale, int fq, const int32_t* block_tables, int num_blocks,
+               float scale, void* workspace, int32_t* status, cudaStream_t st) {
     // 5-D views of each pool, one per box height in kv heads (a row is D values
     // of 2 bytes, or of 1 byte in e4m3).  Rows of more than 128 bytes are
     // viewed as [num_blocks][n_kv][row / 128 B][bs][128 B] (the 128-byte box
     // outside the row, a non-monotonic stride), so a box lands in shared memory
     // as [head][box][row]: consecutive tokens of one box in consecutive
     // 128-byte lines, which the 128-byte swizzle maps to distinct banks.
+    const int head_dim = s.D, block_size = s.bs, num_kv_heads = s.n_kv;
+    const bool fp8 = s.fp8;
     TMaps tm;
     {
         const uint64_t row = (uint64_t)head_dim * (fp8 ? 1 : 2);
@@ -465,17 +569,8 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
                 return PKV_ERR_CUDA;
         }
     }
-
-    // tcgen05 tiles: bf16 head_dim 128, boxes of >= 16 rows, partitions made of
-    // whole 128-token stages, decode rows on tensor cores, and a batch that may
-    // hold a 128-row tile (max_q_len * g >= 128); otherwise the variant
-    // without tile code runs
-    const int GD = (G == 1 || G == 2 || G == 4 || G == 8) ? G : 0;
-    const bool decode_fma = !fp8 && GD > 0 && (flags & PKV_ATTN_DECODE_CUDA_CORES);
-    const bool tc = !fp8 && head_dim == 128 && block_size >= 16 && P % kTcT == 0 && !decode_fma &&
-                    !(flags & PKV_ATTN_NO_TCGEN05) && (long long)max_q_len * G >= kTcRows;
     bool tc_pair = false;
-    if (tc) {
+    if (s.tc) {
         const uint64_t row = 256;
         const uint64_t blk = (uint64_t)block_size * row, head = (uint64_t)num_kv_heads * blk;
         // K (and V unless paired): [num_blocks][n_kv][bs][2 slabs][64], one slab
@@ -506,80 +601,92 @@ int run_attention(void* out, const void* q, const void* k_cache, const void* v_c
     }
 
     uint8_t* ws = static_cast<uint8_t*>(workspace);
-    int* aux = reinterpret_cast<int*>(ws + w.seqaux);
-
-    PlanParams pp{};
-    pp.seq_lens = seq_lens;
-    pp.q_lens = q_lens;
-    pp.items = reinterpret_cast<int4*>(ws + w.items);
-    pp.seqs = reinterpret_cast<int4*>(ws + w.seqs);
-    pp.hdr = reinterpret_cast<int*>(ws + w.hdr);
-    pp.seq_q0 = aux;
-    pp.seq_flag = aux + num_seqs;
-    pp.seq_mq = aux + 2 * num_seqs;
-    pp.seq_full = aux + 3 * num_seqs;
-    pp.row_np = reinterpret_cast<int*>(ws + w.rownp);
-    pp.out = static_cast<__nv_bfloat16*>(out);
-    pp.status = status;
-    pp.num_seqs = num_seqs;
-    pp.total_q = total_q;
-    pp.n_q = num_q_heads;
-    pp.n_kv = num_kv_heads;
-    pp.G = G;
-    pp.D = head_dim;
-    pp.P = P;
-    pp.max_blocks = max_blocks;
-    pp.bs = block_size;
-    pp.max_seq_len = max_seq_len;
-    pp.max_q_len = max_q_len;
-    pp.decode_ok = decode_fma ? 1 : 0;
-    pp.adapt_P = partition_tokens == 0 ? 1 : 0;
-    pp.fp8 = fp8 ? 1 : 0;
-    pp.tc = tc ? 1 : 0;
-    pp.sms = host::sm_count();
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (host::launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, pp) != cudaSuccess) return PKV_ERR_CUDA;
-
     AttnParams ap{};
     ap.out = static_cast<__nv_bfloat16*>(out);
     ap.q = static_cast<const __nv_bfloat16*>(q);
     ap.block_tables = block_tables;
-    ap.items = pp.items;
-    ap.seqs = pp.seqs;
-    ap.hdr = pp.hdr;
-    ap.part_o = reinterpret_cast<float*>(ws + w.o);
-    ap.part_ml = reinterpret_cast<float2*>(ws + w.ml);
+    ap.items = reinterpret_cast<const int4*>(ws + s.w.items);
+    ap.seqs = reinterpret_cast<const int4*>(ws + s.w.seqs);
+    ap.hdr = reinterpret_cast<int*>(ws + s.w.hdr);
+    ap.part_o = reinterpret_cast<float*>(ws + s.w.o);
+    ap.part_ml = reinterpret_cast<float2*>(ws + s.w.ml);
     ap.status = status;
-    ap.max_blocks = max_blocks;
-    ap.n_q = num_q_heads;
-    ap.n_kv = num_kv_heads;
-    ap.G = G;
+    ap.max_blocks = s.max_blocks;
+    ap.n_q = s.n_q;
+    ap.n_kv = s.n_kv;
+    ap.G = s.G;
     ap.bs = block_size;
     ap.num_blocks = num_blocks;
-    ap.np_max = w.np_max;
+    ap.np_max = s.w.np_max;
     ap.row_bytes = head_dim * 2;
     ap.scale_log2 = scale * 1.4426950408889634f;
     ap.k_scale = k_scale;
     ap.v_scale = v_scale;
-    ap.tc = tc ? 1 : 0;
+    ap.scale_pb = (fq & 2) ? 1 : 0;
+    ap.tc = s.tc ? 1 : 0;
     ap.tc_pair = tc_pair ? 1 : 0;
-    const int rc2 = fp8                ? dispatch_attention_fp8_d128(tm, ap, w.max_items, st)
-                    : head_dim == 128 ? dispatch_attention_d128(decode_fma ? GD : 0, tc, tm, ap, w.max_items, st)
-                                      : dispatch_attention_d64(decode_fma ? GD : 0, tm, ap, w.max_items, st);
-    // The combine runs even when no row can span partitions (it then only
-    // waits and exits): it triggers the next kernel of the stream only after
-    // the attention grid has finished, which the next call's planning kernel
-    // relies on before it rewrites the work list.
-    if (rc2 != PKV_OK) return rc2;
+    ap.plan_key = s.key;
+    // transposed items wider than one n-tile are possible when q_len * g > 8
+    const bool wide = (long long)s.max_q_len * s.G > 8;
+    const int rc = fp8 ? dispatch_attention_fp8_d128(fq, tm, ap, s.w.max_items, st)
+                   : head_dim == 128
+                       ? dispatch_attention_d128(s.decode_fma ? s.GD : 0, s.tc, wide, tm, ap, s.w.max_items, st)
+                       : dispatch_attention_d64(s.decode_fma ? s.GD : 0, wide, tm, ap, s.w.max_items, st);
+    if (rc != PKV_OK) return rc;
+    // The combine runs even when no row can span partitions: it writes the NaN
+    // rows of invalid sequences, resets the item queue for the next call over
+    // the same plan, and triggers the next kernel of the stream only after the
+    // attention grid has finished.
     CombineParams cp{};
     cp.out = ap.out;
     cp.part_o = ap.part_o;
     cp.part_ml = ap.part_ml;
-    cp.row_np = pp.row_np;
-    cp.total_q = total_q;
-    cp.n_q = num_q_heads;
-    cp.np_max = w.np_max;
+    cp.row_np = reinterpret_cast<const int*>(ws + s.w.rownp);
+    cp.hdr = ap.hdr;
+    cp.status = status;
+    cp.total_q = s.total_q;
+    cp.n_q = s.n_q;
+    cp.np_max = s.w.np_max;
+    cp.plan_key = s.key;
     return head_dim == 128 ? combine_d128(cp, st) : combine_d64(cp, st);
+}
+
+int run_pointers_ok(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables) {
+    if (!out || !q || !k_cache || !v_cache || !block_tables) return PKV_ERR_NULL;
+    if (!host::aligned16(out) || !host::aligned16(q) || !host::aligned16(k_cache) || !host::aligned16(v_cache))
+        return PKV_ERR_ALIGN;
+    return PKV_OK;
+}
+
+// FP8 format and scale granularity -> the kernel variant's fq bits, or -1.
+int fp8_mode(int kv_format, int scale_mode) {
+    if (kv_format != PKV_FP8_E4M3 && kv_format != PKV_FP8_E5M2) return -1;
+    if (scale_mode != PKV_FP8_SCALE_PER_HEAD && scale_mode != PKV_FP8_SCALE_PER_BLOCK) return -1;
+    return (kv_format == PKV_FP8_E5M2 ? 1 : 0) | (scale_mode == PKV_FP8_SCALE_PER_BLOCK ? 2 : 0);
+}
+
+// Plan + run in one call (bf16 pools with k_scale == nullptr, or FP8 pools
+// with dequantisation scales; fq as in launch_run).
+int attention_call(void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                   const float* v_scale, bool fp8, int fq, const int32_t* block_tables, int max_blocks,
+                   const int32_t* seq_lens, const int32_t* q_lens, int num_seqs, int total_q, int max_q_len,
+                   int max_seq_len, int num_q_heads, int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                   float scale, int partition_tokens, int flags, void* workspace, size_t workspace_bytes,
+                   int32_t* status, void* stream) {
+    Shape s;
+    int rc = check_shape(s, fp8, num_seqs, total_q, max_q_len, max_seq_len, max_blocks, num_q_heads, num_kv_heads,
+                         head_dim, block_size, num_blocks, partition_tokens, flags);
+    if (rc || s.empty) return rc;
+    if (fp8 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
+    if ((rc = run_pointers_ok(out, q, k_cache, v_cache, block_tables))) return rc;
+    if (!seq_lens || !q_lens) return PKV_ERR_NULL;
+    if ((rc = check_workspace(s, workspace, workspace_bytes))) return rc;
+    if ((rc = host::check_device())) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if ((rc = launch_plan(s, seq_lens, q_lens, workspace, status, st))) return rc;
+    return launch_run(s, out, q, k_cache, v_cache, k_scale, v_scale, fq, block_tables, num_blocks, scale, workspace,
+                      status, st);
 }
 
 }  // namespace
@@ -591,10 +698,10 @@ extern "C" int pkv_paged_attention_decode(void* out, const void* q, const void* 
                                           int block_size, int num_blocks, float scale, int partition_tokens,
                                           int flags, void* workspace, size_t workspace_bytes, int32_t* status,
                                           void* stream) {
-    return run_attention(out, q, k_cache, v_cache, nullptr, nullptr, false, block_tables, max_blocks, seq_lens,
-                         q_lens, num_seqs, total_q, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
-                         block_size, num_blocks, scale, partition_tokens, flags, workspace, workspace_bytes, status,
-                         stream);
+    return attention_call(out, q, k_cache, v_cache, nullptr, nullptr, false, 0, block_tables, max_blocks, seq_lens,
+                          q_lens, num_seqs, total_q, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, scale, partition_tokens, flags, workspace, workspace_bytes, status,
+                          stream);
 }
 
 extern "C" int pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -605,8 +712,80 @@ extern "C" int pkv_paged_attention_decode_fp8(void* out, const void* q, const vo
                                               int block_size, int num_blocks, float scale, int partition_tokens,
                                               void* workspace, size_t workspace_bytes, int32_t* status,
                                               void* stream) {
-    return run_attention(out, q, k_cache, v_cache, k_scale, v_scale, true, block_tables, max_blocks, seq_lens,
-                         q_lens, num_seqs, total_q, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
-                         block_size, num_blocks, scale, partition_tokens, 0, workspace, workspace_bytes, status,
-                         stream);
+    return attention_call(out, q, k_cache, v_cache, k_scale, v_scale, true, 0, block_tables, max_blocks, seq_lens,
+                          q_lens, num_seqs, total_q, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, scale, partition_tokens, 0, workspace, workspace_bytes, status,
+                          stream);
+}
+
+extern "C" int pkv_paged_attention_decode_fp8_ex(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                                 const float* k_scale, const float* v_scale, int kv_format,
+                                                 int scale_mode, const int32_t* block_tables, int max_blocks,
+                                                 const int32_t* seq_lens, const int32_t* q_lens, int num_seqs,
+                                                 int total_q, int max_q_len, int max_seq_len, int num_q_heads,
+                                                 int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                                                 float scale, int partition_tokens, void* workspace,
+                                                 size_t workspace_bytes, int32_t* status, void* stream) {
+    const int fq = fp8_mode(kv_format, scale_mode);
+    if (fq < 0) return PKV_ERR_UNSUPPORTED;
+    return attention_call(out, q, k_cache, v_cache, k_scale, v_scale, true, fq, block_tables, max_blocks, seq_lens,
+                          q_lens, num_seqs, total_q, max_q_len, max_seq_len, num_q_heads, num_kv_heads, head_dim,
+                          block_size, num_blocks, scale, partition_tokens, 0, workspace, workspace_bytes, status,
+                          stream);
+}
+
+extern "C" int pkv_attention_plan(const int32_t* seq_lens, const int32_t* q_lens, int num_seqs, int total_q,
+                                  int max_q_len, int max_seq_len, int max_blocks, int num_q_heads, int num_kv_heads,
+                                  int head_dim, int block_size, int partition_tokens, int flags, void* workspace,
+                                  size_t workspace_bytes, int32_t* status, void* stream) {
+    const bool fp8 = (flags & PKV_ATTN_PLAN_FP8) != 0;
+    flags &= ~PKV_ATTN_PLAN_FP8;
+    if (fp8 && flags) return PKV_ERR_SIZE;  // the e4m3 attention takes no other flag
+    Shape s;
+    // the pool size does not enter the plan: any positive count passes the check
+    int rc = check_shape(s, fp8, num_seqs, total_q, max_q_len, max_seq_len, max_blocks, num_q_heads, num_kv_heads,
+                         head_dim, block_size, 1, partition_tokens, flags);
+    if (rc || s.empty) return rc;
+    if (!seq_lens || !q_lens) return PKV_ERR_NULL;
+    if ((rc = check_workspace(s, workspace, workspace_bytes))) return rc;
+    if ((rc = host::check_device())) return rc;
+    return launch_plan(s, seq_lens, q_lens, workspace, status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_paged_attention_run(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int max_blocks, int num_seqs, int total_q,
+                                       int max_q_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int num_blocks, float scale,
+                                       int partition_tokens, int flags, void* workspace, size_t workspace_bytes,
+                                       int32_t* status, void* stream) {
+    Shape s;
+    int rc = check_shape(s, false, num_seqs, total_q, max_q_len, max_seq_len, max_blocks, num_q_heads, num_kv_heads,
+                         head_dim, block_size, num_blocks, partition_tokens, flags);
+    if (rc || s.empty) return rc;
+    if ((rc = run_pointers_ok(out, q, k_cache, v_cache, block_tables))) return rc;
+    if ((rc = check_workspace(s, workspace, workspace_bytes))) return rc;
+    if ((rc = host::check_device())) return rc;
+    return launch_run(s, out, q, k_cache, v_cache, nullptr, nullptr, 0, block_tables, num_blocks, scale, workspace,
+                      status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int pkv_paged_attention_run_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                           const float* k_scale, const float* v_scale, int kv_format, int scale_mode,
+                                           const int32_t* block_tables, int max_blocks, int num_seqs, int total_q,
+                                           int max_q_len, int max_seq_len, int num_q_heads, int num_kv_heads,
+                                           int head_dim, int block_size, int num_blocks, float scale,
+                                           int partition_tokens, void* workspace, size_t workspace_bytes,
+                                           int32_t* status, void* stream) {
+    const int fq = fp8_mode(kv_format, scale_mode);
+    if (fq < 0) return PKV_ERR_UNSUPPORTED;
+    Shape s;
+    int rc = check_shape(s, true, num_seqs, total_q, max_q_len, max_seq_len, max_blocks, num_q_heads, num_kv_heads,
+                         head_dim, block_size, num_blocks, partition_tokens, 0);
+    if (rc || s.empty) return rc;
+    if (!k_scale || !v_scale) return PKV_ERR_NULL;
+    if ((rc = run_pointers_ok(out, q, k_cache, v_cache, block_tables))) return rc;
+    if ((rc = check_workspace(s, workspace, workspace_bytes))) return rc;
+    if ((rc = host::check_device())) return rc;
+    return launch_run(s, out, q, k_cache, v_cache, k_scale, v_scale, fq, block_tables, num_blocks, scale, workspace,
+                      status, static_cast<cudaStream_t>(stream));
 }

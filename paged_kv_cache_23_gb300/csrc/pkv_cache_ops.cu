@@ -256,6 +256,152 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(uint2* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------
+// FP8 pools of either format ("Inference at Scale" section 03: e4m3 or e5m2),
+// with a dequantisation scale per kv head or per (block, kv head) tile.
+//
+// Per-block scales are set when a block is opened: the append that writes a
+// block's row 0 first sets, from that row's values of each kv head, the
+// smallest power of two s = 2^e (e in [-120, 120]) with max|x| <= s * FMAX / 2
+// (FMAX = 448 for e4m3, 57344 for e5m2; NaN values ignored; s = 1 for an
+// all-zero or infinite row), so the opening row uses at most half of the range
+// and later rows may grow to twice its magnitude before they saturate.  A
+// first kernel sets the scales of the blocks this call opens (one warp per
+// (opening token, kv head)); the quantising kernel, its programmatic
+// dependent, then stores every row with its block's scales.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float open_block_scale(float amax, int fmt) {
+    if (!(amax > 0.0f) || isinf(amax)) return 1.0f;
+    const float half = fmt ? 28672.0f : 224.0f;
+    // start from the exponent difference, then settle by exact comparisons
+    int e = ilogbf(amax) - ilogbf(half);
+    e = max(-120, min(120, e));
+    while (e < 120 && ldexpf(half, e) < amax) ++e;
+    while (e > -120 && ldexpf(half, e - 1) >= amax) --e;
+    return ldexpf(1.0f, e);
+}
+
+__global__ void __launch_bounds__(256) fp8_open_blocks_kernel(const uint4* __restrict__ k_new,
+                                                              const uint4* __restrict__ v_new,
+                                                              const int64_t* __restrict__ slots,
+                                                              float* __restrict__ k_scale,
+                                                              float* __restrict__ v_scale, int num_tokens,
+                                                              int num_blocks, int block_size, int num_kv_heads,
+                                                              int chunks_per_row, int fmt) {
+    pdl_wait();
+    pdl_launch();
+    const int lane = threadIdx.x & 31;
+    const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+    const long long cap = (long long)num_blocks * block_size;
+    for (long long wi = blockIdx.x * (long long)(blockDim.x >> 5) + (threadIdx.x >> 5);
+         wi < (long long)num_tokens * num_kv_heads; wi += warps) {
+        const long long t = wi / num_kv_heads;
+        const int h = (int)(wi - t * num_kv_heads);
+        const int64_t s = slots[t];
+        if (s < 0 || s >= cap || s % block_size != 0) continue;  // not a block's opening row
+        float ak = 0.0f, av = 0.0f;
+        const uint4* kr = k_new + (t * num_kv_heads + h) * chunks_per_row;
+        const uint4* vr = v_new + (t * num_kv_heads + h) * chunks_per_row;
+        for (int c = lane; c < chunks_per_row; c += 32) {
+            const uint4 a = ld_nc_v4(kr + c), b = ld_nc_v4(vr + c);
+            const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 xk = bf16x2_to_float2(wa[u]), xv = bf16x2_to_float2(wb[u]);
+                // fmaxf ignores a NaN operand: NaN values do not enter the maximum
+                ak = fmaxf(ak, fmaxf(fabsf(xk.x), fabsf(xk.y)));
+                av = fmaxf(av, fmaxf(fabsf(xv.x), fabsf(xv.y)));
+            }
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            ak = fmaxf(ak, __shfl_xor_sync(kFull, ak, o));
+            av = fmaxf(av, __shfl_xor_sync(kFull, av, o));
+        }
+        if (lane == 0) {
+            const long long blk = s / block_size;
+            k_scale[blk * num_kv_heads + h] = open_block_scale(ak, fmt);
+            v_scale[blk * num_kv_heads + h] = open_block_scale(av, fmt);
+        }
+    }
+}
+
+// fp32 pair -> two FP8 codes of format fmt (round to nearest even, saturating
+// to the largest finite value, NaN kept), lo in the lower byte.
+__device__ __forceinline__ uint32_t f32x2_to_fp8x2(float lo, float hi, int fmt) {
+    return fmt ? (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E5M2)
+               : f32x2_to_e4m3x2(lo, hi);
+}
+
+// Quantising append of either format and scale granularity: code =
+// fp8(x * (1 / scale)), the reciprocal and the product rounded to fp32.
+// 8 values (16 bytes in, 8 out) per thread.
+__global__ void __launch_bounds__(256) kv_append_fp8_ex_kernel(uint2* __restrict__ k_cache,
+                                                               uint2* __restrict__ v_cache,
+                                                               const uint4* __restrict__ k_new,
+                                                               const uint4* __restrict__ v_new,
+                                                               const int64_t* __restrict__ slots,
+                                                               const float* __restrict__ k_scale,
+                                                               const float* __restrict__ v_scale, int num_tokens,
+                                                               int num_blocks, int block_size, int num_kv_heads,
+                                                               int chunks_per_row, int fmt, int per_block,
+                                                               int32_t* status) {
+    pdl_wait();  // the scales of the blocks this call opens are set and visible
+    pdl_launch();
+    const long long per_tok = (long long)num_kv_heads * chunks_per_row;
+    const long long total = (long long)num_tokens * per_tok;
+    const long long cap = (long long)num_blocks * block_size;
+    int bits = 0;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long t = i / per_tok;
+        const long long rem = i - t * per_tok;
+        const int h = (int)(rem / chunks_per_row);
+        const int c = (int)(rem - (long long)h * chunks_per_row);
+        const int64_t s = slots[t];
+        if (s < 0) continue;
+        if (s >= cap) {
+            bits |= PKV_STATUS_BAD_SLOT;
+            continue;
+        }
+        const long long blk = s / block_size;
+        const int row = (int)(s - blk * block_size);
+        const long long dst = ((blk * num_kv_heads + h) * block_size + row) * chunks_per_row + c;
+        const long long si = per_block ? blk * num_kv_heads + h : h;
+        const float ik = __fdiv_rn(1.0f, k_scale[si]), iv = __fdiv_rn(1.0f, v_scale[si]);
+        const uint4 a = ld_nc_v4(k_new + i), b = ld_nc_v4(v_new + i);
+        const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+        uint32_t ck[4], cv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float2 xk = bf16x2_to_float2(wa[u]), xv = bf16x2_to_float2(wb[u]);
+            ck[u] = f32x2_to_fp8x2(__fmul_rn(xk.x, ik), __fmul_rn(xk.y, ik), fmt);
+            cv[u] = f32x2_to_fp8x2(__fmul_rn(xv.x, iv), __fmul_rn(xv.y, iv), fmt);
+        }
+        k_cache[dst] = make_uint2(ck[0] | (ck[1] << 16), ck[2] | (ck[3] << 16));
+        v_cache[dst] = make_uint2(cv[0] | (cv[1] << 16), cv[2] | (cv[3] << 16));
+    }
+    report(status, bits);
+}
+
+// The scales of the copied blocks: pair i copies row src of k_scale / v_scale
+// ([num_blocks][n_kv]) to row dst.
+__global__ void copy_block_scales_kernel(float* __restrict__ k_scale, float* __restrict__ v_scale,
+                                         const int32_t* __restrict__ src_dst, int num_pairs, int num_blocks,
+                                         int num_kv_heads) {
+    pdl_wait();
+    pdl_launch();
+    const long long n = (long long)num_pairs * num_kv_heads;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int pr = (int)(i / num_kv_heads), h = (int)(i - (long long)pr * num_kv_heads);
+        const int32_t s = src_dst[2 * pr], d = src_dst[2 * pr + 1];
+        if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) continue;  // reported by the block copy
+        k_scale[(long long)d * num_kv_heads + h] = k_scale[(long long)s * num_kv_heads + h];
+        v_scale[(long long)d * num_kv_heads + h] = v_scale[(long long)s * num_kv_heads + h];
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Copy blocks: blockIdx.y = pair, grid-stride over the block's 16-byte chunks.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
@@ -480,6 +626,58 @@ extern "C" int pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, cons
                                            (uint4*)k_out, (uint4*)v_out, (const uint4*)k_cache,
                                            (const uint4*)v_cache, block_tables, max_blocks, seq_lens, out_offsets,
                                            num_blocks, block_size, num_kv_heads, head_dim / 8, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_kv_append_fp8_ex(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const void* k_new,
+                                    const void* v_new, const int64_t* slots, int num_tokens, int num_blocks,
+                                    int block_size, int num_kv_heads, int head_dim, int kv_format, int scale_mode,
+                                    int32_t* status, void* stream) {
+    if (num_tokens < 0 || num_blocks < 1 || block_size < 1 || num_kv_heads < 1 || head_dim < 8) return PKV_ERR_SIZE;
+    if (kv_format != PKV_FP8_E4M3 && kv_format != PKV_FP8_E5M2) return PKV_ERR_UNSUPPORTED;
+    if (scale_mode != PKV_FP8_SCALE_PER_HEAD && scale_mode != PKV_FP8_SCALE_PER_BLOCK) return PKV_ERR_UNSUPPORTED;
+    if (head_dim % 8) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !slots || !k_scale || !v_scale) return PKV_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(k_cache) & 7) || (reinterpret_cast<uintptr_t>(v_cache) & 7) ||
+        !host::aligned16(k_new) || !host::aligned16(v_new))
+        return PKV_ERR_ALIGN;
+    const int rc = host::check_device();
+    if (rc) return rc;
+    const int cpr = head_dim / 8;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool pb = scale_mode == PKV_FP8_SCALE_PER_BLOCK;
+    if (pb) {
+        const long long warps = (long long)num_tokens * num_kv_heads;
+        const long long want = (warps + 7) / 8;
+        const int grid = (int)(want < host::sm_count() * 8LL ? want : host::sm_count() * 8LL);
+        if (host::launch_pdl(fp8_open_blocks_kernel, dim3(grid), dim3(256), 0, st, (const uint4*)k_new,
+                             (const uint4*)v_new, slots, k_scale, v_scale, num_tokens, num_blocks, block_size,
+                             num_kv_heads, cpr, kv_format) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    const long long total = (long long)num_tokens * num_kv_heads * cpr;
+    const long long want = (total + 255) / 256;
+    const int grid = (int)(want < host::sm_count() * 8LL ? want : host::sm_count() * 8LL);
+    const cudaError_t e = host::launch_pdl(kv_append_fp8_ex_kernel, dim3(grid), dim3(256), 0, st, (uint2*)k_cache,
+                                           (uint2*)v_cache, (const uint4*)k_new, (const uint4*)v_new, slots,
+                                           (const float*)k_scale, (const float*)v_scale, num_tokens, num_blocks,
+                                           block_size, num_kv_heads, cpr, kv_format, pb ? 1 : 0, status);
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+extern "C" int pkv_copy_blocks_fp8_ex(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                                      const int32_t* src_dst, int num_pairs, int num_blocks, int block_size,
+                                      int num_kv_heads, int head_dim, int scale_mode, int32_t* status, void* stream) {
+    if (scale_mode != PKV_FP8_SCALE_PER_HEAD && scale_mode != PKV_FP8_SCALE_PER_BLOCK) return PKV_ERR_UNSUPPORTED;
+    if (scale_mode == PKV_FP8_SCALE_PER_BLOCK && num_pairs > 0 && (!k_scale || !v_scale)) return PKV_ERR_NULL;
+    const int rc = pkv_copy_blocks_fp8(k_cache, v_cache, src_dst, num_pairs, num_blocks, block_size, num_kv_heads,
+                                       head_dim, status, stream);
+    if (rc || scale_mode != PKV_FP8_SCALE_PER_BLOCK || num_pairs == 0) return rc;
+    const long long n = (long long)num_pairs * num_kv_heads;
+    const int grid = (int)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    const cudaError_t e = host::launch_pdl(copy_block_scales_kernel, dim3(grid), dim3(256), 0, (cudaStream_t)stream,
+                                           k_scale, v_scale, src_dst, num_pairs, num_blocks, num_kv_heads);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -84,6 +84,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
+// Wait bounded by time only (teardown: must not be cut short by an abort).
+__device__ __forceinline__ bool mbar_wait_ns(uint64_t* bar, uint32_t parity) {
+    const unsigned long long t0 = global_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 63u) == 63u && global_ns() - t0 > kWaitNs) return false;
+    }
+}
+
+// Drain of a ring of RS "full" barriers after g stages were issued into it
+// (stage i in slot i % RS): wait for the last phase of every slot used,
+// bounded by time only.
+template <int RS>
+__device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t g) {
+    for (int s = 0; s < RS; ++s) {
+        if (g <= (uint32_t)s) continue;
+        const uint32_t last = g - 1 - ((g - 1 - s) % RS);
+        mbar_wait_ns(&full[s], (last / RS) & 1);
+    }
+}
+
 // ---- TMA (2-D tiled, no multicast) ----------------------------------------
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(

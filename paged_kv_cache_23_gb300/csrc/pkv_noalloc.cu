@@ -11,12 +11,19 @@
 //
 // The array (kScratchBytes, 32 MiB) exists on every GPU that loads this code
 // and stays there until the process exits.  Its device address is looked up
-// once per device, by the first call made with that device current; make that
-// first call before any stream capture starts.  All calls share the array, and
+// once per device and CUDA context, by the first call made with that device
+// current; make that first call before any stream capture starts.  The cached
+// address is keyed on the context's unique id as well as the device ordinal,
+// so after a cudaDeviceReset (or any other teardown and re-creation of the
+// primary context) the next call looks the address up again instead of
+// passing a stale pointer to the kernels -- and that call is then a first
+// call again (before any stream capture).  All calls share the array, and
 // it keeps whatever the last call left in it: the planning kernel re-initialises
 // everything it needs (item queue, per-row partition counts) on every call, but two calls
 // that overlap on the GPU (different streams, or different host threads on the
 // same device without ordering) race on it and give wrong results.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "pkv.h"
@@ -30,17 +37,52 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 constexpr int kMaxDev = 64;
 void* g_addr[kMaxDev] = {nullptr};
+unsigned long long g_ctx_id[kMaxDev] = {0};  // the context each cached address belongs to
 std::mutex g_mu;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+
+// Unique id of the calling thread's current CUDA context, or 0 when there is
+// none (or it has been destroyed).  Context ids are never reused, unlike
+// context handles.  The driver entry points are looked up through the runtime,
+// so the library needs no link to libcuda.
+unsigned long long current_context_id() {
+    if (g_ctx_current == nullptr || g_ctx_get_id == nullptr) {
+        void* f1 = nullptr;
+        void* f2 = nullptr;
+        cudaDriverEntryPointQueryResult q1, q2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 4000, cudaEnableDefault, &q1) != cudaSuccess ||
+            q1 != cudaDriverEntryPointSuccess || f1 == nullptr ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2) != cudaSuccess ||
+            q2 != cudaDriverEntryPointSuccess || f2 == nullptr)
+            return 0;
+        g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f1);
+        g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f2);
+    }
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    return g_ctx_get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
 
 // Device address of g_scratch on the current device (nullptr on failure).
+// Set-up, once per device and context: with the device current,
+// cudaGetSymbolAddress (which also makes the runtime create the device's
+// primary context if there is none yet) gives the array's device address;
+// later calls reuse it while the same context is current, and look it up again
+// after the context was destroyed and re-created (cudaDeviceReset).
 void* scratch_address() {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (g_addr[dev] == nullptr) {
+    const unsigned long long id = current_context_id();
+    if (g_addr[dev] == nullptr || id == 0 || g_ctx_id[dev] != id) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess) return nullptr;
+        const unsigned long long id2 = current_context_id();
+        if (id2 == 0) return nullptr;
         g_addr[dev] = p;
+        g_ctx_id[dev] = id2;
     }
     return g_addr[dev];
 }

@@ -11,10 +11,10 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (attention_auto_partition, attention_workspace_bytes, copy_blocks, copy_blocks_fp8, kv_append_fp8,
-               kv_append_paged,
-               paged_attention_decode_fp8, kv_append, paged_attention_decode, slot_mapping,
-               spec_accept_greedy)
+from . import (PKV_ATTN_PLAN_FP8, attention_plan, attention_workspace_bytes, copy_blocks, copy_blocks_fp8,
+               copy_blocks_fp8_ex, kv_append, kv_append_fp8, kv_append_fp8_ex, kv_append_paged,
+               paged_attention_decode, paged_attention_decode_fp8, paged_attention_decode_fp8_ex,
+               paged_attention_run, paged_attention_run_fp8, slot_mapping, spec_accept_greedy)
 
 
 def to_device_bf16(bits: np.ndarray, device) -> torch.Tensor:
@@ -30,9 +30,9 @@ class DeviceStep:
     """Device-resident inputs of one step, plus outputs and scratch."""
 
     def __init__(self, w, device="cuda", max_seq_len=None, partition_tokens=None, flags=0, fp8=None):
-        """fp8: an e4m3 pool set (workloads.Fp8Pools) for the workload's
-        structure; the step then appends with quantisation and attends over
-        the e4m3 pools."""
+        """fp8: an FP8 pool set (workloads.Fp8Pools: e4m3 or e5m2, scales per
+        kv head or per block) for the workload's structure; the step then
+        appends with quantisation and attends over the FP8 pools."""
         self.w = w
         self.device = torch.device(device)
         dev = self.device
@@ -45,6 +45,10 @@ class DeviceStep:
             self.v_cache = torch.from_numpy(fp8.v_cache).to(dev)
             self.k_scale = torch.from_numpy(fp8.k_scale).to(dev)
             self.v_scale = torch.from_numpy(fp8.v_scale).to(dev)
+            # the e4m3 per-head pools take the original entry points, the
+            # other modes the general ones
+            self.fp8_ex = bool(fp8.fmt or fp8.per_block)
+            self.fp8_mode = dict(kv_format=int(fp8.fmt), scale_mode=int(bool(fp8.per_block)))
         # the per-step inputs live in one device arena (256-byte aligned
         # slices), so a step's host -> device upload is a single copy
         parts = [("q", w.q, torch.bfloat16), ("k_new", w.k_new, torch.bfloat16),
@@ -88,11 +92,14 @@ class DeviceStep:
             self.next_token = torch.empty(B, dtype=torch.int32, device=dev)
 
     def launches_per_step(self) -> int:
-        """Kernels one step() launches: copy_blocks, the fused slot mapping + append
-        (two kernels for e4m3 pools),
-        plan + attention + combine, and the two acceptance kernels."""
-        n = (1 if self.cow.numel() else 0) + ((1 if self.fp8 is None else 2) if self.n_slots else 0) + 2
-        n += 1  # the combine kernel, launched on every call
+        """Kernels one step() launches: copy_blocks (+ the scale copy with
+        per-block FP8 scales), the fused slot mapping + append (slot mapping
+        and append for FP8 pools, + the block-scale kernel with per-block
+        scales), plan + attention + combine, and the two acceptance kernels."""
+        pb = self.fp8 is not None and self.fp8.per_block
+        n = (1 + (1 if pb else 0) if self.cow.numel() else 0)
+        n += ((1 if self.fp8 is None else 2 + (1 if pb else 0)) if self.n_slots else 0)
+        n += 3  # plan, attention and the combine kernel, launched on every call
         return n + (2 if self.spec else 0)
 
     def pinned_inputs(self) -> torch.Tensor:
@@ -126,14 +133,25 @@ class DeviceStep:
         else:
             self.k_cache.copy_(torch.from_numpy(self.fp8.k_cache))
             self.v_cache.copy_(torch.from_numpy(self.fp8.v_cache))
+            self.k_scale.copy_(torch.from_numpy(self.fp8.k_scale))
+            self.v_scale.copy_(torch.from_numpy(self.fp8.v_scale))
 
     def cache_ops(self, stream=None):
         w = self.w
         if self.cow.numel():
-            (copy_blocks if self.fp8 is None else copy_blocks_fp8)(self.k_cache, self.v_cache, self.cow,
-                                                                  status=self.status, stream=stream)
+            if self.fp8 is not None and self.fp8_ex:
+                copy_blocks_fp8_ex(self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.cow,
+                                   scale_mode=self.fp8_mode["scale_mode"], status=self.status, stream=stream)
+            else:
+                (copy_blocks if self.fp8 is None else copy_blocks_fp8)(self.k_cache, self.v_cache, self.cow,
+                                                                      status=self.status, stream=stream)
         if self.n_slots:
-            if self.fp8 is None:
+            if self.fp8 is not None and self.fp8_ex:
+                slot_mapping(self.slots, self.block_tables, self.seq_lens, self.append_lens, w.block_size,
+                             w.num_blocks, status=self.status, stream=stream)
+                kv_append_fp8_ex(self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.k_new, self.v_new,
+                                 self.slots, **self.fp8_mode, status=self.status, stream=stream)
+            elif self.fp8 is None:
                 # slot mapping fused with the append (one launch)
                 kv_append_paged(self.k_cache, self.v_cache, self.k_new, self.v_new, self.block_tables,
                                 self.seq_lens, self.append_lens, self.slots, status=self.status, stream=stream)
@@ -144,6 +162,13 @@ class DeviceStep:
                               self.v_scale, status=self.status, stream=stream)
 
     def attention(self, stream=None):
+        if self.fp8 is not None and self.fp8_ex:
+            paged_attention_decode_fp8_ex(self.out, self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
+                                          self.block_tables, self.seq_lens, self.q_lens, self.max_seq_len,
+                                          self.w.scale, self.workspace, **self.fp8_mode,
+                                          partition_tokens=self.partition_tokens, status=self.status,
+                                          stream=stream, max_q_len=self.max_q_len)
+            return
         if self.fp8 is not None:
             paged_attention_decode_fp8(self.out, self.q, self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                                        self.block_tables, self.seq_lens, self.q_lens, self.max_seq_len, self.w.scale,
@@ -154,6 +179,34 @@ class DeviceStep:
                                self.q_lens, self.max_seq_len, self.w.scale, self.workspace,
                                partition_tokens=self.partition_tokens, flags=self.flags, status=self.status,
                                stream=stream, max_q_len=self.max_q_len)
+
+    def plan(self, stream=None):
+        """The planning half of attention(): the work list for this step's
+        lengths, into the workspace (one plan serves every run() after it)."""
+        w = self.w
+        attention_plan(self.seq_lens, self.q_lens, w.total_q, w.max_blocks, w.n_q, w.n_kv, w.head_dim, w.block_size,
+                       self.max_seq_len, self.workspace, partition_tokens=self.partition_tokens,
+                       flags=PKV_ATTN_PLAN_FP8 if self.fp8 is not None else self.flags, status=self.status,
+                       stream=stream, max_q_len=self.max_q_len)
+
+    def run(self, out=None, q=None, k_cache=None, v_cache=None, k_scale=None, v_scale=None, stream=None):
+        """The attention half over the planned workspace, by default over this
+        step's own buffers; another layer passes its own q, pools and out."""
+        w = self.w
+        out = self.out if out is None else out
+        q = self.q if q is None else q
+        k_cache = self.k_cache if k_cache is None else k_cache
+        v_cache = self.v_cache if v_cache is None else v_cache
+        if self.fp8 is not None:
+            paged_attention_run_fp8(out, q, k_cache, v_cache, self.k_scale if k_scale is None else k_scale,
+                                    self.v_scale if v_scale is None else v_scale, self.block_tables, w.num_seqs,
+                                    self.max_seq_len, w.scale, self.workspace,
+                                    partition_tokens=self.partition_tokens, status=self.status, stream=stream,
+                                    max_q_len=self.max_q_len, **self.fp8_mode)
+            return
+        paged_attention_run(out, q, k_cache, v_cache, self.block_tables, w.num_seqs, self.max_seq_len, w.scale,
+                            self.workspace, partition_tokens=self.partition_tokens, flags=self.flags,
+                            status=self.status, stream=stream, max_q_len=self.max_q_len)
 
     def accept(self, stream=None):
         if self.spec:

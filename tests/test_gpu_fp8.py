@@ -92,7 +92,7 @@ def test_encoding_edges_bit_exact():
     run_and_check(w)
 
 
-def test_full_size_mix_sampled():
+def test_full_size_mix_every_row():
     w = wl.FULL["mix"]()
     pools = wl.fp8_pools(w, 0)
     ds = DeviceStep(w, fp8=pools, max_seq_len=32768)
@@ -106,11 +106,13 @@ def test_full_size_mix_sampled():
         v8[dst] = v8[src]
     slots, _ = oracle.slot_mapping(w.block_tables, w.seq_lens, w.append_lens, w.block_size, w.num_blocks)
     oracle.kv_append_fp8(k8, v8, w.k_new, w.v_new, slots, pools.k_scale, pools.v_scale)
-    assert np.array_equal(ds.k_cache.cpu().numpy(), k8)
-    pick = np.linspace(0, w.num_seqs - 1, 12).astype(int)
-    ref, st = oracle.attention_fp8(w.q[pick], k8, v8, pools.k_scale, pools.v_scale, w.block_tables[pick],
-                                   w.seq_lens[pick], w.q_lens[pick], w.scale)
-    got = wl.bf16_bits_to_f32(bf16_to_bits(ds.out)[pick]).astype(np.float64)
+    assert np.array_equal(ds.k_cache.cpu().numpy(), k8) and np.array_equal(ds.v_cache.cpu().numpy(), v8)
+    # every query row of the batch-256 mix
+    ref, st = oracle.attention_fp8(w.q, k8, v8, pools.k_scale, pools.v_scale, w.block_tables, w.seq_lens,
+                                   w.q_lens, w.scale)
+    assert st == 0
+    got = wl.bf16_bits_to_f32(bf16_to_bits(ds.out)).astype(np.float64)
+    assert np.isfinite(got).all()
     assert np.all(np.abs(got - ref) <= ATOL + RTOL * np.abs(ref))
 
 

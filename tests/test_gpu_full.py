@@ -1,6 +1,7 @@
-"""Full-size workloads on the GPU, checked on sampled sequences against the
-oracle (which computes only the sampled rows) and with properties that hold at
-any size.  Same launch configuration as bench.py for the batch-256 mix."""
+"""Full-size workloads on the GPU, every output row checked element by element
+against the oracle (fp64, OpenMP over sequences: about 0.3 s for the batch-256
+mix and under half a minute for the long-context workload on 16 cores), the
+caches bit-exact over the whole pool.  Same launch configuration as bench.py."""
 import numpy as np
 import pytest
 import torch
@@ -23,15 +24,17 @@ def _oracle_cache(w):
     return k, v, slots
 
 
-def _sampled(w, out_bits, k, v, seqs):
-    rows = np.concatenate([[0], np.cumsum(w.q_lens)])
-    sel = np.concatenate([np.arange(rows[b], rows[b + 1]) for b in seqs])
-    ref, st = oracle.attention(w.q[sel], k, v, w.block_tables[seqs], w.seq_lens[seqs], w.q_lens[seqs], w.scale)
+def _all_rows(w, out_bits, k, v):
+    """Every query row of every sequence against the oracle."""
+    ref, st = oracle.attention(w.q, k, v, w.block_tables, w.seq_lens, w.q_lens, w.scale)
     assert st == 0
-    got = wl.bf16_bits_to_f32(out_bits[sel]).astype(np.float64)
+    got = wl.bf16_bits_to_f32(out_bits).astype(np.float64)
+    assert got.shape == ref.shape
     assert np.isfinite(got).all()
     err = np.abs(got - ref)
-    assert np.all(err <= 1e-2 + 1e-2 * np.abs(ref)), f"max err {err.max():.3e}"
+    bad = err > 1e-2 + 1e-2 * np.abs(ref)
+    assert not bad.any(), f"{bad.sum()} of {bad.size} outside tolerance, max err {err.max():.3e}"
+    return float(err.max())
 
 
 # partition lengths the automatic mode may pick from a floor of 512
@@ -58,31 +61,23 @@ def test_mix_batch256_full_size():
     # caches bit-exact after copy-on-write and append (whole pool)
     assert np.array_equal(bf16_to_bits(ds.k_cache), k)
     assert np.array_equal(bf16_to_bits(ds.v_cache), v)
-    out = bf16_to_bits(ds.out)
-    L = w.seq_lens
-    seqs = sorted(set([int(np.argmax(L)), int(np.argmin(L))] + list(range(0, 256, 23))
-                      + w.meta["sharers"][:4]))
-    _sampled(w, out, k, v, np.array(seqs))
-    assert np.isfinite(wl.bf16_bits_to_f32(out)).all()
-    # sequences with identical context and query would match; sharers with the
-    # same length share every cached position except their own appended row
-    # (property at full size: all rows finite, status clean -- checked above)
+    _all_rows(w, bf16_to_bits(ds.out), k, v)    # all 256 sequences, 32 heads, 128 dims
 
 
 def test_decode_batch64_full_size():
     w = wl.FULL["decode"]()
     ds = _run(w)
     k, v, _ = _oracle_cache(w)
-    out = bf16_to_bits(ds.out)
-    _sampled(w, out, k, v, np.arange(0, 64, 9))
+    assert np.array_equal(bf16_to_bits(ds.k_cache), k) and np.array_equal(bf16_to_bits(ds.v_cache), v)
+    _all_rows(w, bf16_to_bits(ds.out), k, v)    # all 64 sequences
 
 
 def test_spec_batch32_full_size():
     w = wl.FULL["spec"]()
     ds = _run(w)
     k, v, _ = _oracle_cache(w)
-    out = bf16_to_bits(ds.out)
-    _sampled(w, out, k, v, np.array([0, 7, 31]))
+    assert np.array_equal(bf16_to_bits(ds.k_cache), k) and np.array_equal(bf16_to_bits(ds.v_cache), v)
+    _all_rows(w, bf16_to_bits(ds.out), k, v)    # all 32 x 5 query rows
     acc, nxt, am = oracle.spec_accept_greedy(w.logits, w.draft)
     assert np.array_equal(ds.argmax.cpu().numpy(), am)
     assert np.array_equal(ds.accepted.cpu().numpy(), acc)
@@ -92,18 +87,7 @@ def test_spec_batch32_full_size():
 def test_long_context_with_chunk_full_size():
     w = wl.FULL["long"]()
     ds = _run(w)
-    out = bf16_to_bits(ds.out)
-    assert np.isfinite(wl.bf16_bits_to_f32(out)).all()
-    # oracle on one long decode and on sampled rows of the chunk
     k, v, _ = _oracle_cache(w)
-    _sampled(w, out, k, v, np.array([3]))
-    chunk = w.num_seqs - 1
-    rows0 = int(w.q_lens[:chunk].sum())
-    pick = np.array([0, 1, 255, 256, 511])
-    ref, st = oracle.attention(w.q[rows0 + pick], k, v,
-                               np.repeat(w.block_tables[chunk:chunk + 1], len(pick), 0),
-                               (w.seq_lens[chunk] - w.q_lens[chunk] + pick + 1).astype(np.int32),
-                               np.ones(len(pick), np.int32), w.scale)
-    assert st == 0
-    got = wl.bf16_bits_to_f32(out[rows0 + pick]).astype(np.float64)
-    assert np.all(np.abs(got - ref) <= 1e-2 + 1e-2 * np.abs(ref))
+    assert np.array_equal(bf16_to_bits(ds.k_cache), k) and np.array_equal(bf16_to_bits(ds.v_cache), v)
+    # all 8 decodes of 131072 positions and all 512 rows of the chunk
+    _all_rows(w, bf16_to_bits(ds.out), k, v)

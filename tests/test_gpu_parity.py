@@ -255,3 +255,25 @@ def test_spec_accept_random_vocab_sizes(V):
     assert np.array_equal(out[0].cpu().numpy(), am)
     assert np.array_equal(out[1].cpu().numpy(), acc)
     assert np.array_equal(out[2].cpu().numpy(), nxt)
+
+
+@pytest.mark.parametrize("g,ql", [(4, 2), (4, 3), (4, 5), (4, 6), (8, 2), (8, 3), (2, 7), (2, 12), (1, 17),
+                                  (1, 24), (16, 1), (12, 2), (3, 8)])
+@pytest.mark.parametrize("d", [64, 128])
+def test_transposed_tiles_of_several_column_tiles(g, ql, d):
+    """Short multi-query rows: q_len * g <= 16 run as one transposed tile of up
+    to two 8-column n-tiles per kv head, each column with its query's causal
+    limit; wider rows as tcgen05 tiles (automatic partitions, head_dim 128) or
+    mma.sync row tiles (partitions of 64 tokens, or head_dim 64): partial last
+    n-tiles, heads not a power of two, several partitions and a partial last
+    stage."""
+    n_kv = 2
+    w = wl.spec(B=4, lo=ql + 1, hi=300, k=ql, vocab=50, seed=7 * g + ql, n_q=g * n_kv, n_kv=n_kv, d=d, bs=16)
+    run_and_check(w, partition_tokens=64)
+    run_and_check(w)
+
+
+@pytest.mark.parametrize("bs", [1, 4, 32])
+def test_transposed_wide_tiles_block_sizes(bs):
+    w = wl.spec(B=5, lo=6, hi=200, k=5, vocab=50, seed=bs, n_q=32, n_kv=8, d=128, bs=bs)
+    run_and_check(w, partition_tokens=48)
