@@ -1,6 +1,6 @@
 """Query tiles on the tcgen05 tensor cores vs the CPU oracle (GPU required).
 
-A sequence with q_len * g >= 128 (a prefill chunk, a long verification) runs as
+A sequence with q_len * g > 8 (a prefill chunk, a verification) runs as
 tiles of 128 (query, q head) rows of one kv head, with 128-token stages, the
 scores and the output accumulated in tensor memory.  These cases cover every
 head grouping whose g divides 128, ragged last tiles, prefixes that end inside
@@ -70,12 +70,13 @@ def test_stage_edges(prefix, q_len):
     assert tiles_used(ds) == 1
 
 
-def test_below_one_tile_stays_on_mma_sync():
-    # q_len * g = 124 < 128 rows; block_size 8 boxes; a partition that is not whole stages
-    for w, P in ((chunk(32, 8, 31, prefix=300), 0), (chunk(32, 8, 64, prefix=300, bs=8), 0),
-                 (chunk(32, 8, 64, prefix=300), 48)):
+def test_partly_filled_tile_and_the_mma_sync_fallbacks():
+    # q_len * g = 124 rows: one tile with 4 rows unused; block_size 8 boxes and
+    # a partition that is not whole 128-token stages stay on mma.sync
+    for w, P, tiles in ((chunk(32, 8, 31, prefix=300), 0, 1), (chunk(32, 8, 64, prefix=300, bs=8), 0, 0),
+                        (chunk(32, 8, 64, prefix=300), 48, 0)):
         ds, _, _ = run_and_check(w, partition_tokens=P)
-        assert tiles_used(ds) == 0
+        assert tiles_used(ds) == tiles
 
 
 def test_tcgen05_and_mma_sync_paths_agree():
