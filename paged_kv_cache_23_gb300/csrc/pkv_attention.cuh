@@ -47,10 +47,20 @@ namespace pkv {
 constexpr int kTileT = 16;                  // tokens per pipeline stage
 constexpr int kCWarps = 8;                  // consumer warps
 constexpr int kCThreads = kCWarps * 32;
-constexpr int kThreads = kCThreads + 32;    // + producer warp
+// A CTA is three warpgroups: the eight consumer warps, then the producer, the
+// MMA warp and the helper TMA warp of the tcgen05 variant, and one idle warp
+// (the other variant leaves warps 9-11 idle).  With 12 warps every SM
+// sub-partition holds three, which caps the launch at 168 registers a thread;
+// the side warpgroup then gives most of its registers to the consumers
+// (setmaxnreg), so their items can hold up to 24 columns of Q^T and O^T.
+constexpr int kThreads = 12 * 32;
+constexpr int kLaunchRegs = 168;            // registers a thread at launch (65536 / 384, in steps of 8)
+constexpr int kConsumerRegs = 224;
+constexpr int kSideRegs = 56;
+static_assert(kSideRegs * 128 + kConsumerRegs * 256 <= kLaunchRegs * kThreads, "register split exceeds the launch");
 constexpr int kMaxHPS = 8;                  // kv heads per stage
-constexpr int kDecCols = 16;                // (query, q head) columns of a transposed tensor-core tile
-constexpr int kTcMinCols = 8;               // multi-query rows of more columns run as tcgen05 tiles (when enabled)
+constexpr int kDecCols = 24;                // (query, q head) columns of a transposed tensor-core tile
+constexpr int kTcMinCols = kDecCols;        // multi-query rows of more columns run as tcgen05 tiles (when enabled)
 constexpr int kRingSlots = 3;
 constexpr int kSlots = 4;                   // item descriptors in flight
 constexpr int kClaimAhead = 6;              // stages before an item's end at which the next is claimed
@@ -92,7 +102,8 @@ struct AttnParams {
     const int32_t* block_tables;
     const int4* items;   // {b, part, qt, hg}
     const int4* seqs;    // {seq_len, q_len, first query row, kind | hps << 4 | wph << 8 | qt_len << 12}
-    int* hdr;            // [0] item count, [1] queue head, [2] partition length
+    const int* seq_p;    // partition length of each sequence
+    int* hdr;            // [0] item count, [1] queue head, [2] partition length (target length when automatic)
     float* part_o;       // [(row * n_q + h) * np_max + part][D]
     float2* part_ml;     // [(row * n_q + h) * np_max + part] = (m in log2 units, l)
     int32_t* status;
@@ -108,7 +119,8 @@ struct AttnParams {
 
 // Workspace header (ints): [0] item count, [1] queue head (reset to 0 by the
 // planning kernel and again by each call's combine kernel, so one plan serves
-// any number of calls), [2] partition length, [3] tcgen05 tiles present,
+// any number of calls), [2] partition length (explicit) or target item length
+// (automatic: each sequence's own length is in the seq_p array), [3] tcgen05 tiles present,
 // [4] key of the shape the plan was made for.
 enum { HDR_ITEMS = 0, HDR_HEAD = 1, HDR_P = 2, HDR_TC = 3, HDR_KEY = 4 };
 
@@ -335,7 +347,6 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
     // a workspace whose plan was made for another shape runs nothing (the
     // combine kernel then writes every output row NaN and reports it)
     const int num_items = p.hdr[HDR_KEY] == p.plan_key ? p.hdr[HDR_ITEMS] : 0;
-    const int P = p.hdr[HDR_P];  // partition length the planning kernel chose
     const int bsr = p.bs < kTileT ? p.bs : kTileT;
     int next = 0;
     if (lane == 0) next = atomicAdd(&p.hdr[HDR_HEAD], 1);
@@ -349,7 +360,7 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
         if (!end) {
             const int4 it = __ldg(p.items + cur);
             const int4 sq = __ldg(p.seqs + it.x);
-            d = make_desc(it, sq, P);
+            d = make_desc(it, sq, __ldg(p.seq_p + it.x));
         } else {
             d = Desc{0, 0, 1, 0, 0, 0, 0, 0, 0, KIND_END, 1, 1};
         }
@@ -1985,7 +1996,11 @@ __device__ __forceinline__ void consumer(Smem<D, F8>& sm, const AttnParams& p, i
                 // columns of the tile: g heads of each of its nq queries, 8 per n-tile
                 const int ncols = d.nq * p.G;
                 if (NTN == 1 || ncols <= 8) decode_tc_item<D, 1>(sm, p, d, warp, lane, g, ntiles, si, abort);
-                else if constexpr (NTN > 1) decode_tc_item<D, 2>(sm, p, d, warp, lane, g, ntiles, si, abort);
+                else if (NTN == 2 || ncols <= 16) {
+                    if constexpr (NTN > 1) decode_tc_item<D, 2>(sm, p, d, warp, lane, g, ntiles, si, abort);
+                } else {
+                    if constexpr (NTN > 2) decode_tc_item<D, 3>(sm, p, d, warp, lane, g, ntiles, si, abort);
+                }
             } else if (d.kind == KIND_MQ) {
                 mq_item<D>(sm, p, d, warp, lane, g, ntiles, si, abort);
             } else {
@@ -2004,13 +2019,49 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
     return n;
 }
 
+// Tensor memory of the tcgen05 variant, set up by the consumer warps and the
+// MMA warp together: allocated (by consumer warp 0) only when the plan made
+// tiles -- one CTA per SM, so the allocation never waits -- then one named
+// barrier over those nine warps.  Returns whether tensor memory is in use.
+template <int D, bool F8>
+__device__ __forceinline__ bool tc_begin(Smem<D, F8>& sm, const AttnParams& p, int warp, TcState& tc) {
+    const bool use_tc = p.tc != 0 && p.hdr[HDR_TC] != 0 && p.hdr[HDR_KEY] == p.plan_key;
+    if (use_tc) {
+        if (warp == 0) tmem_alloc(&sm.tmem, kTmemCols);
+        tc_fence_before();
+        named_bar(1, kCThreads + 32);  // consumers + the MMA warp, once
+        tc_fence_after();
+        tc.tmem = sm.tmem;
+    }
+    return use_tc;
+}
+
+// Release of the tensor memory once every MMA has completed and every warp is
+// done with it (bounded by time alone: an abort must not skip the release).
+template <int D, bool F8>
+__device__ __forceinline__ void tc_end(Smem<D, F8>& sm, int warp, int lane, bool mma, const TcState& tc) {
+    if (mma && lane == 0) {
+        umma_commit(&sm.tdone);
+        if (!mbar_wait_ns(&sm.tdone, 0)) sm.abort = 1;
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.dbar);
+    if (warp == 0) {
+        if (!mbar_wait_ns(&sm.dbar, 0)) sm.abort = 1;
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tc.tmem, kTmemCols);
+    }
+}
+
 // TC: the variant with tcgen05 tiles (head_dim 128, bf16), launched only for
 // batches that may hold a 128-row tile -- the other variant's item code keeps
 // its register allocation free of the tile's.
 // Threads of a CTA: eight consumer warps, the producer warp, and in the
 // variant with tcgen05 tiles the MMA warp and the helper TMA warp.
 template <bool TC>
-constexpr int kThreadsOf = TC ? kThreads + 64 : kThreads;
+constexpr int kThreadsOf = kThreads;
 
 template <int D, int GD, bool F8, bool TC, int NTN, int FQ>
 __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
@@ -2055,56 +2106,39 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
     __syncthreads();
     pdl_wait();    // the planning kernel's records are complete and visible
     pdl_launch();  // the combine kernel may be scheduled; it waits for this grid to finish
-    if (warp == kCWarps) {
-        producer<D, F8>(sm, &tm, p, lane);
-    } else if (TC && warp == kCWarps + 2) {
-        if constexpr (TC) helper_warp<D, F8>(sm, &tm, p, lane);
+    // Register budgets per warpgroup: each role's code sits wholly inside the
+    // branch that set its budget (code reached from both branches would be
+    // held to the smaller one).
+    if (warp >= kCWarps) {
+        setmaxnreg_dec<kSideRegs>();
+        if (warp == kCWarps) {
+            producer<D, F8>(sm, &tm, p, lane);
+        } else if constexpr (TC) {
+            if (warp == kCWarps + 2) {
+                helper_warp<D, F8>(sm, &tm, p, lane);
+            } else if (warp == kCWarps + 1) {
+                TcState tc{0u, 0u, 0u, 0u};
+                const bool use_tc = tc_begin<D, F8>(sm, p, warp, tc);
+                mma_warp<D, F8>(sm, p, lane, tc);
+                if (use_tc) tc_end<D, F8>(sm, warp, lane, true, tc);
+            }
+            // warp kCWarps + 3: no role
+        }
+        // warps kCWarps + 1 .. + 3 of the variant without tiles: no role
     } else {
-        // consumer warps 0-7 and (tcgen05 variant) the MMA warp kCWarps + 1
-        const bool mma = TC && warp == kCWarps + 1;
+        setmaxnreg_inc<kConsumerRegs>();
         TcState tc{0u, 0u, 0u, 0u};
         bool use_tc = false;
+        if constexpr (TC) use_tc = tc_begin<D, F8>(sm, p, warp, tc);
+        consumer<D, GD, F8, TC, NTN, FQ>(sm, p, warp, lane, tc);
         if constexpr (TC) {
-            // tensor memory only when the plan made tcgen05 tiles (one CTA per
-            // SM, so the allocation never waits)
-            use_tc = p.tc != 0 && p.hdr[HDR_TC] != 0 && p.hdr[HDR_KEY] == p.plan_key;
-            if (use_tc) {
-                if (warp == 0) tmem_alloc(&sm.tmem, kTmemCols);
-                tc_fence_before();
-                named_bar(1, kCThreads + 32);  // consumers + the MMA warp, once
-                tc_fence_after();
-                tc.tmem = sm.tmem;
-            }
-        }
-        if (mma) {
-            if constexpr (TC) mma_warp<D, F8>(sm, p, lane, tc);
-        } else {
-            consumer<D, GD, F8, TC, NTN, FQ>(sm, p, warp, lane, tc);
-        }
-        if constexpr (TC) {
-            if (use_tc) {
-                // every MMA has completed and every warp is done with tensor memory
-                // (bounded by time alone: an abort must not skip the release)
-                if (mma && lane == 0) {
-                    umma_commit(&sm.tdone);
-                    if (!mbar_wait_ns(&sm.tdone, 0)) sm.abort = 1;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.dbar);
-                if (warp == 0) {
-                    if (!mbar_wait_ns(&sm.dbar, 0)) sm.abort = 1;
-                    __syncwarp();
-                    tc_fence_after();
-                    tmem_dealloc(tc.tmem, kTmemCols);
-                }
-            }
+            if (use_tc) tc_end<D, F8>(sm, warp, lane, false, tc);
         }
     }
     if (threadIdx.x == 0 && sm.abort) report(p.status, PKV_STATUS_TIMEOUT);
 }
 
-template <int D, int GD, bool F8 = false, bool TC = false, int NTN = 2, int FQ = 0>
+template <int D, int GD, bool F8 = false, bool TC = false, int NTN = 3, int FQ = 0>
 int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, cudaStream_t st) {
     static int configured[64] = {0};
     int dev = 0;
@@ -2118,6 +2152,13 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     if (!configured[dev]) {
         if (cudaFuncSetAttribute(paged_attention_kernel<D, GD, F8, TC, NTN, FQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        // the warpgroups' setmaxnreg counts add up to kLaunchRegs a thread:
+        // a build that launched with fewer would leave the consumers' request
+        // waiting for registers the CTA does not have, so it is never launched
+        cudaFuncAttributes fa{};
+        if (cudaFuncGetAttributes(&fa, paged_attention_kernel<D, GD, F8, TC, NTN, FQ>) != cudaSuccess ||
+            fa.numRegs != kLaunchRegs || fa.maxThreadsPerBlock < kThreads)
             return PKV_ERR_CUDA;
         configured[dev] = 1;
     }
@@ -2140,7 +2181,7 @@ int dispatch_g(int GD, bool wide, const TMaps& tm, const AttnParams& p, long lon
         case 4: return launch_attention<D, 4>(tm, p, mi, st);
         case 8: return launch_attention<D, 8>(tm, p, mi, st);
         default:
-            return wide ? launch_attention<D, 0, false, false, 2>(tm, p, mi, st)
+            return wide ? launch_attention<D, 0, false, false, 3>(tm, p, mi, st)
                         : launch_attention<D, 0, false, false, 1>(tm, p, mi, st);
     }
 }

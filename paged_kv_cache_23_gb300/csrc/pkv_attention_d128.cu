@@ -4,7 +4,7 @@
 namespace pkv {
 int dispatch_attention_d128(int GD, bool tc, bool wide, const TMaps& tm, const AttnParams& p, long long mi,
                             cudaStream_t st) {
-    if (tc) return launch_attention<128, 0, false, true, 1>(tm, p, mi, st);
+    if (tc) return launch_attention<128, 0, false, true, 3>(tm, p, mi, st);
     return dispatch_g<128>(GD, wide, tm, p, mi, st);
 }
 int combine_d128(const CombineParams& c, cudaStream_t st) { return launch_combine<128>(c, st); }

@@ -15,13 +15,13 @@ struct PlanParams {
     int* seq_q0;     // first query row
     int* seq_flag;   // PKV_STATUS_* bits of the sequence (0 = valid)
     int* seq_mq;     // exclusive prefix of multi-query item counts
-    int* seq_full;   // exclusive prefix of full decode-partition item counts
+    int* seq_p;      // partition length of each sequence (read by the attention kernel)
     int* row_np;     // [total_q] partitions of each query row (-1: row of an invalid sequence)
     int32_t* status;
     int num_seqs, total_q, n_q, n_kv, G, D, P, max_blocks, bs, max_seq_len, max_q_len, decode_ok;
     int fp8;         // e4m3 pool: every row on the transposed tensor-core item
     int tc;          // tcgen05 tiles allowed (head_dim 128, bf16, block_size >= 16, P % 128 == 0)
-    int adapt_P;     // 1: P is a floor; the planning kernel may raise it
+    int adapt_P;     // 1: P is a floor; the planning kernel sizes each sequence's partitions
     int sms;         // SM count (persistent CTAs of the attention kernel)
     int plan_key;    // key of the shape this plan is made for (header int 4)
 };
@@ -40,14 +40,14 @@ struct SeqShape {
 
 // decode_fma: run q_len = 1 rows on the CUDA-core path (else tensor cores).
 // fp8: e4m3 pool -- tiles of up to 16 (query, q head) columns per kv head.
-// bf16 q_len * g <= kDecCols: one tile of q_len queries on the transposed
-// tensor-core item (decode_tc_item); longer multi-query rows on mma.sync
+// bf16 q_len * g <= kDecCols (24): one tile of q_len queries on the
+// transposed tensor-core item (decode_tc_item) -- decode rows and short
+// verifications (k = 5 drafts at g = 4: 20 columns), one warp per kv head,
+// every kv head of a block in one stage; longer multi-query rows on mma.sync
 // row tiles (mq_item).
-// tc: a sequence with more than kTcMinCols (query, q head) rows per kv head
-// runs as tcgen05 tiles of 128 rows (128 / G queries), one kv head each --
-// a speculative verification's 20 rows fill a sixth of a tile, but the
-// accumulators live in tensor memory, so the item costs no registers and
-// streams 128-token stages.
+// tc: a sequence with more than kTcMinCols (= kDecCols) (query, q head) rows
+// per kv head runs as tcgen05 tiles of 128 rows (128 / G queries), one kv
+// head each.
 __device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decode_fma, int fp8, int tc) {
     SeqShape s;
     if (tc && ql * G > kTcMinCols && kTcRows % G == 0) {
@@ -72,10 +72,9 @@ __device__ __forceinline__ SeqShape seq_shape(int ql, int G, int n_kv, int decod
         return s;
     }
     if (ql * G <= kDecCols) {
-        // decode rows and short verifications: one query tile of up to 16
+        // decode rows and short verifications: one query tile of up to 24
         // (query, q head) columns per kv head, one warp per kv head, so every
-        // kv head of a block shares a stage (with tcgen05 tiles enabled, rows
-        // of more than 8 columns are tiles instead)
+        // kv head of a block shares a stage
         s.kind = KIND_DEC;
         s.hps = gcd_pow2(n_kv, kMaxHPS);
         s.wph = 1;
@@ -152,33 +151,58 @@ __device__ __forceinline__ void block_scan_k(int (&v)[K], int (&tot)[K], int* tm
     }
     __syncthreads();
 }
-constexpr int kAutoPMax = 8192;       // automatic partition length: upper bound
-// automatic partition length: target partitions per SM (decode-heavy and
-// multi-query-heavy batches)
-constexpr int kAutoItemsPerSM = 2, kAutoItemsPerSMMQ = 3;
+constexpr int kAutoPMax = 8192;       // automatic partition length: upper bound of the target
+constexpr int kAutoItemsPerSM = 2;    // automatic partition length: target items per SM
 
-// Work list for a batch: multi-query items first (the compute-heavy tiles
-// start early), then every full decode partition, then the decode partition
-// tails ordered longest first (counting sort over kTailBuckets length
-// classes), so the dynamic queue ends on the shortest items.  The list depends
-// only on the lengths, so one plan serves every layer of a decode step.
-//   pass A  one thread per sequence: validity, query rows, item counts and
-//           their prefix sums, tail-length histogram;
-//   pass B  items and per-row partition counts written over the item (row)
-//           index space, one thread per item (row), which finds its sequence
-//           by binary search in the prefix sums -- consecutive threads write
-//           consecutive 16-byte items, so the stores coalesce.
+// Partition length of one sequence.  Explicit: P.  Automatic: the sequence's
+// L positions are cut into n = round(L / C) partitions of (nearly) equal
+// length, C being the batch's target item length, rounded up to whole stages
+// (16 tokens, 128 for tcgen05 tiles) and no shorter than the floor P (so no
+// row ever has more partitions than the workspace holds).  Uniform partitions
+// of one length leave each sequence a short tail and the batch a ragged last
+// wave of the dynamic queue; equal cuts make every item of the batch about C
+// long.
+__device__ __forceinline__ int seq_partition(int L, int C, int P, int align, int adapt) {
+    if (!adapt) return P;
+    const int n = max(1, (L + C / 2) / C);
+    const int pb = ceil_div(ceil_div(L, n), align) * align;
+    return max(pb, P);
+}
+
+// Longest-first class of an item of `len` positions, items no longer than Pn
+// (inv = kTailBuckets / Pn): 0 for the longest.  In fp32: the class only
+// orders the queue, and a 64-bit integer division per item was a third of
+// the planning kernel's time.
+__device__ __forceinline__ int len_bucket(int len, int Pn, float inv) {
+    const int b = __float2int_rz((float)(Pn - len) * inv);
+    return min(kTailBuckets - 1, max(0, b));
+}
+
+// Work list for a batch: multi-query items first (mma.sync rows and tcgen05
+// tiles: compute-heavy, started early), in sequence order; then every
+// decode-style item (decode rows and transposed short verifications) ordered
+// longest first by a counting sort over kTailBuckets length classes, so the
+// dynamic queue ends on the shortest items.  The list depends only on the
+// lengths, so one plan serves every layer of a decode step.
+//   pass A  one thread per sequence: validity, query rows, partition length,
+//           multi-query item counts and their prefix sums, length-class
+//           histogram of the other items;
+//   pass B  multi-query items written over the item index space (one thread
+//           per item, which finds its sequence by binary search in the prefix
+//           sums, so consecutive threads write consecutive 16-byte items);
+//           decode-style items by one thread per sequence into ranges it
+//           reserves in its items' length classes; per-row partition counts.
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constant__ PlanParams pp) {
     __shared__ int tmp[32 * 2];
     __shared__ int hist[kTailBuckets];
-    __shared__ int s_q0[kPlanSmemSeqs], s_mq[kPlanSmemSeqs], s_full[kPlanSmemSeqs], s_flag[kPlanSmemSeqs];
+    __shared__ int s_q0[kPlanSmemSeqs], s_mq[kPlanSmemSeqs], s_p[kPlanSmemSeqs], s_flag[kPlanSmemSeqs];
     __shared__ int4 s_seq[kPlanSmemSeqs];
     const int tid = threadIdx.x;
     const int n = pp.num_seqs;
     const bool small = n <= kPlanSmemSeqs;
     int* a_q0 = small ? s_q0 : pp.seq_q0;
     int* a_mq = small ? s_mq : pp.seq_mq;
-    int* a_full = small ? s_full : pp.seq_full;
+    int* a_p = small ? s_p : pp.seq_p;
     int* a_flag = small ? s_flag : pp.seq_flag;
     const int4* a_seq = small ? s_seq : pp.seqs;  // per-sequence records of pass A (global copy always written)
     if (tid < kTailBuckets) hist[tid] = 0;
@@ -190,43 +214,37 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     // and the work list may still be read by a previous call's kernels.
     pdl_launch();
     pdl_wait();
-    // this thread's first sequence, read once for the partition choice and pass A
+    // this thread's first sequence, read once for the target length and pass A
     const int L0 = tid < n ? pp.seq_lens[tid] : 0, ql0 = tid < n ? pp.q_lens[tid] : 0;
-    int P = pp.P;
+    const int P = pp.P;  // explicit length, or the floor of the automatic ones
+    int C = P;           // target item length
     if (pp.adapt_P) {
-        // automatic partition length: the floor P, raised along the ladder
-        // P, 3P/2, 2P, 3P, 4P, ... (up to kAutoPMax) while the batch would give
-        // more than kAutoItemsPerSM partitions per SM -- fewer, longer items
-        // cost fewer partial results and item switches, and the finer steps
-        // keep the last wave of the dynamic queue from being nearly empty (on
-        // the speculative workload P = 768 beat both 512 and 1024 by 8-12 %)
-        long long tok = 0, tok_mq = 0;
+        // about kAutoItemsPerSM items per SM over the batch's work (positions
+        // x head groups x query tiles), each no shorter than the floor
+        long long tok = 0;
         for (int b = tid; b < n; b += kPlanThreads) {
             const int L = b == tid ? L0 : pp.seq_lens[b], ql = b == tid ? ql0 : pp.q_lens[b];
             if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len || ql > pp.max_q_len) continue;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
-            const bool multi = multi_query_kind(sh.kind) || ql > 1;
-            const long long t = (long long)L * (pp.n_kv / sh.hps) * (multi ? ceil_div(ql, sh.qt) : 1);
-            tok += t;
-            if (multi) tok_mq += t;
+            tok += (long long)L * (pp.n_kv / sh.hps) * ceil_div(ql, sh.qt);
         }
-        // block sums in units of 16 tokens (fit an int for any accepted batch)
+        // block sum in units of 16 tokens (fits an int for any accepted batch)
         const int cap = (1 << 30) / kPlanThreads;
-        int v2[2] = {(int)min(tok >> 4, (long long)cap), (int)min(tok_mq >> 4, (long long)cap)}, t2[2];
-        block_scan_k<2>(v2, t2, tmp);
-        const int tot16 = t2[0], mq16 = t2[1];
-        const long long T = (long long)tot16 << 4;
-        // multi-query items cost more compute per token: a batch made of them
-        // (speculative verification) balances better with more items
-        const int per_sm = 4 * (long long)mq16 > 3 * (long long)tot16 ? kAutoItemsPerSMMQ : kAutoItemsPerSM;
-        while (P < kAutoPMax && T > (long long)P * per_sm * pp.sms) P = (P & (P - 1)) == 0 ? P + P / 2 : P + P / 3;
+        int v1[1] = {(int)min(tok >> 4, (long long)cap)}, t1[1];
+        block_scan_k<1>(v1, t1, tmp);
+        const int per = kAutoItemsPerSM * pp.sms;
+        const int c16 = (t1[0] + per - 1) / per;  // in units of 16 tokens
+        C = max(P, min(kAutoPMax / kTileT, c16) * kTileT);
     }
-    if (tid == 0) pp.hdr[HDR_P] = P;
+    // item lengths are at most Pn: explicit P, or 1.5 C + one 128-token round-up
+    const int Pn = pp.adapt_P ? 2 * C : P;
+    const float inv_pn = (float)kTailBuckets / (float)Pn;
+    if (tid == 0) pp.hdr[HDR_P] = C;
     __syncthreads();
     int bits = 0, any_tc = 0;
     // pass A
     long long carry = 0;
-    int c_mq = 0, c_full = 0;
+    int c_mq = 0;
     for (int base = 0; base < n; base += kPlanThreads) {
         const int b = base + tid;
         int qlc = 0, flag = 0, L = 0, ql = 0;
@@ -241,7 +259,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         }
         int tot;
         const int ex = block_exclusive_scan_1024(qlc, tmp, &tot);
-        int nmq = 0, nfull = 0, q0 = 0;
+        int nmq = 0, q0 = 0;
         if (b < n) {
             const long long q0l = carry + ex;
             if (q0l + qlc > pp.total_q) flag |= PKV_STATUS_BAD_QLEN;  // rows would overflow q/out
@@ -249,59 +267,79 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             bits |= flag;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
             const int ngroups = pp.n_kv / sh.hps;
-            if (flag == 0) {
+            const int pb = seq_partition(L, C, P, sh.kind == KIND_TC ? kTcT : kTileT, pp.adapt_P);
+            if (flag == 0 && ql > 0) {
                 if (sh.kind == KIND_TC) any_tc = 1;
-                if (!multi_query_kind(sh.kind) && ql == 1) {
-                    const int np = ceil_div(L, P);
-                    nfull = (np - 1) * ngroups;
-                    const int tl = L - (np - 1) * P;  // in [1, P]
-                    atomicAdd(&hist[(int)(((long long)(P - tl) * kTailBuckets) / P)], ngroups);
-                } else if (ql > 0) {
-                    nmq = mq_parts_of(L, ql, sh.qt, P) * ngroups;
+                if (multi_query_kind(sh.kind)) {
+                    nmq = mq_parts_of(L, ql, sh.qt, pb) * ngroups;
+                } else {
+                    // query tile qt sees t_vis positions: np - 1 items of pb and a tail
+                    for (int qt = 0; qt * sh.qt < ql; ++qt) {
+                        const int nq = min(sh.qt, ql - qt * sh.qt);
+                        const int tv = L - ql + qt * sh.qt + nq;
+                        const int np = ceil_div(tv, pb);
+                        if (np > 1) atomicAdd(&hist[len_bucket(pb, Pn, inv_pn)], (np - 1) * ngroups);
+                        atomicAdd(&hist[len_bucket(tv - (np - 1) * pb, Pn, inv_pn)], ngroups);
+                    }
                 }
             }
             const int4 rec = make_int4(L, ql, q0, sh.kind | (sh.hps << 4) | (sh.wph << 8) | (sh.qt << 12));
             pp.seqs[b] = rec;
-            if (small) s_seq[b] = rec;
+            pp.seq_p[b] = pb;
+            if (small) {
+                s_seq[b] = rec;
+                s_p[b] = pb;
+            }
             a_flag[b] = flag;
         }
         carry += tot;
-        int v2[2] = {nmq, nfull}, t2[2];
-        block_scan_k<2>(v2, t2, tmp);
+        int v1[1] = {nmq}, t1[1];
+        block_scan_k<1>(v1, t1, tmp);
         if (b < n) {
             a_q0[b] = q0;
-            a_mq[b] = c_mq + v2[0];
-            a_full[b] = c_full + v2[1];
+            a_mq[b] = c_mq + v1[0];
         }
-        c_mq += t2[0];
-        c_full += t2[1];
+        c_mq += t1[0];
     }
-    // tail buckets -> first slot of each bucket (exclusive scan)
+    // length classes -> first slot of each class (exclusive scan), after the
+    // multi-query items
     any_tc = __syncthreads_or(any_tc);
-    int c_tail;
+    int c_dec;
     {
         const int v = tid < kTailBuckets ? hist[tid] : 0;
-        const int ex = block_exclusive_scan_1024(v, tmp, &c_tail);
-        if (tid < kTailBuckets) hist[tid] = c_mq + c_full + ex;
+        const int ex = block_exclusive_scan_1024(v, tmp, &c_dec);
+        if (tid < kTailBuckets) hist[tid] = c_mq + ex;
     }
     if (tid == 0) {
-        pp.hdr[HDR_ITEMS] = c_mq + c_full + c_tail;
+        pp.hdr[HDR_ITEMS] = c_mq + c_dec;
         pp.hdr[HDR_HEAD] = 0;
         pp.hdr[HDR_TC] = any_tc;  // the attention kernel allocates tensor memory only then
         pp.hdr[HDR_KEY] = pp.plan_key;
     }
     __syncthreads();
-    // pass B1: one thread per sequence -- decode tails and invalid sequences
+    // pass B1: one thread per sequence -- decode-style items, reserved per
+    // length class (the order inside a class does not matter: every item's
+    // partial lands at its own (row, partition) index)
     for (int b = tid; b < n; b += kPlanThreads) {
         const int4 sq = a_seq[b];
         const int L = sq.x, ql = sq.y;
-        if (a_flag[b]) continue;  // its rows are written NaN after the wait below
-        if (ql != 1 || multi_query_kind(sq.w & 15)) continue;  // multi-query tiles are counted in pass B2
+        if (a_flag[b] || ql <= 0) continue;  // invalid rows are written NaN by each call's combine kernel
+        if (multi_query_kind(sq.w & 15)) continue;
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
-        const int np = ceil_div(L, P);
-        const int tl = L - (np - 1) * P;
-        const int t0 = atomicAdd(&hist[(int)(((long long)(P - tl) * kTailBuckets) / P)], ngroups);
-        for (int hg = 0; hg < ngroups; ++hg) pp.items[t0 + hg] = make_int4(b, np - 1, 0, hg);
+        const int QT = (sq.w >> 12) & 4095;
+        const int pb = a_p[b];
+        for (int qt = 0; qt * QT < ql; ++qt) {
+            const int nq = min(QT, ql - qt * QT);
+            const int tv = L - ql + qt * QT + nq;
+            const int np = ceil_div(tv, pb);
+            if (np > 1) {
+                int at = atomicAdd(&hist[len_bucket(pb, Pn, inv_pn)], (np - 1) * ngroups);
+                for (int part = 0; part < np - 1; ++part)
+                    for (int hg = 0; hg < ngroups; ++hg) pp.items[at++] = make_int4(b, part, qt, hg);
+            }
+            const int at = atomicAdd(&hist[len_bucket(tv - (np - 1) * pb, Pn, inv_pn)], ngroups);
+            for (int hg = 0; hg < ngroups; ++hg) pp.items[at + hg] = make_int4(b, np - 1, qt, hg);
+        }
     }
     // pass B2: multi-query items
     for (int it = tid; it < c_mq; it += kPlanThreads) {
@@ -310,9 +348,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
         const int4 sq = a_seq[b];
         const int L = sq.x, ql = sq.y, QT = (sq.w >> 12) & 4095;
         const int ngroups = pp.n_kv / ((sq.w >> 4) & 15);
+        const int pb = a_p[b];
         for (int qt = 0; qt * QT < ql; ++qt) {
             const int nq = min(QT, ql - qt * QT);
-            const int cnt = ceil_div(L - ql + qt * QT + nq, P) * ngroups;
+            const int cnt = ceil_div(L - ql + qt * QT + nq, pb) * ngroups;
             if (li < cnt) {
                 const int part = li / ngroups;
                 pp.items[it] = make_int4(b, part, qt, li - part * ngroups);
@@ -321,17 +360,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             li -= cnt;
         }
     }
-    // pass B3: full decode partitions
-    {
-        const int ngroups = pp.n_kv / gcd_pow2(pp.n_kv, kMaxHPS);
-        for (int it = tid; it < c_full; it += kPlanThreads) {
-            const int b = last_le(a_full, n, it);
-            const int li = it - a_full[b];
-            const int part = li / ngroups;
-            pp.items[c_mq + it] = make_int4(b, part, 0, li - part * ngroups);
-        }
-    }
-    // pass B4: partitions per query row; -1 for the rows of an invalid
+    // pass B3: partitions per query row; -1 for the rows of an invalid
     // sequence (inside the q/out extent), which each call's combine kernel
     // writes NaN; 0 for rows past the last sequence's queries
     for (int r = tid; r < pp.total_q; r += kPlanThreads) {
@@ -348,7 +377,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
                 const int QT = (sq.w >> 12) & 4095;
                 const int qt = (r - q0) / QT;
                 const int nq = min(QT, ql - qt * QT);
-                np = ceil_div(L - ql + qt * QT + nq, P);
+                np = ceil_div(L - ql + qt * QT + nq, a_p[b]);
             }
         }
         pp.row_np[r] = np;
@@ -511,7 +540,7 @@ int launch_plan(const Shape& s, const int32_t* seq_lens, const int32_t* q_lens, 
     pp.seq_q0 = aux;
     pp.seq_flag = aux + s.num_seqs;
     pp.seq_mq = aux + 2 * s.num_seqs;
-    pp.seq_full = aux + 3 * s.num_seqs;
+    pp.seq_p = aux + 3 * s.num_seqs;
     pp.row_np = reinterpret_cast<int*>(ws + s.w.rownp);
     pp.status = status;
     pp.num_seqs = s.num_seqs;
@@ -607,6 +636,7 @@ int launch_run(const Shape& s, void* out, const void* q, const void* k_cache, co
     ap.block_tables = block_tables;
     ap.items = reinterpret_cast<const int4*>(ws + s.w.items);
     ap.seqs = reinterpret_cast<const int4*>(ws + s.w.seqs);
+    ap.seq_p = reinterpret_cast<const int*>(ws + s.w.seqaux) + 3 * s.num_seqs;
     ap.hdr = reinterpret_cast<int*>(ws + s.w.hdr);
     ap.part_o = reinterpret_cast<float*>(ws + s.w.o);
     ap.part_ml = reinterpret_cast<float2*>(ws + s.w.ml);
@@ -626,7 +656,7 @@ int launch_run(const Shape& s, void* out, const void* q, const void* k_cache, co
     ap.tc = s.tc ? 1 : 0;
     ap.tc_pair = tc_pair ? 1 : 0;
     ap.plan_key = s.key;
-    // transposed items wider than one n-tile are possible when q_len * g > 8
+    // transposed items wider than one n-tile (8 columns) are possible when q_len * g > 8
     const bool wide = (long long)s.max_q_len * s.G > 8;
     const int rc = fp8 ? dispatch_attention_fp8_d128(fq, tm, ap, s.w.max_items, st)
                    : head_dim == 128

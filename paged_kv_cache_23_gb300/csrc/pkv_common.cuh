@@ -105,6 +105,22 @@ __device__ __forceinline__ void drain_ring(uint64_t* full, uint32_t g) {
     }
 }
 
+// ---- per-warpgroup register budgets --------------------------------------
+// setmaxnreg moves registers between the warpgroups of a CTA: .dec returns
+// registers to the CTA's pool, .inc takes them from it (and waits until the
+// pool holds them), so the counts a kernel asks for must add up to no more
+// than what the CTA was launched with -- the launch code checks that.
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+    static_assert(N % 8 == 0 && N >= 24 && N <= 256, "setmaxnreg count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ---- TMA (2-D tiled, no multicast) ----------------------------------------
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
     asm volatile(

@@ -212,10 +212,24 @@ class DeviceStep:
         if self.spec:
             spec_accept_greedy(self.logits, self.draft, self.argmax, self.accepted, self.next_token, stream=stream)
 
-    def step(self, stream=None):
-        self.cache_ops(stream)
-        self.attention(stream)
-        self.accept(stream)
+    def step(self, stream=None, plan_stream=None):
+        """One decode step.  With `plan_stream`, the plan (which reads only the
+        lengths) runs there while the cache ops run on `stream`, and the
+        attention run waits for it; the plan stream first waits for the work
+        already on `stream` (the previous step's kernels still read the
+        workspace, and the lengths may have just been uploaded there)."""
+        if plan_stream is None:
+            self.cache_ops(stream)
+            self.attention(stream)
+            self.accept(stream)
+            return
+        s = stream if stream is not None else torch.cuda.current_stream(self.device)
+        plan_stream.wait_stream(s)
+        self.plan(plan_stream)
+        self.cache_ops(s)
+        s.wait_stream(plan_stream)
+        self.run(stream=s)
+        self.accept(s)
 
 
 def main(argv=None):

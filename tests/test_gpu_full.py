@@ -37,8 +37,11 @@ def _all_rows(w, out_bits, k, v):
     return float(err.max())
 
 
-# partition lengths the automatic mode may pick from a floor of 512
-AUTO_LADDER = {512, 768, 1024, 1536, 2048, 3072, 4096, 6144, 8192}
+def _auto_target_ok(used: int) -> bool:
+    """The automatic mode's target item length: whole 16-token stages, from the
+    floor of 512 up to 8192 (each sequence is cut into equal partitions of
+    about this length)."""
+    return used % 16 == 0 and 512 <= used <= 8192
 
 
 def _run(w, **kw):
@@ -49,7 +52,7 @@ def _run(w, **kw):
     if ds.partition_tokens in (None, 0):
         # the length the planning kernel used is the int at byte offset 8 of the workspace
         used = int(ds.workspace[8:12].view(torch.int32).item())
-        assert used in AUTO_LADDER, used
+        assert _auto_target_ok(used), used
     return ds
 
 

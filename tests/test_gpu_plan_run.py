@@ -182,3 +182,27 @@ def test_back_to_back_calls_with_lengths_written_on_the_gpu(bs, kind, plan_run):
     want, st = oracle.attention(w.q, k, v, w.block_tables, w.seq_lens, w.q_lens, w.scale)
     assert st == 0
     _close(outs[0], want, f"{kind} bs {bs}")
+
+
+@pytest.mark.parametrize("name", ["decode", "mix", "spec"])
+def test_step_with_the_plan_on_a_side_stream(name):
+    # the bench's step: the plan on its own stream beside the cache ops, the
+    # run after both; every step bit-identical to the one-stream step, and
+    # the first within tolerance of the oracle
+    w = wl.SMALL[name]()
+    ds = DeviceStep(w)
+    ds.step()
+    torch.cuda.synchronize()
+    ref = bf16_to_bits(ds.out)
+    k, v = _oracle_pools(w)
+    want, st = oracle.attention(w.q, k, v, w.block_tables, w.seq_lens, w.q_lens, w.scale)
+    assert st == 0
+    _close(ref, want, name)
+    main, side = torch.cuda.current_stream(), torch.cuda.Stream()
+    for _ in range(5):
+        ds.reset_cache()
+        ds.out.fill_(float("nan"))
+        ds.step(main, side)
+    torch.cuda.synchronize()
+    assert int(ds.status.item()) == 0, pkv.status_bits(int(ds.status.item()))
+    assert np.array_equal(bf16_to_bits(ds.out), ref)
