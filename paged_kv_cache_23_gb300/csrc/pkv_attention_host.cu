@@ -162,11 +162,21 @@ constexpr int kAutoItemsPerSM = 2;    // automatic partition length: target item
 // of one length leave each sequence a short tail and the batch a ragged last
 // wave of the dynamic queue; equal cuts make every item of the batch about C
 // long.
+// adapt: 0 explicit; 1 nearest count, n = round(L / C) (items about C long,
+// up to 1.5 C); 2 ceiling count, n = ceil(L / C) (items at most C long).
 __device__ __forceinline__ int seq_partition(int L, int C, int P, int align, int adapt) {
     if (!adapt) return P;
-    const int n = max(1, (L + C / 2) / C);
+    const int n = adapt == 2 ? max(1, ceil_div(L, C)) : max(1, (L + C / 2) / C);
     const int pb = ceil_div(ceil_div(L, n), align) * align;
     return max(pb, P);
+}
+
+// Items of one sequence for partition length pb: np partitions of each of its
+// query tiles, times its head groups.
+__device__ __forceinline__ int seq_items(int L, int ql, const SeqShape& sh, int pb, int ngroups) {
+    int cnt = 0;
+    for (int qt = 0; qt * sh.qt < ql; ++qt) cnt += ceil_div(L - ql + qt * sh.qt + min(sh.qt, ql - qt * sh.qt), pb);
+    return cnt * ngroups;
 }
 
 // Longest-first class of an item of `len` positions, items no longer than Pn
@@ -197,6 +207,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     __shared__ int hist[kTailBuckets];
     __shared__ int s_q0[kPlanSmemSeqs], s_mq[kPlanSmemSeqs], s_p[kPlanSmemSeqs], s_flag[kPlanSmemSeqs];
     __shared__ int4 s_seq[kPlanSmemSeqs];
+    __shared__ int s_len[kPlanSmemSeqs], s_ql[kPlanSmemSeqs], s_cnt[32];
     const int tid = threadIdx.x;
     const int n = pp.num_seqs;
     const bool small = n <= kPlanSmemSeqs;
@@ -218,23 +229,61 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
     const int L0 = tid < n ? pp.seq_lens[tid] : 0, ql0 = tid < n ? pp.q_lens[tid] : 0;
     const int P = pp.P;  // explicit length, or the floor of the automatic ones
     int C = P;           // target item length
+    int rule = 0;        // seq_partition's adapt mode
     if (pp.adapt_P) {
         // about kAutoItemsPerSM items per SM over the batch's work (positions
         // x head groups x query tiles), each no shorter than the floor
-        long long tok = 0;
+        long long tok = 0, tok_rows = 0;
         for (int b = tid; b < n; b += kPlanThreads) {
             const int L = b == tid ? L0 : pp.seq_lens[b], ql = b == tid ? ql0 : pp.q_lens[b];
+            if (small) {
+                s_len[b] = L;
+                s_ql[b] = ql;
+            }
             if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len || ql > pp.max_q_len) continue;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
-            tok += (long long)L * (pp.n_kv / sh.hps) * ceil_div(ql, sh.qt);
+            const long long t = (long long)L * (pp.n_kv / sh.hps) * ceil_div(ql, sh.qt);
+            tok += t;
+            if (ql > 1 && !multi_query_kind(sh.kind)) tok_rows += t;
         }
-        // block sum in units of 16 tokens (fits an int for any accepted batch)
+        // block sums in units of 16 tokens (fit an int for any accepted batch)
         const int cap = (1 << 30) / kPlanThreads;
-        int v1[1] = {(int)min(tok >> 4, (long long)cap)}, t1[1];
-        block_scan_k<1>(v1, t1, tmp);
+        int v2[2] = {(int)min(tok >> 4, (long long)cap), (int)min(tok_rows >> 4, (long long)cap)}, t2[2];
+        block_scan_k<2>(v2, t2, tmp);
         const int per = kAutoItemsPerSM * pp.sms;
-        const int c16 = (t1[0] + per - 1) / per;  // in units of 16 tokens
+        const int c16 = (t2[0] + per - 1) / per;  // in units of 16 tokens
         C = max(P, min(kAutoPMax / kTileT, c16) * kTileT);
+        rule = 1;
+        if (small && 2LL * t2[1] > t2[0]) {
+            // Mostly multi-row decode-style items (speculative verification):
+            // each writes q_len times the partial results of a decode item, so
+            // the batch runs best as one wave -- the shortest item length whose
+            // items (ceiling counts, every item at most C long) fit on the
+            // SMs.  Warp j tries C_lo (16 + j) / 16, C_lo the length of
+            // perfectly even items; the smallest that fits wins.
+            const int warp = tid >> 5, lane = tid & 31;
+            const int c_lo = max(P / kTileT, (t2[0] + pp.sms - 1) / pp.sms);
+            const int cj = min(kAutoPMax / kTileT, (c_lo * (16 + warp) + 15) / 16) * kTileT;
+            int cnt = 0;
+            for (int b = lane; b < n; b += 32) {
+                const int L = s_len[b], ql = s_ql[b];
+                if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len || ql > pp.max_q_len) continue;
+                const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
+                const int pb = seq_partition(L, cj, P, sh.kind == KIND_TC ? kTcT : kTileT, 2);
+                cnt += seq_items(L, ql, sh, pb, pp.n_kv / sh.hps);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+            if (lane == 0) s_cnt[warp] = cnt;
+            __syncthreads();
+            int best = -1;
+            for (int j = 0; j < 32 && best < 0; ++j)
+                if (s_cnt[j] <= pp.sms) best = j;
+            if (best >= 0) {
+                C = min(kAutoPMax / kTileT, (c_lo * (16 + best) + 15) / 16) * kTileT;
+                rule = 2;
+            }
+        }
     }
     // item lengths are at most Pn: explicit P, or 1.5 C + one 128-token round-up
     const int Pn = pp.adapt_P ? 2 * C : P;
@@ -267,7 +316,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             bits |= flag;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
             const int ngroups = pp.n_kv / sh.hps;
-            const int pb = seq_partition(L, C, P, sh.kind == KIND_TC ? kTcT : kTileT, pp.adapt_P);
+            const int pb = seq_partition(L, C, P, sh.kind == KIND_TC ? kTcT : kTileT, rule);
             if (flag == 0 && ql > 0) {
                 if (sh.kind == KIND_TC) any_tc = 1;
                 if (multi_query_kind(sh.kind)) {

@@ -41,6 +41,17 @@ __device__ __forceinline__ void take(float& bv, int& bi, float v, int i) {
     }
 }
 
+// Per-thread loads in flight in the streaming path: kArgmaxUnroll float4 a
+// chunk, the next chunk issued before the current one is scanned.
+constexpr int kArgmaxUnroll = 4;
+
+// Argmax of each logits row.  A cluster of kArgmaxCluster CTAs owns a row at a
+// time, each CTA one contiguous slice of it; the CTA's best goes to rank 0 by
+// distributed shared memory.  Clusters are persistent: cluster y takes rows y,
+// y + gridDim.y, ..., and in the vectorised path each thread streams its
+// slices of all those rows as one sequence of chunks, the loads of the next
+// chunk in flight while the current one is scanned and while a finished row
+// is reduced, so the row boundaries cost no load latency.
 __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads)
     row_argmax_kernel(const float* __restrict__ logits, long long vocab, int rows, int vec4,
                       int32_t* __restrict__ argmax_out) {
@@ -55,39 +66,9 @@ __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmax
     per = (per + 3) & ~3LL;
     const long long lo = rank * per;
     const long long hi = lo + per < vocab ? lo + per : vocab;
-    for (int row = blockIdx.y; row < rows; row += gridDim.y) {
-        const float* x = logits + (long long)row * vocab;
-        float bv = -INFINITY;
-        int bi = kNoIndex;
-        if (vec4) {
-            // lo and vocab are multiples of 4 and the row start is 16-byte aligned
-            const float4* x4 = reinterpret_cast<const float4*>(x + lo);
-            const long long n4 = hi > lo ? (hi - lo) >> 2 : 0;
-            long long j = tid;
-            for (; j + 3 * kArgmaxThreads < n4; j += 4 * kArgmaxThreads) {
-                float4 v[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) v[u] = __ldg(x4 + j + u * kArgmaxThreads);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int base = (int)(lo + 4 * (j + u * kArgmaxThreads));
-                    take(bv, bi, v[u].x, base);
-                    take(bv, bi, v[u].y, base + 1);
-                    take(bv, bi, v[u].z, base + 2);
-                    take(bv, bi, v[u].w, base + 3);
-                }
-            }
-            for (; j < n4; j += kArgmaxThreads) {
-                const float4 v = __ldg(x4 + j);
-                const int base = (int)(lo + 4 * j);
-                take(bv, bi, v.x, base);
-                take(bv, bi, v.y, base + 1);
-                take(bv, bi, v.z, base + 2);
-                take(bv, bi, v.w, base + 3);
-            }
-        } else {
-            for (long long j = lo + tid; j < hi; j += kArgmaxThreads) take(bv, bi, __ldg(x + j), (int)j);
-        }
+    pdl_wait();  // the logits may be the previous kernel's output
+    // the row's best so far: CTA reduction, cluster exchange, rank 0 writes
+    auto finish_row = [&](int row, float bv, int bi) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(kFull, bv, o);
@@ -114,12 +95,72 @@ __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmax
             argmax_out[row] = i;
         }
         cluster.sync();  // cv/ci and wv/wi are reused by the next row
+    };
+    const int nrows = blockIdx.y < rows ? (rows - 1 - (int)blockIdx.y) / (int)gridDim.y + 1 : 0;
+    if (vec4) {
+        // lo and vocab are multiples of 4 and the row start is 16-byte aligned;
+        // chunk c of a row covers float4s [c * kArgmaxUnroll * T, ...) of the
+        // slice, float4 j of the chunk at tid + u * T
+        constexpr int T = kArgmaxThreads;
+        const long long n4 = hi > lo ? (hi - lo) >> 2 : 0;
+        const int cpr = (int)((n4 + kArgmaxUnroll * T - 1) / (kArgmaxUnroll * T));  // chunks per row
+        const int total = nrows * (cpr > 0 ? cpr : 1);
+        auto load_chunk = [&](int g, float4 (&v)[kArgmaxUnroll]) {
+            const int rr = g / (cpr > 0 ? cpr : 1), c = g - rr * (cpr > 0 ? cpr : 1);
+            const int row = (int)blockIdx.y + rr * (int)gridDim.y;
+            const float4* x4 = reinterpret_cast<const float4*>(logits + (long long)row * vocab + lo);
+#pragma unroll
+            for (int u = 0; u < kArgmaxUnroll; ++u) {
+                const long long j = (long long)c * kArgmaxUnroll * T + u * T + tid;
+                v[u] = j < n4 ? __ldg(x4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+        };
+        float4 nxt[kArgmaxUnroll];
+        if (total > 0) load_chunk(0, nxt);
+        float bv = -INFINITY;
+        int bi = kNoIndex;
+        for (int g = 0; g < total; ++g) {
+            float4 cur[kArgmaxUnroll];
+#pragma unroll
+            for (int u = 0; u < kArgmaxUnroll; ++u) cur[u] = nxt[u];
+            if (g + 1 < total) load_chunk(g + 1, nxt);
+            const int cp = cpr > 0 ? cpr : 1;
+            const int rr = g / cp, c = g - rr * cp;
+#pragma unroll
+            for (int u = 0; u < kArgmaxUnroll; ++u) {
+                const long long j = (long long)c * kArgmaxUnroll * T + u * T + tid;
+                if (j < n4) {
+                    const int base = (int)(lo + 4 * j);
+                    take(bv, bi, cur[u].x, base);
+                    take(bv, bi, cur[u].y, base + 1);
+                    take(bv, bi, cur[u].z, base + 2);
+                    take(bv, bi, cur[u].w, base + 3);
+                }
+            }
+            if (c == cp - 1) {
+                finish_row((int)blockIdx.y + rr * (int)gridDim.y, bv, bi);
+                bv = -INFINITY;
+                bi = kNoIndex;
+            }
+        }
+    } else {
+        for (int rr = 0; rr < nrows; ++rr) {
+            const int row = (int)blockIdx.y + rr * (int)gridDim.y;
+            const float* x = logits + (long long)row * vocab;
+            float bv = -INFINITY;
+            int bi = kNoIndex;
+            for (long long j = lo + tid; j < hi; j += kArgmaxThreads) take(bv, bi, __ldg(x + j), (int)j);
+            finish_row(row, bv, bi);
+        }
     }
+    pdl_launch();
 }
 
 __global__ void accept_kernel(const int32_t* __restrict__ argmax, const int32_t* __restrict__ draft, int num_seqs,
                               int k, int32_t* __restrict__ accepted, int32_t* __restrict__ next_token) {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    pdl_wait();  // the argmax kernel's rows are complete and visible
+    pdl_launch();
     if (b >= num_seqs) return;
     const int32_t* am = argmax + (long long)b * (k + 1);
     const int32_t* dr = draft + (long long)b * k;
@@ -411,10 +452,29 @@ extern "C" int pkv_spec_accept_greedy(const float* logits, const int32_t* draft,
     const long long rows = (long long)num_seqs * (k + 1);
     if (rows > 0x7fffffffLL) return PKV_ERR_SIZE;
     const int vec4 = (vocab % 4 == 0) && host::aligned16(logits);
-    dim3 grid(kArgmaxCluster, (unsigned)(rows < 65535 ? rows : 65535));
-    row_argmax_kernel<<<grid, kArgmaxThreads, 0, (cudaStream_t)stream>>>(logits, vocab, (int)rows, vec4, argmax_out);
-    if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
-    accept_kernel<<<(num_seqs + 127) / 128, 128, 0, (cudaStream_t)stream>>>(argmax_out, draft, num_seqs, k, accepted,
-                                                                           next_token);
-    return cudaGetLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    // persistent clusters: as many as are resident at once, at most one per row
+    static int fit_dev[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return PKV_ERR_CUDA;
+    if (fit_dev[dev] == 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(kArgmaxCluster, 1);
+        cfg.blockDim = dim3(kArgmaxThreads);
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, row_argmax_kernel, &cfg) != cudaSuccess || nc < 1) nc = 1;
+        fit_dev[dev] = nc;
+    }
+    const long long fit = fit_dev[dev];
+    long long ny = rows < fit ? rows : fit;
+    if (ny < 1) ny = 1;
+    if (ny > 65535) ny = 65535;
+    dim3 grid(kArgmaxCluster, (unsigned)ny);
+    if (host::launch_pdl(row_argmax_kernel, grid, dim3(kArgmaxThreads), 0, (cudaStream_t)stream, logits, vocab,
+                         (int)rows, vec4, argmax_out) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return host::launch_pdl(accept_kernel, dim3((num_seqs + 127) / 128), dim3(128), 0, (cudaStream_t)stream,
+                            (const int32_t*)argmax_out, draft, num_seqs, k, accepted, next_token) == cudaSuccess
+               ? PKV_OK
+               : PKV_ERR_CUDA;
 }
