@@ -16,6 +16,7 @@ int check_device();
 int sm_count();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned_to(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // cuTensorMapEncodeTiled (bf16 elements, or bytes when `bytes`) through
 // cudaGetDriverEntryPointByVersion, so the library needs no link-time

@@ -21,7 +21,7 @@ namespace cg = cooperative_groups;
 
 namespace pkv {
 
-constexpr int kArgmaxCluster = 8;
+constexpr int kArgmaxCluster = 2;
 constexpr int kArgmaxThreads = 256;
 constexpr int kNoIndex = 0x7fffffff;
 
@@ -41,34 +41,120 @@ __device__ __forceinline__ void take(float& bv, int& bi, float v, int i) {
     }
 }
 
-// Per-thread loads in flight in the streaming path: kArgmaxUnroll float4 a
-// chunk, the next chunk issued before the current one is scanned.
-constexpr int kArgmaxUnroll = 4;
+// max(a, b, c), NaN if any input is NaN (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// VW consecutive floats of one load: 256-bit (VW 8), 128-bit (4) or scalar.
+template <int VW>
+__device__ __forceinline__ void load_vec(const float* p, float* v) {
+    if constexpr (VW == 8) {
+        asm volatile("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                     : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+                     : "l"(p));
+    } else if constexpr (VW == 4) {
+        const float4 q = __ldg(reinterpret_cast<const float4*>(p));
+        v[0] = q.x;
+        v[1] = q.y;
+        v[2] = q.z;
+        v[3] = q.w;
+    } else {
+        v[0] = __ldg(p);
+    }
+}
 
 // Argmax of each logits row.  A cluster of kArgmaxCluster CTAs owns a row at a
-// time, each CTA one contiguous slice of it; the CTA's best goes to rank 0 by
-// distributed shared memory.  Clusters are persistent: cluster y takes rows y,
-// y + gridDim.y, ..., and in the vectorised path each thread streams its
-// slices of all those rows as one sequence of chunks, the loads of the next
-// chunk in flight while the current one is scanned and while a finished row
-// is reduced, so the row boundaries cost no load latency.
-__global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads)
-    row_argmax_kernel(const float* __restrict__ logits, long long vocab, int rows, int vec4,
-                      int32_t* __restrict__ argmax_out) {
+// time, each CTA one contiguous slice of it (a multiple of VW values); the
+// CTA's best goes to rank 0 by distributed shared memory.  Clusters are
+// persistent (cluster y takes rows y, y + gridDim.y, ...).  Each thread streams
+// its part of the slice in chunks of kArgmaxPer values (kArgmaxPer / VW
+// loads), two chunk buffers alternating so the next chunk's loads are in
+// flight while the current one is scanned.
+// At line rate an SM must scan ~5 values per cycle, about one instruction a
+// value at most, so the stream does no index work: a NaN-propagating 3-input
+// max tree per chunk and, when that maximum beats the thread's best (larger,
+// or NaN over a number), a note of the chunk.  At the end of the row the
+// thread reloads that one chunk (just streamed, normally still in L2) and
+// finds the first index of its best there.  A thread's chunks come in
+// increasing index order, so the first chunk holding its maximum holds its
+// first occurrence; threads, warps and CTAs merge with the full order (beats).
+constexpr int kArgmaxPer = 32;  // values per thread and chunk
+template <int VW>
+__global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmaxThreads, 3)
+    row_argmax_kernel(const float* __restrict__ logits, long long vocab, int rows, int32_t* __restrict__ argmax_out) {
+    constexpr int U = kArgmaxPer / VW;  // loads per chunk
+    constexpr int T = kArgmaxThreads;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
     __shared__ float wv[kArgmaxThreads / 32];
     __shared__ int wi[kArgmaxThreads / 32];
-    __shared__ float cv[kArgmaxCluster];
-    __shared__ int ci[kArgmaxCluster];
+    __shared__ float cv[2][kArgmaxCluster];  // by row parity: one cluster barrier per row
+    __shared__ int ci[2][kArgmaxCluster];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     long long per = (vocab + kArgmaxCluster - 1) / kArgmaxCluster;
-    per = (per + 3) & ~3LL;
+    per = (per + VW - 1) / VW * VW;
     const long long lo = rank * per;
     const long long hi = lo + per < vocab ? lo + per : vocab;
+    const long long nv = hi > lo ? (hi - lo) / VW : 0;                        // loads in this CTA's slice
+    const int cpr = (int)((nv + (long long)U * T - 1) / ((long long)U * T));  // chunks per row
+    const int nrows = blockIdx.y < rows ? (rows - 1 - (int)blockIdx.y) / (int)gridDim.y + 1 : 0;
     pdl_wait();  // the logits may be the previous kernel's output
-    // the row's best so far: CTA reduction, cluster exchange, rank 0 writes
-    auto finish_row = [&](int row, float bv, int bi) {
+    // load u of chunk c of a row: slice load c * U * T + u * T + tid (-inf past the slice)
+    auto load_chunk = [&](const float* x, int c, float (&v)[kArgmaxPer]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const long long j = (long long)c * U * T + (long long)u * T + tid;
+            if (j < nv) {
+                load_vec<VW>(x + j * VW, v + u * VW);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VW; ++e) v[u * VW + e] = -INFINITY;
+            }
+        }
+    };
+    auto chunk_max = [&](const float (&v)[kArgmaxPer]) {
+        float m = max3_nan(v[0], v[1], v[2]);
+#pragma unroll
+        for (int e = 3; e + 1 < kArgmaxPer; e += 2) m = max3_nan(m, v[e], v[e + 1]);
+        if constexpr ((kArgmaxPer - 3) % 2) m = max3_nan(m, v[kArgmaxPer - 1], v[kArgmaxPer - 1]);
+        return m;
+    };
+    float a[kArgmaxPer], b[kArgmaxPer];
+    for (int rr = 0; rr < nrows; ++rr) {
+        const int row = (int)blockIdx.y + rr * (int)gridDim.y;
+        const float* x = logits + (long long)row * vocab + lo;
+        float bv = -INFINITY;  // the thread's maximum so far (NaN beats all) ...
+        int bc = -1;           // ... and the first chunk holding it
+        auto note = [&](float m, int c) {
+            if (c * U * T + tid < nv && bv == bv && (m != m || m > bv || bc < 0)) {
+                bv = m;
+                bc = c;
+            }
+        };
+        if (cpr > 0) load_chunk(x, 0, a);
+        int c = 0;
+        for (; c + 1 < cpr; c += 2) {
+            load_chunk(x, c + 1, b);
+            note(chunk_max(a), c);
+            if (c + 2 < cpr) load_chunk(x, c + 2, a);
+            note(chunk_max(b), c + 1);
+        }
+        if (c < cpr) note(chunk_max(a), c);
+        // the first index of the thread's best, from its chunk reloaded
+        int bi = kNoIndex;
+        if (bc >= 0) {
+            load_chunk(x, bc, a);
+            const bool mnan = bv != bv;
+#pragma unroll
+            for (int e = kArgmaxPer - 1; e >= 0; --e) {
+                const long long j = (long long)bc * U * T + (long long)(e / VW) * T + tid;
+                if (j < nv && (mnan ? a[e] != a[e] : a[e] == bv)) bi = (int)(lo + j * VW + e % VW);
+            }
+        }
+        // CTA reduction, then one cluster barrier: rank 0 merges this row's slots
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float ov = __shfl_xor_sync(kFull, bv, o);
@@ -82,75 +168,18 @@ __global__ void __cluster_dims__(kArgmaxCluster, 1, 1) __launch_bounds__(kArgmax
         __syncthreads();
         if (tid == 0) {
             for (int w = 1; w < kArgmaxThreads / 32; ++w) take(bv, bi, wv[w], wi[w]);
-            float* rv = cluster.map_shared_rank(cv, 0);
-            int* ri = cluster.map_shared_rank(ci, 0);
-            rv[rank] = bv;
-            ri[rank] = bi;
+            cluster.map_shared_rank(&cv[rr & 1][0], 0)[rank] = bv;
+            cluster.map_shared_rank(&ci[rr & 1][0], 0)[rank] = bi;
         }
+        // every CTA's slot for this row is written; rank 0 merges it before it
+        // reaches the next row's barrier, so a slot of the same parity is
+        // rewritten only after it was read
         cluster.sync();
         if (rank == 0 && tid == 0) {
-            float v = cv[0];
-            int i = ci[0];
-            for (int r = 1; r < kArgmaxCluster; ++r) take(v, i, cv[r], ci[r]);
+            float v = cv[rr & 1][0];
+            int i = ci[rr & 1][0];
+            for (int r = 1; r < kArgmaxCluster; ++r) take(v, i, cv[rr & 1][r], ci[rr & 1][r]);
             argmax_out[row] = i;
-        }
-        cluster.sync();  // cv/ci and wv/wi are reused by the next row
-    };
-    const int nrows = blockIdx.y < rows ? (rows - 1 - (int)blockIdx.y) / (int)gridDim.y + 1 : 0;
-    if (vec4) {
-        // lo and vocab are multiples of 4 and the row start is 16-byte aligned;
-        // chunk c of a row covers float4s [c * kArgmaxUnroll * T, ...) of the
-        // slice, float4 j of the chunk at tid + u * T
-        constexpr int T = kArgmaxThreads;
-        const long long n4 = hi > lo ? (hi - lo) >> 2 : 0;
-        const int cpr = (int)((n4 + kArgmaxUnroll * T - 1) / (kArgmaxUnroll * T));  // chunks per row
-        const int total = nrows * (cpr > 0 ? cpr : 1);
-        auto load_chunk = [&](int g, float4 (&v)[kArgmaxUnroll]) {
-            const int rr = g / (cpr > 0 ? cpr : 1), c = g - rr * (cpr > 0 ? cpr : 1);
-            const int row = (int)blockIdx.y + rr * (int)gridDim.y;
-            const float4* x4 = reinterpret_cast<const float4*>(logits + (long long)row * vocab + lo);
-#pragma unroll
-            for (int u = 0; u < kArgmaxUnroll; ++u) {
-                const long long j = (long long)c * kArgmaxUnroll * T + u * T + tid;
-                v[u] = j < n4 ? __ldg(x4 + j) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            }
-        };
-        float4 nxt[kArgmaxUnroll];
-        if (total > 0) load_chunk(0, nxt);
-        float bv = -INFINITY;
-        int bi = kNoIndex;
-        for (int g = 0; g < total; ++g) {
-            float4 cur[kArgmaxUnroll];
-#pragma unroll
-            for (int u = 0; u < kArgmaxUnroll; ++u) cur[u] = nxt[u];
-            if (g + 1 < total) load_chunk(g + 1, nxt);
-            const int cp = cpr > 0 ? cpr : 1;
-            const int rr = g / cp, c = g - rr * cp;
-#pragma unroll
-            for (int u = 0; u < kArgmaxUnroll; ++u) {
-                const long long j = (long long)c * kArgmaxUnroll * T + u * T + tid;
-                if (j < n4) {
-                    const int base = (int)(lo + 4 * j);
-                    take(bv, bi, cur[u].x, base);
-                    take(bv, bi, cur[u].y, base + 1);
-                    take(bv, bi, cur[u].z, base + 2);
-                    take(bv, bi, cur[u].w, base + 3);
-                }
-            }
-            if (c == cp - 1) {
-                finish_row((int)blockIdx.y + rr * (int)gridDim.y, bv, bi);
-                bv = -INFINITY;
-                bi = kNoIndex;
-            }
-        }
-    } else {
-        for (int rr = 0; rr < nrows; ++rr) {
-            const int row = (int)blockIdx.y + rr * (int)gridDim.y;
-            const float* x = logits + (long long)row * vocab;
-            float bv = -INFINITY;
-            int bi = kNoIndex;
-            for (long long j = lo + tid; j < hi; j += kArgmaxThreads) take(bv, bi, __ldg(x + j), (int)j);
-            finish_row(row, bv, bi);
         }
     }
     pdl_launch();
@@ -451,28 +480,37 @@ extern "C" int pkv_spec_accept_greedy(const float* logits, const int32_t* draft,
     if (rc) return rc;
     const long long rows = (long long)num_seqs * (k + 1);
     if (rows > 0x7fffffffLL) return PKV_ERR_SIZE;
-    const int vec4 = (vocab % 4 == 0) && host::aligned16(logits);
-    // persistent clusters: as many as are resident at once, at most one per row
-    static int fit_dev[64] = {0};
+    // persistent clusters, as many as are resident at once (at most one per
+    // row); 256-bit loads where every slice start is 32-byte aligned, else
+    // 128-bit or scalar loads
+    const int vw = (vocab % 8 == 0 && host::aligned_to(logits, 32)) ? 8
+                   : (vocab % 4 == 0 && host::aligned16(logits)) ? 4 : 1;
+    const int vi = vw == 8 ? 2 : vw == 4 ? 1 : 0;
+    static int fit_dev[64][3] = {};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64) return PKV_ERR_CUDA;
-    if (fit_dev[dev] == 0) {
+    if (fit_dev[dev][vi] == 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(kArgmaxCluster, 1);
         cfg.blockDim = dim3(kArgmaxThreads);
         int nc = 0;
-        if (cudaOccupancyMaxActiveClusters(&nc, row_argmax_kernel, &cfg) != cudaSuccess || nc < 1) nc = 1;
-        fit_dev[dev] = nc;
+        const cudaError_t oe = vw == 8   ? cudaOccupancyMaxActiveClusters(&nc, row_argmax_kernel<8>, &cfg)
+                               : vw == 4 ? cudaOccupancyMaxActiveClusters(&nc, row_argmax_kernel<4>, &cfg)
+                                         : cudaOccupancyMaxActiveClusters(&nc, row_argmax_kernel<1>, &cfg);
+        if (oe != cudaSuccess || nc < 1) nc = 1;
+        fit_dev[dev][vi] = nc;
     }
-    const long long fit = fit_dev[dev];
-    long long ny = rows < fit ? rows : fit;
+    long long ny = rows < fit_dev[dev][vi] ? rows : fit_dev[dev][vi];
     if (ny < 1) ny = 1;
     if (ny > 65535) ny = 65535;
-    dim3 grid(kArgmaxCluster, (unsigned)ny);
-    if (host::launch_pdl(row_argmax_kernel, grid, dim3(kArgmaxThreads), 0, (cudaStream_t)stream, logits, vocab,
-                         (int)rows, vec4, argmax_out) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    const dim3 grid(kArgmaxCluster, (unsigned)ny), block(kArgmaxThreads);
+    const cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t le =
+        vw == 8   ? host::launch_pdl(row_argmax_kernel<8>, grid, block, 0, st, logits, vocab, (int)rows, argmax_out)
+        : vw == 4 ? host::launch_pdl(row_argmax_kernel<4>, grid, block, 0, st, logits, vocab, (int)rows, argmax_out)
+                  : host::launch_pdl(row_argmax_kernel<1>, grid, block, 0, st, logits, vocab, (int)rows, argmax_out);
+    if (le != cudaSuccess) return PKV_ERR_CUDA;
     return host::launch_pdl(accept_kernel, dim3((num_seqs + 127) / 128), dim3(128), 0, (cudaStream_t)stream,
                             (const int32_t*)argmax_out, draft, num_seqs, k, accepted, next_token) == cudaSuccess
                ? PKV_OK
