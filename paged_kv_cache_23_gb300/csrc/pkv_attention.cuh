@@ -48,8 +48,9 @@ constexpr int kTileT = 16;                  // tokens per pipeline stage
 constexpr int kCWarps = 8;                  // consumer warps
 constexpr int kCThreads = kCWarps * 32;
 // A CTA is three warpgroups: the eight consumer warps, then the producer, the
-// MMA warp and the helper TMA warp of the tcgen05 variant, and one idle warp
-// (the other variant leaves warps 9-11 idle).  With 12 warps every SM
+// MMA warp and the helper TMA warp of the tcgen05 variant (idle in the other
+// variant), and the V warp, which issues the V copies of 16-token stages
+// beside the producer's K copies.  With 12 warps every SM
 // sub-partition holds three, which caps the launch at 168 registers a thread;
 // the side warpgroup then gives most of its registers to the consumers
 // (setmaxnreg), so their items can hold up to 24 columns of Q^T and O^T.
@@ -334,7 +335,107 @@ __device__ __forceinline__ bool produce_tc(Smem<D, F8>& sm, const TMaps* tm, con
 }
 
 // ---------------------------------------------------------------------------
-// Producer warp: item queue, block-table reads, TMA stage stream.
+// The 16-token stages of one item (not a tcgen05 tile): block-table entries,
+// slot waits and TMA copies, one box per tensor and block holding every head
+// of the group.  Two warps share each stage, each issuing the copies of one
+// tensor: a warp sustains only a couple of copies per microsecond, and a
+// stage of an FP8 pool is two 16 KB copies.
+//   vwarp false (the producer): claims the next item a few stages ahead,
+//     reports bad blocks, stores FP8 per-block scales, arms the stage's
+//     barrier with both tensors' bytes and copies K;
+//   vwarp true (the V warp): copies V once the slot is free (its copies may
+//     land before the producer's arrival; the phase cannot complete without it).
+// Lane e < ne handles the stage's block e (ne blocks per stage when
+// block_size < 16); for per-block FP8 scales lanes 16 + e load V's.
+// Returns false when the pipeline was aborted (a wait gave up).
+// ---------------------------------------------------------------------------
+template <int D, bool F8>
+__device__ __forceinline__ bool stream_item(Smem<D, F8>& sm, const TMaps* tm, const AttnParams& p, const Desc& d,
+                                            int si, int lane, uint32_t& g, int& next, bool vwarp) {
+    constexpr int RS = Geo<D, F8>::kSlots;
+    volatile int* abort = &sm.abort;
+    const int bsr = p.bs < kTileT ? p.bs : kTileT;
+    const CUtensorMap* map = vwarp ? &tm->v[log2i(d.hps)] : &tm->k[log2i(d.hps)];
+    const uint32_t op_bytes = (uint32_t)d.hps * bsr * Geo<D, F8>::kRow;
+    const int tb = d.t_begin / kTileT, te = (d.t_end + kTileT - 1) / kTileT;
+    const int32_t* bt = p.block_tables + (long long)d.b * p.max_blocks;
+    const int e_lim = (d.t_end + p.bs - 1) / p.bs;
+    int tab_base = tb * kTileT / p.bs;
+    int tab = tab_base + lane < e_lim ? __ldg(bt + tab_base + lane) : 0;
+    int tab_next = tab_base + 32 + lane < e_lim ? __ldg(bt + tab_base + 32 + lane) : 0;
+    // the next item is claimed a few stages before this one's last, so a
+    // CTA never holds a second item for long and the queue balances finely
+    const int i_claim = max(tb, te - kClaimAhead);
+    const int be = lane & 15;  // this lane's block of the stage
+    for (int i = tb; i < te; ++i, ++g) {
+        if (!vwarp && i == i_claim && lane == 0) next = atomicAdd(&p.hdr[HDR_HEAD], 1);
+        const int t0 = i * kTileT;
+        const int tvalid = min(kTileT, d.t_end - t0);
+        const int e0 = t0 / p.bs;
+        const int ne = p.bs >= kTileT ? 1 : (tvalid + p.bs - 1) / p.bs;
+        if (e0 >= tab_base + 32) {
+            // entries advance by at most 16 per stage: shift in the prefetched batch
+            tab = tab_next;
+            tab_base += 32;
+            const int en = tab_base + 32 + lane;
+            tab_next = en < e_lim ? __ldg(bt + en) : 0;
+        }
+        const int off = e0 - tab_base + be;  // in [0, 48)
+        const int lo = __shfl_sync(kFull, tab, off & 31);
+        const int hi = __shfl_sync(kFull, tab_next, off & 31);
+        int my = off < 32 ? lo : hi;
+        const bool in = be < ne;
+        const bool okb = !in || (my >= 0 && my < p.num_blocks);
+        if (!okb) my = 0;
+        const int s = (int)(g % RS);
+        // FP8 pools with per-block scales (producer): lane 16 v + e loads the K
+        // (v = 0) or V (v = 1) scales of block e for the group's kv heads now,
+        // and stores them into the slot's scale rows once the slot is free --
+        // before the barrier is armed, so the consumers' wait on it orders them
+        float scv[kMaxHPS];
+        const bool pbs = F8 && !vwarp && p.scale_pb != 0;
+        if (pbs && in) {
+            const float* src = ((lane >> 4) ? p.v_scale : p.k_scale) + (long long)my * p.n_kv + d.hg * d.hps;
+#pragma unroll
+            for (int h = 0; h < kMaxHPS; ++h) scv[h] = h < d.hps ? __ldg(src + h) : 0.f;
+        }
+        bool got = true;
+        const unsigned badmask = __ballot_sync(kFull, !okb);
+        if (lane == 0) {
+            if (!vwarp && badmask) {
+                sm.poison[si] = 1;
+                report(p.status, PKV_STATUS_BAD_BLOCK);
+            }
+            got = mbar_wait(&sm.empty[s], ((g / RS) & 1) ^ 1, abort);
+        }
+        if (!__shfl_sync(kFull, got, 0)) return false;  // never arm a barrier whose previous phase is open
+        if (pbs) {
+            if (in) {
+#pragma unroll
+                for (int h = 0; h < kMaxHPS; ++h)
+                    if (h < d.hps) sm.scl[s][lane >> 4][be][h] = scv[h];
+            }
+            __syncwarp();
+        }
+        if (!vwarp && lane == 0) mbar_arrive_expect_tx(&sm.full[s], 2u * ne * op_bytes);
+        if (in && lane < 16) {
+            const int row0 = p.bs > kTileT ? (t0 % p.bs) : 0;
+            // map dimensions {column of a 128-byte box, row, box, kv head,
+            // block}; rows of a single box: {column, box, row, ...}
+            uint8_t* dst = &sm.kv[s][vwarp ? 1 : 0][be * op_bytes];
+            if constexpr (Geo<D, F8>::kNB > 1)
+                tma_load_5d(dst, map, 0, row0, 0, d.hg * d.hps, my, &sm.full[s]);
+            else
+                tma_load_5d(dst, map, 0, 0, row0, d.hg * d.hps, my, &sm.full[s]);
+        }
+        __syncwarp();
+    }
+    return true;
+}
+
+// ---------------------------------------------------------------------------
+// Producer warp: item queue and descriptors; the K copies of 16-token stages,
+// both tensors of tcgen05 tile stages (with the helper warp).
 // ---------------------------------------------------------------------------
 template <int D, bool F8>
 __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const AttnParams& p, int lane) {
@@ -347,7 +448,6 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
     // a workspace whose plan was made for another shape runs nothing (the
     // combine kernel then writes every output row NaN and reports it)
     const int num_items = p.hdr[HDR_KEY] == p.plan_key ? p.hdr[HDR_ITEMS] : 0;
-    const int bsr = p.bs < kTileT ? p.bs : kTileT;
     int next = 0;
     if (lane == 0) next = atomicAdd(&p.hdr[HDR_HEAD], 1);
     next = __shfl_sync(kFull, next, 0);
@@ -376,100 +476,53 @@ __device__ __forceinline__ void producer(Smem<D, F8>& sm, const TMaps* tm, const
         if (end) break;
         if (d.kind == KIND_TC) {
             if (!produce_tc<D, F8>(sm, tm, p, d, si, lane, g, next, false)) break;
-            next = __shfl_sync(kFull, next, 0);
-            continue;
+        } else {
+            if (!stream_item<D, F8>(sm, tm, p, d, si, lane, g, next, false)) break;
         }
-        const CUtensorMap* mk = &tm->k[log2i(d.hps)];
-        const CUtensorMap* mv = &tm->v[log2i(d.hps)];
-        const uint32_t op_bytes = (uint32_t)d.hps * bsr * Geo<D, F8>::kRow;
-        const int tb = d.t_begin / kTileT, te = (d.t_end + kTileT - 1) / kTileT;
-        const int32_t* bt = p.block_tables + (long long)d.b * p.max_blocks;
-        bool stopped = false;
-        const int e_lim = (d.t_end + p.bs - 1) / p.bs;
-        int tab_base = tb * kTileT / p.bs;
-        int tab = tab_base + lane < e_lim ? __ldg(bt + tab_base + lane) : 0;
-        int tab_next = tab_base + 32 + lane < e_lim ? __ldg(bt + tab_base + 32 + lane) : 0;
-        // the next item is claimed a few stages before this one's last, so a
-        // CTA never holds a second item for long and the queue balances finely
-        const int i_claim = max(tb, te - kClaimAhead);
-        for (int i = tb; i < te; ++i, ++g) {
-            if (i == i_claim && lane == 0) next = atomicAdd(&p.hdr[HDR_HEAD], 1);
-            const int t0 = i * kTileT;
-            const int tvalid = min(kTileT, d.t_end - t0);
-            const int e0 = t0 / p.bs;
-            const int ne = p.bs >= kTileT ? 1 : (tvalid + p.bs - 1) / p.bs;
-            if (e0 >= tab_base + 32) {
-                // entries advance by at most 16 per stage: shift in the prefetched batch
-                tab = tab_next;
-                tab_base += 32;
-                const int en = tab_base + 32 + lane;
-                tab_next = en < e_lim ? __ldg(bt + en) : 0;
-            }
-            // lanes 2e and 2e+1 issue the K and the V copy of the stage's block e
-            const int off = e0 - tab_base + (lane >> 1);  // in [0, 48)
-            const int lo = __shfl_sync(kFull, tab, off & 31);
-            const int hi = __shfl_sync(kFull, tab_next, off & 31);
-            int my = off < 32 ? lo : hi;
-            const bool in = (lane >> 1) < ne;
-            const bool okb = !in || (my >= 0 && my < p.num_blocks);
-            if (!okb) my = 0;
-            const unsigned badmask = __ballot_sync(kFull, !okb);
-            const int s = (int)(g % RS);
-            // FP8 pools with per-block scales: lane 2e + v loads the K (v = 0)
-            // or V (v = 1) scales of the stage's block e for the group's kv
-            // heads now, and stores them into the slot's scale rows once the
-            // slot is free -- before the barrier is armed, so the consumers'
-            // wait on it orders them
-            float scv[kMaxHPS];
-            const bool pbs = F8 && p.scale_pb != 0;
-            if (pbs && in) {
-                const float* src = ((lane & 1) ? p.v_scale : p.k_scale) + (long long)my * p.n_kv + d.hg * d.hps;
-#pragma unroll
-                for (int h = 0; h < kMaxHPS; ++h) scv[h] = h < d.hps ? __ldg(src + h) : 0.f;
-            }
-            bool got = true;
-            if (lane == 0) {
-                if (badmask) {
-                    sm.poison[si] = 1;
-                    report(p.status, PKV_STATUS_BAD_BLOCK);
-                }
-                got = mbar_wait(&sm.empty[s], ((g / RS) & 1) ^ 1, abort);
-            }
-            if (!__shfl_sync(kFull, got, 0)) {
-                stopped = true;  // never arm a barrier whose previous phase is still open
-                break;
-            }
-            if (pbs) {
-                if (in) {
-#pragma unroll
-                    for (int h = 0; h < kMaxHPS; ++h)
-                        if (h < d.hps) sm.scl[s][lane & 1][lane >> 1][h] = scv[h];
-                }
-                __syncwarp();
-            }
-            if (lane == 0) mbar_arrive_expect_tx(&sm.full[s], 2u * ne * op_bytes);
-            // one box per tensor and block: every head of the group, 16 (or block_size) rows
-            if (in) {
-                const int row0 = p.bs > kTileT ? (t0 % p.bs) : 0;
-                const int v = lane & 1;
-                // map dimensions {column of a 128-byte box, row, box, kv head,
-                // block}; rows of a single box: {column, box, row, ...}
-                if constexpr (Geo<D, F8>::kNB > 1)
-                    tma_load_5d(&sm.kv[s][v][(lane >> 1) * op_bytes], v ? mv : mk, 0, row0, 0, d.hg * d.hps, my,
-                                &sm.full[s]);
-                else
-                    tma_load_5d(&sm.kv[s][v][(lane >> 1) * op_bytes], v ? mv : mk, 0, 0, row0, d.hg * d.hps, my,
-                                &sm.full[s]);
-            }
-            __syncwarp();
-        }
-        if (stopped) break;
         next = __shfl_sync(kFull, next, 0);
     }
     // drain: wait until every issued stage has landed, bounded by time only --
     // an abort must not cut it short, or the CTA could exit with copies still
     // landing in its shared memory
     if (lane == 0) drain_ring<RS>(sm.full, g);
+}
+
+// The V warp's item loop: it follows the item sequence (and the ring's stage
+// count) and copies V of every 16-token stage (tcgen05 tiles are the
+// producer's and the helper warp's).
+template <int D, bool F8>
+__device__ __forceinline__ void v_warp(Smem<D, F8>& sm, const TMaps* tm, const AttnParams& p, int lane) {
+    volatile int* abort = &sm.abort;
+    uint32_t g = 0;
+    int unused = 0;
+    bool aborted = false;
+    for (int islot = 0;; ++islot) {
+        const int si = islot % kSlots;
+        if (!mbar_wait(&sm.ifull[si], (islot / kSlots) & 1, abort)) {
+            aborted = true;
+            break;
+        }
+        const Desc d = sm.desc[si];
+        if (d.kind == KIND_END) break;
+        const int T = d.kind == KIND_TC ? kTcT : kTileT;
+        const int ntiles = (d.t_end + T - 1) / T - d.t_begin / T;
+        if (d.kind != KIND_TC) {
+            uint32_t gg = g;
+            if (!stream_item<D, F8>(sm, tm, p, d, si, lane, gg, unused, true)) {
+                g = gg;  // stages up to the last one this warp waited for
+                aborted = true;
+                break;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.iempty[si]);
+        g += (uint32_t)(d.kind == KIND_TC ? ntiles + 1 : ntiles);
+    }
+    // This warp's copies land on the producer's barriers: after the last item
+    // g is the producer's own stage count, and the drain waits for the latest
+    // phase of every slot; after an abort, for the stages it copied into,
+    // bounded by time only.
+    if (lane == 0 && (aborted || g > 0)) drain_ring<Geo<D, F8>::kSlots>(sm.full, g);
 }
 
 // ---------------------------------------------------------------------------
@@ -2085,7 +2138,7 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
         }
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(&sm.ifull[i], 1);
-            mbar_init(&sm.iempty[i], kCWarps + (TC ? 2 : 0));  // + the MMA and helper warps
+            mbar_init(&sm.iempty[i], kCWarps + 1 + (TC ? 2 : 0));  // + the V warp, the MMA and helper warps
         }
         if constexpr (TC) {
             mbar_init(&sm.sbar[0], 1);
@@ -2113,6 +2166,8 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
         setmaxnreg_dec<kSideRegs>();
         if (warp == kCWarps) {
             producer<D, F8>(sm, &tm, p, lane);
+        } else if (warp == kCWarps + 3) {
+            v_warp<D, F8>(sm, &tm, p, lane);
         } else if constexpr (TC) {
             if (warp == kCWarps + 2) {
                 helper_warp<D, F8>(sm, &tm, p, lane);
@@ -2122,9 +2177,8 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
                 mma_warp<D, F8>(sm, p, lane, tc);
                 if (use_tc) tc_end<D, F8>(sm, warp, lane, true, tc);
             }
-            // warp kCWarps + 3: no role
         }
-        // warps kCWarps + 1 .. + 3 of the variant without tiles: no role
+        // warps kCWarps + 1 and + 2 of the variant without tiles: no role
     } else {
         setmaxnreg_inc<kConsumerRegs>();
         TcState tc{0u, 0u, 0u, 0u};

@@ -171,6 +171,13 @@ __device__ __forceinline__ int seq_partition(int L, int C, int P, int align, int
     return max(pb, P);
 }
 
+// Granularity of automatic partition lengths: whole stages -- 128 tokens for
+// tcgen05 tiles, 32 (two 16-token stages) for FP8 pools, whose items consume
+// stages in pairs, else 16.
+__device__ __forceinline__ int part_align(int kind, int fp8) {
+    return kind == KIND_TC ? kTcT : fp8 ? 2 * kTileT : kTileT;
+}
+
 // Items of one sequence for partition length pb: np partitions of each of its
 // query tiles, times its head groups.
 __device__ __forceinline__ int seq_items(int L, int ql, const SeqShape& sh, int pb, int ngroups) {
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
                 const int L = s_len[b], ql = s_ql[b];
                 if (L <= 0 || ql <= 0 || ql > L || L > pp.max_seq_len || ql > pp.max_q_len) continue;
                 const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
-                const int pb = seq_partition(L, cj, P, sh.kind == KIND_TC ? kTcT : kTileT, 2);
+                const int pb = seq_partition(L, cj, P, part_align(sh.kind, pp.fp8), 2);
                 cnt += seq_items(L, ql, sh, pb, pp.n_kv / sh.hps);
             }
 #pragma unroll
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const __grid_constan
             bits |= flag;
             const SeqShape sh = seq_shape(ql, pp.G, pp.n_kv, pp.decode_ok, pp.fp8, pp.tc);
             const int ngroups = pp.n_kv / sh.hps;
-            const int pb = seq_partition(L, C, P, sh.kind == KIND_TC ? kTcT : kTileT, rule);
+            const int pb = seq_partition(L, C, P, part_align(sh.kind, pp.fp8), rule);
             if (flag == 0 && ql > 0) {
                 if (sh.kind == KIND_TC) any_tc = 1;
                 if (multi_query_kind(sh.kind)) {
