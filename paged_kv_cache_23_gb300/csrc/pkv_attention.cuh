@@ -17,21 +17,26 @@
 //     group): multi-query items first, then every full decode partition, then
 //     the partition tails longest first, so the dynamic queue ends on short
 //     items.  It also records how many partitions each query row has.
-//   * The attention kernel is persistent, one CTA per SM: one producer warp and
-//     eight consumer warps.  A pipeline stage is 16 tokens of K and V for a
-//     group of kv heads of one block -- for the 8B shape all 8 heads, 32 KB of
-//     K plus 32 KB of V -- fetched with one 5-D TMA box per tensor (128-byte
-//     swizzle) into a 3-slot, 192 KB shared-memory ring.  A TMA-issuing thread
-//     sustains only a couple of copies per microsecond whatever their size, so
-//     copies have to be tens of KB for one producer warp to keep HBM busy.
-//   * Single-query rows (decode, q_len = 1) run on tensor cores (mma.sync
+//   * The attention kernel is persistent, one CTA per SM, three warpgroups:
+//     eight consumer warps (224 registers each) and a side warpgroup (56
+//     each, by setmaxnreg) holding the producer warp, the V warp and, in the
+//     variant with tcgen05 tiles, the MMA and helper TMA warps.  A pipeline
+//     stage is 16 tokens of K and V for a group of kv heads of one block --
+//     for the 8B shape all 8 heads, 32 KB of K plus 32 KB of V -- fetched
+//     with one 5-D TMA box per tensor (128-byte swizzle) into a 3-slot,
+//     192 KB shared-memory ring, the producer copying K and the V warp V.  A
+//     TMA-issuing warp sustains only a couple of copies per microsecond
+//     whatever their size, so copies have to be tens of KB to keep HBM busy.
+//   * Decode rows and short verifications run on tensor cores (mma.sync
 //     m16n8k16 bf16 -> fp32), one warp per kv head, in the transposed form
-//     S^T = K Q^T: the 16 tokens of a stage on M, the g query heads of the GQA
-//     group on N, so g = 4 pads N = 8 rather than M = 16.  A CUDA-core variant
-//     (8 lanes per token, packed fp32x2 FMAs) is kept behind a flag.
-//   * Multi-query rows (speculative k > 1, prefill chunks) also run on tensor
-//     cores, rows = (query, head) pairs, 16 per warp; the warps of one kv head
-//     split its rows; each row's causal limit is applied to the scores.
+//     S^T = K Q^T: the 16 tokens of a stage on M, the (query, q head) columns
+//     of the kv head on N -- up to 24 (three n-tiles), so k = 5 drafts at
+//     g = 4 stream exactly like decode; each column's causal limit is applied
+//     to its scores.  A CUDA-core variant for q_len = 1 (8 lanes per token,
+//     packed fp32x2 FMAs) is kept behind a flag.
+//   * Wider multi-query rows (prefill chunks) run as tcgen05 tiles of 128
+//     rows, or, with those off, on mma.sync row tiles (16 (query, head) rows
+//     per warp, the warps of one kv head splitting its rows).
 //   * Consumer warps run independently: each waits for its own stages and
 //     releases them as it finishes, with no CTA-wide barrier per item.
 //   * A partition's partial (O, m, l) goes to the workspace; a separate combine
