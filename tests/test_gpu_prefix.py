@@ -125,7 +125,7 @@ def test_scenario_against_oracle():
     torch.cuda.synchronize()
     assert np.array_equal(cached.cpu().numpy(), n_ref)
     assert np.array_equal(bt_gpu.cpu().numpy(), bt_ref)
-    # round 3: the second half finishes; ref counts drop
+    # phase 3: the second half finishes; ref counts drop
     rel = np.where(np.arange(B) >= half, n_ref, 0).astype(np.int32)
     pkv.prefix_release(table, h_dev, t32(rel), status=st)
     cache.release(hashes, rel)
