@@ -76,11 +76,12 @@ constexpr int kPlanThreads = 1024;
 constexpr int kTailBuckets = 256;           // tail-length classes of the longest-first ordering
 
 // tcgen05 chunk tiles: 128 rows = (query, q head) pairs of one kv head, stages
-// of 128 tokens, tensor-memory columns [S0 | S1 | O_0 | O_1] (P over S).
+// of 128 tokens, tensor-memory columns [S | P0 P1 | O_0 | O_1]: one fp32 S
+// buffer, two bf16 P buffers (two values a column) by stage parity.
 constexpr int kTcT = 128;                   // tokens per stage
 constexpr int kTcRows = 128;                // tile rows (the MMA's M)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0, kTmemO = 256;
+constexpr uint32_t kTmemS = 0, kTmemP = 128, kTmemO = 256;
 
 // KIND_DEC: q_len = 1 rows on tensor cores; KIND_DECF: on CUDA cores; KIND_MQ:
 // q_len > 1 on mma.sync; KIND_TC: query tiles of 128 rows on tcgen05.
@@ -164,7 +165,7 @@ struct Smem {
     // P ready is double-buffered by stage parity: the softmax warps may finish
     // stages k and k + 1 before the MMA warp waits for stage k's phase (it
     // issues S_{k+1} first), and one barrier would then have moved on twice
-    uint64_t sbar[2], obar[2], pready[2][2], xbar, ebar, qbar, tdone, dbar;
+    uint64_t sbar, sfree, obar[2], pready[2][2], xbar, ebar, qbar, tdone, dbar;
     uint32_t tmem;
     float red[kTC ? 2 : 1][2][kTcRows];                       // [m, l][half][row]
 };
@@ -1253,14 +1254,19 @@ __device__ __forceinline__ void tc_item(Smem<D, false>& sm, const AttnParams& p,
     for (int i = 0; i < ntiles; ++i) {
         const uint32_t k = st.k + i;
         const int b = (int)(k & 1);
-        const uint32_t scol = kTmemS + (uint32_t)b * kTcT + (uint32_t)hh * 64;
-        mbar_wait(&sm.sbar[b], (k >> 1) & 1, abort);
+        const uint32_t scol = kTmemS + (uint32_t)hh * 64;
+        const uint32_t pcol = kTmemP + (uint32_t)b * (kTcT / 2) + (uint32_t)hh * 32;
+        mbar_wait(&sm.sbar, k & 1, abort);
         __syncwarp();  // tcgen05.ld/st are warp-collective: reconverge after the polling wait
         tc_fence_after();
         uint32_t sv[64];
         tmem_ld32(tl + scol, sv);
         tmem_ld32(tl + scol + 32, sv + 32);
         tmem_wait_ld();
+        // S_k is in registers: the MMA warp may overwrite the S buffer with S_{k+1}
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.sfree);
         // column j of this half holds stage token 64 hh + j, visible iff 64 hh + j <= lr
         const int lr = last - (tb + i) * kTcT;
         const bool full = lr >= 64 * hh + 63;
@@ -1330,9 +1336,15 @@ __device__ __forceinline__ void tc_item(Smem<D, false>& sm, const AttnParams& p,
             }
         }
         l += ls;
-        // P over the first 32 of this half's S columns (this thread has read them;
-        // the MMA warp refills the buffer only after PV_k)
-        tmem_st32(tl + scol, sv);
+        // P_k into P buffer k & 1, once PV_{k-2} has read that buffer (within a
+        // tile; an earlier tile's last PVs completed before its end)
+        if (i >= 2) {
+            const uint32_t k2 = k - 2;
+            mbar_wait(&sm.obar[k2 & 1], (k2 >> 1) & 1, abort);
+            __syncwarp();
+            tc_fence_after();
+        }
+        tmem_st32(tl + pcol, sv);
         tmem_wait_st();
         if (i == ntiles - 1) {
             // the last V stage has landed (its slot is released only by PV_k):
@@ -1432,26 +1444,32 @@ __device__ __forceinline__ void tc_mma(Smem<D, false>& sm, const Desc& d, int la
     constexpr uint32_t kIdPV = umma_idesc_bf16(kTcRows, D, true);
     constexpr int kSlab = kTcT * 128;
     if (lane == 0) {
-        const uint32_t qa = smem_u32(sm.qbuf);
-        // S_i = Q K_i^T into S buffer (k + i) & 1
+        // One thread issues every MMA, so the per-MMA work is kept to a few
+        // adds: each operand's shared-memory descriptor is built once (per
+        // tile for Q, per slot for K and V) and the k-step offsets are added
+        // to its address field (address >> 4, 14 bits; every offset stays
+        // inside its buffer, so no carry leaves the field).
+        const uint64_t qdesc = umma_desc_sw128(smem_u32(sm.qbuf), 0);
+        // S_i = Q K_i^T into the S buffer
         auto issue_s = [&](int i) -> bool {
             const uint32_t gi = gbase + i;
             const int s = (int)(gi % kRingSlots);
             if (!mbar_wait(&sm.full[s], (gi / kRingSlots) & 1, abort)) return false;
             tc_fence_after();
-            const uint32_t kb = smem_u32(&sm.kv[s][0][0]);
-            const uint32_t dst = st.tmem + kTmemS + ((st.k + i) & 1) * kTcT;
+            const uint64_t kdesc = umma_desc_sw128(smem_u32(&sm.kv[s][0][0]), 0);
+            const uint32_t dst = st.tmem + kTmemS;
 #pragma unroll
             for (int xs = 0; xs < 2; ++xs)
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    umma_ss(dst, umma_desc_sw128(qa + xs * kSlab + kk * 32, 0),
-                            umma_desc_sw128(kb + xs * kSlab + kk * 32, 0), kIdS, (xs | kk) != 0);
-            umma_commit(&sm.sbar[(st.k + i) & 1]);
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t off = (uint64_t)((xs * kSlab + kk * 32) >> 4);
+                    umma_ss(dst, qdesc + off, kdesc + off, kIdS, (xs | kk) != 0);
+                }
+            umma_commit(&sm.sbar);
             return true;
         };
-        // Q written; the previous tile's last PV (which read the S buffer S_0
-        // reuses) completed before the softmax warps wrote this Q
+        // Q written; the softmax warps wrote it after their previous tile had
+        // ended, so they no longer need the S buffer S_0 overwrites
         bool ok = mbar_wait(&sm.qbar, st.tiles & 1, abort) && issue_s(0);
         if (ok) {
             // slot gbase holds K_0 alone: free once S_0 has read it
@@ -1463,8 +1481,10 @@ __device__ __forceinline__ void tc_mma(Smem<D, false>& sm, const Desc& d, int la
             const uint32_t k = st.k + i;
             const int b = (int)(k & 1);
             if (i + 1 < ntiles) {
-                // S_{k+1} reuses the buffer whose P_{k-1} PV_{k-1} reads
-                if (i >= 1) ok = mbar_wait(&sm.obar[(k - 1) & 1], ((k - 1) >> 1) & 1, abort);
+                // S_{k+1} overwrites S_k once every softmax warp holds S_k in
+                // registers -- early in the softmax of stage k, so the tensor pipe
+                // runs S_{k+1} beside it and PV_{k-1} (P lives in its own buffers)
+                ok = mbar_wait(&sm.sfree, k & 1, abort);
                 ok = ok && issue_s(i + 1);
             }
             const uint32_t gv = gbase + i + 1;
@@ -1472,6 +1492,7 @@ __device__ __forceinline__ void tc_mma(Smem<D, false>& sm, const Desc& d, int la
             ok = ok && mbar_wait(&sm.full[sv], (gv / kRingSlots) & 1, abort);
             if (!ok) break;
             const uint32_t vb = smem_u32(&sm.kv[sv][1][0]);
+            const uint64_t vdesc = pair ? umma_desc_sw128(vb, 2048) : umma_desc_sw128(vb, kSlab);
             // PV_k, each half once its four warps have written P
             for (int h = 0; h < 2; ++h) {
                 ok = mbar_wait(&sm.pready[h][k & 1], (k >> 1) & 1, abort);
@@ -1481,10 +1502,10 @@ __device__ __forceinline__ void tc_mma(Smem<D, false>& sm, const Desc& d, int la
                 // 4 h + kk of a paired V stage ([slab][16 rows] at 4 KB steps)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
-                    const uint64_t bd = pair ? umma_desc_sw128(vb + (4 * h + kk) * 4096, 2048)
-                                             : umma_desc_sw128(vb + (64 * h + 16 * kk) * 128, kSlab);
-                    umma_ts(st.tmem + kTmemO + h * D, st.tmem + kTmemS + b * kTcT + 64 * h + 8 * kk, bd, kIdPV,
-                            i > 0 || kk > 0);
+                    const uint64_t bd =
+                        vdesc + (uint64_t)((pair ? (4 * h + kk) * 4096 : (64 * h + 16 * kk) * 128) >> 4);
+                    umma_ts(st.tmem + kTmemO + h * D, st.tmem + kTmemP + b * (kTcT / 2) + 32 * h + 8 * kk, bd,
+                            kIdPV, i > 0 || kk > 0);
                 }
             }
             if (!ok) break;
@@ -2146,8 +2167,8 @@ __global__ void __launch_bounds__(kThreadsOf<TC>, 1)
             mbar_init(&sm.iempty[i], kCWarps + 1 + (TC ? 2 : 0));  // + the V warp, the MMA and helper warps
         }
         if constexpr (TC) {
-            mbar_init(&sm.sbar[0], 1);
-            mbar_init(&sm.sbar[1], 1);
+            mbar_init(&sm.sbar, 1);
+            mbar_init(&sm.sfree, kCWarps);
             mbar_init(&sm.obar[0], 1);
             mbar_init(&sm.obar[1], 1);
             for (int h = 0; h < 2; ++h)
