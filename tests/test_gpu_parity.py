@@ -257,6 +257,40 @@ def test_spec_accept_random_vocab_sizes(V):
     assert np.array_equal(out[2].cpu().numpy(), nxt)
 
 
+@pytest.mark.parametrize("V,shift", [(1004, 0), (128256, 0), (128256, 4), (9000, 2)])
+def test_argmax_load_widths_and_ties(V, shift):
+    # rows of a multiple of 8 values on a 32-byte boundary take 256-bit loads,
+    # a multiple of 4 on a 16-byte boundary 128-bit loads, the rest scalar loads
+    # (shift: the logits start `shift` floats into their buffer); ties between a
+    # thread's chunks (the first chunk holding the maximum is re-read), between
+    # the CTAs of a row, equal zeros of both signs, two NaNs
+    rng = np.random.default_rng(V + shift)
+    B, k = 6, 3
+    lg = rng.standard_normal((B, k + 1, V)).astype(np.float32)
+    second = 17 + 8192 if V > 17 + 8192 else V - 20
+    lg[0, 0, 17] = lg[0, 0, second] = 50.0        # one thread, chunks 0 and 1 (8-wide loads)
+    lg[0, 1, 5] = lg[0, 1, V - 5] = 60.0          # the row's two CTAs
+    lg[1, 0, :] = -1.0
+    lg[1, 0, 100] = -0.0
+    lg[1, 0, 50] = 0.0                            # +0 at 50 before -0 at 100: 50 wins
+    lg[2, 2, V // 3] = np.nan
+    lg[2, 2, V // 2] = np.nan                     # the first NaN wins
+    lg[3, 1, :] = -np.inf                         # all -inf: index 0
+    top = lg.argmax(-1)
+    dr = np.where(rng.random((B, k)) < 0.7, top[:, :k], (top[:, :k] + 1) % V).astype(np.int32)
+    acc, nxt, am = oracle.spec_accept_greedy(lg, dr)
+    buf = torch.empty(lg.size + 8, dtype=torch.float32, device="cuda")
+    lgt = buf[shift:shift + lg.size].view(lg.shape)
+    lgt.copy_(torch.from_numpy(lg))
+    out = [torch.empty((B, k + 1), dtype=torch.int32, device="cuda"), torch.empty(B, dtype=torch.int32, device="cuda"),
+           torch.empty(B, dtype=torch.int32, device="cuda")]
+    pkv.spec_accept_greedy(lgt, torch.from_numpy(dr).cuda(), *out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out[0].cpu().numpy(), am)
+    assert np.array_equal(out[1].cpu().numpy(), acc)
+    assert np.array_equal(out[2].cpu().numpy(), nxt)
+
+
 @pytest.mark.parametrize("g,ql", [(4, 2), (4, 3), (4, 5), (4, 6), (8, 2), (8, 3), (2, 7), (2, 12), (1, 17),
                                   (1, 24), (16, 1), (12, 2), (3, 8)])
 @pytest.mark.parametrize("d", [64, 128])
