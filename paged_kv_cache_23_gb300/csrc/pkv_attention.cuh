@@ -117,6 +117,7 @@ struct AttnParams {
     const float* k_scale;  // FP8 pools: dequantisation scales per kv head, or [num_blocks][n_kv] (null for bf16)
     const float* v_scale;
     int scale_pb;          // FP8 pools: 1 = a scale per (block, kv head) tile
+    int scale_bulk;        // per-block scale rows are 16-byte aligned multiples of 16 bytes: fetched by bulk copies
     int max_blocks, n_q, n_kv, G, bs, num_blocks, np_max, row_bytes;
     int tc;              // tcgen05 tiles possible: tensor memory is allocated when the plan made some
     int tc_pair;         // tcgen05 stages of block_size 16: one V box holds both slabs of a block
@@ -154,7 +155,7 @@ struct Smem {
     };
     // FP8 pools with per-block scales: the K and V scales of each block of a
     // stage for its kv heads, [slot][K,V][block of the stage][head of the stage]
-    float scl[F8 ? G::kSlots : 1][2][F8 ? kTileT : 1][kMaxHPS];
+    alignas(16) float scl[F8 ? G::kSlots : 1][2][F8 ? kTileT : 1][kMaxHPS];
     Desc desc[kSlots];
     int poison[kSlots];
     int abort;
@@ -400,10 +401,17 @@ __device__ __forceinline__ bool stream_item(Smem<D, F8>& sm, const TMaps* tm, co
         // before the barrier is armed, so the consumers' wait on it orders them
         float scv[kMaxHPS];
         const bool pbs = F8 && !vwarp && p.scale_pb != 0;
-        if (pbs && in) {
+        // aligned scale rows travel as bulk copies on the stage's barrier
+        const bool pbulk = pbs && p.scale_bulk != 0;
+        const uint32_t scl_bytes = (uint32_t)d.hps * 4u;
+        if (pbs && !pbulk && in) {
+            // the scale rows (a few MB) are kept in L2 under evict-last: the
+            // K/V stream would otherwise push them out, and a load that misses
+            // to HBM here holds up every copy of the stage
+            const uint64_t keep = l2_evict_last_policy();
             const float* src = ((lane >> 4) ? p.v_scale : p.k_scale) + (long long)my * p.n_kv + d.hg * d.hps;
 #pragma unroll
-            for (int h = 0; h < kMaxHPS; ++h) scv[h] = h < d.hps ? __ldg(src + h) : 0.f;
+            for (int h = 0; h < kMaxHPS; ++h) scv[h] = h < d.hps ? ld_keep_l2(src + h, keep) : 0.f;
         }
         bool got = true;
         const unsigned badmask = __ballot_sync(kFull, !okb);
@@ -415,7 +423,7 @@ __device__ __forceinline__ bool stream_item(Smem<D, F8>& sm, const TMaps* tm, co
             got = mbar_wait(&sm.empty[s], ((g / RS) & 1) ^ 1, abort);
         }
         if (!__shfl_sync(kFull, got, 0)) return false;  // never arm a barrier whose previous phase is open
-        if (pbs) {
+        if (pbs && !pbulk) {
             if (in) {
 #pragma unroll
                 for (int h = 0; h < kMaxHPS; ++h)
@@ -423,7 +431,13 @@ __device__ __forceinline__ bool stream_item(Smem<D, F8>& sm, const TMaps* tm, co
             }
             __syncwarp();
         }
-        if (!vwarp && lane == 0) mbar_arrive_expect_tx(&sm.full[s], 2u * ne * op_bytes);
+        if (!vwarp && lane == 0)
+            mbar_arrive_expect_tx(&sm.full[s], 2u * ne * op_bytes + (pbulk ? 2u * ne * scl_bytes : 0u));
+        if (pbulk && in) {
+            // lane 16 v + e: the K (v = 0) or V (v = 1) scale row of block e
+            const float* src = ((lane >> 4) ? p.v_scale : p.k_scale) + (long long)my * p.n_kv + d.hg * d.hps;
+            bulk_load(&sm.scl[s][lane >> 4][be][0], src, scl_bytes, &sm.full[s]);
+        }
         if (in && lane < 16) {
             const int row0 = p.bs > kTileT ? (t0 % p.bs) : 0;
             // map dimensions {column of a 128-byte box, row, box, kv head,

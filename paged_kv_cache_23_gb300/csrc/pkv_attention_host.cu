@@ -709,6 +709,15 @@ int launch_run(const Shape& s, void* out, const void* q, const void* k_cache, co
     ap.k_scale = k_scale;
     ap.v_scale = v_scale;
     ap.scale_pb = (fq & 2) ? 1 : 0;
+    {
+        // FP8 items take gcd_pow2(n_kv, 8) kv heads a stage: their scale rows
+        // are that many floats at (block * n_kv + group * hps) floats
+        const int hps = gcd_pow2(s.n_kv, kMaxHPS);
+        ap.scale_bulk = ap.scale_pb && (hps * 4) % 16 == 0 && (s.n_kv * 4) % 16 == 0 &&
+                                host::aligned16(k_scale) && host::aligned16(v_scale)
+                            ? 1
+                            : 0;
+    }
     ap.tc = s.tc ? 1 : 0;
     ap.tc_pair = tc_pair ? 1 : 0;
     ap.plan_key = s.key;
