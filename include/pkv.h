@@ -149,8 +149,8 @@ int pkv_gather_kv(void* k_out, void* v_out, const void* k_cache, const void* v_c
  * Smallest partition length pkv_paged_attention_decode uses when
  * partition_tokens is 0, for a batch of num_seqs sequences no longer than
  * max_seq_len (512, doubled while a sequence would have more than 1024
- * partitions).  It sizes the workspace; the call itself may take a longer
- * partition (see partition_tokens below).
+ * partitions).  It sizes the workspace; the call itself gives each sequence
+ * a partition length of its own, never shorter (see partition_tokens below).
  */
 int pkv_attention_auto_partition(int num_seqs, int total_q, int num_kv_heads, int max_seq_len);
 
@@ -186,25 +186,32 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *   q_lens        int32 [num_seqs]: 1 = decode, k > 1 = speculative verify
  *                 or a prefill chunk, 0 = no rows
  *   max_q_len     host bound on every q_len (a larger q_len is BAD_QLEN);
- *                 the tcgen05 tile code runs only when max_q_len * g >= 128
+ *                 the tcgen05 tile code runs only when max_q_len * g > 24
  *   max_seq_len   host bound on every seq_len (sizes the workspace)
  *   head_dim      64 or 128; block_size a power of two in [1, 256];
  *                 g = num_q_heads / num_kv_heads an integer in [1, 64]
- *   partition_tokens  multiple of 16, at most 1024 partitions per sequence;
- *                 or 0: automatic -- the planning kernel starts from
- *                 P0 = pkv_attention_auto_partition(...) and raises it along
- *                 P0, 3P0/2, 2P0, 3P0, 4P0, ... (up to 8192) while the batch
- *                 would give more than 2 partitions per SM (3 when
- *                 multi-query rows make up most of the work; fewer, longer
- *                 partitions cost fewer partial results); the length used is
- *                 the int at byte offset 8 of the workspace after the call
+ *   partition_tokens  multiple of 16, at most 1024 partitions per sequence,
+ *                 every sequence cut at multiples of it; or 0: automatic --
+ *                 the planning kernel cuts each sequence into nearly equal
+ *                 partitions (whole 16-token stages; 32 for FP8 pools, 128
+ *                 for tcgen05 tiles) of at least
+ *                 P0 = pkv_attention_auto_partition(...): about
+ *                 round(L / C) of them for a target length C of the batch's
+ *                 work over two items per SM (up to 8192), or, for a batch
+ *                 made mostly of multi-row decode-style sequences (speculative
+ *                 verification), the shortest length whose items fit on the
+ *                 SMs in one wave; the target C is the int at byte offset 8 of
+ *                 the workspace after the call
  *   flags         0, or an OR of PKV_ATTN_DECODE_CUDA_CORES (q_len = 1 rows
  *                 on the CUDA-core FMA path; by default every row uses the
  *                 tensor cores, measured faster on GB300) and
- *                 PKV_ATTN_NO_TCGEN05.  By default (head_dim 128, block_size
- *                 >= 16, partition length a multiple of 128, decode rows on
- *                 tensor cores) a sequence with q_len * g >= 128 runs as
- *                 tiles of 128 (query, q head) rows
+ *                 PKV_ATTN_NO_TCGEN05.  A sequence with q_len * g <= 24
+ *                 (query, q head) columns per kv head -- decode rows, and
+ *                 speculative verification of up to 6 tokens at g = 4 -- runs
+ *                 on the transposed tensor-core item.  By default (head_dim
+ *                 128, block_size >= 16, partition length a multiple of 128,
+ *                 decode rows on tensor cores) a sequence with q_len * g > 24
+ *                 runs as tiles of 128 (query, q head) rows
  *                 of one kv head on the tcgen05 tensor cores (accumulators in
  *                 tensor memory, 128-token stages); PKV_ATTN_NO_TCGEN05 keeps
  *                 it on the mma.sync multi-query path
