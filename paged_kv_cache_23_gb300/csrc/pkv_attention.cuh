@@ -763,13 +763,14 @@ __device__ __forceinline__ void decode_item(Smem<D, false>& sm, const AttnParams
 //   O^T[D x 8 NTN]  += V_tile^T[D x 16] . P^T[16 x 8 NTN]   (NTN D/16 mma)
 // A decode row (q_len = 1) is a tile of one query: its g <= 8 heads fill one
 // n-tile, so g = 4 pads half of N instead of three quarters of M.  A short
-// multi-query row of q_len <= 16 / g queries is one tile of two n-tiles, so
-// every kv head of a block still shares one stage (32 KB copies of K and of V
-// at the 8B shape) and each column applies its query's causal limit.  (Three
-// n-tiles were measured: the accumulators and query fragments of 24 columns
-// do not fit the warp's 168 registers, and the spills made a speculative
-// verification twice as slow as on mma.sync row tiles.)  P^T's B fragments
-// are the S^T accumulators transposed in registers (movmatrix).
+// multi-query row of q_len <= 24 / g queries is one tile of up to three
+// n-tiles, so every kv head of a block still shares one stage (32 KB copies of
+// K and of V at the 8B shape) and each column applies its query's causal
+// limit.  Three n-tiles hold 48 registers of Q^T fragments and 96 of O^T
+// accumulators: they fit the consumer warpgroups' 224 registers (at the
+// launch's 168 they spilled, and a speculative verification ran twice as slow
+// as on mma.sync row tiles).  P^T's B fragments are the S^T accumulators
+// transposed in registers (movmatrix).
 // ---------------------------------------------------------------------------
 template <int D, int NTN>
 __device__ __forceinline__ void decode_tc_item(Smem<D, false>& sm, const AttnParams& p, const Desc& d, int warp, int lane,
