@@ -2150,15 +2150,13 @@ __device__ __forceinline__ void tc_end(Smem<D, F8>& sm, int warp, int lane, bool
 }
 
 // TC: the variant with tcgen05 tiles (head_dim 128, bf16), launched only for
-// batches that may hold a 128-row tile -- the other variant's item code keeps
-// its register allocation free of the tile's.
-// Threads of a CTA: eight consumer warps, the producer warp, and in the
-// variant with tcgen05 tiles the MMA warp and the helper TMA warp.
-template <bool TC>
-constexpr int kThreadsOf = kThreads;
+// batches that may hold a tile (a row of more than kTcMinCols columns) -- the
+// other variant carries none of the tile code.  Both launch kThreads threads:
+// eight consumer warps and the side warpgroup (producer, MMA and helper warps
+// of the tile variant, V warp).
 
 template <int D, int GD, bool F8, bool TC, int NTN, int FQ>
-__global__ void __launch_bounds__(kThreadsOf<TC>, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     paged_attention_kernel(const __grid_constant__ TMaps tm, const __grid_constant__ AttnParams p) {
     static_assert(!TC || Smem<D, F8>::kTC, "tcgen05 tiles need the head_dim 128 bf16 layout");
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -2261,7 +2259,7 @@ int launch_attention(const TMaps& tm, const AttnParams& p, long long max_items, 
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
     const cudaError_t e =
-        host::launch_pdl(paged_attention_kernel<D, GD, F8, TC, NTN, FQ>, dim3((unsigned)grid), dim3(kThreadsOf<TC>), smem, st,
+        host::launch_pdl(paged_attention_kernel<D, GD, F8, TC, NTN, FQ>, dim3((unsigned)grid), dim3(kThreads), smem, st,
                          tm, p);
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
