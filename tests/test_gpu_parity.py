@@ -236,6 +236,19 @@ def test_spec_accept_golden_and_nan_rows():
         assert int(acc[0]) == c["accepted"] and int(nxt[0]) == c["next_token"], c["name"]
 
 
+def test_batches_above_1024_sequences():
+    # the planning kernel keeps per-sequence records in shared memory up to
+    # 1024 sequences and in the workspace beyond; automatic partitions
+    run_and_check(wl.decode(1500, 5, 80, 21, n_q=8, n_kv=2, d=64, bs=16))
+    run_and_check(wl.spec(B=1100, lo=4, hi=60, k=3, vocab=40, seed=22, n_q=8, n_kv=2, d=64, bs=16))
+
+
+def test_verification_batch_too_large_for_one_wave():
+    # 400 verification sequences: every one-wave length still gives more
+    # items than SMs, so the planner falls back to about two items per SM
+    run_and_check(wl.spec(B=400, lo=20, hi=400, k=5, vocab=40, seed=23, n_q=32, n_kv=8, d=128, bs=16))
+
+
 @pytest.mark.parametrize("V", [1, 7, 1000, 128256, 128257])
 def test_spec_accept_random_vocab_sizes(V):
     rng = np.random.default_rng(V)
