@@ -8,10 +8,10 @@
 // the bonus token after k accepted drafts).
 //
 // The row argmax over a 128K vocabulary is an HBM scan.  Each row is split
-// across a thread-block cluster of 8 CTAs; partial (value, index) winners are
-// combined through distributed shared memory in the cluster's rank-0 CTA.  A
-// second tiny kernel turns the k+1 argmaxes of a sequence into the accepted
-// length and the next token.
+// across a thread-block cluster of two CTAs (persistent clusters, several rows
+// each); partial (value, index) winners are combined through distributed
+// shared memory in the cluster's rank-0 CTA.  A second tiny kernel turns the
+// k+1 argmaxes of a sequence into the accepted length and the next token.
 #include <cooperative_groups.h>
 
 #include "pkv_common.cuh"
