@@ -394,8 +394,10 @@ def run_gpu(args):
     if args.layers > 1:
         return run_layers(args, w, ds, b, pools, spec, stream, device, ws, rank, local, parity)
 
-    # the plan reads only the lengths: it runs on a side stream while the
-    # step's cache ops run, and the attention run waits for it
+    # the plan reads only the lengths: in a step that copies blocks on write
+    # it runs on a side stream while the cache ops run, and the attention run
+    # waits for it; otherwise the step runs in stream order
+    # (DeviceStep.plan_beside_cache_ops)
     plan_stream = torch.cuda.Stream(device)
 
     def step():
@@ -475,7 +477,8 @@ def run_gpu(args):
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": load_traffic() if args.workload == "mix" else None,
                          "kernel": "pkv_paged_attention_run (attention + combine kernels; the plan is made once "
-                                   "per step, on a side stream beside the cache ops)",
+                                   "per step, " + ("on a side stream beside the cache ops)" if ds.plan_beside_cache_ops()
+                                                   else "in stream order after the append)"),
                          "peak_kind": peak_kind, "attention_ms": attn_avg, "call_ms_with_plan": call_ms,
                          "frac_of_nominal_8tbs": achieved / 8000.0},
             "clocks": clocks, "e2e": e2e, "gpu_launches": ds.launches_per_step() * args.steps, "status": st, "parity": parity}
@@ -495,7 +498,8 @@ def parity_check(w, ds, device, pools=None):
     import oracle
     from paged_kv_cache_23_gb300 import workloads as wl
     from paged_kv_cache_23_gb300.runner import bf16_to_bits
-    # the step as the timed region runs it: the plan on a side stream
+    # the step as the timed region runs it (the plan on a side stream where
+    # the step copies blocks on write)
     ds.step(torch.cuda.current_stream(device), torch.cuda.Stream(device))
     torch.cuda.synchronize()
     kv = _oracle_cache(w, pools)
@@ -646,7 +650,7 @@ def end_to_end(ds, w, args, stream, device, ws):
     h2d = host.numel()
     d2h = out_hosts[0].numel() * out_hosts[0].element_size()
     up_s, dn_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
-    plan_stream = torch.cuda.Stream(device)  # the plan beside the cache ops, as in the device-timed step
+    plan_stream = torch.cuda.Stream(device)  # the step's streams as in the device-timed step
     up = [torch.cuda.Event() for _ in range(2)]
     done = [torch.cuda.Event() for _ in range(2)]
     free = [torch.cuda.Event() for _ in range(2)]

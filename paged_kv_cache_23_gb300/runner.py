@@ -212,13 +212,24 @@ class DeviceStep:
         if self.spec:
             spec_accept_greedy(self.logits, self.draft, self.argmax, self.accepted, self.next_token, stream=stream)
 
+    def plan_beside_cache_ops(self) -> bool:
+        """Whether a step's plan runs on a side stream beside its cache ops:
+        only when the step copies blocks on write.  Copy plus append are long
+        enough to hide the plan and the two cross-stream waits; beside the
+        append alone the waits cost more than the overlap saves, and the plan
+        runs in stream order, where programmatic launch overlaps each kernel's
+        start with the previous one's end."""
+        return bool(self.cow.numel())
+
     def step(self, stream=None, plan_stream=None):
-        """One decode step.  With `plan_stream`, the plan (which reads only the
+        """One decode step.  With `plan_stream` (and a step that copies blocks
+        on write, `plan_beside_cache_ops`), the plan (which reads only the
         lengths) runs there while the cache ops run on `stream`, and the
         attention run waits for it; the plan stream first waits for the work
         already on `stream` (the previous step's kernels still read the
-        workspace, and the lengths may have just been uploaded there)."""
-        if plan_stream is None:
+        workspace, and the lengths may have just been uploaded there).
+        Otherwise every kernel of the step runs in order on `stream`."""
+        if plan_stream is None or not self.plan_beside_cache_ops():
             self.cache_ops(stream)
             self.attention(stream)
             self.accept(stream)

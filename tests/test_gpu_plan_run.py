@@ -184,13 +184,15 @@ def test_back_to_back_calls_with_lengths_written_on_the_gpu(bs, kind, plan_run):
     _close(outs[0], want, f"{kind} bs {bs}")
 
 
-@pytest.mark.parametrize("name", ["decode", "mix", "spec"])
+@pytest.mark.parametrize("name", ["decode", "mix", "spec", "tiny"])
 def test_step_with_the_plan_on_a_side_stream(name):
-    # the bench's step: the plan on its own stream beside the cache ops, the
-    # run after both; every step bit-identical to the one-stream step, and
-    # the first within tolerance of the oracle
+    # the bench's step: in a step that copies blocks on write (mix, tiny) the
+    # plan on its own stream beside the cache ops and the run after both, else
+    # every kernel in order on the main stream; every step bit-identical to the
+    # one-stream step, and the first within tolerance of the oracle
     w = wl.SMALL[name]()
     ds = DeviceStep(w)
+    assert ds.plan_beside_cache_ops() == (name in ("mix", "tiny"))
     ds.step()
     torch.cuda.synchronize()
     ref = bf16_to_bits(ds.out)
