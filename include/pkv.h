@@ -198,9 +198,10 @@ size_t pkv_attention_workspace_bytes(int num_seqs, int total_q, int num_q_heads,
  *                 P0 = pkv_attention_auto_partition(...): about
  *                 round(L / C) of them for a target length C of the batch's
  *                 work over two items per SM (up to 8192), or, for a batch
- *                 made mostly of multi-row decode-style sequences (speculative
- *                 verification), the shortest length whose items fit on the
- *                 SMs in one wave; the target C is the int at byte offset 8 of
+ *                 of up to 1024 sequences made mostly of multi-row
+ *                 decode-style sequences (speculative verification), the
+ *                 shortest length whose items fit on the SMs in one wave
+ *                 (ceil(L / C) partitions of at most C); the target C is the int at byte offset 8 of
  *                 the workspace after the call
  *   flags         0, or an OR of PKV_ATTN_DECODE_CUDA_CORES (q_len = 1 rows
  *                 on the CUDA-core FMA path; by default every row uses the

@@ -14,9 +14,9 @@
 // How it runs on GB300 (sm_103a):
 //   * A planning kernel turns (seq_lens, q_lens) into per-sequence records and
 //     a list of 16-byte work items (sequence, partition, query tile, head
-//     group): multi-query items first, then every full decode partition, then
-//     the partition tails longest first, so the dynamic queue ends on short
-//     items.  It also records how many partitions each query row has.
+//     group): multi-query items first, then every decode-style item longest
+//     first (a counting sort over length classes), so the dynamic queue ends
+//     on short items.  It also records how many partitions each query row has.
 //   * The attention kernel is persistent, one CTA per SM, three warpgroups:
 //     eight consumer warps (224 registers each) and a side warpgroup (56
 //     each, by setmaxnreg) holding the producer warp, the V warp and, in the
